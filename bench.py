@@ -1,0 +1,505 @@
+"""Benchmark: calibrated E4M3 paged decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|decode32k|long] [--no-cpu-baseline]
+
+One step = one pass of the whole hot path over one batch: quantise-on-append
+of this step's new K/V tokens into the page-4 cache, split-K decode attention
+over the paged cache, and the log-sum-exp combine.  Inputs are seeded
+synthetic tensors (see fp8_paged_kv_e4m3_gb300.inputs).  The headline
+workload is batch 32 x 4096 context, 32 query / 4 kv heads, head_dim 128,
+q_len 1, split-K 4.
+
+Reported (one JSON line on rank 0): achieved HBM GB/s of algorithmic bytes
+per step (KV bytes read + Q + output + block tables + append traffic; the
+FP32 split workspace is not counted), its fraction of the measured HBM
+peak, sequence-steps/s, and the same for the fp16-KV arm with the
+fp16/E4M3 step-time ratio.  L2 is defeated by rotating through copies of
+the KV pools whose total exceeds twice the L2 size.
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU
+with its own seeded batch (the path shards by sequence with no exchange),
+timing is max-over-ranks, and the value is the aggregate.
+
+--impl reference: the CPU oracle (the only other implementation of the
+method here) timed on this host's cores on a bounded sample of the same
+workload, printed in the same format with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "E4M3 paged decode-attn achieved HBM GB/s (% of peak) and seq-steps/s vs FP16"
+L2_BYTES_DEFAULT = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workload accounting
+
+def algorithmic_bytes(w, kv_elem_bytes: int, lens, step_tokens: int):
+    """Bytes the step must move at minimum: every cached K and V element once,
+    Q, the output, the block-table entries of the pages read, the context
+    lengths, and the append (fp16 in, cache dtype out, slot ids)."""
+    Hkv, D = w.num_kv_heads, w.head_dim
+    tokens = int(np.sum(lens))
+    pages = int(np.sum((np.asarray(lens, np.int64) + 3) // 4))
+    kv = 2 * tokens * Hkv * D * kv_elem_bytes
+    q = w.batch * w.q_len * w.num_q_heads * D * 2
+    out = q
+    bt = pages * 4 + w.batch * 4
+    append = step_tokens * Hkv * D * 2 * (2 + kv_elem_bytes) + step_tokens * 4
+    attn = kv + q + bt
+    return {"step": kv + q + out + bt + append, "attention_kernel": attn}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while timing
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() in ("active", "1", "0x1")})
+        under = [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(under), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+
+class Arm:
+    """One arm (E4M3 or fp16 KV) of the decode step, with rotating pool copies."""
+
+    def __init__(self, w, e4m3: bool, dev, seed_rank: int, l2_bytes: int):
+        import torch
+        from fp8_paged_kv_e4m3_gb300 import inputs, kvq
+        self.torch, self.kvq, self.w, self.e4m3, self.dev = torch, kvq, w, e4m3, dev
+        w = rank_workload(w, seed_rank)
+        self.w = w
+        lay = inputs.page_layout(w)
+        self.lay = lay
+        lens = lay.lens.astype(np.int64)
+        total = int(lens.sum())
+        offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        k = inputs.kv_tokens(w, 0, total, "k", device=dev)
+        v = inputs.kv_tokens(w, 0, total, "v", device=dev)
+        self.q = inputs.queries(w, 0, device=dev)
+        if e4m3:
+            self.ks = kvq.calibrate_scale(inputs.calibration_draw(w, 0, "k", device=dev))
+            self.vs = kvq.calibrate_scale(inputs.calibration_draw(w, 0, "v", device=dev))
+            kvq.validate_scales([self.ks], [self.vs])
+        hs, hp = inputs.history_tokens(w, lay)
+        ss, sp = inputs.step_tokens(w, lay)
+        hist_slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, hs, hp)).to(dev)
+        hist_rows = torch.from_numpy(offs[hs] + hp).to(dev)
+        self.step_slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, ss, sp)).to(dev)
+        step_rows = torch.from_numpy(offs[ss] + sp).to(dev)
+        self.k_new = k[step_rows].contiguous()
+        self.v_new = v[step_rows].contiguous()
+        self.bt = torch.from_numpy(lay.block_tables).to(dev)
+        self.cl = torch.from_numpy(lay.lens).to(dev)
+        shape = (lay.num_pages, w.num_kv_heads, 4, w.head_dim)
+        dt = torch.uint8 if e4m3 else torch.float16
+        pool_bytes = 2 * math.prod(shape) * (1 if e4m3 else 2)
+        self.copies = max(1, math.ceil(2 * l2_bytes / pool_bytes))
+        self.pools = []
+        kh, vh = k[hist_rows].contiguous(), v[hist_rows].contiguous()
+        for _ in range(self.copies):
+            kc = torch.zeros(shape, dtype=dt, device=dev)
+            vc = torch.zeros(shape, dtype=dt, device=dev)
+            self._append(kh, vh, hist_slots, kc, vc)
+            self.pools.append((kc, vc))
+        del k, v, kh, vh
+        self.p = kvq.attn_params(self.q, w.num_kv_heads, self.bt.shape[1], w.num_splits)
+        self.S = kvq.num_splits(self.p)
+        self.ws = kvq.alloc_workspace(self.p, dev)
+        self.out = torch.empty_like(self.q)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pool_bytes = pool_bytes
+        self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, w.batch * w.q_len)
+        torch.cuda.synchronize(dev)
+
+    def _append(self, k, v, slots, kc, vc):
+        if self.e4m3:
+            self.kvq.kv_append_e4m3(k, v, slots, kc, vc, self.ks, self.vs, None)
+        else:
+            self.kvq.kv_append_fp16(k, v, slots, kc, vc, None)
+
+    def _attention(self, kc, vc, q=None, bt=None, cl=None):
+        kvq = self.kvq
+        q = self.q if q is None else q
+        bt = self.bt if bt is None else bt
+        cl = self.cl if cl is None else cl
+        if self.e4m3:
+            kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
+                                               num_splits=self.S, err_flag=self.err)
+        else:
+            kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, num_splits=self.S,
+                                               err_flag=self.err)
+
+    def step(self, i, ev=None):
+        kc, vc = self.pools[i % self.copies]
+        self._append(self.k_new, self.v_new, self.step_slots, kc, vc)
+        if ev is not None:
+            ev[0].record()
+        self._attention(kc, vc)
+        if ev is not None:
+            ev[1].record()
+        self.kvq.lse_combine(self.ws, self.out, self.p)
+
+    def time(self, steps, warmup, barrier=None):
+        torch = self.torch
+        for i in range(warmup):
+            self.step(i)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        if barrier:
+            barrier()
+        torch.cuda.synchronize(self.dev)
+        start.record()
+        for i in range(steps):
+            self.step(warmup + i, evs[i])
+        end.record()
+        torch.cuda.synchronize(self.dev)
+        if barrier:
+            barrier()
+        total_ms = start.elapsed_time(end)
+        attn_ms = [a.elapsed_time(b) for a, b in evs]
+        assert self.err.item() == 0, f"device error bits {self.err.item()}"
+        return total_ms, attn_ms
+
+    def time_e2e(self, steps, warmup):
+        """Per step: H2D of the step's inputs from pinned host memory, the
+        three kernels, and a D2H read of the output, all on one stream."""
+        torch = self.torch
+        host = {n: t.cpu().pin_memory() for n, t in
+                (("q", self.q), ("k", self.k_new), ("v", self.v_new), ("slots", self.step_slots),
+                 ("bt", self.bt), ("cl", self.cl))}
+        dev = {n: torch.empty_like(getattr(self, a)) for n, a in
+               (("q", "q"), ("k", "k_new"), ("v", "v_new"), ("slots", "step_slots"), ("bt", "bt"),
+                ("cl", "cl"))}
+        out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def one(i):
+            for n in host:
+                dev[n].copy_(host[n], non_blocking=True)
+            kc, vc = self.pools[i % self.copies]
+            self._append(dev["k"], dev["v"], dev["slots"], kc, vc)
+            self._attention(kc, vc, dev["q"], dev["bt"], dev["cl"])
+            self.kvq.lse_combine(self.ws, self.out, self.p)
+            out_host.copy_(self.out, non_blocking=True)
+
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize(self.dev)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(steps):
+            one(warmup + i)
+        end.record()
+        torch.cuda.synchronize(self.dev)
+        return start.elapsed_time(end) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+
+def oracle_sample_time(w, units: int, seed: int = 0):
+    """Time the oracle on `units` (sequence, kv head) units of the workload:
+    append of the step's tokens into the oracle's own pool, then binary64
+    attention of the unit's query heads.  Pools for the cached history are
+    built beforehand (not timed).  Returns (seconds, algorithmic bytes)."""
+    import torch
+    import oracle
+    from fp8_paged_kv_e4m3_gb300 import inputs
+    lay = inputs.page_layout(w)
+    lens = lay.lens.astype(np.int64)
+    offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    rng = np.random.default_rng(1234 + seed)
+    picks = [(int(b), int(g)) for b, g in
+             zip(rng.integers(0, w.batch, units), rng.integers(0, w.num_kv_heads, units))]
+    q = inputs.queries(w, 0).numpy()
+    G = w.group
+    total_t = 0.0
+    nbytes = 0
+    for b, g in picks:
+        L = int(lens[b])
+        # regenerate only this sequence's rows: draw the layer once per call site
+        k = _seq_rows(w, "k", offs[b], L, g)
+        v = _seq_rows(w, "v", offs[b], L, g)
+        pages = (L + 3) // 4
+        kc = np.zeros((pages, 1, 4, w.head_dim), np.uint8)
+        vc = np.zeros_like(kc)
+        slots = np.arange(L, dtype=np.int32)
+        oracle.append_e4m3(k[: L - w.q_len, None], v[: L - w.q_len, None], slots[: L - w.q_len],
+                           kc, vc, 0.01, 0.01)
+        bt = np.arange(pages, dtype=np.int32)[None]
+        qu = np.ascontiguousarray(q[b:b + 1, :, g * G:(g + 1) * G])
+        t0 = time.perf_counter()
+        oracle.append_e4m3(k[L - w.q_len:, None], v[L - w.q_len:, None], slots[L - w.q_len:],
+                           kc, vc, 0.01, 0.01)
+        oracle.attention(qu, kc, vc, bt, np.array([L], np.int32), 0.01, 0.01)
+        total_t += time.perf_counter() - t0
+        nbytes += 2 * L * w.head_dim + 2 * qu.nbytes + pages * 4 + w.q_len * w.head_dim * 6
+    return total_t, nbytes, len(picks)
+
+
+_SEQ_CACHE = {}
+
+
+def _seq_rows(w, which, off, L, g):
+    from fp8_paged_kv_e4m3_gb300 import inputs
+    key = (w, which)
+    if key not in _SEQ_CACHE:
+        lay = inputs.page_layout(w)
+        total = int(lay.lens.astype(np.int64).sum())
+        _SEQ_CACHE[key] = inputs.kv_tokens(w, 0, total, which).numpy()
+    return np.ascontiguousarray(_SEQ_CACHE[key][off:off + L, g, :])
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle on a bounded sample per step."""
+    per_unit_s, _, _ = oracle_sample_time(w, 1, seed=99)   # calibrate the sample size
+    budget_s = 120.0
+    units = max(1, int(budget_s / max(per_unit_s, 1e-3) / max(1, args.steps + args.warmup)))
+    units = min(units, w.batch * w.num_kv_heads)
+    for i in range(args.warmup):
+        oracle_sample_time(w, units, seed=i)
+    t = 0.0
+    nb = 0
+    for i in range(args.steps):
+        dt, b, _ = oracle_sample_time(w, units, seed=1000 + i)
+        t += dt
+        nb += b
+    gbs = nb / t / 1e9
+    sample = (f"{units} (sequence, kv head) units of the {w.name} workload per step "
+              f"(append of the step token + binary64 attention of {w.group} query heads)")
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# multi-rank helpers (replicas: no data-path exchange, only the timing reduction)
+
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The slowest rank's value (timing is max over ranks)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(step_bytes_per_rank: int, batch_per_rank: int, world: int, ms_max: float):
+    """Whole-job GB/s and sequence-steps/s from the slowest rank's step time:
+    every rank processes its own batch of the same shape (weak scaling)."""
+    return (world * step_bytes_per_rank / (ms_max * 1e-3) / 1e9,
+            world * batch_per_rank / (ms_max * 1e-3))
+
+
+def rank_workload(w, rank: int):
+    """Rank r's replica: same shapes, its own seeded data."""
+    from fp8_paged_kv_e4m3_gb300 import inputs
+    return inputs.get(w.name, seed=rank) if rank else w
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp16", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from fp8_paged_kv_e4m3_gb300 import inputs
+    w = inputs.get(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from fp8_paged_kv_e4m3_gb300 import build as kbuild, kvq
+    kbuild.build()
+    kvq.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+        barrier = lambda: dist.barrier(device_ids=[local_rank])
+    else:
+        barrier = None
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or L2_BYTES_DEFAULT
+    peak, peak_kind = _peaks()
+
+    reduce_max = lambda x: max_over_ranks(x, dev, world)
+
+    arm = Arm(w, True, dev, rank, l2)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        total_ms, attn_ms = arm.time(args.steps, args.warmup, barrier)
+    total_ms = reduce_max(total_ms)
+    ms = total_ms / args.steps
+    attn_avg = reduce_max(sum(attn_ms) / len(attn_ms))
+    step_bytes = arm.bytes["step"]
+    gbs, seq_steps = aggregate(step_bytes, w.batch, world, ms)
+    achieved = arm.bytes["attention_kernel"] / (attn_avg * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = arm.time_e2e(max(5, args.steps // 2), args.warmup)
+    e2e_ms = reduce_max(e2e_ms)
+
+    fp16 = None
+    if not args.no_fp16:
+        del arm.pools
+        torch.cuda.empty_cache()
+        arm16 = Arm(w, False, dev, rank, l2)
+        t16, a16 = arm16.time(args.steps, args.warmup, barrier)
+        ms16 = reduce_max(t16) / args.steps
+        a16avg = reduce_max(sum(a16) / len(a16))
+        fp16 = {"ms_per_step": ms16,
+                "value": world * arm16.bytes["step"] / (ms16 * 1e-3) / 1e9,
+                "seq_steps_per_s": world * w.batch / (ms16 * 1e-3),
+                "attention_kernel_ms": a16avg,
+                "attention_kernel_gbs": arm16.bytes["attention_kernel"] / (a16avg * 1e-3) / 1e9,
+                "pool_copies": arm16.copies}
+        del arm16
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        units = 64
+        t, nb, n = oracle_sample_time(w, units)
+        cpu = {"value": nb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} (sequence, kv head) units of one step ({w.group} query heads each): "
+                         f"append of the step token + binary64 attention, {t:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": f"{w.name}: batch {w.batch} x {w.lens.split(':')[1]} context, "
+                                   f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, head_dim "
+                                   f"{w.head_dim}, q_len {w.q_len}, split-K {arm.S}, page 4",
+                       "global_batch": world * w.batch, "kv_dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
+                       "l2": f"rotating {arm.copies} KV pool copies of {arm.pool_bytes / 1e6:.0f} MB "
+                             f"(> 2 x L2 {l2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_peak": 100.0 * gbs / world / peak,
+            "seq_steps_per_s": seq_steps,
+            "step_bytes": step_bytes,
+            "fp16_arm": fp16,
+            "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "attn_split_kernel (E4M3)", "peak_kind": peak_kind,
+                         "attention_kernel_ms": attn_avg},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,317 @@
+// kvq_api.cu -- the extern "C" entry points declared in include/kvq.h:
+// argument validation (fail closed, before any launch), workspace layout,
+// split-count choice, and the launches.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+static inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static inline bool good_scale(float s) { return std::isfinite(s) && s > 0.0f; }
+
+static inline size_t round256(size_t x) { return (x + 255u) & ~size_t(255u); }
+
+WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t head_dim)
+{
+    WorkspaceLayout w;
+    const size_t units = size_t(rows_total) * size_t(num_splits);
+    w.o_off = 0;
+    w.m_off = round256(units * size_t(head_dim) * sizeof(float));
+    w.l_off = w.m_off + round256(units * sizeof(float));
+    w.total = w.l_off + round256(units * sizeof(float));
+    return w;
+}
+
+int device_sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    return n;
+}
+
+// shape checks shared by every attention entry point; KVQ_OK or an error
+static int check_params(const kvq_attn_params *p)
+{
+    if (!p) return KVQ_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->q_len < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
+        p->num_splits < 0 || p->max_pages_per_seq < 1 || p->max_topk < 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+    if (!std::isfinite(p->sm_scale) || p->sm_scale < 0.0f) return KVQ_ERR_INVALID_ARG;
+    if (p->head_dim != 64 && p->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+    if (p->q_len > 4) return KVQ_ERR_UNSUPPORTED;
+    const int64_t rows = int64_t(p->num_q_heads / p->num_kv_heads) * p->q_len;
+    if (rows > 64) return KVQ_ERR_UNSUPPORTED;
+    if (p->batch > 65535 || p->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (int64_t(p->max_pages_per_seq) * 4 > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+}
+
+static int32_t resolve_splits(const kvq_attn_params *p)
+{
+    if (p->num_splits > 0) return p->num_splits;
+    // Enough CTAs for a few waves of the resident slots (about 3 CTAs per SM),
+    // but no split shorter than 16 pages.
+    const int64_t pairs = int64_t(p->batch > 0 ? p->batch : 1) * p->num_kv_heads;
+    const int64_t target = int64_t(device_sm_count()) * 3 * 2;
+    int64_t s = (target + pairs - 1) / pairs;
+    int64_t cap = (int64_t(p->max_pages_per_seq) + 15) / 16;
+    if (p->max_topk > 0) cap = cap > (p->max_topk + 31) / 32 ? cap : (p->max_topk + 31) / 32;
+    if (s > cap) s = cap;
+    if (s < 1) s = 1;
+    if (s > 1024) s = 1024;
+    return int32_t(s);
+}
+
+struct AttnCall {
+    bool e4m3;
+    const void *q, *k_cache, *v_cache;
+    int64_t num_pages;
+    const int32_t *block_tables, *context_lens;
+    float k_scale, v_scale;
+    const int32_t *topk_idx, *topk_lens;
+    float *workspace;
+    size_t workspace_bytes;
+    void *out;          // null for the partial-only entry points
+    const kvq_attn_params *p;
+    int32_t *err_flag;
+    void *stream;
+};
+
+static int run_attention(const AttnCall &c, bool with_combine)
+{
+    int st = check_params(c.p);
+    if (st != KVQ_OK) return st;
+    const kvq_attn_params &p = *c.p;
+    if (!c.q || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens)
+        return KVQ_ERR_INVALID_ARG;
+    if (with_combine && !c.out) return KVQ_ERR_INVALID_ARG;
+    if (c.num_pages < 1) return KVQ_ERR_INVALID_ARG;
+    if ((c.topk_idx == nullptr) != (c.topk_lens == nullptr)) return KVQ_ERR_INVALID_ARG;
+    if (c.topk_idx && p.max_topk < 1) return KVQ_ERR_INVALID_ARG;
+    if (c.e4m3 && (!good_scale(c.k_scale) || !good_scale(c.v_scale))) return KVQ_ERR_BAD_SCALE;
+    if (!aligned16(c.q) || !aligned16(c.k_cache) || !aligned16(c.v_cache) ||
+        (c.out && !aligned16(c.out)) || !aligned16(c.workspace))
+        return KVQ_ERR_ALIGNMENT;
+    const int32_t S = resolve_splits(&p);
+    const int64_t rows_total = int64_t(p.batch) * p.num_q_heads * p.q_len;
+    const WorkspaceLayout wl = workspace_layout(rows_total, S, p.head_dim);
+    if (!c.workspace || c.workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
+    if (p.batch == 0) return KVQ_OK;
+
+    const int G = p.num_q_heads / p.num_kv_heads;
+    const double sm = p.sm_scale > 0.0f ? double(p.sm_scale) : 1.0 / std::sqrt(double(p.head_dim));
+    const double log2e = 1.4426950408889634;
+    AttnArgs a;
+    a.q = c.q;
+    a.k_cache = c.k_cache;
+    a.v_cache = c.v_cache;
+    a.num_pages = c.num_pages;
+    a.block_tables = c.block_tables;
+    a.context_lens = c.context_lens;
+    a.topk_idx = c.topk_idx;
+    a.topk_lens = c.topk_lens;
+    auto *ws = reinterpret_cast<uint8_t *>(c.workspace);
+    a.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
+    a.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
+    a.ws_l = reinterpret_cast<float *>(ws + wl.l_off);
+    a.err_flag = c.err_flag;
+    a.batch = p.batch;
+    a.q_len = p.q_len;
+    a.num_q_heads = p.num_q_heads;
+    a.num_kv_heads = p.num_kv_heads;
+    a.group = G;
+    a.rows = G * p.q_len;
+    a.num_splits = S;
+    a.max_pages = p.max_pages_per_seq;
+    a.max_topk = c.topk_idx ? p.max_topk : 0;
+    // hoisted scales: the bitcast decoder yields value * 2^-8, folded back here
+    const double kfold = c.e4m3 ? double(c.k_scale) * 256.0 : 1.0;
+    const double vfold = c.e4m3 ? double(c.v_scale) * 256.0 : 1.0;
+    a.qk_scale_log2 = float(sm * log2e * kfold);
+    a.out_scale = float(vfold);
+
+    cudaStream_t stream = static_cast<cudaStream_t>(c.stream);
+    if (launch_attention(c.e4m3, p.head_dim, a, stream) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (with_combine &&
+        launch_combine(a.ws_o, a.ws_m, a.ws_l, c.out, p.batch, p.q_len, p.num_q_heads, p.head_dim, S,
+                       stream) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+    return KVQ_OK;
+}
+
+static int run_append(bool e4m3, const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                      int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim, void *k_cache,
+                      void *v_cache, int64_t num_pages, float k_scale, float v_scale,
+                      int32_t *err_flag, void *stream)
+{
+    if (num_tokens < 0 || num_kv_heads < 1 || head_dim < 1 || num_pages < 1)
+        return KVQ_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return KVQ_ERR_UNSUPPORTED;
+    if (e4m3 && (!good_scale(k_scale) || !good_scale(v_scale))) return KVQ_ERR_BAD_SCALE;
+    if (num_tokens == 0) return KVQ_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return KVQ_ERR_ALIGNMENT;
+    const cudaError_t e = launch_append(e4m3, k_new, v_new, slot_mapping, num_tokens, num_kv_heads,
+                                        head_dim, k_cache, v_cache, num_pages, k_scale, v_scale,
+                                        err_flag, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+int kvq_version(void) { return KVQ_VERSION; }
+
+const char *kvq_status_string(int status)
+{
+    switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_BAD_SCALE: return "K/V scale is not finite and positive";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    default: return "unknown status";
+    }
+}
+
+int kvq_validate_scales(const float *k_scales, const float *v_scales, int32_t num_layers)
+{
+    if (!k_scales || !v_scales || num_layers < 1) return KVQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < num_layers; ++i)
+        if (!good_scale(k_scales[i]) || !good_scale(v_scales[i])) return KVQ_ERR_BAD_SCALE;
+    return KVQ_OK;
+}
+
+int kvq_amax_f16(const void *x, int64_t n, float *amax_out, void *stream)
+{
+    if (!x || !amax_out || n < 1) return KVQ_ERR_INVALID_ARG;
+    return launch_amax(x, n, amax_out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVQ_OK
+               : KVQ_ERR_CUDA;
+}
+
+float kvq_scale_from_amax(float amax)
+{
+    if (!std::isfinite(amax) || !(amax > 0.0f)) return 0.0f;
+    return amax / 448.0f;   // one binary32 division, as the method defines
+}
+
+int kv_append_e4m3(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim, uint8_t *k_cache,
+                   uint8_t *v_cache, int64_t num_pages, float k_scale, float v_scale,
+                   int32_t *err_flag, void *stream)
+{
+    return run_append(true, k_new, v_new, slot_mapping, num_tokens, num_kv_heads, head_dim, k_cache,
+                      v_cache, num_pages, k_scale, v_scale, err_flag, stream);
+}
+
+int kv_append_fp16(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim, void *k_cache,
+                   void *v_cache, int64_t num_pages, int32_t *err_flag, void *stream)
+{
+    return run_append(false, k_new, v_new, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                      k_cache, v_cache, num_pages, 1.0f, 1.0f, err_flag, stream);
+}
+
+int32_t kvq_attn_num_splits(const kvq_attn_params *p)
+{
+    const int st = check_params(p);
+    if (st != KVQ_OK) return st;
+    return resolve_splits(p);
+}
+
+size_t kvq_attn_workspace_bytes(const kvq_attn_params *p)
+{
+    if (check_params(p) != KVQ_OK) return 0;
+    const int64_t rows = int64_t(p->batch) * p->num_q_heads * p->q_len;
+    return workspace_layout(rows, resolve_splits(p), p->head_dim).total;
+}
+
+int paged_decode_attn_e4m3(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                           int64_t num_pages, const int32_t *block_tables,
+                           const int32_t *context_lens, float k_scale, float v_scale,
+                           const int32_t *topk_idx, const int32_t *topk_lens, float *workspace,
+                           size_t workspace_bytes, void *out, const kvq_attn_params *p,
+                           int32_t *err_flag, void *stream)
+{
+    const AttnCall c{true, q, k_cache, v_cache, num_pages, block_tables, context_lens, k_scale,
+                     v_scale, topk_idx, topk_lens, workspace, workspace_bytes, out, p, err_flag,
+                     stream};
+    return run_attention(c, true);
+}
+
+int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cache,
+                           int64_t num_pages, const int32_t *block_tables,
+                           const int32_t *context_lens, const int32_t *topk_idx,
+                           const int32_t *topk_lens, float *workspace, size_t workspace_bytes,
+                           void *out, const kvq_attn_params *p, int32_t *err_flag, void *stream)
+{
+    const AttnCall c{false, q, k_cache, v_cache, num_pages, block_tables, context_lens, 1.0f, 1.0f,
+                     topk_idx, topk_lens, workspace, workspace_bytes, out, p, err_flag, stream};
+    return run_attention(c, true);
+}
+
+int paged_decode_attn_e4m3_partial(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                   int64_t num_pages, const int32_t *block_tables,
+                                   const int32_t *context_lens, float k_scale, float v_scale,
+                                   const int32_t *topk_idx, const int32_t *topk_lens,
+                                   float *workspace, size_t workspace_bytes,
+                                   const kvq_attn_params *p, int32_t *err_flag, void *stream)
+{
+    const AttnCall c{true, q, k_cache, v_cache, num_pages, block_tables, context_lens, k_scale,
+                     v_scale, topk_idx, topk_lens, workspace, workspace_bytes, nullptr, p,
+                     err_flag, stream};
+    return run_attention(c, false);
+}
+
+int paged_decode_attn_fp16_partial(const void *q, const void *k_cache, const void *v_cache,
+                                   int64_t num_pages, const int32_t *block_tables,
+                                   const int32_t *context_lens, const int32_t *topk_idx,
+                                   const int32_t *topk_lens, float *workspace,
+                                   size_t workspace_bytes, const kvq_attn_params *p,
+                                   int32_t *err_flag, void *stream)
+{
+    const AttnCall c{false, q, k_cache, v_cache, num_pages, block_tables, context_lens, 1.0f, 1.0f,
+                     topk_idx, topk_lens, workspace, workspace_bytes, nullptr, p, err_flag, stream};
+    return run_attention(c, false);
+}
+
+int kvq_lse_combine(const float *workspace, size_t workspace_bytes, void *out,
+                    const kvq_attn_params *p, void *stream)
+{
+    const int st = check_params(p);
+    if (st != KVQ_OK) return st;
+    if (!workspace || !out) return KVQ_ERR_INVALID_ARG;
+    if (!aligned16(workspace) || !aligned16(out)) return KVQ_ERR_ALIGNMENT;
+    const int32_t S = resolve_splits(p);
+    const int64_t rows = int64_t(p->batch) * p->num_q_heads * p->q_len;
+    const WorkspaceLayout wl = workspace_layout(rows, S, p->head_dim);
+    if (workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
+    const auto *ws = reinterpret_cast<const uint8_t *>(workspace);
+    const cudaError_t e = launch_combine(reinterpret_cast<const float *>(ws + wl.o_off),
+                                         reinterpret_cast<const float *>(ws + wl.m_off),
+                                         reinterpret_cast<const float *>(ws + wl.l_off), out,
+                                         p->batch, p->q_len, p->num_q_heads, p->head_dim, S,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,622 @@
+// kvq_attn.cu -- split-K paged decode / MTP-verify attention over E4M3 or
+// fp16 page-4 pools, and the log-sum-exp combine.
+//
+// What is computed (PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV
+// capacity path", section Changes; PR "[Model][SM70] Calibrated E4M3 KV cache
+// for Qwen4Exp QSA with MTP", sections Purpose and Status and history):
+// grouped-query attention of q_len = 1 (decode) or 1 + 3 (MTP verify, causal
+// inside the window) query rows over a page-4 cache whose K/V are stored in
+// calibrated E4M3, decoded by a bitcast decoder with the per-layer scales
+// hoisted out of the inner loop, split over the token axis into an FP32
+// workspace, and merged by a log-sum-exp combine.
+//
+// GB300 design (one CTA per (split, kv head, sequence), 5 warps):
+//  * warp 4 (producer) walks the split's pages 8 at a time (one "stage"),
+//    reads the block table a batch ahead, and issues one 1-D bulk TMA copy
+//    per page for K and for V (page chunk = 4 * head_dim contiguous elements
+//    of one kv head) into a ring of NSTAGES shared-memory stages, completing
+//    on the stage's mbarrier.  In top-k mode a stage is 32 listed tokens,
+//    each fetched as one row.
+//  * warps 0..3 (consumers) take whole stages round-robin (or, for many
+//    query rows, share a stage and split the rows).  Per 16-token tile they
+//    load K with ldmatrix, decode E4M3 -> fp16 with the bitcast decoder in
+//    registers, and run S^T = K * Q^T on tensor cores (mma.sync m16n8k16,
+//    tokens on M, query rows on N -- the 8 heads of a GQA group fill N
+//    exactly).  The online softmax runs in the log2 domain with the K scale,
+//    2^8 and log2(e) folded into one multiplier; P is transposed in
+//    registers with movmatrix and multiplied by V^T loaded with
+//    ldmatrix.trans (again decoded in registers).  The V scale and 2^8 are
+//    applied once per output row.
+//  * Page chunks sit 16 bytes apart beyond their size in shared memory, so
+//    the eight rows an ldmatrix reads (the same slot of eight pages) fall
+//    in distinct banks.
+//  * Every wait is bounded (about 2 s); on expiry the kernel reports
+//    KVQ_DEV_TIMEOUT, drains its own copies and exits without writing.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <bool E4M3, int D>
+struct Geometry {
+    static constexpr int kElem = E4M3 ? 1 : 2;
+    static constexpr int kRowBytes = D * kElem;          // one token of one kv head
+    static constexpr int kChunk = 4 * kRowBytes;         // one page of one kv head
+    static constexpr int kPageStride = kChunk + 16;      // bank-skewed page placement
+    static constexpr int kPagesPerStage = 8;
+    static constexpr int kRegion = kPagesPerStage * kPageStride;   // K (or V) part of a stage
+    static constexpr int kStageBytes = 2 * kRegion;
+    static constexpr int kStages = E4M3 ? 8 : 6;
+    static constexpr int kX4 = kRowBytes / 32;           // ldmatrix.x4 per 16-token tile
+    static constexpr int kKSteps = D / 16;               // QK mma k-steps
+    static constexpr int kPVTiles = D / 16;              // PV mma m-tiles (16 channels)
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kTokPosOff = kRingBytes;
+    static constexpr int kBarOff = kTokPosOff + kStages * 32 * 4;
+    static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
+    static constexpr int kBytes = kAbortOff + 16;
+    static_assert(kPageStride % 128 == 16, "page skew must be 16 bytes mod 128");
+};
+
+template <int NT, int RW>
+struct Rows {
+    static constexpr int kPad = RW * NT * 8;             // query rows per CTA, padded
+    static constexpr int kGroups = kConsumerWarps / RW;  // stage groups
+};
+
+template <bool E4M3, int D, int NT, int RW>
+constexpr int smem_bytes()
+{
+    using G = Geometry<E4M3, D>;
+    using R = Rows<NT, RW>;
+    constexpr int merge = R::kGroups * R::kPad * (D + 2) * 4;
+    return G::kBytes > merge ? G::kBytes : merge;
+}
+
+// channel of the O^T accumulator row held by this thread for PV tile `pv`
+// (first = fragment row gid, second = fragment row gid + 8)
+template <bool E4M3>
+__device__ __forceinline__ int2 pv_channels(int pv, int gid)
+{
+    if (E4M3) return make_int2(16 * pv + 2 * gid, 16 * pv + 2 * gid + 1);
+    return make_int2(16 * pv + gid, 16 * pv + 8 + gid);
+}
+
+template <bool E4M3, int D, int NT, int RW>
+__global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
+{
+    using G = Geometry<E4M3, D>;
+    using R = Rows<NT, RW>;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring = smem_u32(smem);
+    int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
+    const uint32_t bar0 = smem_u32(smem + G::kBarOff);   // full[k] = bar0 + 8k, empty[k] = bar0 + 8(S+k)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
+    volatile int *stage_bad = abort_flag + 1;            // any bad entry seen in a stage (sticky)
+
+    // ---- work of this CTA --------------------------------------------------
+    const int L = a.context_lens[b];
+    const bool len_ok = (L >= a.q_len) && (L <= a.max_pages * 4);
+    int topk_n = (a.topk_idx && a.topk_lens) ? a.topk_lens[b] : 0;
+    const bool topk = len_ok && topk_n > 0;
+    if (topk && topk_n > a.max_topk) topk_n = a.max_topk;
+    const int n_items = !len_ok ? 0 : (topk ? topk_n : (L + 3) / 4);
+    const int per = (n_items + a.num_splits - 1) / a.num_splits;
+    const int item0 = min(s * per, n_items);
+    const int item1 = min(item0 + per, n_items);
+    const int ipst = topk ? 32 : G::kPagesPerStage;     // items per stage
+    const int nst = (item1 - item0 + ipst - 1) / ipst;
+
+    if (threadIdx.x == 0) {
+        if (!len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
+        if (len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
+            report(a.err_flag, KVQ_DEV_BAD_TOPK);
+        for (int k = 0; k < G::kStages; ++k) {
+            mbar_init(bar0 + 8 * k, 1);
+            mbar_init(bar0 + 8 * (G::kStages + k), RW);
+        }
+        *abort_flag = 0;
+        *stage_bad = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    float o[NT][G::kPVTiles][4];
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int pv = 0; pv < G::kPVTiles; ++pv)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[j][pv][e] = 0.f;
+        m_run[j][0] = m_run[j][1] = -INFINITY;
+        l_run[j][0] = l_run[j][1] = 0.f;
+    }
+    const int gid = lane >> 2, t = lane & 3;
+    const int rw = warp % RW, sg = warp / RW;
+    int issued = 0;   // stages the producer has issued
+
+    if (warp == kConsumerWarps) {
+        // ================= producer =================
+        const uint64_t pol = l2_policy_evict_first();
+        const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
+        if (!topk) {
+            auto load_bt = [&](int first) -> int {
+                const int it = first + lane;
+                return it < item1 ? __ldg(bt_row + it) : -1;
+            };
+            int bt_cur = load_bt(item0), bt_nxt = load_bt(item0 + 32);
+            for (int st = 0; st < nst; ++st) {
+                const int slot = st % G::kStages;
+                if (st >= G::kStages &&
+                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
+                                       abort_flag, a.err_flag))
+                    break;
+                if (st > 0 && (st & 3) == 0) {
+                    bt_cur = bt_nxt;
+                    bt_nxt = load_bt(item0 + (st + 4) * 8);
+                }
+                const int p = lane & 7;
+                const int item = item0 + st * 8 + p;
+                const int phys = __shfl_sync(kFull, bt_cur, (st & 3) * 8 + p);
+                const bool exists = item < item1;
+                const bool valid = exists && phys >= 0 && (int64_t)phys < a.num_pages;
+                if (lane < 8) {
+                    if (exists && !valid) {
+                        report(a.err_flag, KVQ_DEV_BAD_PAGE);
+                        *stage_bad = 1;
+                    }
+#pragma unroll
+                    for (int sl = 0; sl < 4; ++sl) {
+                        const int pos = item * 4 + sl;
+                        tokpos[slot * 32 + p * 4 + sl] = (valid && pos < L) ? pos : -1;
+                    }
+                }
+                const unsigned vmask = __ballot_sync(kFull, valid && lane < 16);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, __popc(vmask) * G::kChunk);
+                __syncwarp();
+                if (lane < 16 && valid) {
+                    const uint8_t *base =
+                        static_cast<const uint8_t *>(lane < 8 ? a.k_cache : a.v_cache);
+                    const uint8_t *src = base + ((int64_t)phys * a.num_kv_heads + g) * G::kChunk;
+                    const uint32_t dst = ring + slot * G::kStageBytes + (lane < 8 ? 0 : G::kRegion) +
+                                         p * G::kPageStride;
+                    tma_load_1d(dst, src, G::kChunk, bar0 + 8 * slot, pol);
+                }
+                issued = st + 1;
+            }
+        } else {
+            const int32_t *list = a.topk_idx + ((int64_t)b * a.num_kv_heads + g) * a.max_topk;
+            auto load_idx = [&](int st) -> int {
+                const int it = item0 + st * 32 + lane;
+                return (st < nst && it < item1) ? __ldg(list + it) : -1;
+            };
+            auto load_page = [&](int idx) -> int {
+                return (idx >= 0 && idx < L) ? __ldg(bt_row + (idx >> 2)) : -1;
+            };
+            int idx_cur = load_idx(0);
+            int pg_cur = load_page(idx_cur);
+            int idx_nxt = load_idx(1);
+            for (int st = 0; st < nst; ++st) {
+                const int slot = st % G::kStages;
+                if (st >= G::kStages &&
+                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
+                                       abort_flag, a.err_flag))
+                    break;
+                const int pg_nxt = load_page(idx_nxt);
+                const int idx_nxt2 = load_idx(st + 2);
+                const bool exists = item0 + st * 32 + lane < item1;
+                const bool idx_ok = exists && idx_cur >= 0 && idx_cur < L;
+                const bool valid = idx_ok && pg_cur >= 0 && (int64_t)pg_cur < a.num_pages;
+                if (exists && !idx_ok) report(a.err_flag, KVQ_DEV_BAD_TOPK);
+                if (idx_ok && !valid) report(a.err_flag, KVQ_DEV_BAD_PAGE);
+                tokpos[slot * 32 + lane] = valid ? idx_cur : -1;
+                const unsigned vmask = __ballot_sync(kFull, valid);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, __popc(vmask) * 2 * G::kRowBytes);
+                __syncwarp();
+                if (valid) {
+                    const int64_t row = ((int64_t)pg_cur * a.num_kv_heads + g) * 4 + (idx_cur & 3);
+                    const uint32_t dst = ring + slot * G::kStageBytes + (lane >> 2) * G::kPageStride +
+                                         (lane & 3) * G::kRowBytes;
+                    tma_load_1d(dst, static_cast<const uint8_t *>(a.k_cache) + row * G::kRowBytes,
+                                G::kRowBytes, bar0 + 8 * slot, pol);
+                    tma_load_1d(dst + G::kRegion,
+                                static_cast<const uint8_t *>(a.v_cache) + row * G::kRowBytes,
+                                G::kRowBytes, bar0 + 8 * slot, pol);
+                }
+                issued = st + 1;
+                idx_cur = idx_nxt;
+                pg_cur = pg_nxt;
+                idx_nxt = idx_nxt2;
+            }
+        }
+    } else {
+        // ================= consumers =================
+        // Q as mma B fragments, one set per 8-row n-tile.  For E4M3 the K
+        // channels come out of the bitcast decoder paired (d, d+2) and
+        // (d+1, d+3), so Q is gathered in the same order.
+        uint32_t qf[NT][G::kKSteps][2];
+        int lim[NT][2];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int row = (rw * NT + j) * 8 + gid;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int r = (rw * NT + j) * 8 + 2 * t + c;
+                lim[j][c] = (r < a.rows) ? L - a.q_len + r / a.group : 0x7FFFFFFF;
+            }
+            if (row < a.rows) {
+                const int i = row / a.group, h = g * a.group + row % a.group;
+                const __half *qrow = static_cast<const __half *>(a.q) +
+                                     (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D;
+#pragma unroll
+                for (int ks = 0; ks < G::kKSteps; ++ks) {
+                    if (E4M3) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * t);
+                        qf[j][ks][0] = __byte_perm(v.x, v.y, 0x5410);  // (d, d+2)
+                        qf[j][ks][1] = __byte_perm(v.x, v.y, 0x7632);  // (d+1, d+3)
+                    } else {
+                        qf[j][ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * t);
+                        qf[j][ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * t);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < G::kKSteps; ++ks) qf[j][ks][0] = qf[j][ks][1] = 0u;
+            }
+        }
+        // per-lane ldmatrix offset: matrix q = lane/8 reads row (page) lane%8,
+        // token slot half = q&1 of the tile, 16-byte chunk q>>1 of the pair
+        const int mq = lane >> 3;
+        const uint32_t lane_off = (lane & 7) * G::kPageStride + (mq & 1) * G::kRowBytes + (mq >> 1) * 16;
+        const float qk = a.qk_scale_log2;
+        const int first_masked = L - a.q_len + 1;   // positions >= this are masked for some row
+
+        for (int st = sg; st < nst; st += R::kGroups) {
+            const int slot = st % G::kStages;
+            if (!mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag))
+                break;
+            const uint32_t sk = ring + slot * G::kStageBytes + lane_off;
+            const uint32_t sv = sk + G::kRegion;
+            const int32_t *tp = tokpos + slot * 32;
+            const int last_pos = min(item0 + (st + 1) * 8, item1) * 4 - 1;
+            const bool need_mask = topk || *stage_bad || last_pos >= first_masked;
+
+            // ---- S^T = K Q^T (two 16-token tiles: slots {0,1} and {2,3}) ----
+            float sc[NT][2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                uint32_t kr[G::kX4][4];
+#pragma unroll
+                for (int u = 0; u < G::kX4; ++u) ldsm_x4(kr[u], sk + mt * 2 * G::kRowBytes + u * 32);
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[j][mt][e] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < G::kKSteps; ++ks) {
+                    uint32_t af[4];
+                    if (E4M3) {
+                        const uint32_t w0 = kr[ks >> 1][2 * (ks & 1)];
+                        const uint32_t w1 = kr[ks >> 1][2 * (ks & 1) + 1];
+                        af[0] = dec_lo(w0);
+                        af[1] = dec_lo(w1);
+                        af[2] = dec_hi(w0);
+                        af[3] = dec_hi(w1);
+                    } else {
+                        af[0] = kr[ks][0];
+                        af[1] = kr[ks][1];
+                        af[2] = kr[ks][2];
+                        af[3] = kr[ks][3];
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) mma_16816(sc[j][mt], af, qf[j][ks][0], qf[j][ks][1]);
+                }
+            }
+            // ---- scores in the log2 domain, masking ----
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[j][mt][e] *= qk;
+            if (need_mask) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int pa = tp[gid * 4 + 2 * mt], pb = tp[gid * 4 + 2 * mt + 1];
+#pragma unroll
+                    for (int j = 0; j < NT; ++j)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            if (!(pa >= 0 && pa <= lim[j][c])) sc[j][mt][c] = -INFINITY;
+                            if (!(pb >= 0 && pb <= lim[j][c])) sc[j][mt][2 + c] = -INFINITY;
+                        }
+                }
+            }
+            // ---- online softmax (row max across the 8 lanes sharing t) ----
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    float mx = fmaxf(fmaxf(sc[j][0][c], sc[j][0][c + 2]), fmaxf(sc[j][1][c], sc[j][1][c + 2]));
+                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+                    const float m_new = fmaxf(m_run[j][c], mx);
+                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                    const float corr = fast_exp2(m_run[j][c] - m_use);
+                    m_run[j][c] = m_new;
+                    float lsum = l_run[j][c] * corr;
+#pragma unroll
+                    for (int pv = 0; pv < G::kPVTiles; ++pv) {
+                        o[j][pv][c] *= corr;
+                        o[j][pv][c + 2] *= corr;
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < 2; ++mt) {
+                        const float p0 = fast_exp2(sc[j][mt][c] - m_use);
+                        const float p1 = fast_exp2(sc[j][mt][c + 2] - m_use);
+                        sc[j][mt][c] = p0;
+                        sc[j][mt][c + 2] = p1;
+                        lsum += p0 + p1;
+                    }
+                    l_run[j][c] = lsum;
+                }
+            // ---- P^T as mma B fragments: transpose the score tiles in registers ----
+            uint32_t pf[NT][2][2];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    pf[j][mt][0] = movmatrix_trans(pack_half2(sc[j][mt][0], sc[j][mt][1]));
+                    pf[j][mt][1] = movmatrix_trans(pack_half2(sc[j][mt][2], sc[j][mt][3]));
+                }
+            // ---- O^T += V^T P^T ----
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                uint32_t vr[G::kX4][4];
+#pragma unroll
+                for (int u = 0; u < G::kX4; ++u) ldsm_x4_trans(vr[u], sv + mt * 2 * G::kRowBytes + u * 32);
+                if (!E4M3 && need_mask) {
+                    const uint32_t m0 = (tp[(2 * t) * 4 + 2 * mt] >= 0 ? 0x0000FFFFu : 0u) |
+                                        (tp[(2 * t + 1) * 4 + 2 * mt] >= 0 ? 0xFFFF0000u : 0u);
+                    const uint32_t m1 = (tp[(2 * t) * 4 + 2 * mt + 1] >= 0 ? 0x0000FFFFu : 0u) |
+                                        (tp[(2 * t + 1) * 4 + 2 * mt + 1] >= 0 ? 0xFFFF0000u : 0u);
+#pragma unroll
+                    for (int u = 0; u < G::kX4; ++u) {
+                        vr[u][0] &= m0;
+                        vr[u][2] &= m0;
+                        vr[u][1] &= m1;
+                        vr[u][3] &= m1;
+                    }
+                }
+#pragma unroll
+                for (int pv = 0; pv < G::kPVTiles; ++pv) {
+                    uint32_t af[4];
+                    if (E4M3) {
+                        const uint32_t h0 = vr[pv >> 1][2 * (pv & 1)];
+                        const uint32_t h1 = vr[pv >> 1][2 * (pv & 1) + 1];
+                        af[0] = dec_lo(h0);
+                        af[1] = dec_hi(h0);
+                        af[2] = dec_lo(h1);
+                        af[3] = dec_hi(h1);
+                    } else {
+                        af[0] = vr[pv][0];
+                        af[1] = vr[pv][2];
+                        af[2] = vr[pv][1];
+                        af[3] = vr[pv][3];
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) mma_16816(o[j][pv], af, pf[j][mt][0], pf[j][mt][1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));
+        }
+        // full row sums: add the partial sums of the 8 lanes sharing t
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float v = l_run[j][c];
+                v += __shfl_xor_sync(kFull, v, 4);
+                v += __shfl_xor_sync(kFull, v, 8);
+                v += __shfl_xor_sync(kFull, v, 16);
+                l_run[j][c] = v;
+            }
+    }
+
+    // ---- merge the stage groups through shared memory, write the split partial ----
+    __syncthreads();
+    if (*abort_flag) {
+        // Something gave up: before the CTA's shared memory is released, wait
+        // (bounded) for every copy the producer issued, then leave without
+        // writing.  The error bit is already set.
+        if (warp == kConsumerWarps && lane == 0)
+            for (int st = max(0, issued - G::kStages); st < issued; ++st)
+                mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr,
+                                  a.err_flag);
+        __syncthreads();
+        return;
+    }
+    float *mbuf = reinterpret_cast<float *>(smem);    // [groups][kPad][D + 2]: m, l, o[D]
+    constexpr int kRowF = D + 2;
+    if (warp < kConsumerWarps) {
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int row = (rw * NT + j) * 8 + 2 * t + c;
+                float *dst = mbuf + (sg * R::kPad + row) * kRowF;
+                if (gid == 0) {
+                    dst[0] = m_run[j][c];
+                    dst[1] = l_run[j][c];
+                }
+#pragma unroll
+                for (int pv = 0; pv < G::kPVTiles; ++pv) {
+                    const int2 ch = pv_channels<E4M3>(pv, gid);
+                    dst[2 + ch.x] = o[j][pv][c];
+                    dst[2 + ch.y] = o[j][pv][c + 2];
+                }
+            }
+    }
+    __syncthreads();
+    const int S = a.num_splits;
+    for (int idx = threadIdx.x; idx < a.rows * D; idx += kThreads) {
+        const int row = idx / D, d = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < R::kGroups; ++q) M = fmaxf(M, mbuf[(q * R::kPad + row) * kRowF]);
+        const int i = row / a.group, h = g * a.group + row % a.group;
+        const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
+        if (M == -INFINITY) {
+            if (d == 0) {
+                a.ws_m[unit] = -INFINITY;
+                a.ws_l[unit] = 0.f;
+            }
+            continue;
+        }
+        float lsum = 0.f, osum = 0.f;
+#pragma unroll
+        for (int q = 0; q < R::kGroups; ++q) {
+            const float *src = mbuf + (q * R::kPad + row) * kRowF;
+            const float w = fast_exp2(src[0] - M);
+            lsum += w * src[1];
+            osum += w * src[2 + d];
+        }
+        a.ws_o[unit * D + d] = osum / lsum * a.out_scale;
+        if (d == 0) {
+            a.ws_m[unit] = M * kLn2;
+            a.ws_l[unit] = lsum;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp combine: one warp per (b, h, i) row.
+template <int D>
+__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws_o,
+                                                      const float *__restrict__ ws_m,
+                                                      const float *__restrict__ ws_l,
+                                                      __half *__restrict__ out, int rows, int q_len,
+                                                      int num_q_heads, int S)
+{
+    constexpr int V = D / 32;   // channels per lane (4 or 2)
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float *m = ws_m + (int64_t)row * S;
+    const float *l = ws_l + (int64_t)row * S;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s)
+        if (l[s] > 0.f) M = fmaxf(M, m[s]);
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    float W = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < S; ++s) {
+            const float ls = l[s];
+            if (!(ls > 0.f)) continue;
+            const float w = ls * fast_exp2((m[s] - M) * 1.4426950408889634f);
+            W += w;
+            const float *src = ws_o + ((int64_t)row * S + s) * D + lane * V;
+            if (V == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src);
+                acc[0] += w * x.x;
+                acc[1] += w * x.y;
+                acc[2] += w * x.z;
+                acc[3] += w * x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(src);
+                acc[0] += w * x.x;
+                acc[1] += w * x.y;
+            }
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    // row = (b * Hq + h) * q_len + i  ->  out[b][i][h][:]
+    const int i = row % q_len;
+    const int bh = row / q_len;
+    const int h = bh % num_q_heads, b = bh / num_q_heads;
+    __half *dst = out + (((int64_t)b * q_len + i) * num_q_heads + h) * D + lane * V;
+    if (V == 4) {
+        uint2 w;
+        w.x = pack_half2(acc[0] * inv, acc[1] * inv);
+        w.y = pack_half2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = w;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+
+template <bool E4M3, int D, int NT, int RW>
+static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
+{
+    constexpr int bytes = smem_bytes<E4M3, D, NT, RW>();
+    static uint64_t configured = 0;   // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
+    attn_split_kernel<E4M3, D, NT, RW><<<grid, kThreads, bytes, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool E4M3, int D>
+static cudaError_t launch_rows(const AttnArgs &a, cudaStream_t stream)
+{
+    const int tiles = (a.rows + 7) / 8;
+    if (tiles <= 1) return launch_one<E4M3, D, 1, 1>(a, stream);
+    if (tiles <= 2) return launch_one<E4M3, D, 2, 1>(a, stream);
+    if (tiles <= 4) return launch_one<E4M3, D, 2, 2>(a, stream);
+    return launch_one<E4M3, D, 2, 4>(a, stream);
+}
+
+cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream)
+{
+    if (a.batch == 0) return cudaSuccess;
+    if (e4m3) return head_dim == 128 ? launch_rows<true, 128>(a, stream) : launch_rows<true, 64>(a, stream);
+    return head_dim == 128 ? launch_rows<false, 128>(a, stream) : launch_rows<false, 64>(a, stream);
+}
+
+cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws_l, void *out,
+                           int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
+                           int32_t num_splits, cudaStream_t stream)
+{
+    const int rows = batch * num_q_heads * q_len;
+    if (rows == 0) return cudaSuccess;
+    const dim3 grid((rows + 3) / 4);
+    if (head_dim == 128)
+        combine_kernel<128><<<grid, 128, 0, stream>>>(ws_o, ws_m, ws_l, static_cast<__half *>(out),
+                                                      rows, q_len, num_q_heads, num_splits);
+    else
+        combine_kernel<64><<<grid, 128, 0, stream>>>(ws_o, ws_m, ws_l, static_cast<__half *>(out),
+                                                     rows, q_len, num_q_heads, num_splits);
+    return cudaGetLastError();
+}
+
+}  // namespace kvq

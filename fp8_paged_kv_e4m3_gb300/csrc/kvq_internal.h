@@ -1,0 +1,50 @@
+// kvq_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Arguments of one split-K attention launch (device pointers).
+struct AttnArgs {
+    const void *q;               // fp16 [B][q_len][Hq][D]
+    const void *k_cache;         // pools [P][Hkv][4][D]
+    const void *v_cache;
+    int64_t num_pages;
+    const int32_t *block_tables; // [B][max_pages]
+    const int32_t *context_lens; // [B]
+    const int32_t *topk_idx;     // [B][Hkv][max_topk] or null
+    const int32_t *topk_lens;    // [B] or null
+    float *ws_o;                 // [B][Hq][q_len][S][D]
+    float *ws_m;                 // [B][Hq][q_len][S]
+    float *ws_l;                 // [B][Hq][q_len][S]
+    int32_t *err_flag;
+    int32_t batch, q_len, num_q_heads, num_kv_heads, group, rows, num_splits;
+    int32_t max_pages, max_topk;
+    float qk_scale_log2;         // hoisted: sm_scale * log2(e) [* k_scale * 2^8 for E4M3]
+    float out_scale;             // hoisted: v_scale * 2^8 for E4M3, 1 for fp16
+};
+
+struct WorkspaceLayout {
+    size_t o_off, m_off, l_off, total;
+};
+
+WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t head_dim);
+
+cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
+cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws_l, void *out,
+                           int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
+                           int32_t num_splits, cudaStream_t stream);
+cudaError_t launch_append(bool e4m3, const void *k_new, const void *v_new,
+                          const int32_t *slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                          int32_t head_dim, void *k_cache, void *v_cache, int64_t num_pages,
+                          float k_scale, float v_scale, int32_t *err_flag, cudaStream_t stream);
+cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace kvq

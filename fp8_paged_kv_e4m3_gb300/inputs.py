@@ -230,6 +230,12 @@ def kv_tokens(w: Workload, layer: int, n_tokens: int, which: str, device="cpu") 
     return _draw_kv(w, n_tokens, layer, purpose, device)
 
 
+def prefill_tokens(w: Workload, layer: int, which: str, device="cpu") -> torch.Tensor:
+    """K or V of the new sequence's prefill chunk, fp16 [prefill_chunk, Hkv, D]."""
+    purpose = _DATA * 2 + (0 if which == "k" else 1) + 300
+    return _draw_kv(w, w.prefill_chunk, layer, purpose, device)
+
+
 def calibration_draw(w: Workload, layer: int, which: str, device="cpu") -> torch.Tensor:
     """A separate draw of the same distribution, used only to calibrate the scale."""
     purpose = _CALIB * 2 + (0 if which == "k" else 1) + 200

@@ -1,0 +1,240 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) calibrated E4M3 paged KV cache.
+ *
+ * The operations follow three pull-request pages that describe the method:
+ *   [P1] "[Model][SM70] Calibrated E4M3 KV cache for Qwen4Exp QSA with MTP"
+ *   [P2] "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path"
+ *   [P3] "[Experiment][SM70] Qualify E4M3 KV with MTP3"
+ * Each declaration below cites the section that defines what it computes.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers marked "device" are CUDA device (or managed) memory on the
+ *    current device; pointers marked "host" are ordinary host memory.  The
+ *    caller owns every buffer.  The library allocates nothing, keeps no
+ *    pointer after a call returns and holds no global state, so calls are
+ *    reentrant.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every GPU call is asynchronous and stream-ordered; none
+ *    synchronises the host, so the calls can be captured in a CUDA graph.
+ *  - Return value: KVQ_OK, or a negative kvq_status.  Errors that the host
+ *    can see (bad sizes, bad scales, misaligned pointers, a short workspace)
+ *    are returned BEFORE anything is launched: the call fails closed and
+ *    leaves every buffer untouched.  A launch failure returns KVQ_ERR_CUDA.
+ *  - `err_flag` (device int32, nullable): errors only the GPU can see -- an
+ *    out-of-range block-table entry, slot or top-k index, or an invalid
+ *    context length -- OR a KVQ_DEV_* bit into *err_flag; the offending
+ *    token is skipped (treated as absent), nothing faults and nothing
+ *    traps.  The caller clears the flag.
+ *  - Page size is 4 tokens ("page4" routes, [P2] Changes).  A K or V pool is
+ *    [num_pages][num_kv_heads][4][head_dim]: one page of one KV head is
+ *    4 * head_dim contiguous elements.  E4M3 pools hold one byte per
+ *    element, fp16 pools two.
+ *  - head_dim is 64 or 128; query rows per KV head (q_len * Hq / Hkv) are
+ *    at most 64; q_len is 1 .. 4 (decode, or MTP verify with 1 + 3 drafts,
+ *    [P1] Purpose).  Other shapes return KVQ_ERR_UNSUPPORTED.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_PAGE_SIZE 4
+#define KVQ_VERSION 1
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = -1,  /* null pointer, negative or inconsistent size   */
+    KVQ_ERR_BAD_SCALE = -2,    /* a K or V scale that is not finite and > 0      */
+    KVQ_ERR_WORKSPACE = -3,    /* workspace missing or smaller than required     */
+    KVQ_ERR_UNSUPPORTED = -4,  /* head_dim / q_len / group shape not supported   */
+    KVQ_ERR_CUDA = -5,         /* a CUDA launch or runtime call failed           */
+    KVQ_ERR_ALIGNMENT = -6     /* a pointer is not 16-byte aligned               */
+} kvq_status;
+
+/* bits OR-ed into *err_flag by the kernels */
+enum {
+    KVQ_DEV_BAD_PAGE = 1,   /* block-table entry outside [0, num_pages): page skipped   */
+    KVQ_DEV_BAD_SLOT = 2,   /* append slot beyond the pool: token not written           */
+    KVQ_DEV_BAD_TOPK = 4,   /* top-k index outside [0, context_len): entry skipped      */
+    KVQ_DEV_BAD_LEN = 8,    /* context_len < q_len or > 4 * max_pages_per_seq: row = 0   */
+    KVQ_DEV_TIMEOUT = 16    /* an internal pipeline wait gave up (~2 s): results invalid */
+};
+
+/* Library version (KVQ_VERSION) and a static string for a status code. */
+int kvq_version(void);
+const char *kvq_status_string(int status);
+
+/* ------------------------------------------------------------------------
+ * Scale gate.  [P2] Changes: "require all 24 finite positive per-layer K/V
+ * scales and refuse startup when the overlay is missing or incomplete";
+ * [P2] Validation boundary: no generic or unit-scale fallback.
+ *   k_scales, v_scales : host float[num_layers]
+ * Returns KVQ_OK when every entry is finite and > 0, KVQ_ERR_BAD_SCALE when
+ * any is not, KVQ_ERR_INVALID_ARG for a null array or num_layers < 1.
+ * There is no default: a caller without calibrated scales cannot proceed.
+ */
+int kvq_validate_scales(const float *k_scales, const float *v_scales, int32_t num_layers);
+
+/* ------------------------------------------------------------------------
+ * Calibration.  [P2] Changes: "add offline calibration"; the calibrated
+ * scale is amax / 448 (448 = largest finite E4M3 value) for one layer's K
+ * or V, amax being the largest |x| of a calibration draw.
+ *
+ * kvq_amax_f16: amax over n fp16 values.
+ *   x        : device fp16[n] (any alignment)
+ *   amax_out : device float[1]; overwritten (not accumulated) with max |x|
+ *              (NaN if any input is NaN, +inf if any is infinite)
+ *   Launches one reduction kernel on `stream`.
+ * kvq_scale_from_amax: host helper, returns amax / 448 in binary32, or 0
+ *   (an invalid scale that kvq_validate_scales refuses) when amax is not
+ *   finite and > 0.
+ */
+int kvq_amax_f16(const void *x, int64_t n, float *amax_out, void *stream);
+float kvq_scale_from_amax(float amax);
+
+/* ------------------------------------------------------------------------
+ * Quantise-on-append.  [P2] Changes: only the main K/V cache is stored in
+ * calibrated E4M3, in page-4 pools; [P2] Changes "mixed catch-up/decode
+ * batches" append prefill chunks and decode tokens alike.
+ *
+ * For every token t with slot_mapping[t] >= 0, page = slot / 4 and
+ * offset = slot % 4, and for every head g and channel d:
+ *     k_cache[page][g][offset][d] = E4M3(fp32(k_new[t][g][d]) / k_scale)
+ *     v_cache[page][g][offset][d] = E4M3(fp32(v_new[t][g][d]) / v_scale)
+ * where "/" is one IEEE binary32 division and E4M3() rounds to nearest
+ * even, saturates finite overflow to +-448 and maps NaN to a NaN code.
+ *   k_new, v_new   : device fp16 [num_tokens][num_kv_heads][head_dim], 16-B aligned
+ *   slot_mapping   : device int32 [num_tokens]; -1 = skip the token;
+ *                    slots >= 4 * num_pages set KVQ_DEV_BAD_SLOT and are skipped
+ *   k_cache, v_cache : device uint8 pools (see conventions), 16-B aligned
+ *   k_scale, v_scale : the layer's calibrated scales (finite, > 0)
+ * Bad scale -> KVQ_ERR_BAD_SCALE; head_dim not a multiple of 8 ->
+ * KVQ_ERR_UNSUPPORTED.  num_tokens == 0 is a no-op.
+ */
+int kv_append_e4m3(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                   uint8_t *k_cache, uint8_t *v_cache, int64_t num_pages,
+                   float k_scale, float v_scale, int32_t *err_flag, void *stream);
+
+/* fp16-KV twin ([P1] Validation: the comparison arm differs only in the KV
+ * cache dtype): the same slots, values copied unchanged into fp16 pools. */
+int kv_append_fp16(const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                   void *k_cache, void *v_cache, int64_t num_pages,
+                   int32_t *err_flag, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Decode / MTP-verify attention over the paged cache.
+ *
+ * For sequence b with context length L (which INCLUDES the q_len tokens
+ * appended this step), query position i (0 <= i < q_len) and query head h,
+ * KV head g = h / (Hq / Hkv) (contiguous grouping, "grouped page4" route,
+ * [P2] Changes):
+ *     keys  J = { j : 0 <= j <= L - q_len + i }                     (dense)
+ *        or J = { j in topk_idx[b][g][0 : topk_lens[b]] : j <= L - q_len + i }
+ *     s_j   = sm_scale * sum_d q[b][i][h][d] * K^_j[d]
+ *     out   = sum_{j in J} exp(s_j - max s) V^_j / sum_{j in J} exp(s_j - max s)
+ * with K^ = decode(k byte) * k_scale and V^ = decode(v byte) * v_scale
+ * (E4M3), or the fp16 values themselves (fp16 twin).  The window of q_len
+ * rows is causal inside itself: MTP3 verifies one target token and three
+ * drafts in one pass ([P1] Purpose).  An empty J gives a zero row.
+ *
+ * Split-K: the work of each (b, g) is cut into num_splits parts -- logical
+ * pages [s*c, (s+1)*c) with c = ceil(ceil(L/4) / num_splits), or top-k list
+ * entries [s*c, (s+1)*c) with c = ceil(topk_lens[b] / num_splits) -- whose
+ * partial results go to an FP32 workspace ([P1] Status and history and
+ * [P3] Problem: the page-4 route's temporary output must be FP32) and are
+ * merged by a log-sum-exp combine.
+ */
+typedef struct {
+    int32_t batch;             /* B: sequences in the call                            */
+    int32_t q_len;             /* 1 (decode) .. 4 (MTP3 verify)                       */
+    int32_t num_q_heads;       /* Hq                                                   */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0                                   */
+    int32_t head_dim;          /* 64 or 128                                            */
+    int32_t num_splits;        /* S >= 1, or 0 = let the library choose (see below)    */
+    int32_t max_pages_per_seq; /* row stride of block_tables                           */
+    int32_t max_topk;          /* row length of topk_idx; 0 when no top-k list is used */
+    float sm_scale;            /* softmax temperature; 0 = 1/sqrt(head_dim)            */
+} kvq_attn_params;
+
+/* The split count a call with these parameters uses: p->num_splits if > 0,
+ * else a count chosen from the shape and the current device's SM count.
+ * Returns a value >= 1, or a negative kvq_status for invalid parameters. */
+int32_t kvq_attn_num_splits(const kvq_attn_params *p);
+
+/* Bytes of FP32 workspace the call needs, 0 for invalid parameters.
+ * Workspace layout (float32, each part starting on a 256-byte boundary):
+ *   tmp_out [B][Hq][q_len][S][head_dim]  partial output of each split,
+ *                                        normalised by its own l
+ *   tmp_max [B][Hq][q_len][S]            m = max score of the split
+ *                                        (natural-log units, -inf if empty)
+ *   tmp_sum [B][Hq][q_len][S]            l = sum of exp(s - m) (0 if empty)
+ * Entries of empty splits (l == 0) leave tmp_out unwritten. */
+size_t kvq_attn_workspace_bytes(const kvq_attn_params *p);
+
+/* Full decode / verify attention: split partials, then the combine.
+ *   q            : device fp16 [B][q_len][Hq][head_dim], 16-B aligned
+ *   k_cache, v_cache : device pools (uint8 E4M3), 16-B aligned
+ *   num_pages    : pool size P
+ *   block_tables : device int32 [B][max_pages_per_seq]; entries past the
+ *                  sequence's last page are not read
+ *   context_lens : device int32 [B] (includes this step's q_len tokens)
+ *   k_scale, v_scale : the layer's calibrated scales (finite, > 0)
+ *   topk_idx     : device int32 [B][Hkv][max_topk] or NULL; per (sequence,
+ *                  KV head) token positions, ascending ([P2] Changes: the
+ *                  shared QSA top-k index workspace)
+ *   topk_lens    : device int32 [B] or NULL; 0 = dense for that sequence
+ *   workspace    : device float32, >= kvq_attn_workspace_bytes(p) bytes,
+ *                  256-B aligned.  FP32 by contract: there is no fp16 form.
+ *   out          : device fp16 [B][q_len][Hq][head_dim], 16-B aligned
+ * Launches two kernels (attention, combine) on `stream`.
+ */
+int paged_decode_attn_e4m3(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                           int64_t num_pages, const int32_t *block_tables,
+                           const int32_t *context_lens, float k_scale, float v_scale,
+                           const int32_t *topk_idx, const int32_t *topk_lens,
+                           float *workspace, size_t workspace_bytes, void *out,
+                           const kvq_attn_params *p, int32_t *err_flag, void *stream);
+
+/* fp16-KV twin: the same computation over fp16 pools, without scales. */
+int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cache,
+                           int64_t num_pages, const int32_t *block_tables,
+                           const int32_t *context_lens,
+                           const int32_t *topk_idx, const int32_t *topk_lens,
+                           float *workspace, size_t workspace_bytes, void *out,
+                           const kvq_attn_params *p, int32_t *err_flag, void *stream);
+
+/* The two halves of the calls above, for callers that merge partials from
+ * several sources (for example partials computed on different devices over
+ * different token ranges) or time the halves separately.
+ * *_partial: the split-K attention kernel alone; fills the workspace.
+ * kvq_lse_combine: the combine alone; reads the workspace, writes `out`:
+ *     M = max_s m_s, w_s = l_s * exp(m_s - M),
+ *     out = sum_s w_s tmp_out_s / sum_s w_s  (0 when every l_s == 0). */
+int paged_decode_attn_e4m3_partial(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                   int64_t num_pages, const int32_t *block_tables,
+                                   const int32_t *context_lens, float k_scale, float v_scale,
+                                   const int32_t *topk_idx, const int32_t *topk_lens,
+                                   float *workspace, size_t workspace_bytes,
+                                   const kvq_attn_params *p, int32_t *err_flag, void *stream);
+int paged_decode_attn_fp16_partial(const void *q, const void *k_cache, const void *v_cache,
+                                   int64_t num_pages, const int32_t *block_tables,
+                                   const int32_t *context_lens,
+                                   const int32_t *topk_idx, const int32_t *topk_lens,
+                                   float *workspace, size_t workspace_bytes,
+                                   const kvq_attn_params *p, int32_t *err_flag, void *stream);
+int kvq_lse_combine(const float *workspace, size_t workspace_bytes, void *out,
+                    const kvq_attn_params *p, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -135,3 +135,33 @@ def torch_reference(q, k_pool_vals, v_pool_vals, block_tables, lens, q_len, topk
 
 def torch_dequant(pool_u8, scale):
     return torch.from_numpy(pool_u8).view(torch.float8_e4m3fn).double().numpy() * float(scale)
+
+
+def oracle_unit(q_rows, k_seq, v_seq, L, ks, vs, e4m3=True, topk_list=None):
+    """Oracle attention of one (sequence, query head) unit from its own data.
+
+    q_rows fp16 [q_len, D]; k_seq / v_seq fp16 [L, D] (the sequence's tokens of
+    the head's kv group, positions 0..L-1); topk_list int32 [n] or None.
+    Builds a one-sequence, one-head problem with an identity block table and
+    returns (out [q_len, D] float64, pool_k bytes [L, D] (E4M3 arm) or None)."""
+    q_len, D = q_rows.shape
+    pages = (L + 3) // 4
+    bt = np.arange(pages, dtype=np.int32)[None, :]
+    slots = np.arange(L, dtype=np.int32)
+    if e4m3:
+        kc = np.full((pages, 1, 4, D), SENTINEL, np.uint8)
+        vc = kc.copy()
+        oracle.append_e4m3(k_seq[:, None, :], v_seq[:, None, :], slots, kc, vc, ks, vs)
+    else:
+        kc = np.zeros((pages, 1, 4, D), np.float16)
+        vc = kc.copy()
+        oracle.append_fp16(k_seq[:, None, :], v_seq[:, None, :], slots, kc, vc)
+        ks = vs = 1.0
+    ti = tl = None
+    if topk_list is not None:
+        ti = np.ascontiguousarray(topk_list, np.int32)[None, None, :]
+        tl = np.array([len(topk_list)], np.int32)
+    out, flags = oracle.attention(np.ascontiguousarray(q_rows)[None, :, None, :], kc, vc, bt,
+                                  np.array([L], np.int32), ks, vs, ti, tl)
+    pool_k = kc.reshape(pages * 4, D)[:L] if e4m3 else None
+    return out[0, :, 0, :], flags, pool_k

@@ -1,0 +1,138 @@
+"""The C ABI library: it builds, loads, exports every symbol include/kvq.h
+declares, and its host-side checks fail closed (CPU only: nothing here
+launches a kernel or touches a device)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from fp8_paged_kv_e4m3_gb300 import build, kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kvq.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("kv_append_e4m3", "kv_append_fp16", "paged_decode_attn_e4m3",
+                 "paged_decode_attn_fp16", "kvq_attn_workspace_bytes", "kvq_validate_scales"):
+        assert must in names
+    assert set(names) == set(kvq.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_has_no_torch_dependency():
+    # plain C ABI: the shared object must not need libtorch / libc10
+    with open(kvq.LIB_PATH, "rb") as f:
+        blob = f.read()
+    assert b"libtorch" not in blob and b"libc10" not in blob
+
+
+def test_version_and_status_strings(lib):
+    assert lib.kvq_version() == 1
+    assert lib.kvq_status_string(0) == b"ok"
+    assert b"scale" in lib.kvq_status_string(-2)
+
+
+def test_scale_gate_fails_closed(lib):
+    ok = [0.01] * 24
+    kvq.validate_scales(ok, ok)
+    for bad in (0.0, -1.0, math.nan, math.inf):
+        k = list(ok)
+        k[7] = bad
+        with pytest.raises(kvq.KvqError) as e:
+            kvq.validate_scales(k, ok)
+        assert e.value.status == -2
+    with pytest.raises(kvq.KvqError):
+        kvq.validate_scales(ok[:23], ok)   # missing entry: no default is substituted
+
+
+def test_scale_from_amax(lib):
+    assert kvq.scale_from_amax(448.0) == 1.0
+    assert kvq.scale_from_amax(56.0) == 0.125
+    for bad in (0.0, -3.0, math.inf, math.nan):
+        assert kvq.scale_from_amax(bad) == 0.0
+
+
+def _params(**kw):
+    p = dict(batch=2, q_len=1, num_q_heads=8, num_kv_heads=2, head_dim=64, num_splits=2,
+             max_pages_per_seq=25, max_topk=0, sm_scale=0.0)
+    p.update(kw)
+    return kvq.AttnParams(**p)
+
+
+def test_workspace_size_matches_layout(lib):
+    p = _params()
+    units = 2 * 8 * 1 * 2
+    r = lambda n: (n + 255) // 256 * 256
+    assert lib.kvq_attn_workspace_bytes(ctypes.byref(p)) == r(units * 64 * 4) + 2 * r(units * 4)
+    assert lib.kvq_attn_num_splits(ctypes.byref(p)) == 2
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 96, -4), ("q_len", 5, -4), ("q_len", 0, -1), ("num_kv_heads", 3, -1),
+    ("num_splits", -1, -1), ("max_pages_per_seq", 0, -1), ("num_q_heads", 136, -4),
+])
+def test_bad_params_are_refused(lib, field, value, status):
+    p = _params(**{field: value})
+    if field == "num_q_heads":
+        p.num_kv_heads = 2    # 68 rows per kv head > 64
+    assert lib.kvq_attn_workspace_bytes(ctypes.byref(p)) == 0
+    assert lib.kvq_attn_num_splits(ctypes.byref(p)) == status
+
+
+FAKE = ctypes.c_void_p(0x10000)     # never dereferenced: every call below fails before a launch
+
+
+def _attn(lib, p, k_scale=0.1, v_scale=0.1, ws_bytes=1 << 20, q=FAKE, ws=FAKE, topk=None):
+    return lib.paged_decode_attn_e4m3(q, FAKE, FAKE, 40, FAKE, FAKE, ctypes.c_float(k_scale),
+                                      ctypes.c_float(v_scale), topk, None, ws, ws_bytes, FAKE,
+                                      ctypes.byref(p), None, None)
+
+
+def test_attention_host_checks_fail_closed(lib):
+    p = _params()
+    assert _attn(lib, p, k_scale=0.0) == -2
+    assert _attn(lib, p, v_scale=math.nan) == -2
+    assert _attn(lib, p, ws_bytes=16) == -3
+    assert _attn(lib, p, ws=None) == -3
+    assert _attn(lib, p, q=ctypes.c_void_p(0x10008)) == -6
+    assert _attn(lib, p, topk=FAKE) == -1          # top-k indices without lengths
+    assert _attn(lib, _params(head_dim=80)) == -4
+
+
+def test_append_host_checks_fail_closed(lib):
+    f = lib.kv_append_e4m3
+    assert f(FAKE, FAKE, FAKE, 4, 2, 64, FAKE, FAKE, 10, ctypes.c_float(0.0), ctypes.c_float(1.0), None, None) == -2
+    assert f(FAKE, FAKE, FAKE, 4, 2, 60, FAKE, FAKE, 10, ctypes.c_float(1.0), ctypes.c_float(1.0), None, None) == -4
+    assert f(FAKE, FAKE, FAKE, -1, 2, 64, FAKE, FAKE, 10, ctypes.c_float(1.0), ctypes.c_float(1.0), None, None) == -1
+    assert f(ctypes.c_void_p(0x10004), FAKE, FAKE, 4, 2, 64, FAKE, FAKE, 10, ctypes.c_float(1.0),
+             ctypes.c_float(1.0), None, None) == -6
+    assert f(None, None, None, 0, 2, 64, None, None, 10, ctypes.c_float(1.0), ctypes.c_float(1.0), None, None) == 0
+
+
+def test_python_binding_refuses_fp16_workspace():
+    """The split workspace is FP32 by contract; an fp16 buffer is refused before any call
+    (the pages' XQA page-4 route broke when handed an fp16 temporary output)."""
+    import torch
+    with pytest.raises(ValueError):
+        # CPU tensors are refused first; the dtype check is exercised on GPU in test_gpu_attention
+        kvq._need(torch.zeros(4, dtype=torch.float16), "workspace", torch.float32)

@@ -1,0 +1,223 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+benchmark times, on sampled (layer, sequence, query head) units that the
+oracle recomputes one by one from the same seeded fp16 inputs.
+
+For each sampled unit: the E4M3 bytes the GPU wrote for that sequence's kv
+head must equal the oracle's quantisation bit for bit, and the attention
+output must match the oracle within atol 2e-3 / rtol 1e-2.  The oracle
+computes its own calibrated scale, which must equal the GPU's.
+
+The oracle runs in a process pool started with "spawn" (workers never
+inherit a CUDA context).
+"""
+import concurrent.futures as cf
+import multiprocessing as mp
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_paged_kv_e4m3_gb300 import build, inputs, kvq
+from tests import _problems as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def pool():
+    build.build()
+    kvq.load()
+    oracle.build()
+    ex = cf.ProcessPoolExecutor(max_workers=max(2, min(16, os.cpu_count() or 2)),
+                                mp_context=mp.get_context("spawn"))
+    yield ex
+    ex.shutdown(cancel_futures=True)
+
+
+class Layer:
+    """One layer of a workload pushed through the GPU path."""
+
+    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True):
+        self.w, self.layer, self.lay, self.e4m3 = w, layer, lay, e4m3
+        lens = lay.lens.astype(np.int64)
+        total = int(lens.sum())
+        self.offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        self.k = inputs.kv_tokens(w, layer, total, "k", device=DEV)
+        self.v = inputs.kv_tokens(w, layer, total, "v", device=DEV)
+        self.q = inputs.queries(w, layer, device=DEV)
+        shape = (lay.num_pages, w.num_kv_heads, 4, w.head_dim)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        self.err = err
+        if e4m3:
+            self.kcal = inputs.calibration_draw(w, layer, "k", device=DEV)
+            self.vcal = inputs.calibration_draw(w, layer, "v", device=DEV)
+            self.ks = kvq.calibrate_scale(self.kcal)
+            self.vs = kvq.calibrate_scale(self.vcal)
+            self.kc = torch.full(shape, P.SENTINEL, dtype=torch.uint8, device=DEV)
+            self.vc = torch.full(shape, P.SENTINEL, dtype=torch.uint8, device=DEV)
+            app = lambda k, v, s: kvq.kv_append_e4m3(k, v, s, self.kc, self.vc, self.ks, self.vs, err)
+        else:
+            self.ks = self.vs = 1.0
+            self.kc = torch.zeros(shape, dtype=torch.float16, device=DEV)
+            self.vc = torch.zeros(shape, dtype=torch.float16, device=DEV)
+            app = lambda k, v, s: kvq.kv_append_fp16(k, v, s, self.kc, self.vc, err)
+        # the cached history, then this step's tokens (one append call each, as a step does)
+        for seq, pos in (inputs.history_tokens(w, lay), inputs.step_tokens(w, lay)):
+            if seq.size == 0:
+                continue
+            rows = torch.from_numpy(self.offs[seq] + pos).to(DEV)
+            slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, seq, pos)).to(DEV)
+            app(self.k[rows].contiguous(), self.v[rows].contiguous(), slots)
+        self.prefill = None
+        if w.prefill_chunk and with_prefill:
+            pk = inputs.prefill_tokens(w, layer, "k", device=DEV)
+            pv = inputs.prefill_tokens(w, layer, "v", device=DEV)
+            app(pk, pv, torch.from_numpy(inputs.prefill_slots(lay)[: w.prefill_chunk]).to(DEV))
+            self.prefill = (pk, pv)
+        self.bt = torch.from_numpy(lay.block_tables).to(DEV)
+        self.cl = torch.from_numpy(lay.lens).to(DEV)
+        ti, tl = inputs.topk_lists(w, lay.lens)
+        self.topk_np = (ti, tl)
+        ti_d = tl_d = None
+        if ti is not None:
+            ti_d, tl_d = torch.from_numpy(ti).to(DEV), torch.from_numpy(tl).to(DEV)
+        p = kvq.attn_params(self.q, w.num_kv_heads, lay.block_tables.shape[1], w.num_splits,
+                            0 if ti is None else ti.shape[2])
+        self.S = kvq.num_splits(p)
+        ws = kvq.alloc_workspace(p, DEV)
+        if e4m3:
+            self.out = kvq.paged_decode_attn_e4m3(self.q, self.kc, self.vc, self.bt, self.cl, self.ks,
+                                                  self.vs, ws, None, ti_d, tl_d, w.num_splits,
+                                                  err_flag=err)
+        else:
+            self.out = kvq.paged_decode_attn_fp16(self.q, self.kc, self.vc, self.bt, self.cl, ws, None,
+                                                  ti_d, tl_d, w.num_splits, err_flag=err)
+        torch.cuda.synchronize()
+        assert err.item() == 0, f"device error bits {err.item()}"
+
+    def oracle_scales(self):
+        if not self.e4m3:
+            return 1.0, 1.0
+        ks = oracle.calibrate_scale(self.kcal.cpu().numpy())
+        vs = oracle.calibrate_scale(self.vcal.cpu().numpy())
+        assert (ks, vs) == (self.ks, self.vs), "GPU calibration differs from the oracle"
+        return ks, vs
+
+    def submit(self, ex, b, h, scales):
+        w = self.w
+        g = h // w.group
+        L = int(self.lay.lens[b])
+        ks, vs = scales
+        k_seq = self.k[self.offs[b]:self.offs[b] + L, g].cpu().numpy()
+        v_seq = self.v[self.offs[b]:self.offs[b] + L, g].cpu().numpy()
+        q_rows = self.q[b, :, h, :].cpu().numpy()
+        ti, tl = self.topk_np
+        lst = None if ti is None or tl[b] == 0 else ti[b, g, : tl[b]]
+        return ex.submit(P.oracle_unit, q_rows, k_seq, v_seq, L, ks, vs, self.e4m3, lst)
+
+    def gpu_pool_rows(self, b, g):
+        """E4M3 bytes the GPU stored for sequence b, kv head g, positions 0..L-1."""
+        L = int(self.lay.lens[b])
+        pos = torch.arange(L, device=DEV)
+        pages = self.bt[b, pos // 4].long()
+        return self.kc[pages, g, pos % 4].cpu().numpy()
+
+
+def _check(layer_obj, ex, units, tag):
+    scales = layer_obj.oracle_scales()
+    futs = [(b, h, layer_obj.submit(ex, b, h, scales)) for b, h in units]
+    got_all = layer_obj.out.float().cpu().numpy()
+    bad = []
+    for b, h, f in futs:
+        ref, flags, pool_k = f.result()
+        assert flags == 0
+        got = got_all[b, :, h, :]
+        ok = P.tolerance_ok(got, ref)
+        if not ok.all():
+            bad.append((b, h, float(np.abs(got - ref).max())))
+        if layer_obj.e4m3 and h % layer_obj.w.group == 0:
+            assert np.array_equal(layer_obj.gpu_pool_rows(b, h // layer_obj.w.group), pool_k), \
+                f"{tag}: pool bytes differ for sequence {b}, kv head {h // layer_obj.w.group}"
+    assert not bad, f"{tag}: {len(bad)} units outside tolerance, e.g. {bad[:4]}"
+
+
+def _sample(rng, w, n):
+    b = rng.integers(0, w.batch, n)
+    h = rng.integers(0, w.num_q_heads, n)
+    h[: n // 2] -= h[: n // 2] % w.group      # half of them are the group's first head (pool check)
+    return list(zip(b.tolist(), h.tolist()))
+
+
+def test_decode_all_units(pool):
+    """batch 32 x 4096, split-K 4: every (sequence, query head) checked."""
+    w = inputs.get("decode")
+    lay = inputs.page_layout(w)
+    L = Layer(w, 0, lay)
+    assert L.S == 4
+    units = [(b, h) for b in range(w.batch) for h in range(w.num_q_heads)]
+    _check(L, pool, units, "decode e4m3")
+
+
+def test_decode_fp16_arm(pool):
+    w = inputs.get("decode")
+    L = Layer(w, 0, inputs.page_layout(w), e4m3=False)
+    _check(L, pool, _sample(np.random.default_rng(1), w, 96), "decode fp16")
+
+
+def test_decode_32k(pool):
+    w = inputs.get("decode32k")
+    L = Layer(w, 0, inputs.page_layout(w))
+    assert L.S == 8
+    _check(L, pool, _sample(np.random.default_rng(2), w, 48), "decode32k")
+
+
+def test_long_context(pool):
+    """batch 4 x 262,144 tokens, split-K 64 with the FP32 workspace and combine."""
+    w = inputs.get("long")
+    L = Layer(w, 0, inputs.page_layout(w))
+    assert L.S == 64
+    _check(L, pool, _sample(np.random.default_rng(3), w, 12), "long")
+
+
+def test_verify_24_layers(pool):
+    """MTP3 verify: 24 layers, each with its own calibrated scales; >= 256 sampled units."""
+    w = inputs.get("verify")
+    lay = inputs.page_layout(w)
+    rng = np.random.default_rng(4)
+    seen = set()
+    for layer in range(w.layers):
+        L = Layer(w, layer, lay)
+        seen.add((L.ks, L.vs))
+        _check(L, pool, _sample(rng, w, 11), f"verify layer {layer}")
+        del L
+        torch.cuda.empty_cache()
+    assert len(seen) == w.layers          # per-layer scales really differ
+
+
+def test_mixed_24_layers(pool):
+    """Mixed batch: 8192-token prefill chunk appended per layer + 48 decodes,
+    half over a top-2048 list; >= 256 sampled units, prefill bytes checked."""
+    w = inputs.get("mixed")
+    lay = inputs.page_layout(w)
+    ti, tl = inputs.topk_lists(w, lay.lens)
+    assert (tl > 0).sum() == 24
+    rng = np.random.default_rng(5)
+    pre_slots = inputs.prefill_slots(lay)[: w.prefill_chunk]
+    for layer in range(w.layers):
+        L = Layer(w, layer, lay)
+        units = _sample(rng, w, 11)
+        _check(L, pool, units, f"mixed layer {layer}")
+        # the prefill chunk's quantised bytes, one kv head per layer
+        g = layer % w.num_kv_heads
+        ks, _ = L.oracle_scales()
+        pk = L.prefill[0][:, g].cpu().numpy()
+        want = oracle.quantize(pk, ks)
+        sl = torch.from_numpy(pre_slots.astype(np.int64)).to(DEV)
+        got = L.kc[sl // 4, g, sl % 4].cpu().numpy()
+        assert np.array_equal(got, want), f"prefill bytes differ, layer {layer}"
+        del L
+        torch.cuda.empty_cache()
