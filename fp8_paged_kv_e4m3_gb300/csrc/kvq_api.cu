@@ -94,6 +94,7 @@ static int run_attention(const AttnCall &c, bool with_combine)
     int st = check_params(c.p);
     if (st != KVQ_OK) return st;
     const kvq_attn_params &p = *c.p;
+    if (p.batch == 0) return KVQ_OK;   // nothing to read or write
     if (!c.q || !c.k_cache || !c.v_cache || !c.block_tables || !c.context_lens)
         return KVQ_ERR_INVALID_ARG;
     if (with_combine && !c.out) return KVQ_ERR_INVALID_ARG;

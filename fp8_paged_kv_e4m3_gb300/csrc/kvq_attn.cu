@@ -14,7 +14,7 @@
 //  * warp 4 (producer) walks the split's pages 8 at a time (one "stage"),
 //    reads the block table a batch ahead, and issues one 1-D bulk TMA copy
 //    per page for K and for V (page chunk = 4 * head_dim contiguous elements
-//    of one kv head) into a ring of NSTAGES shared-memory stages, completing
+//    of one kv head) into a ring of shared-memory stages (about 50 KB per CTA), completing
 //    on the stage's mbarrier.  In top-k mode a stage is 32 listed tokens,
 //    each fetched as one row.
 //  * warps 0..3 (consumers) take whole stages round-robin (or, for many
@@ -46,7 +46,7 @@ constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <bool E4M3, int D>
+template <bool E4M3, int D, int SG>
 struct Geometry {
     static constexpr int kElem = E4M3 ? 1 : 2;
     static constexpr int kRowBytes = D * kElem;          // one token of one kv head
@@ -55,7 +55,13 @@ struct Geometry {
     static constexpr int kPagesPerStage = 8;
     static constexpr int kRegion = kPagesPerStage * kPageStride;   // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kRegion;
-    static constexpr int kStages = E4M3 ? 8 : 6;
+    // The ring gives each of the SG stage groups its own DEPTH slots, so a
+    // slot is only ever waited on by one group, one phase after another (a
+    // parity wait can never alias an older phase).  About 50 KB of ring per
+    // CTA, at least one slot per group.
+    static constexpr int kDepthRaw = 50688 / (SG * kStageBytes);
+    static constexpr int kDepth = kDepthRaw < 1 ? 1 : (kDepthRaw > 4 ? 4 : kDepthRaw);
+    static constexpr int kStages = SG * kDepth;
     static constexpr int kX4 = kRowBytes / 32;           // ldmatrix.x4 per 16-token tile
     static constexpr int kKSteps = D / 16;               // QK mma k-steps
     static constexpr int kPVTiles = D / 16;              // PV mma m-tiles (16 channels)
@@ -76,8 +82,8 @@ struct Rows {
 template <bool E4M3, int D, int NT, int RW>
 constexpr int smem_bytes()
 {
-    using G = Geometry<E4M3, D>;
     using R = Rows<NT, RW>;
+    using G = Geometry<E4M3, D, R::kGroups>;
     constexpr int merge = R::kGroups * R::kPad * (D + 2) * 4;
     return G::kBytes > merge ? G::kBytes : merge;
 }
@@ -91,11 +97,19 @@ __device__ __forceinline__ int2 pv_channels(int pv, int gid)
     return make_int2(16 * pv + gid, 16 * pv + 8 + gid);
 }
 
+// ring slot of stage st: group st % SG owns slots [g*DEPTH, (g+1)*DEPTH)
+template <int SG, int DEPTH>
+__device__ __forceinline__ int ring_slot(int st)
+{
+    return (st % SG) * DEPTH + (st / SG) % DEPTH;
+}
+
 template <bool E4M3, int D, int NT, int RW>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
 {
-    using G = Geometry<E4M3, D>;
     using R = Rows<NT, RW>;
+    using G = Geometry<E4M3, D, R::kGroups>;
+    constexpr int SG = R::kGroups;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -159,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
             };
             int bt_cur = load_bt(item0), bt_nxt = load_bt(item0 + 32);
             for (int st = 0; st < nst; ++st) {
-                const int slot = st % G::kStages;
+                const int slot = ring_slot<SG, G::kDepth>(st);
                 if (st >= G::kStages &&
                     !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
@@ -211,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
             int pg_cur = load_page(idx_cur);
             int idx_nxt = load_idx(1);
             for (int st = 0; st < nst; ++st) {
-                const int slot = st % G::kStages;
+                const int slot = ring_slot<SG, G::kDepth>(st);
                 if (st >= G::kStages &&
                     !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
@@ -286,15 +300,20 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         const float qk = a.qk_scale_log2;
         const int first_masked = L - a.q_len + 1;   // positions >= this are masked for some row
 
-        for (int st = sg; st < nst; st += R::kGroups) {
-            const int slot = st % G::kStages;
+        for (int st = sg; st < nst; st += SG) {
+            const int slot = ring_slot<SG, G::kDepth>(st);
             if (!mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag))
                 break;
             const uint32_t sk = ring + slot * G::kStageBytes + lane_off;
             const uint32_t sv = sk + G::kRegion;
             const int32_t *tp = tokpos + slot * 32;
-            const int last_pos = min(item0 + (st + 1) * 8, item1) * 4 - 1;
-            const bool need_mask = topk || *stage_bad || last_pos >= first_masked;
+            // Mask when some slot of the stage may hold no valid token for some
+            // row: top-k lists, bad pages, a stage with fewer than 8 pages (its
+            // missing slots keep whatever an earlier stage left there), or
+            // positions inside the verify window / past the context end.
+            const int stage_end = item0 + (st + 1) * 8;
+            const bool need_mask = topk || *stage_bad || stage_end > item1 ||
+                                   stage_end * 4 - 1 >= first_masked;
 
             // ---- S^T = K Q^T (two 16-token tiles: slots {0,1} and {2,3}) ----
             float sc[NT][2][4];
@@ -448,8 +467,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         // writing.  The error bit is already set.
         if (warp == kConsumerWarps && lane == 0)
             for (int st = max(0, issued - G::kStages); st < issued; ++st)
-                mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr,
-                                  a.err_flag);
+                mbar_wait_bounded(bar0 + 8 * ring_slot<SG, G::kDepth>(st), (st / G::kStages) & 1,
+                                  nullptr, a.err_flag);
         __syncthreads();
         return;
     }

@@ -123,6 +123,8 @@ def test_gpu_verify_row_equals_shorter_decode():
 
 @pytest.mark.parametrize("lens,q_len,G_,D", [
     ([1, 2, 3, 4], 1, 8, 128),           # one token, page tails
+    ([236, 1000, 33], 1, 8, 128),        # partial last stage landing in a reused ring slot
+    ([236, 1000, 33], 4, 8, 128),
     ([4, 5, 9, 33], 4, 8, 128),          # verify window covering the whole context
     ([257, 31, 64, 100], 1, 16, 64),     # 16 query heads per kv head
     ([70, 130], 4, 16, 64),              # 64 query rows per kv head (largest)
