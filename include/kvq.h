@@ -13,7 +13,8 @@
  *    current device; pointers marked "host" are ordinary host memory.  The
  *    caller owns every buffer.  The library allocates nothing, keeps no
  *    pointer after a call returns and holds no global state, so calls are
- *    reentrant.
+ *    reentrant (the one exception, paged_decode_attn_e4m3_noalloc at the
+ *    end of this file, uses a scratch buffer the library keeps itself).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every GPU call is asynchronous and stream-ordered; none
  *    synchronises the host, so the calls can be captured in a CUDA graph.
@@ -232,6 +233,38 @@ int paged_decode_attn_fp16_partial(const void *q, const void *k_cache, const voi
                                    const kvq_attn_params *p, int32_t *err_flag, void *stream);
 int kvq_lse_combine(const float *workspace, size_t workspace_bytes, void *out,
                     const kvq_attn_params *p, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Allocation-free variant for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot provide a workspace -- code running under another framework's
+ * memory pool that forbids outside cudaMalloc calls, plugins inside a
+ * process whose allocator they do not control, or latency-critical paths
+ * that ban allocation after start-up.
+ *
+ * Same computation, arguments and errors as paged_decode_attn_e4m3, minus
+ * the workspace: the FP32 split partials go to a scratch buffer of
+ * KVQ_NOALLOC_SCRATCH_BYTES that the library keeps in its own device memory
+ * (a file-scope __device__ array, present on every GPU that loads the
+ * library until the process exits).  The call allocates nothing.
+ *  - A problem whose workspace (kvq_attn_workspace_bytes) exceeds
+ *    KVQ_NOALLOC_SCRATCH_BYTES returns KVQ_ERR_WORKSPACE before any launch;
+ *    use paged_decode_attn_e4m3 with your own workspace for those.
+ *  - The first call on a device looks up the buffer's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.  A failed lookup returns KVQ_ERR_CUDA.
+ *  - Every call on a device shares the one buffer, and it keeps the last
+ *    call's contents (nothing in it has to start at zero).  Calls whose GPU
+ *    work overlaps -- e.g. issued on two streams without ordering -- race
+ *    on it and give undefined results: order them.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int paged_decode_attn_e4m3_noalloc(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                   int64_t num_pages, const int32_t *block_tables,
+                                   const int32_t *context_lens, float k_scale, float v_scale,
+                                   const int32_t *topk_idx, const int32_t *topk_lens, void *out,
+                                   const kvq_attn_params *p, int32_t *err_flag, void *stream);
 
 #ifdef __cplusplus
 }
