@@ -137,9 +137,9 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.num_splits = S;
     a.max_pages = p.max_pages_per_seq;
     a.max_topk = c.topk_idx ? p.max_topk : 0;
-    // hoisted scales: the bitcast decoder yields value * 2^-8, folded back here
-    const double kfold = c.e4m3 ? double(c.k_scale) * 256.0 : 1.0;
-    const double vfold = c.e4m3 ? double(c.v_scale) * 256.0 : 1.0;
+    // hoisted per-layer scales (the kernel folds any decoder factor itself)
+    const double kfold = c.e4m3 ? double(c.k_scale) : 1.0;
+    const double vfold = c.e4m3 ? double(c.v_scale) : 1.0;
     a.qk_scale_log2 = float(sm * log2e * kfold);
     a.out_scale = float(vfold);
 

@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
                                                      uint8_t *__restrict__ v_cache, int64_t num_pages,
                                                      float k_scale, float v_scale, int32_t *err_flag)
 {
+    grid_dependency_wait();   // new K/V and slots may come from the previous kernel
+    launch_dependents();
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= num_vecs) return;
     const int64_t tok = idx / vecs_per_token;
@@ -93,15 +95,12 @@ cudaError_t launch_append(bool e4m3, const void *k_new, const void *v_new,
     auto vn = static_cast<const uint4 *>(v_new);
     auto kc = static_cast<uint8_t *>(k_cache);
     auto vc = static_cast<uint8_t *>(v_cache);
+    const dim3 grid((unsigned)blocks);
     if (e4m3)
-        append_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slot_mapping, n, vpt, vph,
-                                                                  head_dim, kc, vc, num_pages,
-                                                                  k_scale, v_scale, err_flag);
-    else
-        append_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(kn, vn, slot_mapping, n, vpt, vph,
-                                                                   head_dim, kc, vc, num_pages,
-                                                                   1.f, 1.f, err_flag);
-    return cudaGetLastError();
+        return launch_pdl(append_kernel<true>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, n,
+                          vpt, vph, head_dim, kc, vc, num_pages, k_scale, v_scale, err_flag);
+    return launch_pdl(append_kernel<false>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, n, vpt,
+                      vph, head_dim, kc, vc, num_pages, 1.f, 1.f, err_flag);
 }
 
 // ---------------------------------------------------------------------------

@@ -6,30 +6,33 @@
 // for Qwen4Exp QSA with MTP", sections Purpose and Status and history):
 // grouped-query attention of q_len = 1 (decode) or 1 + 3 (MTP verify, causal
 // inside the window) query rows over a page-4 cache whose K/V are stored in
-// calibrated E4M3, decoded by a bitcast decoder with the per-layer scales
-// hoisted out of the inner loop, split over the token axis into an FP32
-// workspace, and merged by a log-sum-exp combine.
+// calibrated E4M3, decoded exactly to fp16 with the per-layer scales hoisted
+// out of the inner loop, split over the token axis into an FP32 workspace,
+// and merged by a log-sum-exp combine.
 //
-// GB300 design (one CTA per (split, kv head, sequence), 5 warps):
-//  * warp 4 (producer) walks the split's pages 8 at a time (one "stage"),
-//    reads the block table a batch ahead, and issues one 1-D bulk TMA copy
-//    per page for K and for V (page chunk = 4 * head_dim contiguous elements
-//    of one kv head) into a ring of shared-memory stages (about 50 KB per CTA), completing
-//    on the stage's mbarrier.  In top-k mode a stage is 32 listed tokens,
-//    each fetched as one row.
-//  * warps 0..3 (consumers) take whole stages round-robin (or, for many
-//    query rows, share a stage and split the rows).  Per 16-token tile they
-//    load K with ldmatrix, decode E4M3 -> fp16 with the bitcast decoder in
-//    registers, and run S^T = K * Q^T on tensor cores (mma.sync m16n8k16,
-//    tokens on M, query rows on N -- the 8 heads of a GQA group fill N
-//    exactly).  The online softmax runs in the log2 domain with the K scale,
-//    2^8 and log2(e) folded into one multiplier; P is transposed in
-//    registers with movmatrix and multiplied by V^T loaded with
-//    ldmatrix.trans (again decoded in registers).  The V scale and 2^8 are
-//    applied once per output row.
-//  * Page chunks sit 16 bytes apart beyond their size in shared memory, so
-//    the eight rows an ldmatrix reads (the same slot of eight pages) fall
-//    in distinct banks.
+// GB300 design (one CTA per (split, kv head, sequence), 4 consumer warps and
+// 1 producer warp):
+//  * The producer walks the split's pages one stage at a time (16 pages for
+//    one query-row group, 8 otherwise), reads the block table a batch ahead,
+//    and issues one 1-D bulk TMA copy per page for K and for V (a page of one
+//    kv head = 4 * head_dim contiguous elements) into a ring of about 50 KB
+//    of shared memory, each stage completing on its own mbarrier.  In top-k
+//    mode a stage is 4 tokens per page slot, each fetched as one row.
+//  * Every consumer warp takes part in every stage: warp w owns one (or, for
+//    64 query rows, two) 16-token tiles of the stage and one group of query
+//    rows.  Each warp therefore waits on every phase of every ring slot in
+//    order, and a slot is refilled only after all four warps released it.
+//  * Per 16-token tile: K via ldmatrix, E4M3 -> fp16 by the hardware
+//    conversion (exact), S^T = K Q^T on tensor cores (mma.sync m16n8k16,
+//    tokens on M, query rows on N: the 8 heads of a GQA group fill N
+//    exactly); online softmax in the log2 domain with k_scale * sm_scale *
+//    log2(e) folded into one multiplier; P transposed in registers by
+//    movmatrix; V^T via ldmatrix.trans, decoded (byte permute + conversion,
+//    or the bitcast decoder), O^T += V^T P^T.  v_scale is applied once per
+//    output row.
+//  * Page chunks sit 16 bytes further apart than their size in shared
+//    memory, so the eight rows an ldmatrix reads (one slot of eight pages)
+//    fall in distinct banks.
 //  * Every wait is bounded (about 2 s); on expiry the kernel reports
 //    KVQ_DEV_TIMEOUT, drains its own copies and exits without writing.
 #include <cstdint>
@@ -41,75 +44,78 @@
 
 namespace kvq {
 
+// V fragments: 1 = byte permute + hardware conversion, 0 = bitcast decoder
+// (the decoder of the source pages: exact, value * 2^-8).  K fragments always
+// use the hardware conversion: their byte pairs are adjacent.
+#ifndef KVQ_V_CVT
+#define KVQ_V_CVT 1
+#endif
+
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <bool E4M3, int D, int SG>
+// Work split of the 4 consumer warps: RW warps share the same tokens and
+// split the query rows (NT 8-row tiles each); 4/RW warps split the tokens.
+template <int NT, int RW>
+struct Split {
+    static constexpr int kRowWarps = RW;
+    static constexpr int kTokWarps = kConsumerWarps / RW;
+    static constexpr int kTilesPerWarp = (RW == kConsumerWarps) ? 2 : 1;    // 16-token tiles
+    static constexpr int kTilesPerStage = kTokWarps * kTilesPerWarp;
+    static constexpr int kPagesPerStage = 4 * kTilesPerStage;             // 16 or 8
+    static constexpr int kRowsPad = RW * NT * 8;
+};
+
+template <bool E4M3, int D, int PPS>
 struct Geometry {
     static constexpr int kElem = E4M3 ? 1 : 2;
-    static constexpr int kRowBytes = D * kElem;          // one token of one kv head
-    static constexpr int kChunk = 4 * kRowBytes;         // one page of one kv head
-    static constexpr int kPageStride = kChunk + 16;      // bank-skewed page placement
-    static constexpr int kPagesPerStage = 8;
-    static constexpr int kRegion = kPagesPerStage * kPageStride;   // K (or V) part of a stage
+    static constexpr int kRowBytes = D * kElem;           // one token of one kv head
+    static constexpr int kChunk = 4 * kRowBytes;          // one page of one kv head
+    static constexpr int kPageStride = kChunk + 16;       // bank-skewed page placement
+    static constexpr int kRegion = PPS * kPageStride;     // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kRegion;
-    // The ring gives each of the SG stage groups its own DEPTH slots, so a
-    // slot is only ever waited on by one group, one phase after another (a
-    // parity wait can never alias an older phase).  About 50 KB of ring per
-    // CTA, at least one slot per group.
-    static constexpr int kDepthRaw = 50688 / (SG * kStageBytes);
-    static constexpr int kDepth = kDepthRaw < 1 ? 1 : (kDepthRaw > 4 ? 4 : kDepthRaw);
-    static constexpr int kStages = SG * kDepth;
-    static constexpr int kX4 = kRowBytes / 32;           // ldmatrix.x4 per 16-token tile
-    static constexpr int kKSteps = D / 16;               // QK mma k-steps
-    static constexpr int kPVTiles = D / 16;              // PV mma m-tiles (16 channels)
+    static constexpr int kStagesRaw = 50688 / kStageBytes;   // ~50 KB of ring
+    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kX4 = kRowBytes / 32;            // ldmatrix.x4 per 16-token tile
+    static constexpr int kKSteps = D / 16;                // QK mma k-steps
+    static constexpr int kPVTiles = D / 16;               // PV mma m-tiles (16 channels)
+    static constexpr int kTokPerStage = 4 * PPS;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kTokPosOff = kRingBytes;
-    static constexpr int kBarOff = kTokPosOff + kStages * 32 * 4;
+    static constexpr int kBarOff = kTokPosOff + kStages * kTokPerStage * 4;
     static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
     static constexpr int kBytes = kAbortOff + 16;
     static_assert(kPageStride % 128 == 16, "page skew must be 16 bytes mod 128");
-};
-
-template <int NT, int RW>
-struct Rows {
-    static constexpr int kPad = RW * NT * 8;             // query rows per CTA, padded
-    static constexpr int kGroups = kConsumerWarps / RW;  // stage groups
+    static_assert(kBarOff % 8 == 0, "mbarriers need 8-byte alignment");
 };
 
 template <bool E4M3, int D, int NT, int RW>
 constexpr int smem_bytes()
 {
-    using R = Rows<NT, RW>;
-    using G = Geometry<E4M3, D, R::kGroups>;
-    constexpr int merge = R::kGroups * R::kPad * (D + 2) * 4;
+    using W = Split<NT, RW>;
+    using G = Geometry<E4M3, D, W::kPagesPerStage>;
+    constexpr int merge = W::kTokWarps * W::kRowsPad * (D + 2) * 4;
     return G::kBytes > merge ? G::kBytes : merge;
 }
 
 // channel of the O^T accumulator row held by this thread for PV tile `pv`
 // (first = fragment row gid, second = fragment row gid + 8)
-template <bool E4M3>
+template <bool BYTE_PAIRS>
 __device__ __forceinline__ int2 pv_channels(int pv, int gid)
 {
-    if (E4M3) return make_int2(16 * pv + 2 * gid, 16 * pv + 2 * gid + 1);
+    if (BYTE_PAIRS) return make_int2(16 * pv + 2 * gid, 16 * pv + 2 * gid + 1);
     return make_int2(16 * pv + gid, 16 * pv + 8 + gid);
-}
-
-// ring slot of stage st: group st % SG owns slots [g*DEPTH, (g+1)*DEPTH)
-template <int SG, int DEPTH>
-__device__ __forceinline__ int ring_slot(int st)
-{
-    return (st % SG) * DEPTH + (st / SG) % DEPTH;
 }
 
 template <bool E4M3, int D, int NT, int RW>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
 {
-    using R = Rows<NT, RW>;
-    using G = Geometry<E4M3, D, R::kGroups>;
-    constexpr int SG = R::kGroups;
+    using W = Split<NT, RW>;
+    constexpr int PPS = W::kPagesPerStage;
+    constexpr int MTW = W::kTilesPerWarp;
+    using G = Geometry<E4M3, D, PPS>;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -118,7 +124,20 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
     int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
     const uint32_t bar0 = smem_u32(smem + G::kBarOff);   // full[k] = bar0 + 8k, empty[k] = bar0 + 8(S+k)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
-    volatile int *stage_bad = abort_flag + 1;            // any bad entry seen in a stage (sticky)
+    volatile int *stage_bad = abort_flag + 1;            // a bad entry was seen (sticky)
+
+    // barriers first: this part reads no input and overlaps the previous kernel's tail
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < G::kStages; ++k) {
+            mbar_init(bar0 + 8 * k, 1);
+            mbar_init(bar0 + 8 * (G::kStages + k), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *stage_bad = 0;
+        fence_mbar_init();
+    }
+    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
+    launch_dependents();      // the combine may start launching; it waits for our completion
 
     // ---- work of this CTA --------------------------------------------------
     const int L = a.context_lens[b];
@@ -126,24 +145,17 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
     int topk_n = (a.topk_idx && a.topk_lens) ? a.topk_lens[b] : 0;
     const bool topk = len_ok && topk_n > 0;
     if (topk && topk_n > a.max_topk) topk_n = a.max_topk;
-    const int n_items = !len_ok ? 0 : (topk ? topk_n : (L + 3) / 4);
+    const int n_items = !len_ok ? 0 : (topk ? topk_n : (L + 3) / 4);   // pages or list entries
     const int per = (n_items + a.num_splits - 1) / a.num_splits;
     const int item0 = min(s * per, n_items);
     const int item1 = min(item0 + per, n_items);
-    const int ipst = topk ? 32 : G::kPagesPerStage;     // items per stage
+    const int ipst = topk ? G::kTokPerStage : PPS;        // items per stage
     const int nst = (item1 - item0 + ipst - 1) / ipst;
 
     if (threadIdx.x == 0) {
         if (!len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
         if (len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
             report(a.err_flag, KVQ_DEV_BAD_TOPK);
-        for (int k = 0; k < G::kStages; ++k) {
-            mbar_init(bar0 + 8 * k, 1);
-            mbar_init(bar0 + 8 * (G::kStages + k), RW);
-        }
-        *abort_flag = 0;
-        *stage_bad = 0;
-        fence_mbar_init();
     }
     __syncthreads();
 
@@ -159,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         l_run[j][0] = l_run[j][1] = 0.f;
     }
     const int gid = lane >> 2, t = lane & 3;
-    const int rw = warp % RW, sg = warp / RW;
+    const int rw = warp % RW, tw = warp / RW;
     int issued = 0;   // stages the producer has issued
 
     if (warp == kConsumerWarps) {
@@ -167,27 +179,30 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         const uint64_t pol = l2_policy_evict_first();
         const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
         if (!topk) {
+            constexpr int SPB = 32 / PPS;                 // stages per block-table batch
             auto load_bt = [&](int first) -> int {
                 const int it = first + lane;
                 return it < item1 ? __ldg(bt_row + it) : -1;
             };
             int bt_cur = load_bt(item0), bt_nxt = load_bt(item0 + 32);
+            const int p = lane % PPS;                      // page of the stage this lane copies
+            const bool is_v = lane >= PPS;
+            const bool copier = lane < 2 * PPS;
             for (int st = 0; st < nst; ++st) {
-                const int slot = ring_slot<SG, G::kDepth>(st);
+                const int slot = st % G::kStages;
                 if (st >= G::kStages &&
                     !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
                     break;
-                if (st > 0 && (st & 3) == 0) {
+                if (st > 0 && st % SPB == 0) {
                     bt_cur = bt_nxt;
-                    bt_nxt = load_bt(item0 + (st + 4) * 8);
+                    bt_nxt = load_bt(item0 + (st + SPB) * PPS);
                 }
-                const int p = lane & 7;
-                const int item = item0 + st * 8 + p;
-                const int phys = __shfl_sync(kFull, bt_cur, (st & 3) * 8 + p);
+                const int item = item0 + st * PPS + p;
+                const int phys = __shfl_sync(kFull, bt_cur, (st % SPB) * PPS + p);
                 const bool exists = item < item1;
                 const bool valid = exists && phys >= 0 && (int64_t)phys < a.num_pages;
-                if (lane < 8) {
+                if (lane < PPS) {
                     if (exists && !valid) {
                         report(a.err_flag, KVQ_DEV_BAD_PAGE);
                         *stage_bad = 1;
@@ -195,74 +210,92 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
 #pragma unroll
                     for (int sl = 0; sl < 4; ++sl) {
                         const int pos = item * 4 + sl;
-                        tokpos[slot * 32 + p * 4 + sl] = (valid && pos < L) ? pos : -1;
+                        tokpos[slot * G::kTokPerStage + p * 4 + sl] = (valid && pos < L) ? pos : -1;
                     }
                 }
-                const unsigned vmask = __ballot_sync(kFull, valid && lane < 16);
+                const unsigned vmask = __ballot_sync(kFull, valid && copier);
                 __syncwarp();
                 if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, __popc(vmask) * G::kChunk);
                 __syncwarp();
-                if (lane < 16 && valid) {
-                    const uint8_t *base =
-                        static_cast<const uint8_t *>(lane < 8 ? a.k_cache : a.v_cache);
+                if (copier && valid) {
+                    const uint8_t *base = static_cast<const uint8_t *>(is_v ? a.v_cache : a.k_cache);
                     const uint8_t *src = base + ((int64_t)phys * a.num_kv_heads + g) * G::kChunk;
-                    const uint32_t dst = ring + slot * G::kStageBytes + (lane < 8 ? 0 : G::kRegion) +
+                    const uint32_t dst = ring + slot * G::kStageBytes + (is_v ? G::kRegion : 0) +
                                          p * G::kPageStride;
                     tma_load_1d(dst, src, G::kChunk, bar0 + 8 * slot, pol);
                 }
                 issued = st + 1;
             }
         } else {
+            // top-k: kTokPerStage listed tokens per stage, R per lane
+            constexpr int R = G::kTokPerStage / 32;
             const int32_t *list = a.topk_idx + ((int64_t)b * a.num_kv_heads + g) * a.max_topk;
-            auto load_idx = [&](int st) -> int {
-                const int it = item0 + st * 32 + lane;
+            auto load_idx = [&](int st, int r) -> int {
+                const int it = item0 + st * G::kTokPerStage + r * 32 + lane;
                 return (st < nst && it < item1) ? __ldg(list + it) : -1;
             };
             auto load_page = [&](int idx) -> int {
                 return (idx >= 0 && idx < L) ? __ldg(bt_row + (idx >> 2)) : -1;
             };
-            int idx_cur = load_idx(0);
-            int pg_cur = load_page(idx_cur);
-            int idx_nxt = load_idx(1);
+            int idx_cur[R], pg_cur[R], idx_nxt[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                idx_cur[r] = load_idx(0, r);
+                pg_cur[r] = load_page(idx_cur[r]);
+                idx_nxt[r] = load_idx(1, r);
+            }
             for (int st = 0; st < nst; ++st) {
-                const int slot = ring_slot<SG, G::kDepth>(st);
+                const int slot = st % G::kStages;
                 if (st >= G::kStages &&
                     !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
                     break;
-                const int pg_nxt = load_page(idx_nxt);
-                const int idx_nxt2 = load_idx(st + 2);
-                const bool exists = item0 + st * 32 + lane < item1;
-                const bool idx_ok = exists && idx_cur >= 0 && idx_cur < L;
-                const bool valid = idx_ok && pg_cur >= 0 && (int64_t)pg_cur < a.num_pages;
-                if (exists && !idx_ok) report(a.err_flag, KVQ_DEV_BAD_TOPK);
-                if (idx_ok && !valid) report(a.err_flag, KVQ_DEV_BAD_PAGE);
-                tokpos[slot * 32 + lane] = valid ? idx_cur : -1;
-                const unsigned vmask = __ballot_sync(kFull, valid);
+                int pg_nxt[R], idx_nxt2[R];
+                bool valid[R];
+                int cnt = 0;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    pg_nxt[r] = load_page(idx_nxt[r]);
+                    idx_nxt2[r] = load_idx(st + 2, r);
+                    const int e = r * 32 + lane;                    // token of the stage
+                    const bool exists = item0 + st * G::kTokPerStage + e < item1;
+                    const bool idx_ok = exists && idx_cur[r] >= 0 && idx_cur[r] < L;
+                    valid[r] = idx_ok && pg_cur[r] >= 0 && (int64_t)pg_cur[r] < a.num_pages;
+                    if (exists && !idx_ok) report(a.err_flag, KVQ_DEV_BAD_TOPK);
+                    if (idx_ok && !valid[r]) report(a.err_flag, KVQ_DEV_BAD_PAGE);
+                    tokpos[slot * G::kTokPerStage + e] = valid[r] ? idx_cur[r] : -1;
+                    cnt += __popc(__ballot_sync(kFull, valid[r]));
+                }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, __popc(vmask) * 2 * G::kRowBytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, cnt * 2 * G::kRowBytes);
                 __syncwarp();
-                if (valid) {
-                    const int64_t row = ((int64_t)pg_cur * a.num_kv_heads + g) * 4 + (idx_cur & 3);
-                    const uint32_t dst = ring + slot * G::kStageBytes + (lane >> 2) * G::kPageStride +
-                                         (lane & 3) * G::kRowBytes;
-                    tma_load_1d(dst, static_cast<const uint8_t *>(a.k_cache) + row * G::kRowBytes,
-                                G::kRowBytes, bar0 + 8 * slot, pol);
-                    tma_load_1d(dst + G::kRegion,
-                                static_cast<const uint8_t *>(a.v_cache) + row * G::kRowBytes,
-                                G::kRowBytes, bar0 + 8 * slot, pol);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (valid[r]) {
+                        const int e = r * 32 + lane;
+                        const int64_t row =
+                            ((int64_t)pg_cur[r] * a.num_kv_heads + g) * 4 + (idx_cur[r] & 3);
+                        const uint32_t dst = ring + slot * G::kStageBytes + (e >> 2) * G::kPageStride +
+                                             (e & 3) * G::kRowBytes;
+                        tma_load_1d(dst, static_cast<const uint8_t *>(a.k_cache) + row * G::kRowBytes,
+                                    G::kRowBytes, bar0 + 8 * slot, pol);
+                        tma_load_1d(dst + G::kRegion,
+                                    static_cast<const uint8_t *>(a.v_cache) + row * G::kRowBytes,
+                                    G::kRowBytes, bar0 + 8 * slot, pol);
+                    }
+                    idx_cur[r] = idx_nxt[r];
+                    pg_cur[r] = pg_nxt[r];
+                    idx_nxt[r] = idx_nxt2[r];
                 }
                 issued = st + 1;
-                idx_cur = idx_nxt;
-                pg_cur = pg_nxt;
-                idx_nxt = idx_nxt2;
             }
         }
     } else {
         // ================= consumers =================
-        // Q as mma B fragments, one set per 8-row n-tile.  For E4M3 the K
-        // channels come out of the bitcast decoder paired (d, d+2) and
-        // (d+1, d+3), so Q is gathered in the same order.
+        // Q as mma B fragments, one set per 8-row n-tile; k-step ks of this
+        // lane covers channels 16ks + 4t .. +3 (E4M3: the pairs the hardware
+        // conversion makes from adjacent K bytes) or 16ks + 2t, +1 and
+        // 16ks + 8 + 2t, +1 (fp16).
         uint32_t qf[NT][G::kKSteps][2];
         int lim[NT][2];
 #pragma unroll
@@ -281,8 +314,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                 for (int ks = 0; ks < G::kKSteps; ++ks) {
                     if (E4M3) {
                         const uint2 v = *reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * t);
-                        qf[j][ks][0] = __byte_perm(v.x, v.y, 0x5410);  // (d, d+2)
-                        qf[j][ks][1] = __byte_perm(v.x, v.y, 0x7632);  // (d+1, d+3)
+                        qf[j][ks][0] = v.x;   // (d, d+1)
+                        qf[j][ks][1] = v.y;   // (d+2, d+3)
                     } else {
                         qf[j][ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * t);
                         qf[j][ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * t);
@@ -294,48 +327,58 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
             }
         }
         // per-lane ldmatrix offset: matrix q = lane/8 reads row (page) lane%8,
-        // token slot half = q&1 of the tile, 16-byte chunk q>>1 of the pair
+        // token slot (q&1) of the tile's slot pair, 16-byte chunk (q>>1) of the pair
         const int mq = lane >> 3;
         const uint32_t lane_off = (lane & 7) * G::kPageStride + (mq & 1) * G::kRowBytes + (mq >> 1) * 16;
+        // this warp's tiles: tile index tg -> page group tg/2, slot pair tg%2
+        uint32_t tile_off[MTW];
+        int tile_pg[MTW], tile_sp[MTW];
+#pragma unroll
+        for (int k = 0; k < MTW; ++k) {
+            const int tg = tw * MTW + k;
+            tile_pg[k] = tg >> 1;
+            tile_sp[k] = tg & 1;
+            tile_off[k] = tile_pg[k] * 8 * G::kPageStride + tile_sp[k] * 2 * G::kRowBytes + lane_off;
+        }
         const float qk = a.qk_scale_log2;
         const int first_masked = L - a.q_len + 1;   // positions >= this are masked for some row
 
-        for (int st = sg; st < nst; st += SG) {
-            const int slot = ring_slot<SG, G::kDepth>(st);
+        for (int st = 0; st < nst; ++st) {
+            const int slot = st % G::kStages;
             if (!mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag))
                 break;
-            const uint32_t sk = ring + slot * G::kStageBytes + lane_off;
+            const uint32_t sk = ring + slot * G::kStageBytes;
             const uint32_t sv = sk + G::kRegion;
-            const int32_t *tp = tokpos + slot * 32;
+            const int32_t *tp = tokpos + slot * G::kTokPerStage;
             // Mask when some slot of the stage may hold no valid token for some
-            // row: top-k lists, bad pages, a stage with fewer than 8 pages (its
-            // missing slots keep whatever an earlier stage left there), or
-            // positions inside the verify window / past the context end.
-            const int stage_end = item0 + (st + 1) * 8;
+            // row: top-k lists, bad pages, a stage with missing pages (their
+            // slots keep whatever an earlier stage left there), or positions
+            // inside the verify window / past the context end.
+            const int stage_end = item0 + (st + 1) * PPS;
             const bool need_mask = topk || *stage_bad || stage_end > item1 ||
                                    stage_end * 4 - 1 >= first_masked;
 
-            // ---- S^T = K Q^T (two 16-token tiles: slots {0,1} and {2,3}) ----
-            float sc[NT][2][4];
+            // ---- S^T = K Q^T, one 16-token tile at a time ----
+            float sc[NT][MTW][4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int k = 0; k < MTW; ++k) {
                 uint32_t kr[G::kX4][4];
 #pragma unroll
-                for (int u = 0; u < G::kX4; ++u) ldsm_x4(kr[u], sk + mt * 2 * G::kRowBytes + u * 32);
+                for (int u = 0; u < G::kX4; ++u) ldsm_x4(kr[u], sk + tile_off[k] + u * 32);
 #pragma unroll
                 for (int j = 0; j < NT; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[j][mt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) sc[j][k][e] = 0.f;
 #pragma unroll
                 for (int ks = 0; ks < G::kKSteps; ++ks) {
                     uint32_t af[4];
                     if (E4M3) {
                         const uint32_t w0 = kr[ks >> 1][2 * (ks & 1)];
                         const uint32_t w1 = kr[ks >> 1][2 * (ks & 1) + 1];
-                        af[0] = dec_lo(w0);
-                        af[1] = dec_lo(w1);
-                        af[2] = dec_hi(w0);
-                        af[3] = dec_hi(w1);
+                        af[0] = cvt_lo(w0);
+                        af[1] = cvt_lo(w1);
+                        af[2] = cvt_hi(w0);
+                        af[3] = cvt_hi(w1);
                     } else {
                         af[0] = kr[ks][0];
                         af[1] = kr[ks][1];
@@ -343,26 +386,27 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                         af[3] = kr[ks][3];
                     }
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) mma_16816(sc[j][mt], af, qf[j][ks][0], qf[j][ks][1]);
+                    for (int j = 0; j < NT; ++j) mma_16816(sc[j][k], af, qf[j][ks][0], qf[j][ks][1]);
                 }
             }
             // ---- scores in the log2 domain, masking ----
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt)
+                for (int k = 0; k < MTW; ++k)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[j][mt][e] *= qk;
+                    for (int e = 0; e < 4; ++e) sc[j][k][e] *= qk;
             if (need_mask) {
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    const int pa = tp[gid * 4 + 2 * mt], pb = tp[gid * 4 + 2 * mt + 1];
+                for (int k = 0; k < MTW; ++k) {
+                    const int pbase = (tile_pg[k] * 8 + gid) * 4 + 2 * tile_sp[k];
+                    const int pa = tp[pbase], pb = tp[pbase + 1];
 #pragma unroll
                     for (int j = 0; j < NT; ++j)
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            if (!(pa >= 0 && pa <= lim[j][c])) sc[j][mt][c] = -INFINITY;
-                            if (!(pb >= 0 && pb <= lim[j][c])) sc[j][mt][2 + c] = -INFINITY;
+                            if (!(pa >= 0 && pa <= lim[j][c])) sc[j][k][c] = -INFINITY;
+                            if (!(pb >= 0 && pb <= lim[j][c])) sc[j][k][2 + c] = -INFINITY;
                         }
                 }
             }
@@ -371,7 +415,9 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
             for (int j = 0; j < NT; ++j)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    float mx = fmaxf(fmaxf(sc[j][0][c], sc[j][0][c + 2]), fmaxf(sc[j][1][c], sc[j][1][c + 2]));
+                    float mx = fmaxf(sc[j][0][c], sc[j][0][c + 2]);
+#pragma unroll
+                    for (int k = 1; k < MTW; ++k) mx = fmaxf(mx, fmaxf(sc[j][k][c], sc[j][k][c + 2]));
                     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
                     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
                     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
@@ -386,35 +432,41 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                         o[j][pv][c + 2] *= corr;
                     }
 #pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        const float p0 = fast_exp2(sc[j][mt][c] - m_use);
-                        const float p1 = fast_exp2(sc[j][mt][c + 2] - m_use);
-                        sc[j][mt][c] = p0;
-                        sc[j][mt][c + 2] = p1;
+                    for (int k = 0; k < MTW; ++k) {
+                        const float p0 = fast_exp2(sc[j][k][c] - m_use);
+                        const float p1 = fast_exp2(sc[j][k][c + 2] - m_use);
+                        sc[j][k][c] = p0;
+                        sc[j][k][c + 2] = p1;
                         lsum += p0 + p1;
                     }
                     l_run[j][c] = lsum;
                 }
             // ---- P^T as mma B fragments: transpose the score tiles in registers ----
-            uint32_t pf[NT][2][2];
+            uint32_t pf[NT][MTW][2];
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    pf[j][mt][0] = movmatrix_trans(pack_half2(sc[j][mt][0], sc[j][mt][1]));
-                    pf[j][mt][1] = movmatrix_trans(pack_half2(sc[j][mt][2], sc[j][mt][3]));
+                for (int k = 0; k < MTW; ++k) {
+                    pf[j][k][0] = movmatrix_trans(pack_half2(sc[j][k][0], sc[j][k][1]));
+                    pf[j][k][1] = movmatrix_trans(pack_half2(sc[j][k][2], sc[j][k][3]));
                 }
             // ---- O^T += V^T P^T ----
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
+            for (int k = 0; k < MTW; ++k) {
                 uint32_t vr[G::kX4][4];
 #pragma unroll
-                for (int u = 0; u < G::kX4; ++u) ldsm_x4_trans(vr[u], sv + mt * 2 * G::kRowBytes + u * 32);
-                if (!E4M3 && need_mask) {
-                    const uint32_t m0 = (tp[(2 * t) * 4 + 2 * mt] >= 0 ? 0x0000FFFFu : 0u) |
-                                        (tp[(2 * t + 1) * 4 + 2 * mt] >= 0 ? 0xFFFF0000u : 0u);
-                    const uint32_t m1 = (tp[(2 * t) * 4 + 2 * mt + 1] >= 0 ? 0x0000FFFFu : 0u) |
-                                        (tp[(2 * t + 1) * 4 + 2 * mt + 1] >= 0 ? 0xFFFF0000u : 0u);
+                for (int u = 0; u < G::kX4; ++u) ldsm_x4_trans(vr[u], sv + tile_off[k] + u * 32);
+                if (need_mask) {
+                    // Slots that hold no token may contain any bits -- fp16 NaN, or
+                    // the E4M3 NaN codes 0x7F/0xFF, which the conversion turns into
+                    // NaN -- so their V is zeroed (P = 0 alone would give 0 * NaN).
+                    // Token (page 2t) sits in the low half of each word, (page 2t+1)
+                    // in the high half, for both element sizes.
+                    const int q0 = (tile_pg[k] * 8 + 2 * t) * 4 + 2 * tile_sp[k];
+                    const uint32_t m0 = (tp[q0] >= 0 ? 0x0000FFFFu : 0u) |
+                                        (tp[q0 + 4] >= 0 ? 0xFFFF0000u : 0u);
+                    const uint32_t m1 = (tp[q0 + 1] >= 0 ? 0x0000FFFFu : 0u) |
+                                        (tp[q0 + 5] >= 0 ? 0xFFFF0000u : 0u);
 #pragma unroll
                     for (int u = 0; u < G::kX4; ++u) {
                         vr[u][0] &= m0;
@@ -427,12 +479,22 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                 for (int pv = 0; pv < G::kPVTiles; ++pv) {
                     uint32_t af[4];
                     if (E4M3) {
+                        // bytes of a word: (token A, d) (A, d+1) (B, d) (B, d+1)
                         const uint32_t h0 = vr[pv >> 1][2 * (pv & 1)];
                         const uint32_t h1 = vr[pv >> 1][2 * (pv & 1) + 1];
+#if KVQ_V_CVT
+                        const uint32_t p0 = __byte_perm(h0, 0, 0x3120);
+                        const uint32_t p1 = __byte_perm(h1, 0, 0x3120);
+                        af[0] = cvt_lo(p0);
+                        af[1] = cvt_hi(p0);
+                        af[2] = cvt_lo(p1);
+                        af[3] = cvt_hi(p1);
+#else
                         af[0] = dec_lo(h0);
                         af[1] = dec_hi(h0);
                         af[2] = dec_lo(h1);
                         af[3] = dec_hi(h1);
+#endif
                     } else {
                         af[0] = vr[pv][0];
                         af[1] = vr[pv][2];
@@ -440,7 +502,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                         af[3] = vr[pv][3];
                     }
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) mma_16816(o[j][pv], af, pf[j][mt][0], pf[j][mt][1]);
+                    for (int j = 0; j < NT; ++j) mma_16816(o[j][pv], af, pf[j][k][0], pf[j][k][1]);
                 }
             }
             __syncwarp();
@@ -459,7 +521,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
             }
     }
 
-    // ---- merge the stage groups through shared memory, write the split partial ----
+    // ---- merge the token warps through shared memory, write the split partial ----
     __syncthreads();
     if (*abort_flag) {
         // Something gave up: before the CTA's shared memory is released, wait
@@ -467,12 +529,12 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         // writing.  The error bit is already set.
         if (warp == kConsumerWarps && lane == 0)
             for (int st = max(0, issued - G::kStages); st < issued; ++st)
-                mbar_wait_bounded(bar0 + 8 * ring_slot<SG, G::kDepth>(st), (st / G::kStages) & 1,
-                                  nullptr, a.err_flag);
+                mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr,
+                                  a.err_flag);
         __syncthreads();
         return;
     }
-    float *mbuf = reinterpret_cast<float *>(smem);    // [groups][kPad][D + 2]: m, l, o[D]
+    float *mbuf = reinterpret_cast<float *>(smem);    // [token warps][kRowsPad][D + 2]: m, l, o[D]
     constexpr int kRowF = D + 2;
     if (warp < kConsumerWarps) {
 #pragma unroll
@@ -480,7 +542,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const int row = (rw * NT + j) * 8 + 2 * t + c;
-                float *dst = mbuf + (sg * R::kPad + row) * kRowF;
+                float *dst = mbuf + (tw * W::kRowsPad + row) * kRowF;
                 if (gid == 0) {
                     dst[0] = m_run[j][c];
                     dst[1] = l_run[j][c];
@@ -495,11 +557,13 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
     }
     __syncthreads();
     const int S = a.num_splits;
+    // the bitcast decoder yields V * 2^-8; the hardware conversion V itself
+    constexpr float kVFold = (E4M3 && !KVQ_V_CVT) ? 256.f : 1.f;
     for (int idx = threadIdx.x; idx < a.rows * D; idx += kThreads) {
         const int row = idx / D, d = idx % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < R::kGroups; ++q) M = fmaxf(M, mbuf[(q * R::kPad + row) * kRowF]);
+        for (int q = 0; q < W::kTokWarps; ++q) M = fmaxf(M, mbuf[(q * W::kRowsPad + row) * kRowF]);
         const int i = row / a.group, h = g * a.group + row % a.group;
         const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
         if (M == -INFINITY) {
@@ -511,13 +575,13 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         }
         float lsum = 0.f, osum = 0.f;
 #pragma unroll
-        for (int q = 0; q < R::kGroups; ++q) {
-            const float *src = mbuf + (q * R::kPad + row) * kRowF;
+        for (int q = 0; q < W::kTokWarps; ++q) {
+            const float *src = mbuf + (q * W::kRowsPad + row) * kRowF;
             const float w = fast_exp2(src[0] - M);
             lsum += w * src[1];
             osum += w * src[2 + d];
         }
-        a.ws_o[unit * D + d] = osum / lsum * a.out_scale;
+        a.ws_o[unit * D + d] = osum / lsum * (a.out_scale * kVFold);
         if (d == 0) {
             a.ws_m[unit] = M * kLn2;
             a.ws_l[unit] = lsum;
@@ -537,6 +601,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     constexpr int V = D / 32;   // channels per lane (4 or 2)
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    grid_dependency_wait();   // the partials come from the attention kernel
+    launch_dependents();
     if (row >= rows) return;
     const float *m = ws_m + (int64_t)row * S;
     const float *l = ws_l + (int64_t)row * S;
@@ -601,8 +667,7 @@ static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-    attn_split_kernel<E4M3, D, NT, RW><<<grid, kThreads, bytes, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(attn_split_kernel<E4M3, D, NT, RW>, grid, dim3(kThreads), bytes, stream, a);
 }
 
 template <bool E4M3, int D>
@@ -629,13 +694,12 @@ cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws
     const int rows = batch * num_q_heads * q_len;
     if (rows == 0) return cudaSuccess;
     const dim3 grid((rows + 3) / 4);
+    __half *o = static_cast<__half *>(out);
     if (head_dim == 128)
-        combine_kernel<128><<<grid, 128, 0, stream>>>(ws_o, ws_m, ws_l, static_cast<__half *>(out),
-                                                      rows, q_len, num_q_heads, num_splits);
-    else
-        combine_kernel<64><<<grid, 128, 0, stream>>>(ws_o, ws_m, ws_l, static_cast<__half *>(out),
-                                                     rows, q_len, num_q_heads, num_splits);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<128>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o, rows,
+                          q_len, num_q_heads, num_splits);
+    return launch_pdl(combine_kernel<64>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o, rows,
+                      q_len, num_q_heads, num_splits);
 }
 
 }  // namespace kvq

@@ -19,6 +19,22 @@ __device__ __forceinline__ void report(int32_t *err_flag, int bits)
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel in the stream has
+// finished; it must call grid_dependency_wait() before touching any memory
+// that earlier work writes.  launch_dependents() lets the next kernel start
+// its own prologue early.  Both are no-ops when there is no such dependency.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // shared-memory addresses and mbarriers
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -183,6 +199,26 @@ __device__ __forceinline__ uint32_t dec_hi(uint32_t x)
 __device__ __forceinline__ uint32_t dec_lo(uint32_t x)
 {
     return dec_hi(x << 8);
+}
+
+// Hardware E4M3 -> fp16 conversion (exact: every E4M3 value is an fp16
+// value).  cvt_lo takes bytes 0,1 of x, cvt_hi bytes 2,3; the lower byte
+// becomes the lower half.  Unlike the bitcast decoder the result is the
+// value itself, not value * 2^-8.
+__device__ __forceinline__ uint32_t cvt_lo(uint32_t x)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+        : "=r"(d) : "r"(x));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t cvt_hi(uint32_t x)
+{
+    uint32_t d;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}"
+        : "=r"(d) : "r"(x));
+    return d;
 }
 
 }  // namespace kvq

@@ -25,8 +25,8 @@ struct AttnArgs {
     int32_t *err_flag;
     int32_t batch, q_len, num_q_heads, num_kv_heads, group, rows, num_splits;
     int32_t max_pages, max_topk;
-    float qk_scale_log2;         // hoisted: sm_scale * log2(e) [* k_scale * 2^8 for E4M3]
-    float out_scale;             // hoisted: v_scale * 2^8 for E4M3, 1 for fp16
+    float qk_scale_log2;         // hoisted: sm_scale * log2(e) [* k_scale for E4M3]
+    float out_scale;             // hoisted: v_scale for E4M3, 1 for fp16
 };
 
 struct WorkspaceLayout {
@@ -46,5 +46,25 @@ cudaError_t launch_append(bool e4m3, const void *k_new, const void *v_new,
 cudaError_t launch_amax(const void *x, int64_t n, float *amax_out, cudaStream_t stream);
 
 int device_sm_count();
+
+// Launch `kernel` on `stream` with programmatic stream serialisation, so that
+// it may begin while the previous kernel in the stream drains (the kernel
+// waits with griddepcontrol.wait before reading its inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace kvq

@@ -33,17 +33,19 @@ def to_dev(a, dtype=None):
     return t if dtype is None else t.to(dtype)
 
 
-def device_problem(pr: P.HostProblem, e4m3: bool = True) -> DeviceProblem:
+def device_problem(pr: P.HostProblem, e4m3: bool = True, sentinel: int = P.SENTINEL) -> DeviceProblem:
+    """Pools pre-filled with `sentinel` (a byte; for fp16 pools the 16-bit
+    pattern sentinel * 0x101), then filled by the library's append."""
     dev = torch.device("cuda")
     w = pr.w
     shape = (pr.P, w.num_kv_heads, 4, w.head_dim)
     if e4m3:
-        kc = torch.full(shape, P.SENTINEL, dtype=torch.uint8, device=dev)
-        vc = torch.full(shape, P.SENTINEL, dtype=torch.uint8, device=dev)
+        kc = torch.full(shape, sentinel, dtype=torch.uint8, device=dev)
+        vc = torch.full(shape, sentinel, dtype=torch.uint8, device=dev)
         ks = kvq.calibrate_scale(to_dev(pr.k_calib))
         vs = kvq.calibrate_scale(to_dev(pr.v_calib))
     else:
-        fill = torch.tensor(P.SENTINEL * 0x101, dtype=torch.int32).to(torch.int16)
+        fill = torch.tensor(sentinel * 0x101, dtype=torch.int32).to(torch.int16)
         kc = torch.empty(shape, dtype=torch.float16, device=dev)
         kc.view(torch.int16).fill_(int(fill))
         vc = kc.clone()

@@ -143,6 +143,20 @@ def test_shapes_match_oracle(lens, q_len, G_, D, e4m3):
         G.assert_close(out.float().cpu().numpy(), _oracle_out(dp), f"{lens} q{q_len} G{G_} D{D} S{S}")
 
 
+@pytest.mark.parametrize("e4m3", [True, False])
+@pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
+def test_nan_bits_in_unowned_slots_do_not_leak(name, e4m3):
+    """Unowned slots (the tail of each sequence's last page, pages nobody
+    owns) filled with NaN patterns: 0x7F (E4M3 NaN) or 0x7F7F (fp16 NaN)."""
+    dp = G.device_problem(P.host_problem(name), e4m3, sentinel=0x7F)
+    for S in (1, 2, 3):
+        out = G.run_attention(dp, num_splits=S)
+        torch.cuda.synchronize()
+        got = out.float().cpu().numpy()
+        assert np.isfinite(got).all()
+        G.assert_close(got, _oracle_out(dp), f"{name} e4m3={e4m3} S={S} NaN sentinel")
+
+
 def test_more_splits_than_pages_gives_empty_splits():
     dp = G.device_problem(P.host_problem("tiny"))
     out = G.run_attention(dp, num_splits=40)     # sequence 0 has 10 pages: 30 empty splits
