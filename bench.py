@@ -58,20 +58,42 @@ def _peaks():
 # ---------------------------------------------------------------------------
 # workload accounting
 
-def algorithmic_bytes(w, kv_elem_bytes: int, lens, step_tokens: int):
-    """Bytes the step must move at minimum: every cached K and V element once,
-    Q, the output, the block-table entries of the pages read, the context
-    lengths, and the append (fp16 in, cache dtype out, slot ids)."""
+def algorithmic_bytes(w, kv_elem_bytes: int, lens, step_tokens: int, topk=(None, None)):
+    """Bytes the step must move at minimum: every K and V element attended
+    once (all cached tokens of a dense sequence; the listed tokens of a top-k
+    sequence, plus its list and block-table entries), Q, the output, the
+    block-table entries of the pages read, the context lengths, and the
+    append (fp16 in, cache dtype out, slot ids)."""
     Hkv, D = w.num_kv_heads, w.head_dim
-    tokens = int(np.sum(lens))
-    pages = int(np.sum((np.asarray(lens, np.int64) + 3) // 4))
+    lens = np.asarray(lens, np.int64)
+    ti, tl = topk
+    dense = np.ones(lens.shape, bool) if tl is None else (np.asarray(tl) == 0)
+    tokens = int(lens[dense].sum())
+    pages = int(((lens[dense] + 3) // 4).sum())
     kv = 2 * tokens * Hkv * D * kv_elem_bytes
+    listed = 0 if tl is None else int(np.asarray(tl)[~dense].sum())     # per kv head
+    kv += 2 * listed * Hkv * D * kv_elem_bytes
+    lists = listed * Hkv * 4 * 2
     q = w.batch * w.q_len * w.num_q_heads * D * 2
     out = q
     bt = pages * 4 + w.batch * 4
     append = step_tokens * Hkv * D * 2 * (2 + kv_elem_bytes) + step_tokens * 4
-    attn = kv + q + bt
-    return {"step": kv + q + out + bt + append, "attention_kernel": attn}
+    attn = kv + q + bt + lists
+    return {"step": kv + q + out + bt + lists + append, "attention_kernel": attn}
+
+
+def describe(w, splits) -> str:
+    kind, *rest = w.lens.split(":")
+    ctx = {"fixed": lambda: f"{rest[0]} context", "list": lambda: f"contexts {rest[0]}",
+           "loguniform": lambda: f"contexts log-uniform {rest[0]}-{rest[1]}",
+           "uniform": lambda: f"contexts uniform {rest[0]}-{rest[1]}"}[kind]()
+    extra = ""
+    if w.topk:
+        extra += f", {int(round(w.topk_fraction * 100))}% of sequences over top-{w.topk} lists"
+    if w.prefill_chunk:
+        extra += f", {w.prefill_chunk}-token prefill chunk appended"
+    return (f"{w.name}: batch {w.batch}, {ctx}, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
+            f"head_dim {w.head_dim}, q_len {w.q_len}, split-K {splits}, page 4{extra}; one layer")
 
 
 # ---------------------------------------------------------------------------
@@ -164,6 +186,18 @@ class Arm:
         step_rows = torch.from_numpy(offs[ss] + sp).to(dev)
         self.k_new = k[step_rows].contiguous()
         self.v_new = v[step_rows].contiguous()
+        if w.prefill_chunk:
+            # the step also appends a new sequence's prefill chunk (mixed batches)
+            pk = inputs.prefill_tokens(w, 0, "k", device=dev)
+            pv = inputs.prefill_tokens(w, 0, "v", device=dev)
+            pslots = torch.from_numpy(inputs.prefill_slots(lay)[: w.prefill_chunk]).to(dev)
+            self.k_new = torch.cat([self.k_new, pk]).contiguous()
+            self.v_new = torch.cat([self.v_new, pv]).contiguous()
+            self.step_slots = torch.cat([self.step_slots, pslots]).contiguous()
+        ti, tl = inputs.topk_lists(w, lay.lens)
+        self.topk_idx = None if ti is None else torch.from_numpy(ti).to(dev)
+        self.topk_lens = None if tl is None else torch.from_numpy(tl).to(dev)
+        self.topk_np = (ti, tl)
         self.bt = torch.from_numpy(lay.block_tables).to(dev)
         self.cl = torch.from_numpy(lay.lens).to(dev)
         shape = (lay.num_pages, w.num_kv_heads, 4, w.head_dim)
@@ -178,13 +212,15 @@ class Arm:
             self._append(kh, vh, hist_slots, kc, vc)
             self.pools.append((kc, vc))
         del k, v, kh, vh
-        self.p = kvq.attn_params(self.q, w.num_kv_heads, self.bt.shape[1], w.num_splits)
+        self.p = kvq.attn_params(self.q, w.num_kv_heads, self.bt.shape[1], w.num_splits,
+                                 0 if self.topk_idx is None else self.topk_idx.shape[2])
         self.S = kvq.num_splits(self.p)
         self.ws = kvq.alloc_workspace(self.p, dev)
         self.out = torch.empty_like(self.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.pool_bytes = pool_bytes
-        self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, w.batch * w.q_len)
+        self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, int(self.step_slots.numel()),
+                                       self.topk_np)
         torch.cuda.synchronize(dev)
 
     def _append(self, k, v, slots, kc, vc):
@@ -200,10 +236,11 @@ class Arm:
         cl = self.cl if cl is None else cl
         if self.e4m3:
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
-                                               num_splits=self.S, err_flag=self.err)
-        else:
-            kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, num_splits=self.S,
+                                               self.topk_idx, self.topk_lens, num_splits=self.S,
                                                err_flag=self.err)
+        else:
+            kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, self.topk_idx,
+                                               self.topk_lens, num_splits=self.S, err_flag=self.err)
 
     def step(self, i, ev=None):
         kc, vc = self.pools[i % self.copies]
@@ -510,9 +547,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": f"{w.name}: batch {w.batch} x {w.lens.split(':')[1]} context, "
-                                   f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, head_dim "
-                                   f"{w.head_dim}, q_len {w.q_len}, split-K {arm.S}, page 4",
+            "config": {"workload": describe(w, arm.S),
                        "global_batch": world * w.batch, "kv_dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
                        "l2": f"rotating {arm.copies} KV pool copies of {arm.pool_bytes / 1e6:.0f} MB "
                              f"(> 2 x L2 {l2 / 1e6:.0f} MB)",

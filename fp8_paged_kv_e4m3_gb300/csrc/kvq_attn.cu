@@ -11,13 +11,16 @@
 // and merged by a log-sum-exp combine.
 //
 // GB300 design (one CTA per (split, kv head, sequence), 4 consumer warps and
-// 1 producer warp):
-//  * The producer walks the split's pages one stage at a time (16 pages for
-//    one query-row group, 8 otherwise), reads the block table a batch ahead,
-//    and issues one 1-D bulk TMA copy per page for K and for V (a page of one
-//    kv head = 4 * head_dim contiguous elements) into a ring of about 50 KB
-//    of shared memory, each stage completing on its own mbarrier.  In top-k
-//    mode a stage is 4 tokens per page slot, each fetched as one row.
+// 2 producer warps):
+//  * Two producer warps walk the split's pages one stage at a time (16 pages
+//    for one query-row group, 8 otherwise), read the block table a batch
+//    ahead, and issue one 1-D bulk TMA copy per page -- one warp for K, the
+//    other for V (a page of one kv head = 4 * head_dim contiguous elements)
+//    -- into a ring of about 50 KB of shared memory, each stage completing
+//    on its own mbarrier.  A single warp issues bulk copies at a limited
+//    rate (about 27 million per second measured on GB300, whatever their
+//    size), so splitting K and V doubles the CTA's copy rate.  In top-k mode
+//    a stage is 4 tokens per page slot, each fetched as one row.
 //  * Every consumer warp takes part in every stage: warp w owns one (or, for
 //    64 query rows, two) 16-token tiles of the stage and one group of query
 //    rows.  Each warp therefore waits on every phase of every ring slot in
@@ -52,7 +55,8 @@ namespace kvq {
 #endif
 
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kProducerWarps = 2;   // K pages and V pages
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -96,7 +100,7 @@ constexpr int smem_bytes()
 {
     using W = Split<NT, RW>;
     using G = Geometry<E4M3, D, W::kPagesPerStage>;
-    constexpr int merge = W::kTokWarps * W::kRowsPad * (D + 2) * 4;
+    constexpr int merge = (W::kTokWarps * W::kRowsPad * (D + 2) + W::kRowsPad * W::kTokWarps) * 4;
     return G::kBytes > merge ? G::kBytes : merge;
 }
 
@@ -110,7 +114,8 @@ __device__ __forceinline__ int2 pv_channels(int pv, int gid)
 }
 
 template <bool E4M3, int D, int NT, int RW>
-__global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
+    attn_split_kernel(const AttnArgs a)
 {
     using W = Split<NT, RW>;
     constexpr int PPS = W::kPagesPerStage;
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
     // barriers first: this part reads no input and overlaps the previous kernel's tail
     if (threadIdx.x == 0) {
         for (int k = 0; k < G::kStages; ++k) {
-            mbar_init(bar0 + 8 * k, 1);
+            mbar_init(bar0 + 8 * k, kProducerWarps);   // one arrive.expect_tx per producer
             mbar_init(bar0 + 8 * (G::kStages + k), kConsumerWarps);
         }
         *abort_flag = 0;
@@ -140,6 +145,14 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
     launch_dependents();      // the combine may start launching; it waits for our completion
 
     // ---- work of this CTA --------------------------------------------------
+    // The producers' first block-table batch is fetched speculatively for a
+    // sequence that fills its block-table row, in parallel with the context
+    // length; it is refetched below if the real split starts elsewhere.
+    const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
+    const int spec_per = (a.max_pages + a.num_splits - 1) / a.num_splits;
+    const int spec0 = min(s * spec_per, a.max_pages);
+    int bt_spec = -1;
+    if (warp >= kConsumerWarps && spec0 + lane < a.max_pages) bt_spec = __ldg(bt_row + spec0 + lane);
     const int L = a.context_lens[b];
     const bool len_ok = (L >= a.q_len) && (L <= a.max_pages * 4);
     int topk_n = (a.topk_idx && a.topk_lens) ? a.topk_lens[b] : 0;
@@ -172,22 +185,23 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
     }
     const int gid = lane >> 2, t = lane & 3;
     const int rw = warp % RW, tw = warp / RW;
-    int issued = 0;   // stages the producer has issued
+    int issued = 0;   // stages this producer has issued
 
-    if (warp == kConsumerWarps) {
-        // ================= producer =================
+    if (warp >= kConsumerWarps) {
+        // ================= producers: the first moves K, the second V =================
         const uint64_t pol = l2_policy_evict_first();
-        const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
+        const bool is_v = warp == kConsumerWarps + 1;
+        const uint8_t *pool = static_cast<const uint8_t *>(is_v ? a.v_cache : a.k_cache);
         if (!topk) {
             constexpr int SPB = 32 / PPS;                 // stages per block-table batch
             auto load_bt = [&](int first) -> int {
                 const int it = first + lane;
                 return it < item1 ? __ldg(bt_row + it) : -1;
             };
-            int bt_cur = load_bt(item0), bt_nxt = load_bt(item0 + 32);
+            int bt_cur = (item0 == spec0) ? (item0 + lane < item1 ? bt_spec : -1) : load_bt(item0);
+            int bt_nxt = load_bt(item0 + 32);
             const int p = lane % PPS;                      // page of the stage this lane copies
-            const bool is_v = lane >= PPS;
-            const bool copier = lane < 2 * PPS;
+            const bool copier = lane < PPS;
             for (int st = 0; st < nst; ++st) {
                 const int slot = st % G::kStages;
                 if (st >= G::kStages &&
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                 const int phys = __shfl_sync(kFull, bt_cur, (st % SPB) * PPS + p);
                 const bool exists = item < item1;
                 const bool valid = exists && phys >= 0 && (int64_t)phys < a.num_pages;
-                if (lane < PPS) {
+                if (!is_v && lane < PPS) {
                     if (exists && !valid) {
                         report(a.err_flag, KVQ_DEV_BAD_PAGE);
                         *stage_bad = 1;
@@ -218,8 +232,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                 if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, __popc(vmask) * G::kChunk);
                 __syncwarp();
                 if (copier && valid) {
-                    const uint8_t *base = static_cast<const uint8_t *>(is_v ? a.v_cache : a.k_cache);
-                    const uint8_t *src = base + ((int64_t)phys * a.num_kv_heads + g) * G::kChunk;
+                    const uint8_t *src = pool + ((int64_t)phys * a.num_kv_heads + g) * G::kChunk;
                     const uint32_t dst = ring + slot * G::kStageBytes + (is_v ? G::kRegion : 0) +
                                          p * G::kPageStride;
                     tma_load_1d(dst, src, G::kChunk, bar0 + 8 * slot, pol);
@@ -261,13 +274,15 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                     const bool exists = item0 + st * G::kTokPerStage + e < item1;
                     const bool idx_ok = exists && idx_cur[r] >= 0 && idx_cur[r] < L;
                     valid[r] = idx_ok && pg_cur[r] >= 0 && (int64_t)pg_cur[r] < a.num_pages;
-                    if (exists && !idx_ok) report(a.err_flag, KVQ_DEV_BAD_TOPK);
-                    if (idx_ok && !valid[r]) report(a.err_flag, KVQ_DEV_BAD_PAGE);
-                    tokpos[slot * G::kTokPerStage + e] = valid[r] ? idx_cur[r] : -1;
+                    if (!is_v) {
+                        if (exists && !idx_ok) report(a.err_flag, KVQ_DEV_BAD_TOPK);
+                        if (idx_ok && !valid[r]) report(a.err_flag, KVQ_DEV_BAD_PAGE);
+                        tokpos[slot * G::kTokPerStage + e] = valid[r] ? idx_cur[r] : -1;
+                    }
                     cnt += __popc(__ballot_sync(kFull, valid[r]));
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, cnt * 2 * G::kRowBytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, cnt * G::kRowBytes);
                 __syncwarp();
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
@@ -275,13 +290,9 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
                         const int e = r * 32 + lane;
                         const int64_t row =
                             ((int64_t)pg_cur[r] * a.num_kv_heads + g) * 4 + (idx_cur[r] & 3);
-                        const uint32_t dst = ring + slot * G::kStageBytes + (e >> 2) * G::kPageStride +
-                                             (e & 3) * G::kRowBytes;
-                        tma_load_1d(dst, static_cast<const uint8_t *>(a.k_cache) + row * G::kRowBytes,
-                                    G::kRowBytes, bar0 + 8 * slot, pol);
-                        tma_load_1d(dst + G::kRegion,
-                                    static_cast<const uint8_t *>(a.v_cache) + row * G::kRowBytes,
-                                    G::kRowBytes, bar0 + 8 * slot, pol);
+                        const uint32_t dst = ring + slot * G::kStageBytes + (is_v ? G::kRegion : 0) +
+                                             (e >> 2) * G::kPageStride + (e & 3) * G::kRowBytes;
+                        tma_load_1d(dst, pool + row * G::kRowBytes, G::kRowBytes, bar0 + 8 * slot, pol);
                     }
                     idx_cur[r] = idx_nxt[r];
                     pg_cur[r] = pg_nxt[r];
@@ -527,10 +538,10 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
         // Something gave up: before the CTA's shared memory is released, wait
         // (bounded) for every copy the producer issued, then leave without
         // writing.  The error bit is already set.
-        if (warp == kConsumerWarps && lane == 0)
+        if (warp >= kConsumerWarps && lane == 0)   // each producer: the stages it issued
             for (int st = max(0, issued - G::kStages); st < issued; ++st)
                 mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr,
-                                  a.err_flag);
+                                  a.err_flag, 100000000ull);
         __syncthreads();
         return;
     }
@@ -556,36 +567,56 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a)
             }
     }
     __syncthreads();
+    // Per row: the merge weights of the token warps (w_q / l, v_scale folded
+    // in), and the split's m and l; an empty row gets m = -inf, l = 0 and no
+    // output.
+    constexpr int TW = W::kTokWarps;
     const int S = a.num_splits;
     // the bitcast decoder yields V * 2^-8; the hardware conversion V itself
     constexpr float kVFold = (E4M3 && !KVQ_V_CVT) ? 256.f : 1.f;
-    for (int idx = threadIdx.x; idx < a.rows * D; idx += kThreads) {
-        const int row = idx / D, d = idx % D;
+    float *coef = mbuf + TW * W::kRowsPad * kRowF;        // [kRowsPad][TW]
+    for (int row = threadIdx.x; row < a.rows; row += kThreads) {
         float M = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < W::kTokWarps; ++q) M = fmaxf(M, mbuf[(q * W::kRowsPad + row) * kRowF]);
+        for (int q = 0; q < TW; ++q) M = fmaxf(M, mbuf[(q * W::kRowsPad + row) * kRowF]);
         const int i = row / a.group, h = g * a.group + row % a.group;
         const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
-        if (M == -INFINITY) {
-            if (d == 0) {
-                a.ws_m[unit] = -INFINITY;
-                a.ws_l[unit] = 0.f;
-            }
-            continue;
-        }
-        float lsum = 0.f, osum = 0.f;
+        float w[TW];
+        float lsum = 0.f;
 #pragma unroll
-        for (int q = 0; q < W::kTokWarps; ++q) {
+        for (int q = 0; q < TW; ++q) {
             const float *src = mbuf + (q * W::kRowsPad + row) * kRowF;
-            const float w = fast_exp2(src[0] - M);
-            lsum += w * src[1];
-            osum += w * src[2 + d];
+            w[q] = (M == -INFINITY) ? 0.f : fast_exp2(src[0] - M);
+            lsum += w[q] * src[1];
         }
-        a.ws_o[unit * D + d] = osum / lsum * (a.out_scale * kVFold);
-        if (d == 0) {
-            a.ws_m[unit] = M * kLn2;
-            a.ws_l[unit] = lsum;
+        const float inv = lsum > 0.f ? a.out_scale * kVFold / lsum : 0.f;
+#pragma unroll
+        for (int q = 0; q < TW; ++q) coef[row * TW + q] = w[q] * inv;
+        a.ws_m[unit] = lsum > 0.f ? M * kLn2 : -INFINITY;
+        a.ws_l[unit] = lsum;
+    }
+    __syncthreads();
+    // o = sum_q coef_q * o_q, four channels per thread, stored as float4
+    for (int idx = threadIdx.x * 4; idx < a.rows * D; idx += kThreads * 4) {
+        const int row = idx / D, d = idx % D;
+        const float *cf = coef + row * TW;
+        bool any = false;
+#pragma unroll
+        for (int q = 0; q < TW; ++q) any |= cf[q] != 0.f;
+        if (!any) continue;                        // empty row: tmp_out stays unwritten
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < TW; ++q) {
+            const float c = cf[q];
+            const float *src = mbuf + (q * W::kRowsPad + row) * kRowF + 2 + d;
+            acc.x += c * src[0];
+            acc.y += c * src[1];
+            acc.z += c * src[2];
+            acc.w += c * src[3];
         }
+        const int i = row / a.group, h = g * a.group + row % a.group;
+        const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
+        *reinterpret_cast<float4 *>(a.ws_o + unit * D + d) = acc;
     }
 }
 
