@@ -112,8 +112,9 @@ def describe(w, splits) -> str:
         extra += f", {int(round(w.topk_fraction * 100))}% of sequences over top-{w.topk} lists"
     if w.prefill_chunk:
         extra += f", {w.prefill_chunk}-token prefill chunk appended"
+    split = f"split-K {splits}" + (f" of {w.split_pages} pages" if w.split_pages else "")
     return (f"{w.name}: batch {w.batch}, {ctx}, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
-            f"head_dim {w.head_dim}, q_len {w.q_len}, split-K {splits}, page 4{extra}; one layer")
+            f"head_dim {w.head_dim}, q_len {w.q_len}, {split}, page 4{extra}; one layer")
 
 
 # ---------------------------------------------------------------------------
@@ -233,7 +234,8 @@ class Arm:
             self.pools.append((kc, vc))
         del k, v, kh, vh
         self.p = kvq.attn_params(self.q, w.num_kv_heads, self.bt.shape[1], w.num_splits,
-                                 0 if self.topk_idx is None else self.topk_idx.shape[2])
+                                 0 if self.topk_idx is None else self.topk_idx.shape[2],
+                                 split_pages=w.split_pages)
         self.S = kvq.num_splits(self.p)
         self.ws = kvq.alloc_workspace(self.p, dev)
         self.out = torch.empty_like(self.q)
@@ -257,10 +259,11 @@ class Arm:
         if self.e4m3:
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
-                                               err_flag=self.err)
+                                               err_flag=self.err, split_pages=self.w.split_pages)
         else:
             kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, self.topk_idx,
-                                               self.topk_lens, num_splits=self.S, err_flag=self.err)
+                                               self.topk_lens, num_splits=self.S, err_flag=self.err,
+                                               split_pages=self.w.split_pages)
 
     def step(self, i, ev=None):
         kc, vc = self.pools[i % self.copies]

@@ -40,12 +40,21 @@ int device_sm_count()
     return n;
 }
 
+// Fewest fixed-size splits that give every page and list entry a split.
+static int64_t splits_to_cover(const kvq_attn_params *p)
+{
+    const int64_t sp = p->split_pages;
+    int64_t s = (int64_t(p->max_pages_per_seq) + sp - 1) / sp;
+    const int64_t t = (int64_t(p->max_topk) + 4 * sp - 1) / (4 * sp);
+    return s > t ? s : t;
+}
+
 // shape checks shared by every attention entry point; KVQ_OK or an error
 static int check_params(const kvq_attn_params *p)
 {
     if (!p) return KVQ_ERR_INVALID_ARG;
     if (p->batch < 0 || p->q_len < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
-        p->num_splits < 0 || p->max_pages_per_seq < 1 || p->max_topk < 0)
+        p->num_splits < 0 || p->max_pages_per_seq < 1 || p->max_topk < 0 || p->split_pages < 0)
         return KVQ_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
     if (!std::isfinite(p->sm_scale) || p->sm_scale < 0.0f) return KVQ_ERR_INVALID_ARG;
@@ -55,12 +64,21 @@ static int check_params(const kvq_attn_params *p)
     if (rows > 64) return KVQ_ERR_UNSUPPORTED;
     if (p->batch > 65535 || p->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (int64_t(p->max_pages_per_seq) * 4 > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+    // fixed-size splits must give every page and list entry a split
+    if (p->split_pages > 0 && p->num_splits > 0 && splits_to_cover(p) > p->num_splits)
+        return KVQ_ERR_INVALID_ARG;
+    if (p->split_pages > 0 && p->num_splits == 0 && splits_to_cover(p) > 65535)
+        return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
 }
 
 static int32_t resolve_splits(const kvq_attn_params *p)
 {
     if (p->num_splits > 0) return p->num_splits;
+    if (p->split_pages > 0) {
+        const int64_t s = splits_to_cover(p);   // <= 65535 (checked)
+        return int32_t(s < 1 ? 1 : s);
+    }
     // Enough CTAs for a few waves of the resident slots (about 3 CTAs per SM),
     // but no split shorter than 16 pages.
     const int64_t pairs = int64_t(p->batch > 0 ? p->batch : 1) * p->num_kv_heads;
@@ -135,6 +153,7 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.group = G;
     a.rows = G * p.q_len;
     a.num_splits = S;
+    a.split_pages = p.split_pages;
     a.max_pages = p.max_pages_per_seq;
     a.max_topk = c.topk_idx ? p.max_topk : 0;
     // hoisted per-layer scales (the kernel folds any decoder factor itself)

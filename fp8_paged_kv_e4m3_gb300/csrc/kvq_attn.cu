@@ -149,8 +149,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     // sequence that fills its block-table row, in parallel with the context
     // length; it is refetched below if the real split starts elsewhere.
     const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
-    const int spec_per = (a.max_pages + a.num_splits - 1) / a.num_splits;
-    const int spec0 = min(s * spec_per, a.max_pages);
+    const int64_t spec_per = a.split_pages > 0 ? (int64_t)a.split_pages
+                                               : (int64_t)(a.max_pages + a.num_splits - 1) / a.num_splits;
+    const int spec0 = (int)min((int64_t)s * spec_per, (int64_t)a.max_pages);
     int bt_spec = -1;
     if (warp >= kConsumerWarps && spec0 + lane < a.max_pages) bt_spec = __ldg(bt_row + spec0 + lane);
     const int L = a.context_lens[b];
@@ -159,9 +160,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     const bool topk = len_ok && topk_n > 0;
     if (topk && topk_n > a.max_topk) topk_n = a.max_topk;
     const int n_items = !len_ok ? 0 : (topk ? topk_n : (L + 3) / 4);   // pages or list entries
-    const int per = (n_items + a.num_splits - 1) / a.num_splits;
-    const int item0 = min(s * per, n_items);
-    const int item1 = min(item0 + per, n_items);
+    // split s covers items [s * per, (s + 1) * per): an equal share of this
+    // sequence, or a fixed number of pages (4 list entries per page)
+    const int64_t per = a.split_pages > 0 ? (topk ? 4 * (int64_t)a.split_pages : (int64_t)a.split_pages)
+                                          : (int64_t)(n_items + a.num_splits - 1) / a.num_splits;
+    const int item0 = (int)min((int64_t)s * per, (int64_t)n_items);
+    const int item1 = (int)min(item0 + per, (int64_t)n_items);
     const int ipst = topk ? G::kTokPerStage : PPS;        // items per stage
     const int nst = (item1 - item0 + ipst - 1) / ipst;
 
@@ -621,8 +625,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp combine: one warp per (b, h, i) row.
-template <int D>
+// Log-sum-exp combine.  WPR warps per (b, h, i) row (4 rows of one warp each,
+// or one row of 4 warps for long split lists): every warp finds the row's
+// M = max m_s and W = sum l_s exp(m_s - M) with the lanes reading the splits'
+// (m, l) side by side; warp w then sums w_s * o_s over splits w, w + WPR, ...
+// with independent loads in flight, and the warps add their sums in shared
+// memory.
+template <int D, int WPR>
 __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws_o,
                                                       const float *__restrict__ ws_m,
                                                       const float *__restrict__ ws_l,
@@ -630,40 +639,80 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
                                                       int num_q_heads, int S)
 {
     constexpr int V = D / 32;   // channels per lane (4 or 2)
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    constexpr int kRowsPerCta = 4 / WPR;
+    constexpr int kUnroll = 4;
+    __shared__ float red[WPR > 1 ? WPR - 1 : 1][D];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kRowsPerCta + warp / WPR;
+    const int wr = warp % WPR;   // this warp's share of the splits
     grid_dependency_wait();   // the partials come from the attention kernel
     launch_dependents();
-    if (row >= rows) return;
+    const bool live = row < rows;
     const float *m = ws_m + (int64_t)row * S;
     const float *l = ws_l + (int64_t)row * S;
+    // row max over the non-empty splits, lanes striding over s
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s)
-        if (l[s] > 0.f) M = fmaxf(M, m[s]);
+    if (live)
+        for (int s = lane; s < S; s += 32)
+            if (l[s] > 0.f) M = fmaxf(M, m[s]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float W = 0.f;
+    if (live && M != -INFINITY)
+        for (int s = lane; s < S; s += 32) {
+            const float ls = l[s];
+            if (ls > 0.f) W += ls * fast_exp2((m[s] - M) * 1.4426950408889634f);
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(kFull, W, off);
+
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    float W = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
-            const float ls = l[s];
-            if (!(ls > 0.f)) continue;
-            const float w = ls * fast_exp2((m[s] - M) * 1.4426950408889634f);
-            W += w;
-            const float *src = ws_o + ((int64_t)row * S + s) * D + lane * V;
-            if (V == 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(src);
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
-                acc[2] += w * x.z;
-                acc[3] += w * x.w;
-            } else {
-                const float2 x = *reinterpret_cast<const float2 *>(src);
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
+    if (live && M != -INFINITY) {
+        const float *src0 = ws_o + (int64_t)row * S * D + lane * V;
+        for (int s0 = wr; s0 < S; s0 += WPR * kUnroll) {
+            float w[kUnroll];
+            float x[kUnroll][V];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int s = s0 + u * WPR;
+                const float ls = s < S ? l[s] : 0.f;
+                w[u] = ls > 0.f ? ls * fast_exp2((m[s] - M) * 1.4426950408889634f) : 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v) x[u][v] = 0.f;
+                if (w[u] != 0.f) {   // empty splits leave tmp_out unwritten: never read it
+                    if (V == 4) {
+                        const float4 t4 = *reinterpret_cast<const float4 *>(src0 + (int64_t)s * D);
+                        x[u][0] = t4.x;
+                        x[u][1] = t4.y;
+                        x[u][2] = t4.z;
+                        x[u][3] = t4.w;
+                    } else {
+                        const float2 t2 = *reinterpret_cast<const float2 *>(src0 + (int64_t)s * D);
+                        x[u][0] = t2.x;
+                        x[u][1] = t2.y;
+                    }
+                }
             }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v] += w[u] * x[u][v];
         }
     }
+    if (WPR > 1) {
+        if (wr > 0)
+#pragma unroll
+            for (int v = 0; v < V; ++v) red[wr - 1][lane * V + v] = acc[v];
+        __syncthreads();
+        if (wr > 0) return;
+#pragma unroll
+        for (int q = 0; q < WPR - 1; ++q)
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] += red[q][lane * V + v];
+    }
+    if (!live) return;
     const float inv = W > 0.f ? 1.f / W : 0.f;
     // row = (b * Hq + h) * q_len + i  ->  out[b][i][h][:]
     const int i = row % q_len;
@@ -671,10 +720,10 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     const int h = bh % num_q_heads, b = bh / num_q_heads;
     __half *dst = out + (((int64_t)b * q_len + i) * num_q_heads + h) * D + lane * V;
     if (V == 4) {
-        uint2 w;
-        w.x = pack_half2(acc[0] * inv, acc[1] * inv);
-        w.y = pack_half2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2 *>(dst) = w;
+        uint2 o2;
+        o2.x = pack_half2(acc[0] * inv, acc[1] * inv);
+        o2.y = pack_half2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = o2;
     } else {
         *reinterpret_cast<uint32_t *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
     }
@@ -724,12 +773,20 @@ cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws
 {
     const int rows = batch * num_q_heads * q_len;
     if (rows == 0) return cudaSuccess;
-    const dim3 grid((rows + 3) / 4);
     __half *o = static_cast<__half *>(out);
+    if (num_splits >= 16) {   // one row per CTA, four warps over its splits
+        const dim3 grid(rows);
+        if (head_dim == 128)
+            return launch_pdl(combine_kernel<128, 4>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o,
+                              rows, q_len, num_q_heads, num_splits);
+        return launch_pdl(combine_kernel<64, 4>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o,
+                          rows, q_len, num_q_heads, num_splits);
+    }
+    const dim3 grid((rows + 3) / 4);
     if (head_dim == 128)
-        return launch_pdl(combine_kernel<128>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o, rows,
-                          q_len, num_q_heads, num_splits);
-    return launch_pdl(combine_kernel<64>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o, rows,
+        return launch_pdl(combine_kernel<128, 1>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o,
+                          rows, q_len, num_q_heads, num_splits);
+    return launch_pdl(combine_kernel<64, 1>, grid, dim3(128), 0, stream, ws_o, ws_m, ws_l, o, rows,
                       q_len, num_q_heads, num_splits);
 }
 

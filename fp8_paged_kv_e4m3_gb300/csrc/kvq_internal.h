@@ -24,6 +24,7 @@ struct AttnArgs {
     float *ws_l;                 // [B][Hq][q_len][S]
     int32_t *err_flag;
     int32_t batch, q_len, num_q_heads, num_kv_heads, group, rows, num_splits;
+    int32_t split_pages;   // 0 = equal division of each sequence, else pages per split
     int32_t max_pages, max_topk;
     float qk_scale_log2;         // hoisted: sm_scale * log2(e) [* k_scale for E4M3]
     float out_scale;             // hoisted: v_scale for E4M3, 1 for fp16

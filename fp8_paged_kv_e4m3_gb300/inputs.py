@@ -60,6 +60,7 @@ class Workload:
     prefill_chunk: int = 0        # extra tokens appended for one new sequence
     spare_pages: float = 0.125    # pool slack beyond the pages in use
     seed: int = 0
+    split_pages: int = 0          # 0 = equal split division; > 0 = pages per split
 
     @property
     def group(self) -> int:

@@ -40,7 +40,7 @@ class AttnParams(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("max_topk", ctypes.c_int32),
-                ("sm_scale", ctypes.c_float)]
+                ("sm_scale", ctypes.c_float), ("split_pages", ctypes.c_int32)]
 
 
 EXPORTS = ("kvq_version", "kvq_status_string", "kvq_validate_scales", "kvq_amax_f16",
@@ -197,10 +197,10 @@ def kv_append_fp16(k_new, v_new, slot_mapping, k_cache, v_cache,
 # attention
 
 def attn_params(q: torch.Tensor, num_kv_heads: int, max_pages_per_seq: int, num_splits: int = 0,
-                max_topk: int = 0, sm_scale: float = 0.0) -> AttnParams:
+                max_topk: int = 0, sm_scale: float = 0.0, split_pages: int = 0) -> AttnParams:
     B, q_len, Hq, D = q.shape
     return AttnParams(B, q_len, Hq, num_kv_heads, D, num_splits, max_pages_per_seq, max_topk,
-                      sm_scale)
+                      sm_scale, split_pages)
 
 
 def num_splits(p: AttnParams) -> int:
@@ -236,7 +236,7 @@ def workspace_views(ws: torch.Tensor, p: AttnParams):
 
 
 def _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
-                topk_lens, cache_dtype, num_splits_, sm_scale):
+                topk_lens, cache_dtype, num_splits_, sm_scale, split_pages):
     _need(q, "q", torch.float16, 4)
     B, q_len, Hq, D = q.shape
     _need(k_cache, "k_cache", cache_dtype, 4)
@@ -263,16 +263,18 @@ def _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out,
         if topk_idx.shape[:2] != (B, Hkv) or topk_lens.shape[0] != B:
             raise ValueError("topk_idx must be [B, Hkv, K], topk_lens [B]")
         max_topk = topk_idx.shape[2]
-    p = AttnParams(B, q_len, Hq, Hkv, D, num_splits_, block_tables.shape[1], max_topk, sm_scale)
+    p = AttnParams(B, q_len, Hq, Hkv, D, num_splits_, block_tables.shape[1], max_topk, sm_scale,
+                   split_pages)
     return p
 
 
 def paged_decode_attn_e4m3(q, k_cache, v_cache, block_tables, context_lens, k_scale: float,
                            v_scale: float, workspace, out=None, topk_idx=None, topk_lens=None,
-                           num_splits: int = 0, sm_scale: float = 0.0, err_flag=None):
+                           num_splits: int = 0, sm_scale: float = 0.0, err_flag=None,
+                           split_pages: int = 0):
     """Decode / verify attention over E4M3 pools; returns `out` (fp16, shape of q)."""
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
-                    topk_lens, torch.uint8, num_splits, sm_scale)
+                    topk_lens, torch.uint8, num_splits, sm_scale, split_pages)
     if out is None:
         out = torch.empty_like(q)
     _check("paged_decode_attn_e4m3", load().paged_decode_attn_e4m3(
@@ -285,10 +287,10 @@ def paged_decode_attn_e4m3(q, k_cache, v_cache, block_tables, context_lens, k_sc
 
 def paged_decode_attn_fp16(q, k_cache, v_cache, block_tables, context_lens, workspace, out=None,
                            topk_idx=None, topk_lens=None, num_splits: int = 0,
-                           sm_scale: float = 0.0, err_flag=None):
+                           sm_scale: float = 0.0, err_flag=None, split_pages: int = 0):
     """fp16-KV twin of paged_decode_attn_e4m3."""
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
-                    topk_lens, torch.float16, num_splits, sm_scale)
+                    topk_lens, torch.float16, num_splits, sm_scale, split_pages)
     if out is None:
         out = torch.empty_like(q)
     _check("paged_decode_attn_fp16", load().paged_decode_attn_fp16(
@@ -301,9 +303,9 @@ def paged_decode_attn_fp16(q, k_cache, v_cache, block_tables, context_lens, work
 def paged_decode_attn_e4m3_partial(q, k_cache, v_cache, block_tables, context_lens,
                                    k_scale: float, v_scale: float, workspace, topk_idx=None,
                                    topk_lens=None, num_splits: int = 0, sm_scale: float = 0.0,
-                                   err_flag=None) -> AttnParams:
+                                   err_flag=None, split_pages: int = 0) -> AttnParams:
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, None, topk_idx,
-                    topk_lens, torch.uint8, num_splits, sm_scale)
+                    topk_lens, torch.uint8, num_splits, sm_scale, split_pages)
     _check("paged_decode_attn_e4m3_partial", load().paged_decode_attn_e4m3_partial(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
         _ptr(context_lens), ctypes.c_float(k_scale), ctypes.c_float(v_scale), _ptr(topk_idx),
@@ -314,9 +316,10 @@ def paged_decode_attn_e4m3_partial(q, k_cache, v_cache, block_tables, context_le
 
 def paged_decode_attn_fp16_partial(q, k_cache, v_cache, block_tables, context_lens, workspace,
                                    topk_idx=None, topk_lens=None, num_splits: int = 0,
-                                   sm_scale: float = 0.0, err_flag=None) -> AttnParams:
+                                   sm_scale: float = 0.0, err_flag=None,
+                                   split_pages: int = 0) -> AttnParams:
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, None, topk_idx,
-                    topk_lens, torch.float16, num_splits, sm_scale)
+                    topk_lens, torch.float16, num_splits, sm_scale, split_pages)
     _check("paged_decode_attn_fp16_partial", load().paged_decode_attn_fp16_partial(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
         _ptr(context_lens), _ptr(topk_idx), _ptr(topk_lens), _ptr(workspace),

@@ -146,12 +146,20 @@ int kv_append_fp16(const void *k_new, const void *v_new, const int32_t *slot_map
  * rows is causal inside itself: MTP3 verifies one target token and three
  * drafts in one pass ([P1] Purpose).  An empty J gives a zero row.
  *
- * Split-K: the work of each (b, g) is cut into num_splits parts -- logical
- * pages [s*c, (s+1)*c) with c = ceil(ceil(L/4) / num_splits), or top-k list
- * entries [s*c, (s+1)*c) with c = ceil(topk_lens[b] / num_splits) -- whose
+ * Split-K: the work of each (b, g) is cut into num_splits parts whose
  * partial results go to an FP32 workspace ([P1] Status and history and
  * [P3] Problem: the page-4 route's temporary output must be FP32) and are
- * merged by a log-sum-exp combine.
+ * merged by a log-sum-exp combine.  Split s covers
+ *   split_pages == 0 (equal division of each sequence):
+ *     logical pages [s*c, (s+1)*c), c = ceil(ceil(L/4) / num_splits), or
+ *     top-k list entries [s*c, (s+1)*c), c = ceil(topk_lens[b] / num_splits);
+ *   split_pages  > 0 (fixed-size splits, for batches of mixed lengths):
+ *     logical pages [s*split_pages, (s+1)*split_pages), or top-k list entries
+ *     [s*4*split_pages, (s+1)*4*split_pages); splits past a sequence's end
+ *     are empty, so a short sequence uses few splits and a long one many,
+ *     and every split does about the same work.
+ * The pages leave the partition open; any partition gives the same result
+ * up to rounding.
  */
 typedef struct {
     int32_t batch;             /* B: sequences in the call                            */
@@ -163,10 +171,17 @@ typedef struct {
     int32_t max_pages_per_seq; /* row stride of block_tables                           */
     int32_t max_topk;          /* row length of topk_idx; 0 when no top-k list is used */
     float sm_scale;            /* softmax temperature; 0 = 1/sqrt(head_dim)            */
+    int32_t split_pages;       /* 0 = equal division; > 0 = pages per split (above).
+                                  Needs num_splits * split_pages >= max_pages_per_seq
+                                  and num_splits * 4 * split_pages >= max_topk, so
+                                  that every page and list entry has a split;
+                                  otherwise the call returns KVQ_ERR_INVALID_ARG */
 } kvq_attn_params;
 
-/* The split count a call with these parameters uses: p->num_splits if > 0,
- * else a count chosen from the shape and the current device's SM count.
+/* The split count a call with these parameters uses: p->num_splits if > 0;
+ * else, with split_pages > 0, the fewest splits that cover max_pages_per_seq
+ * pages and max_topk list entries; else a count chosen from the shape and
+ * the current device's SM count.
  * Returns a value >= 1, or a negative kvq_status for invalid parameters. */
 int32_t kvq_attn_num_splits(const kvq_attn_params *p);
 

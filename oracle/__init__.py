@@ -113,7 +113,7 @@ def _configure(lib):
                  ctypes.c_int, ctypes.c_int, f64]
     lib.oracle_attn.argtypes = attn_args + [P, P]
     lib.oracle_attn.restype = ctypes.c_int
-    lib.oracle_attn_partials.argtypes = attn_args + [ctypes.c_int, P, P, P]
+    lib.oracle_attn_partials.argtypes = attn_args + [ctypes.c_int, ctypes.c_int, P, P, P]
     lib.oracle_attn_partials.restype = ctypes.c_int
     lib.oracle_combine.argtypes = [P, P, P, i64, ctypes.c_int, ctypes.c_int, P]
     lib.oracle_combine.restype = None
@@ -263,8 +263,11 @@ def attention(q, k_cache, v_cache, block_tables, context_lens, k_scale=1.0, v_sc
 
 
 def attention_partials(q, k_cache, v_cache, block_tables, context_lens, num_splits,
-                       k_scale=1.0, v_scale=1.0, topk_idx=None, topk_lens=None, sm_scale=None):
-    """Per-split partials: o [B][Hq][q_len][S][D], m and l [B][Hq][q_len][S]."""
+                       k_scale=1.0, v_scale=1.0, topk_idx=None, topk_lens=None, sm_scale=None,
+                       split_pages=0):
+    """Per-split partials: o [B][Hq][q_len][S][D], m and l [B][Hq][q_len][S].
+    split_pages = 0 divides each sequence into S equal parts; > 0 gives every
+    split that many pages (4 list entries per page in top-k mode)."""
     keep, args, (B, q_len, Hq, D) = _attn_common(q, k_cache, v_cache, block_tables,
                                                  context_lens, k_scale, v_scale,
                                                  topk_idx, topk_lens, sm_scale)
@@ -272,7 +275,7 @@ def attention_partials(q, k_cache, v_cache, block_tables, context_lens, num_spli
     o = np.zeros((B, Hq, q_len, S, D), dtype=np.float64)
     m = np.zeros((B, Hq, q_len, S), dtype=np.float64)
     l = np.zeros((B, Hq, q_len, S), dtype=np.float64)
-    flags = _load().oracle_attn_partials(*args, S, _ptr(o), _ptr(m), _ptr(l))
+    flags = _load().oracle_attn_partials(*args, S, int(split_pages), _ptr(o), _ptr(m), _ptr(l))
     del keep
     if flags < 0:
         raise ValueError("oracle_attn_partials: bad arguments")

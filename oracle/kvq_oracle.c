@@ -445,18 +445,22 @@ static int oracle_attention(const oracle_problem *pr, double *out, double *lse)
 
 /* Split partials, for checking the FP32 split workspace ([P1] Status and
  * history / [P3] Problem: the page-4 route writes an FP32 temporary output).
- * Split s of a sequence covers logical pages [s*c, (s+1)*c) with
- * c = ceil(npages / S) (dense), or list entries [s*c, (s+1)*c) with
- * c = ceil(topk_len / S) (top-k).  Per (b, h, i, s): o normalised by its own
- * l, m = max score, l = sum exp(s - m).  Layout o [B][Hq][q_len][S][D],
+ * The pages leave the partition open; two readings are implemented.  With
+ * split_pages == 0, split s of a sequence covers logical pages
+ * [s*c, (s+1)*c) with c = ceil(npages / S) (dense), or list entries
+ * [s*c, (s+1)*c) with c = ceil(topk_len / S) (top-k).  With split_pages > 0,
+ * c = split_pages pages (dense) or 4 * split_pages list entries (top-k), the
+ * same for every sequence.  Per (b, h, i, s): o normalised by its own l,
+ * m = max score, l = sum exp(s - m).  Layout o [B][Hq][q_len][S][D],
  * m and l [B][Hq][q_len][S]. */
-static int oracle_partials(const oracle_problem *pr, int S, double *o, double *m, double *l)
+static int oracle_partials(const oracle_problem *pr, int S, int split_pages, double *o, double *m,
+                           double *l)
 {
     int b, h, i, s, flags = 0;
     int32_t *keys, *sub;
     double *scores;
     int cap = pr->max_pages * 4 + pr->max_topk + 1;
-    if (!check_problem(pr) || S < 1)
+    if (!check_problem(pr) || S < 1 || split_pages < 0)
         return ORACLE_BAD_ARG;
     keys = (int32_t *)malloc(sizeof(int32_t) * cap);
     sub = (int32_t *)malloc(sizeof(int32_t) * cap);
@@ -480,16 +484,16 @@ static int oracle_partials(const oracle_problem *pr, int S, double *o, double *m
                     int ns = 0;
                     if (!use_topk) {
                         int npages = (L + 3) / 4;
-                        int c = (npages + S - 1) / S;
-                        int lo = s * c * 4, hi = (s + 1) * c * 4;
+                        int64_t c = split_pages > 0 ? split_pages : (npages + S - 1) / S;
+                        int64_t lo = s * c * 4, hi = (s + 1) * c * 4;
                         for (k = 0; k < n; ++k)
                             if (keys[k] >= lo && keys[k] < hi)
                                 sub[ns++] = keys[k];
                     } else {
                         /* split by list entry, then keep the causal/valid ones */
                         int cnt = pr->topk_lens[b] < pr->max_topk ? pr->topk_lens[b] : pr->max_topk;
-                        int c = (cnt + S - 1) / S;
-                        int lo = s * c, hi = (s + 1) * c, e;
+                        int64_t c = split_pages > 0 ? 4 * (int64_t)split_pages : (cnt + S - 1) / S;
+                        int64_t lo = s * c, hi = (s + 1) * c, e;
                         const int32_t *list = pr->topk_idx + ((int64_t)b * pr->Hkv + g) * pr->max_topk;
                         int pos = L - pr->q_len + i;
                         for (e = lo; e < hi && e < cnt; ++e) {
@@ -575,8 +579,8 @@ int oracle_attn_partials(const uint16_t *q, const void *k_cache, const void *v_c
                          int64_t P, const int32_t *block_tables, const int32_t *context_lens,
                          double k_scale, double v_scale, const int32_t *topk_idx,
                          const int32_t *topk_lens, int B, int q_len, int Hq, int Hkv, int D,
-                         int max_pages, int max_topk, double sm_scale, int S, double *o, double *m,
-                         double *l)
+                         int max_pages, int max_topk, double sm_scale, int S, int split_pages,
+                         double *o, double *m, double *l)
 {
     oracle_problem pr;
     pr.q = q;
@@ -598,5 +602,5 @@ int oracle_attn_partials(const uint16_t *q, const void *k_cache, const void *v_c
     pr.max_pages = max_pages;
     pr.max_topk = topk_idx ? max_topk : 0;
     pr.sm_scale = sm_scale;
-    return oracle_partials(&pr, S, o, m, l);
+    return oracle_partials(&pr, S, split_pages, o, m, l);
 }

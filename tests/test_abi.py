@@ -74,7 +74,7 @@ def test_scale_from_amax(lib):
 
 def _params(**kw):
     p = dict(batch=2, q_len=1, num_q_heads=8, num_kv_heads=2, head_dim=64, num_splits=2,
-             max_pages_per_seq=25, max_topk=0, sm_scale=0.0)
+             max_pages_per_seq=25, max_topk=0, sm_scale=0.0, split_pages=0)
     p.update(kw)
     return kvq.AttnParams(**p)
 
@@ -97,6 +97,23 @@ def test_bad_params_are_refused(lib, field, value, status):
         p.num_kv_heads = 2    # 68 rows per kv head > 64
     assert lib.kvq_attn_workspace_bytes(ctypes.byref(p)) == 0
     assert lib.kvq_attn_num_splits(ctypes.byref(p)) == status
+
+
+def test_fixed_size_splits_must_cover_every_page(lib):
+    # 25 pages in splits of 8 pages need 4 splits
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(num_splits=0, split_pages=8))) == 4
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(num_splits=4, split_pages=8))) == 4
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(num_splits=9, split_pages=8))) == 9
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(num_splits=3, split_pages=8))) == -1
+    assert lib.kvq_attn_workspace_bytes(ctypes.byref(_params(num_splits=3, split_pages=8))) == 0
+    # a top-k list of 200 entries in splits of 8 pages (32 entries) needs 7
+    p = _params(num_splits=0, split_pages=8, max_topk=200)
+    assert lib.kvq_attn_num_splits(ctypes.byref(p)) == 7
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(num_splits=6, split_pages=8, max_topk=200))) == -1
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(split_pages=-1))) == -1
+    # more than 65535 automatic splits is refused
+    assert lib.kvq_attn_num_splits(ctypes.byref(_params(num_splits=0, split_pages=1,
+                                                        max_pages_per_seq=70000))) == -4
 
 
 FAKE = ctypes.c_void_p(0x10000)     # never dereferenced: every call below fails before a launch

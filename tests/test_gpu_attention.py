@@ -41,6 +41,52 @@ def test_tiny_matches_oracle(name, e4m3, S):
 
 @pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
 @pytest.mark.parametrize("e4m3", [True, False])
+@pytest.mark.parametrize("split_pages,extra", [(2, 1), (8, 0), (16, 3)])
+def test_fixed_size_split_partials_match_oracle(name, e4m3, split_pages, extra):
+    dp = G.device_problem(P.host_problem(name), e4m3)
+    S = -(-dp.block_tables.shape[1] // split_pages) + extra
+    ws, p = G.run_attention(dp, num_splits=S, partial=True, split_pages=split_pages)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    o, m, l = [x.cpu().numpy() for x in kvq.workspace_views(ws, p)]
+    pr = dp.host
+    kc, vc, ks, vs = P.oracle_pools(pr, e4m3, (dp.k_scale, dp.v_scale) if e4m3 else None)
+    ro, rm, rl, _ = oracle.attention_partials(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens,
+                                              S, ks, vs, split_pages=split_pages)
+    nonempty = rl > 0
+    assert np.array_equal(l > 0, nonempty)
+    assert np.isneginf(m[~nonempty]).all()
+    G.assert_close(m[nonempty], rm[nonempty], "tmp_max", atol=1e-4, rtol=1e-5)
+    G.assert_close(l[nonempty], rl[nonempty], "tmp_sum", atol=1e-4, rtol=2e-3)
+    G.assert_close(o[nonempty], ro[nonempty], "tmp_out")
+    out = G.run_attention(dp, num_splits=0, split_pages=split_pages)
+    torch.cuda.synchronize()
+    G.assert_close(out.float().cpu().numpy(), _oracle_out(dp), f"{name} split_pages={split_pages}")
+
+
+@pytest.mark.parametrize("split_pages", [1, 3])
+def test_fixed_size_splits_topk_match_oracle(split_pages):
+    w = inputs.get("tiny_verify", topk=24, topk_fraction=0.5)
+    for e4m3 in (True, False):
+        dp = G.device_problem(P.host_problem(w), e4m3)
+        out = G.run_attention(dp, num_splits=0, split_pages=split_pages)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        G.assert_close(out.float().cpu().numpy(), _oracle_out(dp), f"top-k split_pages={split_pages}")
+
+
+@pytest.mark.parametrize("S", [16, 40])
+def test_combine_with_many_splits(S):
+    """Split lists of 16 or more go to the four-warps-per-row combine."""
+    dp = G.device_problem(P.host_problem("tiny_verify"), True)
+    out = G.run_attention(dp, num_splits=S)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    G.assert_close(out.float().cpu().numpy(), _oracle_out(dp), f"S={S}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
+@pytest.mark.parametrize("e4m3", [True, False])
 def test_workspace_partials_match_oracle(name, e4m3):
     dp = G.device_problem(P.host_problem(name), e4m3)
     S = 3

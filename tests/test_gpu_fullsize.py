@@ -86,16 +86,17 @@ class Layer:
         if ti is not None:
             ti_d, tl_d = torch.from_numpy(ti).to(DEV), torch.from_numpy(tl).to(DEV)
         p = kvq.attn_params(self.q, w.num_kv_heads, lay.block_tables.shape[1], w.num_splits,
-                            0 if ti is None else ti.shape[2])
+                            0 if ti is None else ti.shape[2], split_pages=w.split_pages)
         self.S = kvq.num_splits(p)
         ws = kvq.alloc_workspace(p, DEV)
         if e4m3:
             self.out = kvq.paged_decode_attn_e4m3(self.q, self.kc, self.vc, self.bt, self.cl, self.ks,
                                                   self.vs, ws, None, ti_d, tl_d, w.num_splits,
-                                                  err_flag=err)
+                                                  err_flag=err, split_pages=w.split_pages)
         else:
             self.out = kvq.paged_decode_attn_fp16(self.q, self.kc, self.vc, self.bt, self.cl, ws, None,
-                                                  ti_d, tl_d, w.num_splits, err_flag=err)
+                                                  ti_d, tl_d, w.num_splits, err_flag=err,
+                                                  split_pages=w.split_pages)
         torch.cuda.synchronize()
         assert err.item() == 0, f"device error bits {err.item()}"
 

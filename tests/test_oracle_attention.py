@@ -227,6 +227,82 @@ def test_split_partials_combine_to_full(tiny, S):
     np.testing.assert_allclose(tot.transpose(0, 2, 1), lse, rtol=1e-12)
 
 
+def _brute_split_max(pr, K, s_lo, s_hi, b, h, i, topk=None):
+    """Max score over the keys of row (b, h, i) whose position lies in
+    [s_lo, s_hi) -- or, with a list, whose list entry index does -- by a
+    direct dot product over the dequantised pool values (numpy)."""
+    L = int(pr.layout.lens[b])
+    g = h // pr.w.group
+    pos = L - pr.w.q_len + i
+    if topk is None:
+        keys = [j for j in range(s_lo, min(s_hi, pos + 1))]
+    else:
+        lst, n = topk
+        keys = [int(t) for t in lst[b, g, s_lo:min(s_hi, n[b])] if 0 <= t <= pos]
+    if not keys:
+        return None
+    bt = pr.layout.block_tables[b]
+    q = pr.q[b, i, h].astype(np.float64)
+    sc = [float(K[bt[j // 4], g, j % 4] @ q) / np.sqrt(pr.w.head_dim) for j in keys]
+    return max(sc)
+
+
+@pytest.mark.parametrize("split_pages,extra", [(1, 0), (3, 0), (8, 2), (25, 0), (40, 1)])
+def test_fixed_size_split_partials(tiny, split_pages, extra):
+    """Fixed-size splits: split s holds pages [s*sp, (s+1)*sp) of every
+    sequence; splits past a sequence's end are empty; the partials still
+    combine to the full attention."""
+    pr, kc, vc, ks, vs = tiny
+    max_pages = pr.layout.block_tables.shape[1]
+    S = -(-max_pages // split_pages) + extra
+    out, _ = oracle.attention(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens, ks, vs)
+    o, m, l, flags = oracle.attention_partials(pr.q, kc, vc, pr.layout.block_tables,
+                                               pr.layout.lens, S, ks, vs, split_pages=split_pages)
+    assert flags == 0
+    np.testing.assert_allclose(oracle.combine(o, m, l).transpose(0, 2, 1, 3), out, rtol=1e-12,
+                               atol=1e-13)
+    K = P.torch_dequant(kc, ks)
+    for b in range(pr.w.batch):
+        for s in range(S):
+            for h in (0, pr.w.num_q_heads - 1):
+                for i in range(pr.w.q_len):
+                    want = _brute_split_max(pr, K, 4 * s * split_pages, 4 * (s + 1) * split_pages,
+                                            b, h, i)
+                    if want is None:
+                        assert l[b, h, i, s] == 0 and np.isneginf(m[b, h, i, s])
+                    else:
+                        assert l[b, h, i, s] >= 1.0
+                        np.testing.assert_allclose(m[b, h, i, s], want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("split_pages", [1, 2, 5])
+def test_fixed_size_split_partials_topk(split_pages):
+    w = inputs.get("tiny_verify", topk=24, topk_fraction=0.5)
+    pr = P.host_problem(w)
+    kc, vc, ks, vs = P.oracle_pools(pr)
+    max_topk = pr.topk_idx.shape[2]
+    S = max(-(-pr.layout.block_tables.shape[1] // split_pages), -(-max_topk // (4 * split_pages)))
+    out, _ = oracle.attention(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens, ks, vs,
+                              pr.topk_idx, pr.topk_lens)
+    o, m, l, flags = oracle.attention_partials(pr.q, kc, vc, pr.layout.block_tables,
+                                               pr.layout.lens, S, ks, vs, pr.topk_idx,
+                                               pr.topk_lens, split_pages=split_pages)
+    assert flags == 0
+    np.testing.assert_allclose(oracle.combine(o, m, l).transpose(0, 2, 1, 3), out, rtol=1e-12,
+                               atol=1e-13)
+    K = P.torch_dequant(kc, ks)
+    b = int(np.nonzero(pr.topk_lens > 0)[0][0])
+    c = 4 * split_pages                                  # list entries per split
+    for s in range(S):
+        for i in range(pr.w.q_len):
+            want = _brute_split_max(pr, K, s * c, (s + 1) * c, b, 0, i,
+                                    topk=(pr.topk_idx, pr.topk_lens))
+            if want is None:
+                assert l[b, 0, i, s] == 0
+            else:
+                np.testing.assert_allclose(m[b, 0, i, s], want, rtol=1e-12, atol=1e-12)
+
+
 def test_topk_all_positions_equals_dense(tiny):
     pr, kc, vc, ks, vs = tiny
     out, _ = oracle.attention(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens, ks, vs)
