@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 
 METRIC = "E4M3 paged decode-attn achieved HBM GB/s (% of peak) and seq-steps/s vs FP16"
 L2_BYTES_DEFAULT = 129 * 1024 * 1024
+GRAPH_STEPS = 10   # steps captured in one CUDA graph
 
 
 def profiled_traffic(kernel_file: str, workload: str):
@@ -78,12 +79,14 @@ def _peaks():
 # ---------------------------------------------------------------------------
 # workload accounting
 
-def algorithmic_bytes(w, kv_elem_bytes: int, lens, step_tokens: int, topk=(None, None)):
+def algorithmic_bytes(w, kv_elem_bytes: int, lens, topk=(None, None)):
     """Bytes the step must move at minimum: every K and V element attended
     once (all cached tokens of a dense sequence; the listed tokens of a top-k
     sequence, plus its list and block-table entries), Q, the output, the
     block-table entries of the pages read, the context lengths, and the
-    append (fp16 in, cache dtype out, slot ids)."""
+    append of the step's B * q_len tokens and of a prefill chunk (fp16 in,
+    cache dtype out, slot ids).  "attention_kernel" is the split attention
+    kernel's share."""
     Hkv, D = w.num_kv_heads, w.head_dim
     lens = np.asarray(lens, np.int64)
     ti, tl = topk
@@ -97,9 +100,10 @@ def algorithmic_bytes(w, kv_elem_bytes: int, lens, step_tokens: int, topk=(None,
     q = w.batch * w.q_len * w.num_q_heads * D * 2
     out = q
     bt = pages * 4 + w.batch * 4
-    append = step_tokens * Hkv * D * 2 * (2 + kv_elem_bytes) + step_tokens * 4
+    appended = w.batch * w.q_len + w.prefill_chunk
+    append = appended * (Hkv * D * 2 * (2 + kv_elem_bytes) + 4)
     attn = kv + q + bt + lists
-    return {"step": kv + q + out + bt + lists + append, "attention_kernel": attn}
+    return {"step": attn + out + append, "attention_kernel": attn}
 
 
 def describe(w, splits) -> str:
@@ -205,10 +209,12 @@ class Arm:
         hist_rows = torch.from_numpy(offs[hs] + hp).to(dev)
         self.step_slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, ss, sp)).to(dev)
         step_rows = torch.from_numpy(offs[ss] + sp).to(dev)
-        self.k_new = k[step_rows].contiguous()
+        self.k_new = k[step_rows].contiguous()        # [B * q_len, Hkv, D], rows in (b, i) order
         self.v_new = v[step_rows].contiguous()
-        if w.prefill_chunk:
-            # the step also appends a new sequence's prefill chunk (mixed batches)
+        self.prefill = w.prefill_chunk > 0
+        if self.prefill:
+            # the step also appends a new sequence's prefill chunk (mixed
+            # batches), in the same append call as the decode tokens
             pk = inputs.prefill_tokens(w, 0, "k", device=dev)
             pv = inputs.prefill_tokens(w, 0, "v", device=dev)
             pslots = torch.from_numpy(inputs.prefill_slots(lay)[: w.prefill_chunk]).to(dev)
@@ -241,8 +247,8 @@ class Arm:
         self.out = torch.empty_like(self.q)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.pool_bytes = pool_bytes
-        self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, int(self.step_slots.numel()),
-                                       self.topk_np)
+        self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, self.topk_np)
+        self.launches = 3   # kernels of one step: append, attention, combine
         torch.cuda.synchronize(dev)
 
     def _append(self, k, v, slots, kc, vc):
@@ -265,38 +271,46 @@ class Arm:
                                                self.topk_lens, num_splits=self.S, err_flag=self.err,
                                                split_pages=self.w.split_pages)
 
-    def step(self, i, ev=None):
+    def step(self, i):
+        """One step on pool copy i: append of the step's tokens, split-K
+        attention, log-sum-exp combine (three launches chained with
+        programmatic dependent launch)."""
         kc, vc = self.pools[i % self.copies]
         self._append(self.k_new, self.v_new, self.step_slots, kc, vc)
-        if ev is not None:
-            ev[0].record()
         self._attention(kc, vc)
-        if ev is not None:
-            ev[1].record()
         self.kvq.lse_combine(self.ws, self.out, self.p)
 
     def capture(self):
-        """One CUDA graph per pool copy holding a whole step (append, attention,
-        combine); replaying them removes host launch cost from the step time."""
+        """CUDA graphs of the step: one per pool copy holding one step, and
+        one holding GRAPH_STEPS consecutive steps (cycling the copies), as a
+        serving loop captures many layers in one graph; replaying them
+        removes host launch cost and most of the gap between graphs."""
         torch = self.torch
         for i in range(2):                       # warm up (sets kernel attributes) before capture
             self.step(i)
         torch.cuda.synchronize(self.dev)
-        self.graphs = []
+        graphs = []
         for r in range(self.copies):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 self.step(r)
-            self.graphs.append(g)
+            graphs.append(g)
+        many = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(many):
+            for r in range(GRAPH_STEPS):
+                self.step(r)
         torch.cuda.synchronize(self.dev)
+        self.graphs, self.many = graphs, many
 
     def time(self, steps, warmup, barrier=None):
-        """Exactly `steps` whole steps (graph replays) between two events."""
+        """Exactly `steps` whole steps between two events: replays of the
+        GRAPH_STEPS-step graph, then one-step graphs for the remainder."""
         torch = self.torch
         if not getattr(self, "graphs", None):
             self.capture()
+        graphs, many = self.graphs, self.many
         for i in range(warmup):
-            self.graphs[i % self.copies].replay()
+            graphs[i % self.copies].replay()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
         if barrier:
@@ -304,8 +318,10 @@ class Arm:
         torch.cuda.synchronize(self.dev)
         torch.cuda.nvtx.range_push("kvq_timed")
         start.record()
-        for i in range(steps):
-            self.graphs[(warmup + i) % self.copies].replay()
+        for _ in range(steps // GRAPH_STEPS):
+            many.replay()
+        for i in range(steps % GRAPH_STEPS):
+            graphs[i % self.copies].replay()
         end.record()
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(self.dev)
@@ -315,36 +331,50 @@ class Arm:
         return start.elapsed_time(end)
 
     def time_kernel(self, steps, warmup):
-        """Average duration of the attention kernel: `steps` back-to-back
+        """Average duration of the split attention kernel: `steps` back-to-back
         launches over the rotating pool copies, between two events on the
         launching stream (the queue stays full, so host launch time is hidden)."""
         torch = self.torch
+        run = self._attention
         for i in range(warmup):
             kc, vc = self.pools[i % self.copies]
-            self._attention(kc, vc)
+            run(kc, vc)
         torch.cuda.synchronize(self.dev)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.nvtx.range_push("kvq_kernel_timed")
         start.record()
         for i in range(steps):
             kc, vc = self.pools[(warmup + i) % self.copies]
-            self._attention(kc, vc)
+            run(kc, vc)
         end.record()
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(self.dev)
         assert self.err.item() == 0, f"device error bits {self.err.item()}"
         return start.elapsed_time(end) / steps
 
+    def step_percentiles(self, steps):
+        """Per-step durations (ms) of graph replays, each between its own
+        events: (p10, median, p90)."""
+        torch = self.torch
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        torch.cuda.synchronize(self.dev)
+        evs[0].record()
+        for i in range(steps):
+            self.graphs[i % self.copies].replay()
+            evs[i + 1].record()
+        torch.cuda.synchronize(self.dev)
+        d = np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(steps)])
+        return tuple(float(x) for x in np.percentile(d, [10, 50, 90]))
+
     def time_e2e(self, steps, warmup):
         """Per step: H2D of the step's inputs from pinned host memory, the
-        three kernels, and a D2H read of the output, all on one stream."""
+        step's kernels through the public calls, and a D2H read of the output,
+        all on one stream."""
         torch = self.torch
-        host = {n: t.cpu().pin_memory() for n, t in
-                (("q", self.q), ("k", self.k_new), ("v", self.v_new), ("slots", self.step_slots),
-                 ("bt", self.bt), ("cl", self.cl))}
-        dev = {n: torch.empty_like(getattr(self, a)) for n, a in
-               (("q", "q"), ("k", "k_new"), ("v", "v_new"), ("slots", "step_slots"), ("bt", "bt"),
-                ("cl", "cl"))}
+        src = {"q": self.q, "k": self.k_new, "v": self.v_new, "slots": self.step_slots,
+               "bt": self.bt, "cl": self.cl}
+        host = {n: t.cpu().pin_memory() for n, t in src.items()}
+        dev = {n: torch.empty_like(t) for n, t in src.items()}
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_host.numel() * out_host.element_size()
@@ -530,13 +560,14 @@ def main():
     arm.capture()
     with ClockSampler(torch.cuda.current_device()) as clk:
         total_ms = arm.time(args.steps, args.warmup, barrier)
-        attn_avg = arm.time_kernel(args.steps, args.warmup)
+        kern_avg = arm.time_kernel(args.steps, args.warmup)
     total_ms = reduce_max(total_ms)
     ms = total_ms / args.steps
-    attn_avg = reduce_max(attn_avg)
+    kern_avg = reduce_max(kern_avg)
     step_bytes = arm.bytes["step"]
     gbs, seq_steps = aggregate(step_bytes, w.batch, world, ms)
-    achieved = arm.bytes["attention_kernel"] / (attn_avg * 1e-3) / 1e9
+    achieved = arm.bytes["attention_kernel"] / (kern_avg * 1e-3) / 1e9
+    pct = arm.step_percentiles(max(20, args.steps))   # context: per-step spread (one graph each)
 
     arm.graphs = None
     e2e_ms, h2d, d2h = arm.time_e2e(max(5, args.steps // 2), args.warmup)
@@ -584,17 +615,20 @@ def main():
             "step_bytes": step_bytes,
             "fp16_arm": fp16,
             "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+            "step_ms_p10_p50_p90_one_graph_each": pct,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
                          "traffic": profiled_traffic("kvq_attn.cu", w.name),
                          "kernel": "attn_split_kernel (E4M3)", "peak_kind": peak_kind,
-                         "attention_kernel_ms": attn_avg},
+                         "attention_kernel_ms": kern_avg,
+                         "bytes_per_launch": arm.bytes["attention_kernel"]},
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": 3 * args.steps,
-            "launch": "CUDA graph per step (append, attention, combine; programmatic dependent launch)",
+            "gpu_launches": arm.launches * args.steps,
+            "launch": f"CUDA graphs of {GRAPH_STEPS} steps (append, attention, combine per step; "
+                      "programmatic dependent launch)",
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
