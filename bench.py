@@ -249,6 +249,7 @@ class Arm:
         self.pool_bytes = pool_bytes
         self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, self.topk_np)
         self.launches = 3   # kernels of one step: append, attention, combine
+        self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
         torch.cuda.synchronize(dev)
 
     def _append(self, k, v, slots, kc, vc):
@@ -265,7 +266,8 @@ class Arm:
         if self.e4m3:
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
-                                               err_flag=self.err, split_pages=self.w.split_pages)
+                                               err_flag=self.err, split_pages=self.w.split_pages,
+                                               bitcast_decode=self.bitcast)
         else:
             kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, self.topk_idx,
                                                self.topk_lens, num_splits=self.S, err_flag=self.err,
@@ -568,6 +570,9 @@ def main():
     gbs, seq_steps = aggregate(step_bytes, w.batch, world, ms)
     achieved = arm.bytes["attention_kernel"] / (kern_avg * 1e-3) / 1e9
     pct = arm.step_percentiles(max(20, args.steps))   # context: per-step spread (one graph each)
+    arm.bitcast = True                                  # context: the pages' bitcast decoder
+    bitcast_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
+    arm.bitcast = False
 
     arm.graphs = None
     e2e_ms, h2d, d2h = arm.time_e2e(max(5, args.steps // 2), args.warmup)
@@ -621,7 +626,10 @@ def main():
                          "traffic": profiled_traffic("kvq_attn.cu", w.name),
                          "kernel": "attn_split_kernel (E4M3)", "peak_kind": peak_kind,
                          "attention_kernel_ms": kern_avg,
-                         "bytes_per_launch": arm.bytes["attention_kernel"]},
+                         "bytes_per_launch": arm.bytes["attention_kernel"],
+                         "decoder": "hardware E4M3 conversion",
+                         "bitcast_decoder_ms": bitcast_ms,
+                         "bitcast_decoder_gbs": arm.bytes["attention_kernel"] / (bitcast_ms * 1e-3) / 1e9},
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -1,627 +1,19 @@
-// kvq_attn.cu -- split-K paged decode / MTP-verify attention over E4M3 or
-// fp16 page-4 pools, and the log-sum-exp combine.
-//
-// What is computed (PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV
-// capacity path", section Changes; PR "[Model][SM70] Calibrated E4M3 KV cache
-// for Qwen4Exp QSA with MTP", sections Purpose and Status and history):
-// grouped-query attention of q_len = 1 (decode) or 1 + 3 (MTP verify, causal
-// inside the window) query rows over a page-4 cache whose K/V are stored in
-// calibrated E4M3, decoded exactly to fp16 with the per-layer scales hoisted
-// out of the inner loop, split over the token axis into an FP32 workspace,
-// and merged by a log-sum-exp combine.
-//
-// GB300 design (one CTA per (split, kv head, sequence), 4 consumer warps and
-// 2 producer warps):
-//  * Two producer warps walk the split's pages one stage at a time (16 pages
-//    for one query-row group, 8 otherwise), read the block table a batch
-//    ahead, and issue one 1-D bulk TMA copy per page -- one warp for K, the
-//    other for V (a page of one kv head = 4 * head_dim contiguous elements)
-//    -- into a ring of about 50 KB of shared memory, each stage completing
-//    on its own mbarrier.  A single warp issues bulk copies at a limited
-//    rate (about 27 million per second measured on GB300, whatever their
-//    size), so splitting K and V doubles the CTA's copy rate.  In top-k mode
-//    a stage is 4 tokens per page slot, each fetched as one row.
-//  * Every consumer warp takes part in every stage: warp w owns one (or, for
-//    64 query rows, two) 16-token tiles of the stage and one group of query
-//    rows.  Each warp therefore waits on every phase of every ring slot in
-//    order, and a slot is refilled only after all four warps released it.
-//  * Per 16-token tile: K via ldmatrix, E4M3 -> fp16 by the hardware
-//    conversion (exact), S^T = K Q^T on tensor cores (mma.sync m16n8k16,
-//    tokens on M, query rows on N: the 8 heads of a GQA group fill N
-//    exactly); online softmax in the log2 domain with k_scale * sm_scale *
-//    log2(e) folded into one multiplier; P transposed in registers by
-//    movmatrix; V^T via ldmatrix.trans, decoded (byte permute + conversion,
-//    or the bitcast decoder), O^T += V^T P^T.  v_scale is applied once per
-//    output row.
-//  * Page chunks sit 16 bytes further apart than their size in shared
-//    memory, so the eight rows an ldmatrix reads (one slot of eight pages)
-//    fall in distinct banks.
-//  * Every wait is bounded (about 2 s); on expiry the kernel reports
-//    KVQ_DEV_TIMEOUT, drains its own copies and exits without writing.
-#include <cstdint>
-#include <cuda_fp16.h>
-#include <cuda_runtime.h>
-
-#include "kvq_device.cuh"
-#include "kvq_internal.h"
+// kvq_attn.cu -- instantiations of the split attention kernel with the
+// hardware E4M3 conversion and for fp16 pools, the dispatch to the bitcast
+// decoder's instantiations, and the log-sum-exp combine kernel.
+#include "kvq_attn_kernel.cuh"
 
 namespace kvq {
 
-// V fragments: 1 = byte permute + hardware conversion, 0 = bitcast decoder
-// (the decoder of the source pages: exact, value * 2^-8).  K fragments always
-// use the hardware conversion: their byte pairs are adjacent.
-#ifndef KVQ_V_CVT
-#define KVQ_V_CVT 1
-#endif
-
-constexpr int kConsumerWarps = 4;
-constexpr int kProducerWarps = 2;   // K pages and V pages
-constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
-constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr float kLn2 = 0.69314718055994530942f;
-
-// Work split of the 4 consumer warps: RW warps share the same tokens and
-// split the query rows (NT 8-row tiles each); 4/RW warps split the tokens.
-template <int NT, int RW>
-struct Split {
-    static constexpr int kRowWarps = RW;
-    static constexpr int kTokWarps = kConsumerWarps / RW;
-    static constexpr int kTilesPerWarp = (RW == kConsumerWarps) ? 2 : 1;    // 16-token tiles
-    static constexpr int kTilesPerStage = kTokWarps * kTilesPerWarp;
-    static constexpr int kPagesPerStage = 4 * kTilesPerStage;             // 16 or 8
-    static constexpr int kRowsPad = RW * NT * 8;
-};
-
-template <bool E4M3, int D, int PPS>
-struct Geometry {
-    static constexpr int kElem = E4M3 ? 1 : 2;
-    static constexpr int kRowBytes = D * kElem;           // one token of one kv head
-    static constexpr int kChunk = 4 * kRowBytes;          // one page of one kv head
-    static constexpr int kPageStride = kChunk + 16;       // bank-skewed page placement
-    static constexpr int kRegion = PPS * kPageStride;     // K (or V) part of a stage
-    static constexpr int kStageBytes = 2 * kRegion;
-    static constexpr int kStagesRaw = 50688 / kStageBytes;   // ~50 KB of ring
-    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
-    static constexpr int kX4 = kRowBytes / 32;            // ldmatrix.x4 per 16-token tile
-    static constexpr int kKSteps = D / 16;                // QK mma k-steps
-    static constexpr int kPVTiles = D / 16;               // PV mma m-tiles (16 channels)
-    static constexpr int kTokPerStage = 4 * PPS;
-    static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kTokPosOff = kRingBytes;
-    static constexpr int kBarOff = kTokPosOff + kStages * kTokPerStage * 4;
-    static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
-    static constexpr int kBytes = kAbortOff + 16;
-    static_assert(kPageStride % 128 == 16, "page skew must be 16 bytes mod 128");
-    static_assert(kBarOff % 8 == 0, "mbarriers need 8-byte alignment");
-};
-
-template <bool E4M3, int D, int NT, int RW>
-constexpr int smem_bytes()
+cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream)
 {
-    using W = Split<NT, RW>;
-    using G = Geometry<E4M3, D, W::kPagesPerStage>;
-    constexpr int merge = (W::kTokWarps * W::kRowsPad * (D + 2) + W::kRowsPad * W::kTokWarps) * 4;
-    return G::kBytes > merge ? G::kBytes : merge;
-}
-
-// channel of the O^T accumulator row held by this thread for PV tile `pv`
-// (first = fragment row gid, second = fragment row gid + 8)
-template <bool BYTE_PAIRS>
-__device__ __forceinline__ int2 pv_channels(int pv, int gid)
-{
-    if (BYTE_PAIRS) return make_int2(16 * pv + 2 * gid, 16 * pv + 2 * gid + 1);
-    return make_int2(16 * pv + gid, 16 * pv + 8 + gid);
-}
-
-template <bool E4M3, int D, int NT, int RW>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
-    attn_split_kernel(const AttnArgs a)
-{
-    using W = Split<NT, RW>;
-    constexpr int PPS = W::kPagesPerStage;
-    constexpr int MTW = W::kTilesPerWarp;
-    using G = Geometry<E4M3, D, PPS>;
-    extern __shared__ __align__(128) uint8_t smem[];
-
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t ring = smem_u32(smem);
-    int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
-    const uint32_t bar0 = smem_u32(smem + G::kBarOff);   // full[k] = bar0 + 8k, empty[k] = bar0 + 8(S+k)
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
-    volatile int *stage_bad = abort_flag + 1;            // a bad entry was seen (sticky)
-
-    // barriers first: this part reads no input and overlaps the previous kernel's tail
-    if (threadIdx.x == 0) {
-        for (int k = 0; k < G::kStages; ++k) {
-            mbar_init(bar0 + 8 * k, kProducerWarps);   // one arrive.expect_tx per producer
-            mbar_init(bar0 + 8 * (G::kStages + k), kConsumerWarps);
-        }
-        *abort_flag = 0;
-        *stage_bad = 0;
-        fence_mbar_init();
-    }
-    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
-    launch_dependents();      // the combine may start launching; it waits for our completion
-
-    // ---- work of this CTA --------------------------------------------------
-    // The producers' first block-table batch is fetched speculatively for a
-    // sequence that fills its block-table row, in parallel with the context
-    // length; it is refetched below if the real split starts elsewhere.
-    const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
-    const int64_t spec_per = a.split_pages > 0 ? (int64_t)a.split_pages
-                                               : (int64_t)(a.max_pages + a.num_splits - 1) / a.num_splits;
-    const int spec0 = (int)min((int64_t)s * spec_per, (int64_t)a.max_pages);
-    int bt_spec = -1;
-    if (warp >= kConsumerWarps && spec0 + lane < a.max_pages) bt_spec = __ldg(bt_row + spec0 + lane);
-    const int L = a.context_lens[b];
-    const bool len_ok = (L >= a.q_len) && (L <= a.max_pages * 4);
-    int topk_n = (a.topk_idx && a.topk_lens) ? a.topk_lens[b] : 0;
-    const bool topk = len_ok && topk_n > 0;
-    if (topk && topk_n > a.max_topk) topk_n = a.max_topk;
-    const int n_items = !len_ok ? 0 : (topk ? topk_n : (L + 3) / 4);   // pages or list entries
-    // split s covers items [s * per, (s + 1) * per): an equal share of this
-    // sequence, or a fixed number of pages (4 list entries per page)
-    const int64_t per = a.split_pages > 0 ? (topk ? 4 * (int64_t)a.split_pages : (int64_t)a.split_pages)
-                                          : (int64_t)(n_items + a.num_splits - 1) / a.num_splits;
-    const int item0 = (int)min((int64_t)s * per, (int64_t)n_items);
-    const int item1 = (int)min(item0 + per, (int64_t)n_items);
-    const int ipst = topk ? G::kTokPerStage : PPS;        // items per stage
-    const int nst = (item1 - item0 + ipst - 1) / ipst;
-
-    if (threadIdx.x == 0) {
-        if (!len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
-        if (len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
-            report(a.err_flag, KVQ_DEV_BAD_TOPK);
-    }
-    __syncthreads();
-
-    float o[NT][G::kPVTiles][4];
-    float m_run[NT][2], l_run[NT][2];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-#pragma unroll
-        for (int pv = 0; pv < G::kPVTiles; ++pv)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[j][pv][e] = 0.f;
-        m_run[j][0] = m_run[j][1] = -INFINITY;
-        l_run[j][0] = l_run[j][1] = 0.f;
-    }
-    const int gid = lane >> 2, t = lane & 3;
-    const int rw = warp % RW, tw = warp / RW;
-    int issued = 0;   // stages this producer has issued
-
-    if (warp >= kConsumerWarps) {
-        // ================= producers: the first moves K, the second V =================
-        const uint64_t pol = l2_policy_evict_first();
-        const bool is_v = warp == kConsumerWarps + 1;
-        const uint8_t *pool = static_cast<const uint8_t *>(is_v ? a.v_cache : a.k_cache);
-        if (!topk) {
-            constexpr int SPB = 32 / PPS;                 // stages per block-table batch
-            auto load_bt = [&](int first) -> int {
-                const int it = first + lane;
-                return it < item1 ? __ldg(bt_row + it) : -1;
-            };
-            int bt_cur = (item0 == spec0) ? (item0 + lane < item1 ? bt_spec : -1) : load_bt(item0);
-            int bt_nxt = load_bt(item0 + 32);
-            const int p = lane % PPS;                      // page of the stage this lane copies
-            const bool copier = lane < PPS;
-            for (int st = 0; st < nst; ++st) {
-                const int slot = st % G::kStages;
-                if (st >= G::kStages &&
-                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
-                                       abort_flag, a.err_flag))
-                    break;
-                if (st > 0 && st % SPB == 0) {
-                    bt_cur = bt_nxt;
-                    bt_nxt = load_bt(item0 + (st + SPB) * PPS);
-                }
-                const int item = item0 + st * PPS + p;
-                const int phys = __shfl_sync(kFull, bt_cur, (st % SPB) * PPS + p);
-                const bool exists = item < item1;
-                const bool valid = exists && phys >= 0 && (int64_t)phys < a.num_pages;
-                if (!is_v && lane < PPS) {
-                    if (exists && !valid) {
-                        report(a.err_flag, KVQ_DEV_BAD_PAGE);
-                        *stage_bad = 1;
-                    }
-#pragma unroll
-                    for (int sl = 0; sl < 4; ++sl) {
-                        const int pos = item * 4 + sl;
-                        tokpos[slot * G::kTokPerStage + p * 4 + sl] = (valid && pos < L) ? pos : -1;
-                    }
-                }
-                const unsigned vmask = __ballot_sync(kFull, valid && copier);
-                __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, __popc(vmask) * G::kChunk);
-                __syncwarp();
-                if (copier && valid) {
-                    const uint8_t *src = pool + ((int64_t)phys * a.num_kv_heads + g) * G::kChunk;
-                    const uint32_t dst = ring + slot * G::kStageBytes + (is_v ? G::kRegion : 0) +
-                                         p * G::kPageStride;
-                    tma_load_1d(dst, src, G::kChunk, bar0 + 8 * slot, pol);
-                }
-                issued = st + 1;
-            }
-        } else {
-            // top-k: kTokPerStage listed tokens per stage, R per lane
-            constexpr int R = G::kTokPerStage / 32;
-            const int32_t *list = a.topk_idx + ((int64_t)b * a.num_kv_heads + g) * a.max_topk;
-            auto load_idx = [&](int st, int r) -> int {
-                const int it = item0 + st * G::kTokPerStage + r * 32 + lane;
-                return (st < nst && it < item1) ? __ldg(list + it) : -1;
-            };
-            auto load_page = [&](int idx) -> int {
-                return (idx >= 0 && idx < L) ? __ldg(bt_row + (idx >> 2)) : -1;
-            };
-            int idx_cur[R], pg_cur[R], idx_nxt[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                idx_cur[r] = load_idx(0, r);
-                pg_cur[r] = load_page(idx_cur[r]);
-                idx_nxt[r] = load_idx(1, r);
-            }
-            for (int st = 0; st < nst; ++st) {
-                const int slot = st % G::kStages;
-                if (st >= G::kStages &&
-                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
-                                       abort_flag, a.err_flag))
-                    break;
-                int pg_nxt[R], idx_nxt2[R];
-                bool valid[R];
-                int cnt = 0;
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    pg_nxt[r] = load_page(idx_nxt[r]);
-                    idx_nxt2[r] = load_idx(st + 2, r);
-                    const int e = r * 32 + lane;                    // token of the stage
-                    const bool exists = item0 + st * G::kTokPerStage + e < item1;
-                    const bool idx_ok = exists && idx_cur[r] >= 0 && idx_cur[r] < L;
-                    valid[r] = idx_ok && pg_cur[r] >= 0 && (int64_t)pg_cur[r] < a.num_pages;
-                    if (!is_v) {
-                        if (exists && !idx_ok) report(a.err_flag, KVQ_DEV_BAD_TOPK);
-                        if (idx_ok && !valid[r]) report(a.err_flag, KVQ_DEV_BAD_PAGE);
-                        tokpos[slot * G::kTokPerStage + e] = valid[r] ? idx_cur[r] : -1;
-                    }
-                    cnt += __popc(__ballot_sync(kFull, valid[r]));
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * slot, cnt * G::kRowBytes);
-                __syncwarp();
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    if (valid[r]) {
-                        const int e = r * 32 + lane;
-                        const int64_t row =
-                            ((int64_t)pg_cur[r] * a.num_kv_heads + g) * 4 + (idx_cur[r] & 3);
-                        const uint32_t dst = ring + slot * G::kStageBytes + (is_v ? G::kRegion : 0) +
-                                             (e >> 2) * G::kPageStride + (e & 3) * G::kRowBytes;
-                        tma_load_1d(dst, pool + row * G::kRowBytes, G::kRowBytes, bar0 + 8 * slot, pol);
-                    }
-                    idx_cur[r] = idx_nxt[r];
-                    pg_cur[r] = pg_nxt[r];
-                    idx_nxt[r] = idx_nxt2[r];
-                }
-                issued = st + 1;
-            }
-        }
-    } else {
-        // ================= consumers =================
-        // Q as mma B fragments, one set per 8-row n-tile; k-step ks of this
-        // lane covers channels 16ks + 4t .. +3 (E4M3: the pairs the hardware
-        // conversion makes from adjacent K bytes) or 16ks + 2t, +1 and
-        // 16ks + 8 + 2t, +1 (fp16).
-        uint32_t qf[NT][G::kKSteps][2];
-        int lim[NT][2];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int row = (rw * NT + j) * 8 + gid;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int r = (rw * NT + j) * 8 + 2 * t + c;
-                lim[j][c] = (r < a.rows) ? L - a.q_len + r / a.group : 0x7FFFFFFF;
-            }
-            if (row < a.rows) {
-                const int i = row / a.group, h = g * a.group + row % a.group;
-                const __half *qrow = static_cast<const __half *>(a.q) +
-                                     (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D;
-#pragma unroll
-                for (int ks = 0; ks < G::kKSteps; ++ks) {
-                    if (E4M3) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * t);
-                        qf[j][ks][0] = v.x;   // (d, d+1)
-                        qf[j][ks][1] = v.y;   // (d+2, d+3)
-                    } else {
-                        qf[j][ks][0] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * t);
-                        qf[j][ks][1] = *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * t);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < G::kKSteps; ++ks) qf[j][ks][0] = qf[j][ks][1] = 0u;
-            }
-        }
-        // per-lane ldmatrix offset: matrix q = lane/8 reads row (page) lane%8,
-        // token slot (q&1) of the tile's slot pair, 16-byte chunk (q>>1) of the pair
-        const int mq = lane >> 3;
-        const uint32_t lane_off = (lane & 7) * G::kPageStride + (mq & 1) * G::kRowBytes + (mq >> 1) * 16;
-        // this warp's tiles: tile index tg -> page group tg/2, slot pair tg%2
-        uint32_t tile_off[MTW];
-        int tile_pg[MTW], tile_sp[MTW];
-#pragma unroll
-        for (int k = 0; k < MTW; ++k) {
-            const int tg = tw * MTW + k;
-            tile_pg[k] = tg >> 1;
-            tile_sp[k] = tg & 1;
-            tile_off[k] = tile_pg[k] * 8 * G::kPageStride + tile_sp[k] * 2 * G::kRowBytes + lane_off;
-        }
-        const float qk = a.qk_scale_log2;
-        const int first_masked = L - a.q_len + 1;   // positions >= this are masked for some row
-
-        for (int st = 0; st < nst; ++st) {
-            const int slot = st % G::kStages;
-            if (!mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag))
-                break;
-            const uint32_t sk = ring + slot * G::kStageBytes;
-            const uint32_t sv = sk + G::kRegion;
-            const int32_t *tp = tokpos + slot * G::kTokPerStage;
-            // Mask when some slot of the stage may hold no valid token for some
-            // row: top-k lists, bad pages, a stage with missing pages (their
-            // slots keep whatever an earlier stage left there), or positions
-            // inside the verify window / past the context end.
-            const int stage_end = item0 + (st + 1) * PPS;
-            const bool need_mask = topk || *stage_bad || stage_end > item1 ||
-                                   stage_end * 4 - 1 >= first_masked;
-
-            // ---- S^T = K Q^T, one 16-token tile at a time ----
-            float sc[NT][MTW][4];
-#pragma unroll
-            for (int k = 0; k < MTW; ++k) {
-                uint32_t kr[G::kX4][4];
-#pragma unroll
-                for (int u = 0; u < G::kX4; ++u) ldsm_x4(kr[u], sk + tile_off[k] + u * 32);
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[j][k][e] = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < G::kKSteps; ++ks) {
-                    uint32_t af[4];
-                    if (E4M3) {
-                        const uint32_t w0 = kr[ks >> 1][2 * (ks & 1)];
-                        const uint32_t w1 = kr[ks >> 1][2 * (ks & 1) + 1];
-                        af[0] = cvt_lo(w0);
-                        af[1] = cvt_lo(w1);
-                        af[2] = cvt_hi(w0);
-                        af[3] = cvt_hi(w1);
-                    } else {
-                        af[0] = kr[ks][0];
-                        af[1] = kr[ks][1];
-                        af[2] = kr[ks][2];
-                        af[3] = kr[ks][3];
-                    }
-#pragma unroll
-                    for (int j = 0; j < NT; ++j) mma_16816(sc[j][k], af, qf[j][ks][0], qf[j][ks][1]);
-                }
-            }
-            // ---- scores in the log2 domain, masking ----
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int k = 0; k < MTW; ++k)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[j][k][e] *= qk;
-            if (need_mask) {
-#pragma unroll
-                for (int k = 0; k < MTW; ++k) {
-                    const int pbase = (tile_pg[k] * 8 + gid) * 4 + 2 * tile_sp[k];
-                    const int pa = tp[pbase], pb = tp[pbase + 1];
-#pragma unroll
-                    for (int j = 0; j < NT; ++j)
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            if (!(pa >= 0 && pa <= lim[j][c])) sc[j][k][c] = -INFINITY;
-                            if (!(pb >= 0 && pb <= lim[j][c])) sc[j][k][2 + c] = -INFINITY;
-                        }
-                }
-            }
-            // ---- online softmax (row max across the 8 lanes sharing t) ----
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float mx = fmaxf(sc[j][0][c], sc[j][0][c + 2]);
-#pragma unroll
-                    for (int k = 1; k < MTW; ++k) mx = fmaxf(mx, fmaxf(sc[j][k][c], sc[j][k][c + 2]));
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                    const float m_new = fmaxf(m_run[j][c], mx);
-                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                    const float corr = fast_exp2(m_run[j][c] - m_use);
-                    m_run[j][c] = m_new;
-                    float lsum = l_run[j][c] * corr;
-#pragma unroll
-                    for (int pv = 0; pv < G::kPVTiles; ++pv) {
-                        o[j][pv][c] *= corr;
-                        o[j][pv][c + 2] *= corr;
-                    }
-#pragma unroll
-                    for (int k = 0; k < MTW; ++k) {
-                        const float p0 = fast_exp2(sc[j][k][c] - m_use);
-                        const float p1 = fast_exp2(sc[j][k][c + 2] - m_use);
-                        sc[j][k][c] = p0;
-                        sc[j][k][c + 2] = p1;
-                        lsum += p0 + p1;
-                    }
-                    l_run[j][c] = lsum;
-                }
-            // ---- P^T as mma B fragments: transpose the score tiles in registers ----
-            uint32_t pf[NT][MTW][2];
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int k = 0; k < MTW; ++k) {
-                    pf[j][k][0] = movmatrix_trans(pack_half2(sc[j][k][0], sc[j][k][1]));
-                    pf[j][k][1] = movmatrix_trans(pack_half2(sc[j][k][2], sc[j][k][3]));
-                }
-            // ---- O^T += V^T P^T ----
-#pragma unroll
-            for (int k = 0; k < MTW; ++k) {
-                uint32_t vr[G::kX4][4];
-#pragma unroll
-                for (int u = 0; u < G::kX4; ++u) ldsm_x4_trans(vr[u], sv + tile_off[k] + u * 32);
-                if (need_mask) {
-                    // Slots that hold no token may contain any bits -- fp16 NaN, or
-                    // the E4M3 NaN codes 0x7F/0xFF, which the conversion turns into
-                    // NaN -- so their V is zeroed (P = 0 alone would give 0 * NaN).
-                    // Token (page 2t) sits in the low half of each word, (page 2t+1)
-                    // in the high half, for both element sizes.
-                    const int q0 = (tile_pg[k] * 8 + 2 * t) * 4 + 2 * tile_sp[k];
-                    const uint32_t m0 = (tp[q0] >= 0 ? 0x0000FFFFu : 0u) |
-                                        (tp[q0 + 4] >= 0 ? 0xFFFF0000u : 0u);
-                    const uint32_t m1 = (tp[q0 + 1] >= 0 ? 0x0000FFFFu : 0u) |
-                                        (tp[q0 + 5] >= 0 ? 0xFFFF0000u : 0u);
-#pragma unroll
-                    for (int u = 0; u < G::kX4; ++u) {
-                        vr[u][0] &= m0;
-                        vr[u][2] &= m0;
-                        vr[u][1] &= m1;
-                        vr[u][3] &= m1;
-                    }
-                }
-#pragma unroll
-                for (int pv = 0; pv < G::kPVTiles; ++pv) {
-                    uint32_t af[4];
-                    if (E4M3) {
-                        // bytes of a word: (token A, d) (A, d+1) (B, d) (B, d+1)
-                        const uint32_t h0 = vr[pv >> 1][2 * (pv & 1)];
-                        const uint32_t h1 = vr[pv >> 1][2 * (pv & 1) + 1];
-#if KVQ_V_CVT
-                        const uint32_t p0 = __byte_perm(h0, 0, 0x3120);
-                        const uint32_t p1 = __byte_perm(h1, 0, 0x3120);
-                        af[0] = cvt_lo(p0);
-                        af[1] = cvt_hi(p0);
-                        af[2] = cvt_lo(p1);
-                        af[3] = cvt_hi(p1);
-#else
-                        af[0] = dec_lo(h0);
-                        af[1] = dec_hi(h0);
-                        af[2] = dec_lo(h1);
-                        af[3] = dec_hi(h1);
-#endif
-                    } else {
-                        af[0] = vr[pv][0];
-                        af[1] = vr[pv][2];
-                        af[2] = vr[pv][1];
-                        af[3] = vr[pv][3];
-                    }
-#pragma unroll
-                    for (int j = 0; j < NT; ++j) mma_16816(o[j][pv], af, pf[j][k][0], pf[j][k][1]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));
-        }
-        // full row sums: add the partial sums of the 8 lanes sharing t
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float v = l_run[j][c];
-                v += __shfl_xor_sync(kFull, v, 4);
-                v += __shfl_xor_sync(kFull, v, 8);
-                v += __shfl_xor_sync(kFull, v, 16);
-                l_run[j][c] = v;
-            }
-    }
-
-    // ---- merge the token warps through shared memory, write the split partial ----
-    __syncthreads();
-    if (*abort_flag) {
-        // Something gave up: before the CTA's shared memory is released, wait
-        // (bounded) for every copy the producer issued, then leave without
-        // writing.  The error bit is already set.
-        if (warp >= kConsumerWarps && lane == 0)   // each producer: the stages it issued
-            for (int st = max(0, issued - G::kStages); st < issued; ++st)
-                mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr,
-                                  a.err_flag, 100000000ull);
-        __syncthreads();
-        return;
-    }
-    float *mbuf = reinterpret_cast<float *>(smem);    // [token warps][kRowsPad][D + 2]: m, l, o[D]
-    constexpr int kRowF = D + 2;
-    if (warp < kConsumerWarps) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int row = (rw * NT + j) * 8 + 2 * t + c;
-                float *dst = mbuf + (tw * W::kRowsPad + row) * kRowF;
-                if (gid == 0) {
-                    dst[0] = m_run[j][c];
-                    dst[1] = l_run[j][c];
-                }
-#pragma unroll
-                for (int pv = 0; pv < G::kPVTiles; ++pv) {
-                    const int2 ch = pv_channels<E4M3>(pv, gid);
-                    dst[2 + ch.x] = o[j][pv][c];
-                    dst[2 + ch.y] = o[j][pv][c + 2];
-                }
-            }
-    }
-    __syncthreads();
-    // Per row: the merge weights of the token warps (w_q / l, v_scale folded
-    // in), and the split's m and l; an empty row gets m = -inf, l = 0 and no
-    // output.
-    constexpr int TW = W::kTokWarps;
-    const int S = a.num_splits;
-    // the bitcast decoder yields V * 2^-8; the hardware conversion V itself
-    constexpr float kVFold = (E4M3 && !KVQ_V_CVT) ? 256.f : 1.f;
-    float *coef = mbuf + TW * W::kRowsPad * kRowF;        // [kRowsPad][TW]
-    for (int row = threadIdx.x; row < a.rows; row += kThreads) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < TW; ++q) M = fmaxf(M, mbuf[(q * W::kRowsPad + row) * kRowF]);
-        const int i = row / a.group, h = g * a.group + row % a.group;
-        const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
-        float w[TW];
-        float lsum = 0.f;
-#pragma unroll
-        for (int q = 0; q < TW; ++q) {
-            const float *src = mbuf + (q * W::kRowsPad + row) * kRowF;
-            w[q] = (M == -INFINITY) ? 0.f : fast_exp2(src[0] - M);
-            lsum += w[q] * src[1];
-        }
-        const float inv = lsum > 0.f ? a.out_scale * kVFold / lsum : 0.f;
-#pragma unroll
-        for (int q = 0; q < TW; ++q) coef[row * TW + q] = w[q] * inv;
-        a.ws_m[unit] = lsum > 0.f ? M * kLn2 : -INFINITY;
-        a.ws_l[unit] = lsum;
-    }
-    __syncthreads();
-    // o = sum_q coef_q * o_q, four channels per thread, stored as float4
-    for (int idx = threadIdx.x * 4; idx < a.rows * D; idx += kThreads * 4) {
-        const int row = idx / D, d = idx % D;
-        const float *cf = coef + row * TW;
-        bool any = false;
-#pragma unroll
-        for (int q = 0; q < TW; ++q) any |= cf[q] != 0.f;
-        if (!any) continue;                        // empty row: tmp_out stays unwritten
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < TW; ++q) {
-            const float c = cf[q];
-            const float *src = mbuf + (q * W::kRowsPad + row) * kRowF + 2 + d;
-            acc.x += c * src[0];
-            acc.y += c * src[1];
-            acc.z += c * src[2];
-            acc.w += c * src[3];
-        }
-        const int i = row / a.group, h = g * a.group + row % a.group;
-        const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
-        *reinterpret_cast<float4 *>(a.ws_o + unit * D + d) = acc;
-    }
+    if (a.batch == 0) return cudaSuccess;
+    if (e4m3 && a.bitcast_decode) return launch_attention_bitcast(head_dim, a, stream);
+    if (e4m3)
+        return head_dim == 128 ? launch_rows<true, 128, false>(a, stream)
+                               : launch_rows<true, 64, false>(a, stream);
+    return head_dim == 128 ? launch_rows<false, 128, false>(a, stream)
+                           : launch_rows<false, 64, false>(a, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -727,44 +119,6 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     } else {
         *reinterpret_cast<uint32_t *>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
     }
-}
-
-// ---------------------------------------------------------------------------
-// host launchers
-
-template <bool E4M3, int D, int NT, int RW>
-static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
-{
-    constexpr int bytes = smem_bytes<E4M3, D, NT, RW>();
-    static uint64_t configured = 0;   // one bit per device ordinal
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
-    }
-    const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-    return launch_pdl(attn_split_kernel<E4M3, D, NT, RW>, grid, dim3(kThreads), bytes, stream, a);
-}
-
-template <bool E4M3, int D>
-static cudaError_t launch_rows(const AttnArgs &a, cudaStream_t stream)
-{
-    const int tiles = (a.rows + 7) / 8;
-    if (tiles <= 1) return launch_one<E4M3, D, 1, 1>(a, stream);
-    if (tiles <= 2) return launch_one<E4M3, D, 2, 1>(a, stream);
-    if (tiles <= 4) return launch_one<E4M3, D, 2, 2>(a, stream);
-    return launch_one<E4M3, D, 2, 4>(a, stream);
-}
-
-cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream)
-{
-    if (a.batch == 0) return cudaSuccess;
-    if (e4m3) return head_dim == 128 ? launch_rows<true, 128>(a, stream) : launch_rows<true, 64>(a, stream);
-    return head_dim == 128 ? launch_rows<false, 128>(a, stream) : launch_rows<false, 64>(a, stream);
 }
 
 cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws_l, void *out,

@@ -24,6 +24,7 @@ KVQ_OK = 0
 STATUS = {0: "ok", -1: "invalid argument", -2: "bad scale", -3: "workspace", -4: "unsupported",
           -5: "CUDA error", -6: "alignment"}
 DEV_BAD_PAGE, DEV_BAD_SLOT, DEV_BAD_TOPK, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8, 16
+ATTN_BITCAST_DECODE = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -40,7 +41,8 @@ class AttnParams(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("num_splits", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("max_topk", ctypes.c_int32),
-                ("sm_scale", ctypes.c_float), ("split_pages", ctypes.c_int32)]
+                ("sm_scale", ctypes.c_float), ("split_pages", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
 
 
 EXPORTS = ("kvq_version", "kvq_status_string", "kvq_validate_scales", "kvq_amax_f16",
@@ -197,10 +199,11 @@ def kv_append_fp16(k_new, v_new, slot_mapping, k_cache, v_cache,
 # attention
 
 def attn_params(q: torch.Tensor, num_kv_heads: int, max_pages_per_seq: int, num_splits: int = 0,
-                max_topk: int = 0, sm_scale: float = 0.0, split_pages: int = 0) -> AttnParams:
+                max_topk: int = 0, sm_scale: float = 0.0, split_pages: int = 0,
+                bitcast_decode: bool = False) -> AttnParams:
     B, q_len, Hq, D = q.shape
     return AttnParams(B, q_len, Hq, num_kv_heads, D, num_splits, max_pages_per_seq, max_topk,
-                      sm_scale, split_pages)
+                      sm_scale, split_pages, ATTN_BITCAST_DECODE if bitcast_decode else 0)
 
 
 def num_splits(p: AttnParams) -> int:
@@ -236,7 +239,7 @@ def workspace_views(ws: torch.Tensor, p: AttnParams):
 
 
 def _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
-                topk_lens, cache_dtype, num_splits_, sm_scale, split_pages):
+                topk_lens, cache_dtype, num_splits_, sm_scale, split_pages, bitcast_decode=False):
     _need(q, "q", torch.float16, 4)
     B, q_len, Hq, D = q.shape
     _need(k_cache, "k_cache", cache_dtype, 4)
@@ -264,17 +267,17 @@ def _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out,
             raise ValueError("topk_idx must be [B, Hkv, K], topk_lens [B]")
         max_topk = topk_idx.shape[2]
     p = AttnParams(B, q_len, Hq, Hkv, D, num_splits_, block_tables.shape[1], max_topk, sm_scale,
-                   split_pages)
+                   split_pages, ATTN_BITCAST_DECODE if bitcast_decode else 0)
     return p
 
 
 def paged_decode_attn_e4m3(q, k_cache, v_cache, block_tables, context_lens, k_scale: float,
                            v_scale: float, workspace, out=None, topk_idx=None, topk_lens=None,
                            num_splits: int = 0, sm_scale: float = 0.0, err_flag=None,
-                           split_pages: int = 0):
+                           split_pages: int = 0, bitcast_decode: bool = False):
     """Decode / verify attention over E4M3 pools; returns `out` (fp16, shape of q)."""
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
-                    topk_lens, torch.uint8, num_splits, sm_scale, split_pages)
+                    topk_lens, torch.uint8, num_splits, sm_scale, split_pages, bitcast_decode)
     if out is None:
         out = torch.empty_like(q)
     _check("paged_decode_attn_e4m3", load().paged_decode_attn_e4m3(
@@ -303,9 +306,10 @@ def paged_decode_attn_fp16(q, k_cache, v_cache, block_tables, context_lens, work
 def paged_decode_attn_e4m3_partial(q, k_cache, v_cache, block_tables, context_lens,
                                    k_scale: float, v_scale: float, workspace, topk_idx=None,
                                    topk_lens=None, num_splits: int = 0, sm_scale: float = 0.0,
-                                   err_flag=None, split_pages: int = 0) -> AttnParams:
+                                   err_flag=None, split_pages: int = 0,
+                                   bitcast_decode: bool = False) -> AttnParams:
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, None, topk_idx,
-                    topk_lens, torch.uint8, num_splits, sm_scale, split_pages)
+                    topk_lens, torch.uint8, num_splits, sm_scale, split_pages, bitcast_decode)
     _check("paged_decode_attn_e4m3_partial", load().paged_decode_attn_e4m3_partial(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
         _ptr(context_lens), ctypes.c_float(k_scale), ctypes.c_float(v_scale), _ptr(topk_idx),

@@ -176,7 +176,17 @@ typedef struct {
                                   and num_splits * 4 * split_pages >= max_topk, so
                                   that every page and list entry has a split;
                                   otherwise the call returns KVQ_ERR_INVALID_ARG */
+    int32_t flags;             /* KVQ_ATTN_* bits below; other bits are refused     */
 } kvq_attn_params;
+
+/* E4M3 decoder of the attention kernels.  Default: the hardware conversion
+ * (cvt.rn.f16x2.e4m3x2), exact.  KVQ_ATTN_BITCAST_DECODE: the bitcast decoder
+ * of [P2] Changes (the E4M3 sign, exponent and mantissa bits placed into the
+ * fp16 bit pattern, which is the value times 2^-8, exact; the 2^8 is folded
+ * into the hoisted scales).  Both decode every byte to the same value up to
+ * that power of two, so the outputs are identical; the flag selects the
+ * instruction mix only.  Ignored for the fp16 twins. */
+#define KVQ_ATTN_BITCAST_DECODE 1
 
 /* The split count a call with these parameters uses: p->num_splits if > 0;
  * else, with split_pages > 0, the fewest splits that cover max_pages_per_seq

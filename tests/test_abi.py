@@ -74,7 +74,7 @@ def test_scale_from_amax(lib):
 
 def _params(**kw):
     p = dict(batch=2, q_len=1, num_q_heads=8, num_kv_heads=2, head_dim=64, num_splits=2,
-             max_pages_per_seq=25, max_topk=0, sm_scale=0.0, split_pages=0)
+             max_pages_per_seq=25, max_topk=0, sm_scale=0.0, split_pages=0, flags=0)
     p.update(kw)
     return kvq.AttnParams(**p)
 
@@ -90,6 +90,7 @@ def test_workspace_size_matches_layout(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 96, -4), ("q_len", 5, -4), ("q_len", 0, -1), ("num_kv_heads", 3, -1),
     ("num_splits", -1, -1), ("max_pages_per_seq", 0, -1), ("num_q_heads", 136, -4),
+    ("flags", 2, -1), ("flags", -1, -1),
 ])
 def test_bad_params_are_refused(lib, field, value, status):
     p = _params(**{field: value})

@@ -40,6 +40,34 @@ def test_tiny_matches_oracle(name, e4m3, S):
 
 
 @pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
+@pytest.mark.parametrize("S", [1, 2, 4, 0])
+def test_bitcast_decoder_matches_oracle_and_hardware_conversion(name, S):
+    """The pages' bitcast decoder (value * 2^-8, the 2^8 folded into the
+    hoisted scales) against the oracle, and bit for bit against the hardware
+    conversion: the two decode every byte to the same value up to a power of
+    two, so every product and sum scales exactly."""
+    dp = G.device_problem(P.host_problem(name), True)
+    hw = G.run_attention(dp, num_splits=S)
+    bc = G.run_attention(dp, num_splits=S, bitcast_decode=True)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    G.assert_close(bc.float().cpu().numpy(), _oracle_out(dp), f"bitcast {name} S={S}")
+    assert torch.equal(bc.view(torch.int16), hw.view(torch.int16))
+
+
+def test_bitcast_decoder_topk_and_nan_slots():
+    w = inputs.get("tiny_verify", topk=24, topk_fraction=0.5)
+    dp = G.device_problem(P.host_problem(w), True, sentinel=0x7F)   # NaN codes in unowned slots
+    for S in (1, 3):
+        hw = G.run_attention(dp, num_splits=S)
+        bc = G.run_attention(dp, num_splits=S, bitcast_decode=True)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        G.assert_close(bc.float().cpu().numpy(), _oracle_out(dp), f"bitcast top-k S={S}")
+        assert torch.equal(bc.view(torch.int16), hw.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
 @pytest.mark.parametrize("e4m3", [True, False])
 @pytest.mark.parametrize("split_pages,extra", [(2, 1), (8, 0), (16, 3)])
 def test_fixed_size_split_partials_match_oracle(name, e4m3, split_pages, extra):

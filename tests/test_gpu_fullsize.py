@@ -41,7 +41,7 @@ def pool():
 class Layer:
     """One layer of a workload pushed through the GPU path."""
 
-    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True):
+    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True, bitcast=False):
         self.w, self.layer, self.lay, self.e4m3 = w, layer, lay, e4m3
         lens = lay.lens.astype(np.int64)
         total = int(lens.sum())
@@ -92,7 +92,8 @@ class Layer:
         if e4m3:
             self.out = kvq.paged_decode_attn_e4m3(self.q, self.kc, self.vc, self.bt, self.cl, self.ks,
                                                   self.vs, ws, None, ti_d, tl_d, w.num_splits,
-                                                  err_flag=err, split_pages=w.split_pages)
+                                                  err_flag=err, split_pages=w.split_pages,
+                                                  bitcast_decode=bitcast)
         else:
             self.out = kvq.paged_decode_attn_fp16(self.q, self.kc, self.vc, self.bt, self.cl, ws, None,
                                                   ti_d, tl_d, w.num_splits, err_flag=err,
@@ -161,6 +162,9 @@ def test_decode_all_units(pool):
     assert L.S == 4
     units = [(b, h) for b in range(w.batch) for h in range(w.num_q_heads)]
     _check(L, pool, units, "decode e4m3")
+    # the bitcast decoder in the same launch configuration: bit-identical output
+    Lb = Layer(w, 0, lay, bitcast=True)
+    assert torch.equal(Lb.out.view(torch.int16), L.out.view(torch.int16))
 
 
 def test_decode_fp16_arm(pool):
