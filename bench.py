@@ -623,7 +623,7 @@ def main():
             "step_ms_p10_p50_p90_one_graph_each": pct,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
-                         "traffic": profiled_traffic("kvq_attn.cu", w.name),
+                         "traffic": profiled_traffic("kvq_attn_kernel.cuh", w.name),
                          "kernel": "attn_split_kernel (E4M3)", "peak_kind": peak_kind,
                          "attention_kernel_ms": kern_avg,
                          "bytes_per_launch": arm.bytes["attention_kernel"],
