@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
 
             // ---- S^T = K Q^T, one 16-token tile at a time ----
             float sc[NT][MTW][4];
+            float sc2[NT > 1 ? NT : 1][MTW][4];
 #pragma unroll
             for (int k = 0; k < MTW; ++k) {
                 uint32_t kr[G::kX4][4];
@@ -392,6 +393,12 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                 for (int j = 0; j < NT; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[j][k][e] = 0.f;
+                if (NT > 1) {
+#pragma unroll
+                    for (int j = 0; j < (NT > 1 ? NT : 1); ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc2[j][k][e] = 0.f;
+                }
 #pragma unroll
                 for (int ks = 0; ks < G::kKSteps; ++ks) {
                     uint32_t af[4];
@@ -415,8 +422,21 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                         af[2] = kr[ks][2];
                         af[3] = kr[ks][3];
                     }
+                    // with several row tiles, odd k-steps accumulate separately:
+                    // twice the independent MMA chains per warp
+                    if (NT > 1 && (ks & 1)) {
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) mma_16816(sc[j][k], af, qf[j][ks][0], qf[j][ks][1]);
+                        for (int j = 0; j < NT; ++j) mma_16816(sc2[j][k], af, qf[j][ks][0], qf[j][ks][1]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) mma_16816(sc[j][k], af, qf[j][ks][0], qf[j][ks][1]);
+                    }
+                }
+                if (NT > 1) {
+#pragma unroll
+                    for (int j = 0; j < NT; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[j][k][e] += sc2[j][k][e];
                 }
             }
             // ---- scores in the log2 domain, masking ----
@@ -441,6 +461,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                 }
             }
             // ---- online softmax (row max across the 8 lanes sharing t) ----
+            // The O rescale is skipped while no row of the warp raised its
+            // running max (a factor of exactly 1): after the first tiles a new
+            // maximum is rare, and this saves 8 multiplies per row and tile.
+            float corr[NT][2];
+            bool raised = false;
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -453,14 +478,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
                     const float m_new = fmaxf(m_run[j][c], mx);
                     const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                    const float corr = fast_exp2(m_run[j][c] - m_use);
+                    const bool up = m_new != m_run[j][c];
+                    corr[j][c] = up ? fast_exp2(m_run[j][c] - m_use) : 1.f;
+                    raised |= up;
                     m_run[j][c] = m_new;
-                    float lsum = l_run[j][c] * corr;
-#pragma unroll
-                    for (int pv = 0; pv < G::kPVTiles; ++pv) {
-                        o[j][pv][c] *= corr;
-                        o[j][pv][c + 2] *= corr;
-                    }
+                    float lsum = l_run[j][c] * corr[j][c];
 #pragma unroll
                     for (int k = 0; k < MTW; ++k) {
                         const float p0 = fast_exp2(sc[j][k][c] - m_use);
@@ -471,6 +493,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                     }
                     l_run[j][c] = lsum;
                 }
+            if (__any_sync(kFull, raised)) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j)
+#pragma unroll
+                    for (int pv = 0; pv < G::kPVTiles; ++pv) {
+                        o[j][pv][0] *= corr[j][0];
+                        o[j][pv][2] *= corr[j][0];
+                        o[j][pv][1] *= corr[j][1];
+                        o[j][pv][3] *= corr[j][1];
+                    }
+            }
             // ---- P^T as mma B fragments: transpose the score tiles in registers ----
             uint32_t pf[NT][MTW][2];
 #pragma unroll
