@@ -110,93 +110,51 @@ __device__ __forceinline__ int2 pv_channels(int pv, int gid)
     return make_int2(16 * pv + gid, 16 * pv + 8 + gid);
 }
 
-// BITCAST selects the E4M3 decoder: false = the hardware conversion
-// (cvt.rn.f16x2.e4m3x2, the value itself); true = the bitcast decoder of the
-// source pages (E4M3 bits placed into fp16 bits, the value * 2^-8, exact),
-// with the 2^8 folded into the hoisted scales.  Both give the same fp16
-// values up to that power of two, so the outputs are identical.
-template <bool E4M3, int D, int NT, int RW, bool BITCAST>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
-    attn_split_kernel(const AttnArgs a)
+// The split's share of one (sequence, kv head): the context length, the
+// mode, and the items (logical pages, or top-k list entries) it covers --
+// split s covers items [s * per, (s + 1) * per): an equal share of this
+// sequence, or a fixed number of pages (4 list entries per page).
+struct SplitRange {
+    const int32_t *bt_row;
+    int L, item0, item1, spec0;
+    bool len_ok, topk;
+};
+
+__device__ __forceinline__ SplitRange split_range(const AttnArgs &a, int s, int b)
 {
-    using W = Split<NT, RW>;
-    constexpr int PPS = W::kPagesPerStage;
-    constexpr int MTW = W::kTilesPerWarp;
-    using G = Geometry<E4M3, D, PPS>;
-    extern __shared__ __align__(128) uint8_t smem[];
-
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t ring = smem_u32(smem);
-    int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
-    const uint32_t bar0 = smem_u32(smem + G::kBarOff);   // full[k] = bar0 + 8k, empty[k] = bar0 + 8(S+k)
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
-    volatile int *stage_bad = abort_flag + 1;            // a bad entry was seen (sticky)
-
-    // barriers first: this part reads no input and overlaps the previous kernel's tail
-    if (threadIdx.x == 0) {
-        for (int k = 0; k < G::kStages; ++k) {
-            mbar_init(bar0 + 8 * k, kProducerWarps);   // one arrive.expect_tx per producer
-            mbar_init(bar0 + 8 * (G::kStages + k), kConsumerWarps);
-        }
-        *abort_flag = 0;
-        *stage_bad = 0;
-        fence_mbar_init();
-    }
-    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
-    launch_dependents();      // the combine may start launching; it waits for our completion
-
-    // ---- work of this CTA --------------------------------------------------
-    // The producers' first block-table batch is fetched speculatively for a
-    // sequence that fills its block-table row, in parallel with the context
-    // length; it is refetched below if the real split starts elsewhere.
-    const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
+    SplitRange r;
+    r.bt_row = a.block_tables + (int64_t)b * a.max_pages;
     const int64_t spec_per = a.split_pages > 0 ? (int64_t)a.split_pages
                                                : (int64_t)(a.max_pages + a.num_splits - 1) / a.num_splits;
-    const int spec0 = (int)min((int64_t)s * spec_per, (int64_t)a.max_pages);
-    int bt_spec = -1;
-    if (warp >= kConsumerWarps && spec0 + lane < a.max_pages) bt_spec = __ldg(bt_row + spec0 + lane);
-    const int L = a.context_lens[b];
-    const bool len_ok = (L >= a.q_len) && (L <= a.max_pages * 4);
+    r.spec0 = (int)min((int64_t)s * spec_per, (int64_t)a.max_pages);
+    r.L = a.context_lens[b];
+    r.len_ok = (r.L >= a.q_len) && (r.L <= a.max_pages * 4);
     int topk_n = (a.topk_idx && a.topk_lens) ? a.topk_lens[b] : 0;
-    const bool topk = len_ok && topk_n > 0;
-    if (topk && topk_n > a.max_topk) topk_n = a.max_topk;
-    const int n_items = !len_ok ? 0 : (topk ? topk_n : (L + 3) / 4);   // pages or list entries
-    // split s covers items [s * per, (s + 1) * per): an equal share of this
-    // sequence, or a fixed number of pages (4 list entries per page)
-    const int64_t per = a.split_pages > 0 ? (topk ? 4 * (int64_t)a.split_pages : (int64_t)a.split_pages)
+    r.topk = r.len_ok && topk_n > 0;
+    if (r.topk && topk_n > a.max_topk) topk_n = a.max_topk;
+    const int n_items = !r.len_ok ? 0 : (r.topk ? topk_n : (r.L + 3) / 4);
+    const int64_t per = a.split_pages > 0 ? (r.topk ? 4 * (int64_t)a.split_pages : (int64_t)a.split_pages)
                                           : (int64_t)(n_items + a.num_splits - 1) / a.num_splits;
-    const int item0 = (int)min((int64_t)s * per, (int64_t)n_items);
-    const int item1 = (int)min(item0 + per, (int64_t)n_items);
-    const int ipst = topk ? G::kTokPerStage : PPS;        // items per stage
-    const int nst = (item1 - item0 + ipst - 1) / ipst;
+    r.item0 = (int)min((int64_t)s * per, (int64_t)n_items);
+    r.item1 = (int)min(r.item0 + per, (int64_t)n_items);
+    return r;
+}
 
-    if (threadIdx.x == 0) {
-        if (!len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
-        if (len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
-            report(a.err_flag, KVQ_DEV_BAD_TOPK);
-    }
-    __syncthreads();
-
-    float o[NT][G::kPVTiles][4];
-    float m_run[NT][2], l_run[NT][2];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-#pragma unroll
-        for (int pv = 0; pv < G::kPVTiles; ++pv)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[j][pv][e] = 0.f;
-        m_run[j][0] = m_run[j][1] = -INFINITY;
-        l_run[j][0] = l_run[j][1] = 0.f;
-    }
-    const int gid = lane >> 2, t = lane & 3;
-    const int rw = warp % RW, tw = warp / RW;
-    int issued = 0;   // stages this producer has issued
-
-    if (warp >= kConsumerWarps) {
-        // ================= producers: the first moves K, the second V =================
+// One producer warp (K pages when !is_v, V pages otherwise) walks the
+// split's nst stages: it reads the block table a batch ahead, waits for the
+// stage's ring slot to be released, records the token positions (K warp),
+// and issues one 1-D bulk copy per page (dense) or per listed token row
+// (top-k), completing on the slot's full mbarrier.  Returns the stages issued.
+template <class G, int PPS>
+__device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRange &r, int nst, int b, int g,
+                                              int lane, bool is_v, int bt_spec, uint32_t ring, uint32_t bar0,
+                                              int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad)
+{
+    const int item0 = r.item0, item1 = r.item1, L = r.L, spec0 = r.spec0;
+    const bool topk = r.topk;
+    const int32_t *bt_row = r.bt_row;
+    int issued = 0;
         const uint64_t pol = l2_policy_evict_first();
-        const bool is_v = warp == kConsumerWarps + 1;
         const uint8_t *pool = static_cast<const uint8_t *>(is_v ? a.v_cache : a.k_cache);
         if (!topk) {
             constexpr int SPB = 32 / PPS;                 // stages per block-table batch
@@ -307,6 +265,85 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                 issued = st + 1;
             }
         }
+    return issued;
+}
+
+// BITCAST selects the E4M3 decoder: false = the hardware conversion
+// (cvt.rn.f16x2.e4m3x2, the value itself); true = the bitcast decoder of the
+// source pages (E4M3 bits placed into fp16 bits, the value * 2^-8, exact),
+// with the 2^8 folded into the hoisted scales.  Both give the same fp16
+// values up to that power of two, so the outputs are identical.
+template <bool E4M3, int D, int NT, int RW, bool BITCAST>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
+    attn_split_kernel(const AttnArgs a)
+{
+    using W = Split<NT, RW>;
+    constexpr int PPS = W::kPagesPerStage;
+    constexpr int MTW = W::kTilesPerWarp;
+    using G = Geometry<E4M3, D, PPS>;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring = smem_u32(smem);
+    int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
+    const uint32_t bar0 = smem_u32(smem + G::kBarOff);   // full[k] = bar0 + 8k, empty[k] = bar0 + 8(S+k)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
+    volatile int *stage_bad = abort_flag + 1;            // a bad entry was seen (sticky)
+
+    // barriers first: this part reads no input and overlaps the previous kernel's tail
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < G::kStages; ++k) {
+            mbar_init(bar0 + 8 * k, kProducerWarps);   // one arrive.expect_tx per producer
+            mbar_init(bar0 + 8 * (G::kStages + k), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        *stage_bad = 0;
+        fence_mbar_init();
+    }
+    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
+    launch_dependents();      // the combine may start launching; it waits for our completion
+
+    // ---- work of this CTA --------------------------------------------------
+    // The producers' first block-table batch is fetched speculatively for a
+    // sequence that fills its block-table row, in parallel with the context
+    // length; it is refetched below if the real split starts elsewhere.
+    const SplitRange sr = split_range(a, s, b);
+    const int32_t *bt_row = sr.bt_row;
+    const int L = sr.L, item0 = sr.item0, item1 = sr.item1;
+    const bool len_ok = sr.len_ok, topk = sr.topk;
+    int bt_spec = -1;
+    if (warp >= kConsumerWarps && sr.spec0 + lane < a.max_pages) bt_spec = __ldg(bt_row + sr.spec0 + lane);
+    const int ipst = topk ? G::kTokPerStage : PPS;        // items per stage
+    const int nst = (item1 - item0 + ipst - 1) / ipst;
+
+    if (threadIdx.x == 0) {
+        if (!len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
+        if (len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
+            report(a.err_flag, KVQ_DEV_BAD_TOPK);
+    }
+    __syncthreads();
+
+    float o[NT][G::kPVTiles][4];
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int pv = 0; pv < G::kPVTiles; ++pv)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[j][pv][e] = 0.f;
+        m_run[j][0] = m_run[j][1] = -INFINITY;
+        l_run[j][0] = l_run[j][1] = 0.f;
+    }
+    const int gid = lane >> 2, t = lane & 3;
+    const int rw = warp % RW, tw = warp / RW;
+    int issued = 0;   // stages this producer has issued
+
+    if (warp >= kConsumerWarps) {
+        // ================= producers: the first moves K, the second V =================
+        const bool is_v = warp == kConsumerWarps + 1;
+        issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos, abort_flag,
+                                        stage_bad);
     } else {
         // ================= consumers =================
         // Q as mma B fragments, one set per 8-row n-tile; k-step ks of this

@@ -1,0 +1,484 @@
+// kvq_attn_tc.cu -- split-K paged attention for many query rows per kv head
+// (MTP verify: G heads x q_len rows, 16 < rows <= 64) on the fifth-generation
+// tensor cores (tcgen05.mma, accumulators in tensor memory).
+//
+// What is computed is the same as attn_split_kernel -- PR "[Model][SM70][FP8]
+// Integrate calibrated E4M3 QSA KV capacity path", section Changes; PR
+// "[Model][SM70] Calibrated E4M3 KV cache for Qwen4Exp QSA with MTP", sections
+// Purpose and Status and history: grouped-query attention of q_len rows,
+// causal inside the verify window, over a page-4 E4M3 (or fp16) cache with the
+// per-layer scales hoisted, split over the token axis into the same FP32
+// workspace partials.
+//
+// Design (one CTA per (split, kv head, sequence); 7 warps):
+//  * warps 4, 5: the producers of the split kernel -- 1-D bulk copies of K and
+//    V pages (16 pages = 64 tokens per staging stage) into a shared ring.
+//  * warps 0-3 ("workers", warp q owns tensor-memory lanes 32q..32q+31): per
+//    tile of 128 tokens (two staging stages) each worker converts its 32
+//    tokens -- K rows to fp16 straight into tensor memory (the A operand of
+//    S^T = K Q^T, token t in lane t), V rows to fp16 in shared memory (the
+//    MN-major A operand of O^T = V^T P^T) -- then reads S^T back (thread =
+//    token, one column per query row), runs the online softmax in the log2
+//    domain with the scores' scale hoisted, and writes P^T (fp16, MN-major)
+//    to shared memory.  Row maxima and sums over the 128 tokens are reduced
+//    across the lanes by a butterfly transpose and across the four workers
+//    through shared memory.  The O^T accumulator (lane = channel, column =
+//    query row) is rescaled in tensor memory only when a row's maximum rises
+//    by more than 2^8 over the reference used so far; the exact maximum is
+//    tracked apart and restored in the epilogue.
+//  * warp 6: allocates tensor memory; one thread issues the MMAs (M = 128
+//    tokens or channels, N = rows padded to 16/32/64, K = 16 per instruction)
+//    and commits their completion to mbarriers.
+//  * Every wait is bounded (about 2 s); on expiry the CTA reports
+//    KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor memory
+//    and exits without writing.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvq_attn_kernel.cuh"
+#include "kvq_tcgen05.cuh"
+
+namespace kvq {
+
+constexpr int kTcWorkers = 4;
+constexpr int kTcMmaWarp = kConsumerWarps + kProducerWarps;   // 6
+constexpr int kTcThreads = 32 * (kTcMmaWarp + 1);             // 224
+constexpr int kTcTile = 128;                                  // tokens per MMA tile
+constexpr int kTcD = 128;                                     // head_dim of this kernel
+constexpr int kTcPPS = 16;                                    // pages per staging stage (64 tokens)
+
+// shared memory after the staging ring of Geometry<E4M3, 128, 16>
+template <bool E4M3, int NR>
+struct TcLayout {
+    using G = Geometry<E4M3, kTcD, kTcPPS>;
+    static constexpr int kQ = (G::kBytes + 1023) & ~1023;   // Q: NR x 128 fp16, K-major
+    static constexpr int kV = kQ + NR * 256;                 // V^T: 128 ch x 128 tok fp16, MN-major
+    static constexpr int kP = kV + kTcTile * kTcD * 2;       // P^T: NR x 128 tok fp16, MN-major
+    static constexpr int kWmax = kP + NR * 256;              // [2][4][NR] float: per-worker row maxima
+    static constexpr int kPriv = kWmax + 2 * 4 * NR * 4;     // [4][3][NR] float: per-worker m_ref, corr, coef
+    static constexpr int kLsum = kPriv + 4 * 3 * NR * 4;     // [4][NR] float: per-worker row sums
+    static constexpr int kBar = kLsum + 4 * NR * 4;          // 7 mbarriers
+    static constexpr int kTmemSlot = kBar + 7 * 8;
+    static constexpr int kBytes = kTmemSlot + 16;
+    // tensor-memory columns: K tile (64: 128 fp16 per lane), S^T (NR), O^T (NR)
+    static constexpr int kColK = 0, kColS = 64, kColO = 64 + NR;
+    static constexpr int kCols = (64 + 2 * NR) <= 128 ? 128 : 256;
+};
+
+// Lane r of the warp ends with the maximum (or sum) over the warp's 32 lanes
+// of value v[r] (r < 32): a butterfly that halves the set each step.
+template <bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) {
+        const bool hi = (lane & k) != 0;
+#pragma unroll
+        for (int i = 0; i < k; ++i) {
+            const float send = hi ? v[i] : v[i + k];
+            const float keep = hi ? v[i + k] : v[i];
+            const float recv = __shfl_xor_sync(kFull, send, k);
+            v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    return v[0];   // row `lane`
+}
+
+template <bool E4M3, int NR>
+__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a)
+{
+    constexpr int D = kTcD, PPS = kTcPPS;
+    using G = Geometry<E4M3, D, PPS>;
+    using T = TcLayout<E4M3, NR>;
+    constexpr int NH = NR <= 32 ? 1 : 2;                      // rows per lane after a transpose-reduce
+    extern __shared__ __align__(1024) uint8_t smem[];
+
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring = smem_u32(smem);
+    int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
+    const uint32_t bar0 = smem_u32(smem + G::kBarOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
+    volatile int *stage_bad = abort_flag + 1;
+    const uint32_t tb = smem_u32(smem + T::kBar);
+    const uint32_t b_ops = tb, b_s = tb + 8, b_p = tb + 16, b_pv = tb + 24, b_x = tb + 32, b_l = tb + 40,
+                   b_drain = tb + 48;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::kTmemSlot);
+
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < G::kStages; ++k) {
+            mbar_init(bar0 + 8 * k, kProducerWarps);
+            mbar_init(bar0 + 8 * (G::kStages + k), 2);   // each staging stage feeds two workers
+        }
+        mbar_init(b_ops, kTcWorkers);
+        mbar_init(b_s, 1);
+        mbar_init(b_p, kTcWorkers);
+        mbar_init(b_pv, 1);
+        mbar_init(b_x, kTcWorkers);
+        mbar_init(b_l, kTcWorkers);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        *stage_bad = 0;
+        fence_mbar_init();
+    }
+    if (warp == kTcMmaWarp) tmem_alloc(smem_u32(tmem_slot), T::kCols);
+    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
+
+    const SplitRange sr = split_range(a, s, b);
+    const int L = sr.L;
+    int bt_spec = -1;
+    if (warp >= kConsumerWarps && warp < kTcMmaWarp && sr.spec0 + lane < a.max_pages)
+        bt_spec = __ldg(sr.bt_row + sr.spec0 + lane);
+    const int ipst = sr.topk ? G::kTokPerStage : PPS;
+    const int nst = (sr.item1 - sr.item0 + ipst - 1) / ipst;   // staging stages
+    const int ntiles = (nst + 1) / 2;
+    if (threadIdx.x == 0) {
+        if (!sr.len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
+        if (sr.len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
+            report(a.err_flag, KVQ_DEV_BAD_TOPK);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // only now may a dependent grid start: this CTA already holds its tensor
+    // memory, so a dependent CTA cannot take the columns it waits for
+    launch_dependents();
+    const uint32_t tmem = *tmem_slot;
+    int issued = 0;
+
+    if (warp >= kConsumerWarps && warp < kTcMmaWarp) {
+        // ================= producers =================
+        issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, warp == kConsumerWarps + 1, bt_spec, ring,
+                                        bar0, tokpos, abort_flag, stage_bad);
+    } else if (warp == kTcMmaWarp) {
+        // ================= MMA issue (one thread) =================
+        if (lane == 0) {
+            const uint32_t q_addr = smem_u32(smem + T::kQ), v_addr = smem_u32(smem + T::kV),
+                           p_addr = smem_u32(smem + T::kP);
+            const uint32_t id_qk = umma_idesc_f16(kTcTile, NR, false, false);
+            const uint32_t id_pv = umma_idesc_f16(kTcTile, NR, true, true);
+            for (int t = 0; t < ntiles; ++t) {
+                if (!mbar_wait_bounded(b_ops, t & 1, abort_flag, a.err_flag)) break;
+                tc_fence_after();
+                // S^T[tok][row] = sum_d K[tok][d] Q[row][d]: A = K tile (tensor memory), B = Q (K-major)
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    umma_tmem_a(tmem + T::kColS, tmem + T::kColK + ks * 8,
+                                umma_desc(q_addr + ks * 256, 128, (D / 8) * 128), id_qk, ks > 0);
+                umma_commit(b_s);
+                if (!mbar_wait_bounded(b_p, t & 1, abort_flag, a.err_flag)) break;
+                tc_fence_after();
+                // O^T[ch][row] += sum_tok V[tok][ch] P[tok][row]: A = V^T, B = P^T, both MN-major
+#pragma unroll
+                for (int ks = 0; ks < kTcTile / 16; ++ks)
+                    umma_smem_a(tmem + T::kColO, umma_desc(v_addr + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128),
+                                umma_desc(p_addr + ks * 2 * NR * 16, NR * 16, 128), id_pv, t > 0 || ks > 0);
+                umma_commit(b_pv);
+            }
+            // every MMA issued so far completes before the tensor memory is freed
+            umma_commit(b_drain);
+            mbar_wait_bounded(b_drain, 0, nullptr, a.err_flag, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ================= workers: conversion, softmax, epilogue =================
+        const int q = warp;                          // tensor-memory lane quadrant
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int tt = 32 * q + lane;                // token of the tile (S^T lane), channel of O^T
+        const float qk = a.qk_scale_log2;
+        const int win0 = L - a.q_len;                // row i sees positions <= win0 + i
+        float *wmax = reinterpret_cast<float *>(smem + T::kWmax);
+        float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 3 * NR;   // m_ref, corr, coef
+        float *lsum = reinterpret_cast<float *>(smem + T::kLsum);
+
+        // Q rows (padding rows zero) into the K-major Q tile: element (r, d) at
+        // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2
+        for (int idx = tt; idx < NR * (D / 8); idx += 32 * kTcWorkers) {
+            const int r = idx / (D / 8), c = idx % (D / 8);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < a.rows) {
+                const int i = r / a.group, h = g * a.group + r % a.group;
+                v = *reinterpret_cast<const uint4 *>(static_cast<const __half *>(a.q) +
+                                                     (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D + 8 * c);
+            }
+            *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
+        }
+
+        // per-row state, row (NH == 1 ? lane : lane and lane + 32) of this lane
+        float m_ref[NH], m_true[NH], l_w[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            m_ref[h] = -INFINITY;
+            m_true[h] = -INFINITY;
+            l_w[h] = 0.f;
+        }
+        bool ok = true;
+        for (int t = 0; t < ntiles && ok; ++t) {
+            // V^T and P^T are reused: the previous tile's PV must be done
+            if (t > 0 && !mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            const int st = 2 * t + (q >> 1);         // staging stage of this warp's 32 tokens
+            const int j = (q & 1) * 32 + lane;       // token of that stage
+            const bool have = st < nst;
+            const int slot = st % G::kStages;
+            if (have && !mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag)) {
+                ok = false;
+                break;
+            }
+            const int pos = have ? tokpos[slot * G::kTokPerStage + j] : -1;
+            const uint8_t *krow = smem + slot * G::kStageBytes + (j >> 2) * G::kPageStride + (j & 3) * G::kRowBytes;
+            const uint8_t *vrow = krow + G::kRegion;
+            // ---- K row -> fp16 in tensor memory (token tt in lane tt, channels 2c, 2c+1 in column c) ----
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {            // 16 columns = 32 channels per store
+                uint32_t w[16];
+                if (E4M3) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint4 x = have ? *reinterpret_cast<const uint4 *>(krow + 32 * h + 16 * u)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                        w[8 * u + 0] = cvt_lo(x.x);
+                        w[8 * u + 1] = cvt_hi(x.x);
+                        w[8 * u + 2] = cvt_lo(x.y);
+                        w[8 * u + 3] = cvt_hi(x.y);
+                        w[8 * u + 4] = cvt_lo(x.z);
+                        w[8 * u + 5] = cvt_hi(x.z);
+                        w[8 * u + 6] = cvt_lo(x.w);
+                        w[8 * u + 7] = cvt_hi(x.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 x = have ? *reinterpret_cast<const uint4 *>(krow + 64 * h + 16 * u)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                        w[4 * u + 0] = x.x;
+                        w[4 * u + 1] = x.y;
+                        w[4 * u + 2] = x.z;
+                        w[4 * u + 3] = x.w;
+                    }
+                }
+                tmem_st16(tmem + lane_base + T::kColK + 16 * h, w);
+            }
+            // ---- V row -> fp16 V^T tile (MN-major): (ch, tok) at (tok/8)*2048 + (ch/8)*128 + (tok%8)*16 ----
+            // a slot without a token is zeroed: its bits may be NaN, and P = 0 alone leaves 0 * NaN
+            {
+                uint8_t *vdst = smem + T::kV + (tt >> 3) * ((D / 8) * 128) + (tt & 7) * 16;
+                const bool vok = have && pos >= 0;
+#pragma unroll
+                for (int c = 0; c < D / 16; ++c) {   // 16 channels per step
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
+                    if (vok) {
+                        if (E4M3) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(vrow + 16 * c);
+                            lo = make_uint4(cvt_lo(x.x), cvt_hi(x.x), cvt_lo(x.y), cvt_hi(x.y));
+                            hi = make_uint4(cvt_lo(x.z), cvt_hi(x.z), cvt_lo(x.w), cvt_hi(x.w));
+                        } else {
+                            lo = *reinterpret_cast<const uint4 *>(vrow + 32 * c);
+                            hi = *reinterpret_cast<const uint4 *>(vrow + 32 * c + 16);
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(vdst + (2 * c) * 128) = lo;
+                    *reinterpret_cast<uint4 *>(vdst + (2 * c + 1) * 128) = hi;
+                }
+            }
+            __syncwarp();
+            if (have && lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));   // staging slot consumed
+            tmem_wait_st();
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_ops);
+
+            // ---- S^T of this warp's 32 tokens: one column per query row ----
+            if (!mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            tc_fence_after();
+            float x[NR];
+#pragma unroll
+            for (int c = 0; c < NR; c += 16) {
+                uint32_t r16[16];
+                tmem_ld16(tmem + lane_base + T::kColS + c, r16);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[c + e] = __uint_as_float(r16[e]);
+            }
+            // scores in the log2 domain; row r (window row r / G) sees positions <= win0 + r / G
+            const int rmin = pos < 0 ? NR : (pos > win0 ? a.group * (pos - win0) : 0);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) x[r] = (r >= rmin && r < a.rows) ? x[r] * qk : -INFINITY;
+
+            // ---- row maxima over the tile: lanes, then the four workers ----
+            float tmax[NH];
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                float v[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) v[r] = (32 * h + r < NR) ? x[32 * h + r] : -INFINITY;
+                tmax[h] = warp_transpose_reduce<true>(v, lane);
+                if (32 * h + lane < NR) wmax[((t & 1) * 4 + q) * NR + 32 * h + lane] = tmax[h];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_x);
+            if (!mbar_wait_bounded(b_x, t & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            bool rescale = false;
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                const int r = 32 * h + lane;
+                float mx = -INFINITY;
+                if (r < NR)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, wmax[((t & 1) * 4 + w) * NR + r]);
+                m_true[h] = fmaxf(m_true[h], mx);
+                float corr = 1.f;
+                // a new reference only when the maximum rises more than 2^8 above it
+                if (mx > -INFINITY && (m_ref[h] == -INFINITY || mx > m_ref[h] + 8.f)) {
+                    corr = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(m_ref[h] - mx);
+                    m_ref[h] = mx;
+                    rescale = true;
+                }
+                if (r < NR) {
+                    priv[r] = (m_ref[h] == -INFINITY) ? 0.f : m_ref[h];
+                    priv[NR + r] = corr;
+                }
+                l_w[h] *= corr;
+            }
+            __syncwarp();
+            // ---- P = exp2(score - reference), row sums ----
+#pragma unroll
+            for (int r = 0; r < NR; ++r) x[r] = fast_exp2(x[r] - priv[r]);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                float v[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) v[r] = (32 * h + r < NR) ? x[32 * h + r] : 0.f;
+                l_w[h] += warp_transpose_reduce<false>(v, lane);
+            }
+            // ---- O^T columns of rows whose reference moved (the previous PV is complete) ----
+            if (t > 0 && __any_sync(kFull, rescale)) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < NR; c += 16) {
+                    uint32_t r16[16];
+                    tmem_ld16(tmem + lane_base + T::kColO + c, r16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * priv[NR + c + e]);
+                    tmem_st16(tmem + lane_base + T::kColO + c, r16);
+                }
+                tmem_wait_st();
+            }
+            // ---- P^T (fp16, MN-major): (row, tok) at (tok/8) * NR*16 + (row/8) * 128 + (tok%8) * 16 ----
+            {
+                uint8_t *pdst = smem + T::kP + (tt >> 3) * (NR * 16) + (tt & 7) * 16;
+#pragma unroll
+                for (int c = 0; c < NR / 8; ++c) {
+                    uint4 v;
+                    v.x = pack_half2(x[8 * c + 0], x[8 * c + 1]);
+                    v.y = pack_half2(x[8 * c + 2], x[8 * c + 3]);
+                    v.z = pack_half2(x[8 * c + 4], x[8 * c + 5]);
+                    v.w = pack_half2(x[8 * c + 6], x[8 * c + 7]);
+                    *reinterpret_cast<uint4 *>(pdst + c * 128) = v;
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p);
+        }
+
+        // ---- epilogue: the split's partial (o normalised, m, l) per row ----
+        if (ok && !*abort_flag) {
+            bool have_o = ntiles > 0;
+            if (have_o && !mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag)) have_o = false;
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < NH; ++h)
+                if (32 * h + lane < NR) lsum[q * NR + 32 * h + lane] = l_w[h];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_l);
+            if (mbar_wait_bounded(b_l, 0, abort_flag, a.err_flag) && !*abort_flag) {
+                const int S = a.num_splits;
+                // per row: total l (relative to the reference), the coefficient v_scale / l
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    const int r = 32 * h + lane;
+                    if (r >= NR) continue;
+                    float lt = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) lt += lsum[w * NR + r];
+                    priv[2 * NR + r] = lt > 0.f ? a.out_scale / lt : 0.f;
+                    if (q == 0 && r < a.rows) {
+                        const int i = r / a.group, hh = g * a.group + r % a.group;
+                        const int64_t unit = (((int64_t)b * a.num_q_heads + hh) * a.q_len + i) * S + s;
+                        // the sum relative to the exact maximum, m in natural-log units
+                        a.ws_m[unit] = lt > 0.f ? m_true[h] * kLn2 : -INFINITY;
+                        a.ws_l[unit] = lt > 0.f ? lt * fast_exp2(m_ref[h] - m_true[h]) : 0.f;
+                    }
+                }
+                __syncwarp();
+                if (have_o) {
+#pragma unroll
+                    for (int c = 0; c < NR; c += 16) {
+                        uint32_t r16[16];
+                        tmem_ld16(tmem + lane_base + T::kColO + c, r16);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int r = c + e;
+                            const float coef = priv[2 * NR + r];
+                            if (r < a.rows && coef != 0.f) {
+                                const int i = r / a.group, hh = g * a.group + r % a.group;
+                                const int64_t unit = (((int64_t)b * a.num_q_heads + hh) * a.q_len + i) * S + s;
+                                a.ws_o[unit * D + tt] = __uint_as_float(r16[e]) * coef;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown: copies drained, MMAs complete (the MMA thread waited), tensor memory freed ----
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && warp >= kConsumerWarps && warp < kTcMmaWarp && lane == 0)
+        for (int st = max(0, issued - G::kStages); st < issued; ++st)
+            mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr, a.err_flag,
+                              100000000ull);
+    tc_fence_after();
+    __syncthreads();
+    if (warp == kTcMmaWarp) tmem_dealloc(tmem, T::kCols);
+}
+
+template <bool E4M3, int NR>
+static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
+{
+    constexpr int bytes = TcLayout<E4M3, NR>::kBytes;
+    static uint64_t configured = 0;   // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
+    return launch_pdl(attn_tc_kernel<E4M3, NR>, grid, dim3(kTcThreads), bytes, stream, a);
+}
+
+bool tc_supported(int head_dim, int rows) { return head_dim == kTcD && rows > 8 && rows <= 64; }
+
+cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t stream)
+{
+    if (a.batch == 0) return cudaSuccess;
+    if (e4m3) {
+        if (a.rows <= 16) return launch_tc_one<true, 16>(a, stream);
+        if (a.rows <= 32) return launch_tc_one<true, 32>(a, stream);
+        return launch_tc_one<true, 64>(a, stream);
+    }
+    if (a.rows <= 16) return launch_tc_one<false, 16>(a, stream);
+    if (a.rows <= 32) return launch_tc_one<false, 32>(a, stream);
+    return launch_tc_one<false, 64>(a, stream);
+}
+
+}  // namespace kvq

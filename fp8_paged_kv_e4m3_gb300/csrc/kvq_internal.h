@@ -29,6 +29,7 @@ struct AttnArgs {
     float qk_scale_log2;         // hoisted: sm_scale * log2(e) [* k_scale for E4M3]
     float out_scale;             // hoisted: v_scale for E4M3, 1 for fp16
     bool bitcast_decode;         // E4M3: the bitcast decoder instead of the hardware conversion
+    bool tcgen05;                // many-row tiles on the tcgen05 kernel
 };
 
 struct WorkspaceLayout {
@@ -39,6 +40,8 @@ WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t
 
 cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_bitcast(int head_dim, const AttnArgs &a, cudaStream_t stream);
+cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t stream);
+bool tc_supported(int head_dim, int rows);
 cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws_l, void *out,
                            int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim,
                            int32_t num_splits, cudaStream_t stream);
