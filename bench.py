@@ -250,7 +250,7 @@ class Arm:
         self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, self.topk_np)
         self.launches = 3   # kernels of one step: append, attention, combine
         self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
-        self.tcgen05 = False  # many-row tiles: the mma.sync kernel (default) or the tcgen05 kernel
+        self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
         torch.cuda.synchronize(dev)
 
@@ -269,11 +269,11 @@ class Arm:
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
                                                err_flag=self.err, split_pages=self.w.split_pages,
-                                               bitcast_decode=self.bitcast, tcgen05=self.tcgen05)
+                                               bitcast_decode=self.bitcast, mma_sync=self.mma_sync)
         else:
             kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, self.topk_idx,
                                                self.topk_lens, num_splits=self.S, err_flag=self.err,
-                                               split_pages=self.w.split_pages, tcgen05=self.tcgen05)
+                                               split_pages=self.w.split_pages, mma_sync=self.mma_sync)
 
     def step(self, i):
         """One step on pool copy i: append of the step's tokens, split-K
@@ -575,11 +575,11 @@ def main():
     arm.bitcast = True                                  # context: the pages' bitcast decoder
     bitcast_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
     arm.bitcast = False
-    tcgen05_ms = None
-    if arm.uses_tc:                                     # context: the same shape on the tcgen05 kernel
-        arm.tcgen05 = True
-        tcgen05_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
-        arm.tcgen05 = False
+    mma_sync_ms = None
+    if arm.uses_tc:                                     # context: the same shape on the mma.sync kernel
+        arm.mma_sync = True
+        mma_sync_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
+        arm.mma_sync = False
 
     arm.graphs = None
     e2e_ms, h2d, d2h = arm.time_e2e(max(5, args.steps // 2), args.warmup)
@@ -631,13 +631,14 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
                          "traffic": profiled_traffic("kvq_attn_kernel.cuh", w.name),
-                         "kernel": "attn_split_kernel (E4M3)", "peak_kind": peak_kind,
+                         "kernel": ("attn_tc_kernel (E4M3, tcgen05)" if arm.uses_tc
+                                    else "attn_split_kernel (E4M3)"), "peak_kind": peak_kind,
                          "attention_kernel_ms": kern_avg,
                          "bytes_per_launch": arm.bytes["attention_kernel"],
                          "decoder": "hardware E4M3 conversion",
                          "bitcast_decoder_ms": bitcast_ms,
                          "bitcast_decoder_gbs": arm.bytes["attention_kernel"] / (bitcast_ms * 1e-3) / 1e9,
-                         "tcgen05_kernel_ms": tcgen05_ms},
+                         "mma_sync_kernel_ms": mma_sync_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

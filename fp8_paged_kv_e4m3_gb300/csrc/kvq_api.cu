@@ -56,7 +56,7 @@ static int check_params(const kvq_attn_params *p)
     if (p->batch < 0 || p->q_len < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
         p->num_splits < 0 || p->max_pages_per_seq < 1 || p->max_topk < 0 || p->split_pages < 0)
         return KVQ_ERR_INVALID_ARG;
-    if (p->flags & ~int32_t(KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_TCGEN05)) return KVQ_ERR_INVALID_ARG;
+    if (p->flags & ~int32_t(KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC)) return KVQ_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
     if (!std::isfinite(p->sm_scale) || p->sm_scale < 0.0f) return KVQ_ERR_INVALID_ARG;
     if (p->head_dim != 64 && p->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
@@ -163,7 +163,7 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.qk_scale_log2 = float(sm * log2e * kfold);
     a.out_scale = float(vfold);
     a.bitcast_decode = (p.flags & KVQ_ATTN_BITCAST_DECODE) != 0;
-    a.tcgen05 = (p.flags & KVQ_ATTN_TCGEN05) != 0;
+    a.mma_sync = (p.flags & KVQ_ATTN_MMA_SYNC) != 0;
 
     cudaStream_t stream = static_cast<cudaStream_t>(c.stream);
     if (launch_attention(c.e4m3, p.head_dim, a, stream) != cudaSuccess) return KVQ_ERR_CUDA;

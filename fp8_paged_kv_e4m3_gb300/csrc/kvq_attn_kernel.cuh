@@ -69,7 +69,10 @@ struct Split {
     static constexpr int kRowsPad = RW * NT * 8;
 };
 
-template <bool E4M3, int D, int PPS>
+// MIN_STAGES: a consumer that waits on one stage out of several in flight
+// (the tcgen05 kernel's workers) needs the ring to hold all of them, or its
+// wait could see the phase parity of the slot's previous use.
+template <bool E4M3, int D, int PPS, int MIN_STAGES = 2>
 struct Geometry {
     static constexpr int kElem = E4M3 ? 1 : 2;
     static constexpr int kRowBytes = D * kElem;           // one token of one kv head
@@ -78,7 +81,8 @@ struct Geometry {
     static constexpr int kRegion = PPS * kPageStride;     // K (or V) part of a stage
     static constexpr int kStageBytes = 2 * kRegion;
     static constexpr int kStagesRaw = 50688 / kStageBytes;   // ~50 KB of ring
-    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kStagesClamped = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kStages = kStagesClamped < MIN_STAGES ? MIN_STAGES : kStagesClamped;
     static constexpr int kX4 = kRowBytes / 32;            // ldmatrix.x4 per 16-token tile
     static constexpr int kKSteps = D / 16;                // QK mma k-steps
     static constexpr int kPVTiles = D / 16;               // PV mma m-tiles (16 channels)

@@ -46,24 +46,35 @@ constexpr int kTcMmaWarp = kConsumerWarps + kProducerWarps;   // 6
 constexpr int kTcThreads = 32 * (kTcMmaWarp + 1);             // 224
 constexpr int kTcTile = 128;                                  // tokens per MMA tile
 constexpr int kTcD = 128;                                     // head_dim of this kernel
-constexpr int kTcPPS = 16;                                    // pages per staging stage (64 tokens)
+// pages per staging stage: 16 (64 tokens) for E4M3, 8 (32 tokens) for fp16, so
+// that the staging ring keeps two CTAs per SM for both element sizes
+template <bool E4M3> constexpr int tc_pps() { return E4M3 ? 16 : 8; }
+// staging stages per 128-token tile; the ring holds at least that many, since a
+// worker waits only on its own stage of the tile, which must never be a slot's
+// next-but-one phase
+template <bool E4M3> constexpr int tc_spt() { return kTcTile / (4 * tc_pps<E4M3>()); }
+template <bool E4M3> using TcGeometry = Geometry<E4M3, kTcD, tc_pps<E4M3>(), tc_spt<E4M3>()>;
 
 // shared memory after the staging ring of Geometry<E4M3, 128, 16>
 template <bool E4M3, int NR>
 struct TcLayout {
-    using G = Geometry<E4M3, kTcD, kTcPPS>;
+    using G = TcGeometry<E4M3>;
     static constexpr int kQ = (G::kBytes + 1023) & ~1023;   // Q: NR x 128 fp16, K-major
     static constexpr int kV = kQ + NR * 256;                 // V^T: 128 ch x 128 tok fp16, MN-major
     static constexpr int kP = kV + kTcTile * kTcD * 2;       // P^T: NR x 128 tok fp16, MN-major
     static constexpr int kWmax = kP + NR * 256;              // [2][4][NR] float: per-worker row maxima
-    static constexpr int kPriv = kWmax + 2 * 4 * NR * 4;     // [4][3][NR] float: per-worker m_ref, corr, coef
-    static constexpr int kLsum = kPriv + 4 * 3 * NR * 4;     // [4][NR] float: per-worker row sums
-    static constexpr int kBar = kLsum + 4 * NR * 4;          // 7 mbarriers
-    static constexpr int kTmemSlot = kBar + 7 * 8;
+    static constexpr int kPriv = kWmax + 2 * 4 * NR * 4;     // [4][4][NR] float: per-worker reference,
+                                                             //   correction, coefficient, reference in use
+    static constexpr int kLsum = kPriv + 4 * 4 * NR * 4;     // [4][NR] float: per-worker row sums
+    static constexpr int kMend = kLsum + 4 * NR * 4;         // [4][NR] float: per-worker final row maxima
+    static constexpr int kFlag = kMend + 4 * NR * 4;         // [2][4] int: per-worker "left the band" flags
+    static constexpr int kBar = kFlag + 2 * 4 * 4;           // 8 mbarriers
+    static constexpr int kTmemSlot = kBar + 8 * 8;
     static constexpr int kBytes = kTmemSlot + 16;
-    // tensor-memory columns: K tile (64: 128 fp16 per lane), S^T (NR), O^T (NR)
-    static constexpr int kColK = 0, kColS = 64, kColO = 64 + NR;
-    static constexpr int kCols = (64 + 2 * NR) <= 128 ? 128 : 256;
+    // tensor-memory columns: K tile (64: 128 fp16 per lane), S^T (NR), O^T (NR), the row
+    // sums L^T (NR, every lane the same: a ones tile times P^T), the ones tile (64)
+    static constexpr int kColK = 0, kColS = 64, kColO = 64 + NR, kColL = 64 + 2 * NR, kColOnes = 64 + 3 * NR;
+    static constexpr int kCols = (128 + 3 * NR) <= 128 ? 128 : ((128 + 3 * NR) <= 256 ? 256 : 512);
 };
 
 // Lane r of the warp ends with the maximum (or sum) over the warp's 32 lanes
@@ -85,11 +96,17 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
     return v[0];   // row `lane`
 }
 
+// Two CTAs per SM when NR <= 32: the bound is stated for 256 threads so that
+// registers stay at 128 per thread -- with 7 warps per CTA, two CTAs put four
+// warps on some SM sub-partitions, whose register files hold 4 x 128 x 32.
 template <bool E4M3, int NR>
-__global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a)
+__global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const AttnArgs a)
 {
-    constexpr int D = kTcD, PPS = kTcPPS;
-    using G = Geometry<E4M3, D, PPS>;
+    constexpr int D = kTcD, PPS = tc_pps<E4M3>();
+    using G = TcGeometry<E4M3>;
+    constexpr int SPT = tc_spt<E4M3>();                       // staging stages per tile: 2 or 4
+    static_assert(G::kStages >= SPT, "the ring must hold a whole tile's staging stages");
+    constexpr int WPS = kTcWorkers / SPT;                     // workers per staging stage: 2 or 1
     using T = TcLayout<E4M3, NR>;
     constexpr int NH = NR <= 32 ? 1 : 2;                      // rows per lane after a transpose-reduce
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -102,22 +119,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
     volatile int *stage_bad = abort_flag + 1;
     const uint32_t tb = smem_u32(smem + T::kBar);
-    const uint32_t b_ops = tb, b_s = tb + 8, b_p = tb + 16, b_pv = tb + 24, b_x = tb + 32, b_l = tb + 40,
-                   b_drain = tb + 48;
+    const uint32_t b_k = tb, b_s = tb + 8, b_p = tb + 16, b_pv = tb + 24, b_x = tb + 32, b_l = tb + 40,
+                   b_drain = tb + 48, b_y = tb + 56;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::kTmemSlot);
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < G::kStages; ++k) {
             mbar_init(bar0 + 8 * k, kProducerWarps);
-            mbar_init(bar0 + 8 * (G::kStages + k), 2);   // each staging stage feeds two workers
+            mbar_init(bar0 + 8 * (G::kStages + k), WPS);   // released by the workers it feeds
         }
-        mbar_init(b_ops, kTcWorkers);
+        mbar_init(b_k, kTcWorkers);
         mbar_init(b_s, 1);
         mbar_init(b_p, kTcWorkers);
         mbar_init(b_pv, 1);
         mbar_init(b_x, kTcWorkers);
         mbar_init(b_l, kTcWorkers);
         mbar_init(b_drain, 1);
+        mbar_init(b_y, kTcWorkers);
         *abort_flag = 0;
         *stage_bad = 0;
         fence_mbar_init();
@@ -132,7 +150,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         bt_spec = __ldg(sr.bt_row + sr.spec0 + lane);
     const int ipst = sr.topk ? G::kTokPerStage : PPS;
     const int nst = (sr.item1 - sr.item0 + ipst - 1) / ipst;   // staging stages
-    const int ntiles = (nst + 1) / 2;
+    const int ntiles = (nst + SPT - 1) / SPT;
     if (threadIdx.x == 0) {
         if (!sr.len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
         if (sr.len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
@@ -158,8 +176,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
                            p_addr = smem_u32(smem + T::kP);
             const uint32_t id_qk = umma_idesc_f16(kTcTile, NR, false, false);
             const uint32_t id_pv = umma_idesc_f16(kTcTile, NR, true, true);
+            const uint32_t id_l = umma_idesc_f16(kTcTile, NR, false, true);
             for (int t = 0; t < ntiles; ++t) {
-                if (!mbar_wait_bounded(b_ops, t & 1, abort_flag, a.err_flag)) break;
+                if (!mbar_wait_bounded(b_k, t & 1, abort_flag, a.err_flag)) break;
                 tc_fence_after();
                 // S^T[tok][row] = sum_d K[tok][d] Q[row][d]: A = K tile (tensor memory), B = Q (K-major)
 #pragma unroll
@@ -174,6 +193,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
                 for (int ks = 0; ks < kTcTile / 16; ++ks)
                     umma_smem_a(tmem + T::kColO, umma_desc(v_addr + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128),
                                 umma_desc(p_addr + ks * 2 * NR * 16, NR * 16, 128), id_pv, t > 0 || ks > 0);
+                // L^T[lane][row] += sum_tok 1 * P[tok][row]: the row sums, accumulated like O^T
+#pragma unroll
+                for (int ks = 0; ks < kTcTile / 16; ++ks)
+                    umma_tmem_a(tmem + T::kColL, tmem + T::kColOnes + ks * 8,
+                                umma_desc(p_addr + ks * 2 * NR * 16, NR * 16, 128), id_l, t > 0 || ks > 0);
                 umma_commit(b_pv);
             }
             // every MMA issued so far completes before the tensor memory is freed
@@ -189,8 +213,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
         const float qk = a.qk_scale_log2;
         const int win0 = L - a.q_len;                // row i sees positions <= win0 + i
         float *wmax = reinterpret_cast<float *>(smem + T::kWmax);
-        float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 3 * NR;   // m_ref, corr, coef
+        float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 4 * NR;   // reference, corr, coef, in use
         float *lsum = reinterpret_cast<float *>(smem + T::kLsum);
+        // the final maxima get a buffer of their own: a worker may still read the
+        // last tile's exchange in wmax while another has reached the epilogue
+        float *mend = reinterpret_cast<float *>(smem + T::kMend);
 
         // Q rows (padding rows zero) into the K-major Q tile: element (r, d) at
         // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2
@@ -205,20 +232,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
         }
 
-        // per-row state, row (NH == 1 ? lane : lane and lane + 32) of this lane
-        float m_ref[NH], m_true[NH], l_w[NH];
+        // Per row, the reference of the exponentials lives in the worker's private
+        // shared copy (all four workers hold the same values): priv[r] (-inf while
+        // the row has none), priv[3 NR + r] (the same, 0 while none).  This
+        // thread keeps, per row, the running maximum and the sum over its tokens.
+        int *flag = reinterpret_cast<int *>(smem + T::kFlag);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-            m_ref[h] = -INFINITY;
-            m_true[h] = -INFINITY;
-            l_w[h] = 0.f;
+        for (int h = 0; h < NH; ++h)
+            if (32 * h + lane < NR) {
+                priv[32 * h + lane] = -INFINITY;
+                priv[3 * NR + 32 * h + lane] = 0.f;
+            }
+        __syncwarp();
+        float mt[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) mt[r] = -INFINITY;
+        {   // the ones tile (fp16 1.0 pairs), A operand of the row sums
+            uint32_t ones[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ones[e] = 0x3C003C00u;
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) tmem_st16(tmem + lane_base + T::kColOnes + c, ones);
+            tmem_wait_st();
         }
+        int nband = 0;   // times a row left the band (the same count on every worker)
         bool ok = true;
         for (int t = 0; t < ntiles && ok; ++t) {
-            // V^T and P^T are reused: the previous tile's PV must be done
-            if (t > 0 && !mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
-            const int st = 2 * t + (q >> 1);         // staging stage of this warp's 32 tokens
-            const int j = (q & 1) * 32 + lane;       // token of that stage
+            const int st = SPT * t + q / WPS;        // staging stage of this warp's 32 tokens
+            // token of that stage: the 8 lanes of a quarter warp take the same slot of 8
+            // different pages, whose 16-byte rows sit in distinct banks (page stride
+            // = 16 mod 128); tile slot tt holds this token in S^T, V^T and P^T alike
+            const int j = (q % WPS) * 32 + ((lane & 7) << 2) + (lane >> 3);
             const bool have = st < nst;
             const int slot = st % G::kStages;
             if (have && !mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag)) {
@@ -228,7 +272,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             const int pos = have ? tokpos[slot * G::kTokPerStage + j] : -1;
             const uint8_t *krow = smem + slot * G::kStageBytes + (j >> 2) * G::kPageStride + (j & 3) * G::kRowBytes;
             const uint8_t *vrow = krow + G::kRegion;
-            // ---- K row -> fp16 in tensor memory (token tt in lane tt, channels 2c, 2c+1 in column c) ----
+            // ---- K row -> fp16 in tensor memory (token tt in lane tt, channels 2c, 2c+1 in column c);
+            // the K tile is free: the previous tile's S^T is complete ----
 #pragma unroll
             for (int h = 0; h < 4; ++h) {            // 16 columns = 32 channels per store
                 uint32_t w[16];
@@ -259,9 +304,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
                 }
                 tmem_st16(tmem + lane_base + T::kColK + 16 * h, w);
             }
-            // ---- V row -> fp16 V^T tile (MN-major): (ch, tok) at (tok/8)*2048 + (ch/8)*128 + (tok%8)*16 ----
-            // a slot without a token is zeroed: its bits may be NaN, and P = 0 alone leaves 0 * NaN
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_k);           // S^T of this tile may start
+            // ---- V row -> fp16 V^T tile (MN-major): (ch, tok) at (tok/8)*2048 + (ch/8)*128 + (tok%8)*16;
+            // V^T and P^T are reused: the previous tile's PV must be complete ----
+            if (t > 0 && !mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
             {
+                // a slot without a token is zeroed: its bits may be NaN, and P = 0 alone leaves 0 * NaN
                 uint8_t *vdst = smem + T::kV + (tt >> 3) * ((D / 8) * 128) + (tt & 7) * 16;
                 const bool vok = have && pos >= 0;
 #pragma unroll
@@ -283,11 +334,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             }
             __syncwarp();
             if (have && lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));   // staging slot consumed
-            tmem_wait_st();
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_ops);
 
             // ---- S^T of this warp's 32 tokens: one column per query row ----
             if (!mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag)) { ok = false; break; }
@@ -303,69 +349,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             }
             // scores in the log2 domain; row r (window row r / G) sees positions <= win0 + r / G
             const int rmin = pos < 0 ? NR : (pos > win0 ? a.group * (pos - win0) : 0);
+            if (rmin == 0 && a.rows == NR) {
 #pragma unroll
-            for (int r = 0; r < NR; ++r) x[r] = (r >= rmin && r < a.rows) ? x[r] * qk : -INFINITY;
-
-            // ---- row maxima over the tile: lanes, then the four workers ----
-            float tmax[NH];
+                for (int r = 0; r < NR; ++r) x[r] *= qk;
+            } else {
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                float v[32];
-#pragma unroll
-                for (int r = 0; r < 32; ++r) v[r] = (32 * h + r < NR) ? x[32 * h + r] : -INFINITY;
-                tmax[h] = warp_transpose_reduce<true>(v, lane);
-                if (32 * h + lane < NR) wmax[((t & 1) * 4 + q) * NR + 32 * h + lane] = tmax[h];
+                for (int r = 0; r < NR; ++r) x[r] = (r >= rmin && r < a.rows) ? x[r] * qk : -INFINITY;
             }
+
+            // ---- running maxima; does any score leave the band of 2^8 above its row's reference? ----
+            bool over = false;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                mt[r] = fmaxf(mt[r], x[r]);
+                over |= x[r] > priv[r] + 8.f;   // a row without a reference: any finite score
+            }
+            over = __any_sync(kFull, over);
+            if (lane == 0) flag[(t & 1) * 4 + q] = over ? 1 : 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(b_x);
             if (!mbar_wait_bounded(b_x, t & 1, abort_flag, a.err_flag)) { ok = false; break; }
-            bool rescale = false;
+            const bool band = (flag[(t & 1) * 4 + 0] | flag[(t & 1) * 4 + 1] | flag[(t & 1) * 4 + 2] |
+                               flag[(t & 1) * 4 + 3]) != 0;
+            if (band) {
+                // rare: the tile's exact row maxima, then new references where a maximum
+                // rose more than 2^8 above the old one (the same decision on every worker)
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                const int r = 32 * h + lane;
-                float mx = -INFINITY;
-                if (r < NR)
+                for (int h = 0; h < NH; ++h) {
+                    float v[32];
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, wmax[((t & 1) * 4 + w) * NR + r]);
-                m_true[h] = fmaxf(m_true[h], mx);
-                float corr = 1.f;
-                // a new reference only when the maximum rises more than 2^8 above it
-                if (mx > -INFINITY && (m_ref[h] == -INFINITY || mx > m_ref[h] + 8.f)) {
-                    corr = (m_ref[h] == -INFINITY) ? 0.f : fast_exp2(m_ref[h] - mx);
-                    m_ref[h] = mx;
-                    rescale = true;
+                    for (int r = 0; r < 32; ++r) v[r] = (32 * h + r < NR) ? x[32 * h + r] : -INFINITY;
+                    const float m = warp_transpose_reduce<true>(v, lane);
+                    if (32 * h + lane < NR) wmax[q * NR + 32 * h + lane] = m;
                 }
-                if (r < NR) {
-                    priv[r] = (m_ref[h] == -INFINITY) ? 0.f : m_ref[h];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_y);
+                if (!mbar_wait_bounded(b_y, nband & 1, abort_flag, a.err_flag)) { ok = false; break; }
+                ++nband;
+                bool moved = false;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    const int r = 32 * h + lane;
+                    if (r >= NR) continue;
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, wmax[w * NR + r]);
+                    const float ref = priv[r];
+                    float corr = 1.f;
+                    if (mx > -INFINITY && (ref == -INFINITY || mx > ref + 8.f)) {
+                        corr = (ref == -INFINITY) ? 0.f : fast_exp2(ref - mx);
+                        priv[r] = mx;
+                        priv[3 * NR + r] = mx;
+                        moved = true;
+                    }
                     priv[NR + r] = corr;
                 }
-                l_w[h] *= corr;
-            }
-            __syncwarp();
-            // ---- P = exp2(score - reference), row sums ----
+                moved = __any_sync(kFull, moved);
+                __syncwarp();
+                if (moved && t > 0) {
+                    // O^T and L^T columns of the rows whose reference moved (the previous PV is complete)
+                    tc_fence_after();
 #pragma unroll
-            for (int r = 0; r < NR; ++r) x[r] = fast_exp2(x[r] - priv[r]);
+                    for (int c = 0; c < 2 * NR; c += 16) {   // O^T then L^T: adjacent columns
+                        uint32_t r16[16];
+                        tmem_ld16(tmem + lane_base + T::kColO + c, r16);
+                        tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                float v[32];
-#pragma unroll
-                for (int r = 0; r < 32; ++r) v[r] = (32 * h + r < NR) ? x[32 * h + r] : 0.f;
-                l_w[h] += warp_transpose_reduce<false>(v, lane);
-            }
-            // ---- O^T columns of rows whose reference moved (the previous PV is complete) ----
-            if (t > 0 && __any_sync(kFull, rescale)) {
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < NR; c += 16) {
-                    uint32_t r16[16];
-                    tmem_ld16(tmem + lane_base + T::kColO + c, r16);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * priv[NR + c + e]);
-                    tmem_st16(tmem + lane_base + T::kColO + c, r16);
+                        for (int e = 0; e < 16; ++e)
+                            r16[e] = __float_as_uint(__uint_as_float(r16[e]) * priv[NR + ((c + e) % NR)]);
+                        tmem_st16(tmem + lane_base + T::kColO + c, r16);
+                    }
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
             }
+            // ---- P = exp2(score - reference) ----
+#pragma unroll
+            for (int r = 0; r < NR; ++r) x[r] = fast_exp2(x[r] - priv[3 * NR + r]);
             // ---- P^T (fp16, MN-major): (row, tok) at (tok/8) * NR*16 + (row/8) * 128 + (tok%8) * 16 ----
             {
                 uint8_t *pdst = smem + T::kP + (tt >> 3) * (NR * 16) + (tt & 7) * 16;
@@ -384,15 +443,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
             __syncwarp();
             if (lane == 0) mbar_arrive(b_p);
         }
+        // the warp's row maxima: lane r (and r + 32) ends with row r's over the warp's tokens
+        float m_w[NH];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            float v[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) v[r] = (32 * h + r < NR) ? mt[32 * h + r] : -INFINITY;
+            m_w[h] = warp_transpose_reduce<true>(v, lane);
+        }
 
         // ---- epilogue: the split's partial (o normalised, m, l) per row ----
         if (ok && !*abort_flag) {
             bool have_o = ntiles > 0;
             if (have_o && !mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag)) have_o = false;
             tc_fence_after();
+            // the row sums over all tiles, from L^T (every lane holds them)
+            if (have_o) {
+#pragma unroll
+                for (int c = 0; c < NR; c += 16) {
+                    uint32_t r16[16];
+                    tmem_ld16(tmem + lane_base + T::kColL + c, r16);
+                    tmem_wait_ld();
+                    if (lane == 0)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) lsum[q * NR + c + e] = __uint_as_float(r16[e]);
+                }
+            } else if (lane == 0) {
+#pragma unroll
+                for (int r = 0; r < NR; ++r) lsum[q * NR + r] = 0.f;
+            }
 #pragma unroll
             for (int h = 0; h < NH; ++h)
-                if (32 * h + lane < NR) lsum[q * NR + 32 * h + lane] = l_w[h];
+                if (32 * h + lane < NR) mend[q * NR + 32 * h + lane] = m_w[h];
             __syncwarp();
             if (lane == 0) mbar_arrive(b_l);
             if (mbar_wait_bounded(b_l, 0, abort_flag, a.err_flag) && !*abort_flag) {
@@ -402,16 +485,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) attn_tc_kernel(const AttnArgs a
                 for (int h = 0; h < NH; ++h) {
                     const int r = 32 * h + lane;
                     if (r >= NR) continue;
-                    float lt = 0.f;
+                    const float lt = lsum[q * NR + r];   // the whole tile set's sum (from L^T)
+                    float mx = -INFINITY;
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) lt += lsum[w * NR + r];
+                    for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mend[w * NR + r]);
                     priv[2 * NR + r] = lt > 0.f ? a.out_scale / lt : 0.f;
                     if (q == 0 && r < a.rows) {
                         const int i = r / a.group, hh = g * a.group + r % a.group;
                         const int64_t unit = (((int64_t)b * a.num_q_heads + hh) * a.q_len + i) * S + s;
                         // the sum relative to the exact maximum, m in natural-log units
-                        a.ws_m[unit] = lt > 0.f ? m_true[h] * kLn2 : -INFINITY;
-                        a.ws_l[unit] = lt > 0.f ? lt * fast_exp2(m_ref[h] - m_true[h]) : 0.f;
+                        a.ws_m[unit] = lt > 0.f ? mx * kLn2 : -INFINITY;
+                        a.ws_l[unit] = lt > 0.f ? lt * fast_exp2(priv[3 * NR + r] - mx) : 0.f;
                     }
                 }
                 __syncwarp();
@@ -459,6 +543,9 @@ static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
         e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }

@@ -29,7 +29,7 @@ struct AttnArgs {
     float qk_scale_log2;         // hoisted: sm_scale * log2(e) [* k_scale for E4M3]
     float out_scale;             // hoisted: v_scale for E4M3, 1 for fp16
     bool bitcast_decode;         // E4M3: the bitcast decoder instead of the hardware conversion
-    bool tcgen05;                // many-row tiles on the tcgen05 kernel
+    bool mma_sync;               // keep many-row tiles on the mma.sync kernel
 };
 
 struct WorkspaceLayout {

@@ -189,11 +189,11 @@ typedef struct {
 #define KVQ_ATTN_BITCAST_DECODE 1
 
 /* Kernel choice for more than 8 query rows per KV head (G * q_len > 8, e.g.
- * MTP verify) at head_dim 128: KVQ_ATTN_TCGEN05 runs them on the tcgen05
- * kernel (tensor-memory accumulators, M = 128 tokens per MMA) instead of the
- * mma.sync kernel that serves every shape.  Both compute the same partials up
- * to rounding.  Ignored with the bitcast decoder and for other shapes. */
-#define KVQ_ATTN_TCGEN05 2
+ * MTP verify) at head_dim 128: by default the tcgen05 kernel (tensor-memory
+ * accumulators, M = 128 tokens per MMA); KVQ_ATTN_MMA_SYNC keeps such calls
+ * on the mma.sync kernel that serves every shape.  Both compute the same
+ * partials up to rounding.  The bitcast decoder runs on the mma.sync kernel. */
+#define KVQ_ATTN_MMA_SYNC 2
 
 /* The split count a call with these parameters uses: p->num_splits if > 0;
  * else, with split_pages > 0, the fewest splits that cover max_pages_per_seq

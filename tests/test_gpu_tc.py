@@ -1,7 +1,7 @@
-"""GPU parity of the tcgen05 kernel (flag KVQ_ATTN_TCGEN05) for more than 8
-query rows per kv head at head_dim 128 (MTP verify): outputs and FP32 split
-partials against the oracle, and outputs beside the mma.sync kernel, on ragged
-lengths that leave partial 128-token tiles and odd staging stages."""
+"""GPU parity of the tcgen05 kernel, the default for more than 8 query rows per
+kv head at head_dim 128 (MTP verify): outputs and FP32 split partials against
+the oracle, and outputs beside the mma.sync kernel (flag KVQ_ATTN_MMA_SYNC), on
+ragged lengths that leave partial 128-token tiles and odd staging stages."""
 import numpy as np
 import pytest
 import torch
@@ -49,8 +49,8 @@ def test_tc_matches_oracle_and_mma_sync(lens, q_len, group, e4m3):
     dp = _problem(lens, q_len, group, e4m3)
     ref = _oracle_out(dp)
     for S in (1, 3, 0):
-        tc = G.run_attention(dp, num_splits=S, tcgen05=True)
-        ms = G.run_attention(dp, num_splits=S)
+        tc = G.run_attention(dp, num_splits=S)
+        ms = G.run_attention(dp, num_splits=S, mma_sync=True)
         torch.cuda.synchronize()
         assert dp.err.item() == 0
         what = f"{lens} q{q_len} G{group} e4m3={e4m3} S={S}"
@@ -62,7 +62,7 @@ def test_tc_matches_oracle_and_mma_sync(lens, q_len, group, e4m3):
 def test_tc_partials_match_oracle(e4m3):
     dp = _problem([1000, 236, 33, 127], 4, 8, e4m3)
     S = 3
-    ws, p = G.run_attention(dp, num_splits=S, partial=True, tcgen05=True)
+    ws, p = G.run_attention(dp, num_splits=S, partial=True)
     torch.cuda.synchronize()
     assert dp.err.item() == 0
     o, m, l = [x.cpu().numpy() for x in kvq.workspace_views(ws, p)]
@@ -84,7 +84,7 @@ def test_tc_topk_and_nan_slots(e4m3):
     assert dp.topk_lens is not None
     ref = _oracle_out(dp)
     for S in (1, 2):
-        out = G.run_attention(dp, num_splits=S, tcgen05=True)
+        out = G.run_attention(dp, num_splits=S)
         torch.cuda.synchronize()
         assert dp.err.item() == 0
         G.assert_close(out.float().cpu().numpy(), ref, f"tcgen05 top-k e4m3={e4m3} S={S}")
@@ -103,7 +103,7 @@ def test_tc_large_scores_move_the_reference():
     dp = G.device_problem(pr, True)
     ref = _oracle_out(dp)
     for S in (1, 2):
-        out = G.run_attention(dp, num_splits=S, tcgen05=True)
+        out = G.run_attention(dp, num_splits=S)
         torch.cuda.synchronize()
         assert dp.err.item() == 0
         G.assert_close(out.float().cpu().numpy(), ref, f"growing scores S={S}")
