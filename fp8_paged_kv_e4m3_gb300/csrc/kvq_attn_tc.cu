@@ -48,11 +48,11 @@ constexpr int kTcTile = 128;                                  // tokens per MMA 
 constexpr int kTcD = 128;                                     // head_dim of this kernel
 // pages per staging stage: 16 (64 tokens) for E4M3, 8 (32 tokens) for fp16, so
 // that the staging ring keeps two CTAs per SM for both element sizes
-template <bool E4M3> constexpr int tc_pps() { return E4M3 ? 16 : 8; }
+template <bool E4M3> __host__ __device__ constexpr int tc_pps() { return E4M3 ? 16 : 8; }
 // staging stages per 128-token tile; the ring holds at least that many, since a
 // worker waits only on its own stage of the tile, which must never be a slot's
 // next-but-one phase
-template <bool E4M3> constexpr int tc_spt() { return kTcTile / (4 * tc_pps<E4M3>()); }
+template <bool E4M3> __host__ __device__ constexpr int tc_spt() { return kTcTile / (4 * tc_pps<E4M3>()); }
 template <bool E4M3> using TcGeometry = Geometry<E4M3, kTcD, tc_pps<E4M3>(), tc_spt<E4M3>()>;
 
 // shared memory after the staging ring of Geometry<E4M3, 128, 16>
@@ -274,14 +274,19 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             const uint8_t *vrow = krow + G::kRegion;
             // ---- K row -> fp16 in tensor memory (token tt in lane tt, channels 2c, 2c+1 in column c);
             // the K tile is free: the previous tile's S^T is complete ----
+            // all of the row's loads first (krow is a ring address whether or not the slot
+            // holds this tile's token; its scores are masked below), conversions after
+            constexpr int kKV = E4M3 ? 8 : 16;        // 16-byte pieces of a K (or V) row
+            uint4 kx[kKV];
+#pragma unroll
+            for (int u = 0; u < kKV; ++u) kx[u] = *reinterpret_cast<const uint4 *>(krow + 16 * u);
 #pragma unroll
             for (int h = 0; h < 4; ++h) {            // 16 columns = 32 channels per store
                 uint32_t w[16];
                 if (E4M3) {
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const uint4 x = have ? *reinterpret_cast<const uint4 *>(krow + 32 * h + 16 * u)
-                                             : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 x = kx[2 * h + u];
                         w[8 * u + 0] = cvt_lo(x.x);
                         w[8 * u + 1] = cvt_hi(x.x);
                         w[8 * u + 2] = cvt_lo(x.y);
@@ -294,8 +299,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 } else {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const uint4 x = have ? *reinterpret_cast<const uint4 *>(krow + 64 * h + 16 * u)
-                                             : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 x = kx[4 * h + u];
                         w[4 * u + 0] = x.x;
                         w[4 * u + 1] = x.y;
                         w[4 * u + 2] = x.z;
@@ -315,21 +319,23 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 // a slot without a token is zeroed: its bits may be NaN, and P = 0 alone leaves 0 * NaN
                 uint8_t *vdst = smem + T::kV + (tt >> 3) * ((D / 8) * 128) + (tt & 7) * 16;
                 const bool vok = have && pos >= 0;
+                uint4 vx[kKV];
+#pragma unroll
+                for (int u = 0; u < kKV; ++u) vx[u] = *reinterpret_cast<const uint4 *>(vrow + 16 * u);
+                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {   // 16 channels per step
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = make_uint4(0u, 0u, 0u, 0u);
-                    if (vok) {
-                        if (E4M3) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(vrow + 16 * c);
-                            lo = make_uint4(cvt_lo(x.x), cvt_hi(x.x), cvt_lo(x.y), cvt_hi(x.y));
-                            hi = make_uint4(cvt_lo(x.z), cvt_hi(x.z), cvt_lo(x.w), cvt_hi(x.w));
-                        } else {
-                            lo = *reinterpret_cast<const uint4 *>(vrow + 32 * c);
-                            hi = *reinterpret_cast<const uint4 *>(vrow + 32 * c + 16);
-                        }
+                    uint4 lo, hi;
+                    if (E4M3) {
+                        const uint4 x = vx[c];
+                        lo = make_uint4(cvt_lo(x.x), cvt_hi(x.x), cvt_lo(x.y), cvt_hi(x.y));
+                        hi = make_uint4(cvt_lo(x.z), cvt_hi(x.z), cvt_lo(x.w), cvt_hi(x.w));
+                    } else {
+                        lo = vx[2 * c];
+                        hi = vx[2 * c + 1];
                     }
-                    *reinterpret_cast<uint4 *>(vdst + (2 * c) * 128) = lo;
-                    *reinterpret_cast<uint4 *>(vdst + (2 * c + 1) * 128) = hi;
+                    *reinterpret_cast<uint4 *>(vdst + (2 * c) * 128) = vok ? lo : zero;
+                    *reinterpret_cast<uint4 *>(vdst + (2 * c + 1) * 128) = vok ? hi : zero;
                 }
             }
             __syncwarp();
