@@ -126,6 +126,7 @@ static int run_attention(const AttnCall &c, bool with_combine)
         return KVQ_ERR_ALIGNMENT;
     const int32_t S = resolve_splits(&p);
     const int64_t rows_total = int64_t(p.batch) * p.num_q_heads * p.q_len;
+    if (rows_total * S > INT32_MAX) return KVQ_ERR_UNSUPPORTED;   // partials are indexed in 32 bits
     const WorkspaceLayout wl = workspace_layout(rows_total, S, p.head_dim);
     if (!c.workspace || c.workspace_bytes < wl.total) return KVQ_ERR_WORKSPACE;
     if (p.batch == 0) return KVQ_OK;

@@ -114,6 +114,15 @@ __device__ __forceinline__ int2 pv_channels(int pv, int gid)
     return make_int2(16 * pv + gid, 16 * pv + 8 + gid);
 }
 
+// First logical page of split s's speculative block-table read (the same for
+// every sequence: equal division assumes a full block-table row).
+__device__ __forceinline__ int split_spec0(const AttnArgs &a, int s)
+{
+    const int64_t spec_per = a.split_pages > 0 ? (int64_t)a.split_pages
+                                               : (int64_t)(a.max_pages + a.num_splits - 1) / a.num_splits;
+    return (int)min((int64_t)s * spec_per, (int64_t)a.max_pages);
+}
+
 // The split's share of one (sequence, kv head): the context length, the
 // mode, and the items (logical pages, or top-k list entries) it covers --
 // split s covers items [s * per, (s + 1) * per): an equal share of this
@@ -124,16 +133,15 @@ struct SplitRange {
     bool len_ok, topk;
 };
 
-__device__ __forceinline__ SplitRange split_range(const AttnArgs &a, int s, int b)
+// L = context_lens[b], topk_len = topk_lens[b] (0 without a top-k list).
+__device__ __forceinline__ SplitRange split_range(const AttnArgs &a, int s, int b, int L, int topk_len)
 {
     SplitRange r;
     r.bt_row = a.block_tables + (int64_t)b * a.max_pages;
-    const int64_t spec_per = a.split_pages > 0 ? (int64_t)a.split_pages
-                                               : (int64_t)(a.max_pages + a.num_splits - 1) / a.num_splits;
-    r.spec0 = (int)min((int64_t)s * spec_per, (int64_t)a.max_pages);
-    r.L = a.context_lens[b];
+    r.spec0 = split_spec0(a, s);
+    r.L = L;
     r.len_ok = (r.L >= a.q_len) && (r.L <= a.max_pages * 4);
-    int topk_n = (a.topk_idx && a.topk_lens) ? a.topk_lens[b] : 0;
+    int topk_n = topk_len;
     r.topk = r.len_ok && topk_n > 0;
     if (r.topk && topk_n > a.max_topk) topk_n = a.max_topk;
     const int n_items = !r.len_ok ? 0 : (r.topk ? topk_n : (r.L + 3) / 4);
@@ -142,6 +150,127 @@ __device__ __forceinline__ SplitRange split_range(const AttnArgs &a, int s, int 
     r.item0 = (int)min((int64_t)s * per, (int64_t)n_items);
     r.item1 = (int)min(r.item0 + per, (int64_t)n_items);
     return r;
+}
+
+// Longest-first order of the sequences.  The CTAs of blockIdx.z = z attend
+// the sequence of rank z when the sequences are ordered by the work they
+// attend -- context length, or top-k list length -- in classes of a quarter
+// octave, longest class first and by index inside a class.  The block
+// scheduler hands out CTAs roughly in index order, so the long sequences
+// start first and the short ones fill the gaps at the end of the grid.  When
+// every sequence falls in one class the order is the identity, found after a
+// barrier that the CTA's setup needs anyway.  A scheduling choice only:
+// which (sequence, split) a CTA computes does not change any result.
+//
+// Use, by every thread of the CTA after grid_dependency_wait:
+//     SeqPick p = seq_identity(a, z);
+//     const bool keep = lpt_classify(a, scratch, scratch_bytes);
+//     if (!__syncthreads_and(keep)) p = lpt_pick(a, z, scratch);
+// `scratch` is `scratch_bytes` of shared memory that nothing else uses
+// meanwhile; a batch too large for it keeps the identity order.
+constexpr int kWorkClasses = 128;
+constexpr int kLptScratchFixed = (kWorkClasses + 4) * 4;
+
+__device__ __forceinline__ int work_class(const AttnArgs &a, int L, int topk_len)
+{
+    int n = 0;   // items attended; an invalid length attends none
+    if (L >= a.q_len && L <= a.max_pages * 4) n = topk_len > 0 ? min(topk_len, a.max_topk) : L;
+    if (n <= 0) return 0;
+    const int e = 31 - __clz(n);                                         // octave
+    const int quarter = (e >= 2 ? (n >> (e - 2)) : (n << (2 - e))) & 3;   // two bits below the leading one
+    return 1 + 4 * e + quarter;                                          // <= 124
+}
+
+struct SeqPick {
+    int b, L, topk_len;
+};
+
+__device__ __forceinline__ SeqPick seq_identity(const AttnArgs &a, int z)
+{
+    SeqPick p;
+    p.b = z;
+    p.L = __ldg(a.context_lens + z);
+    p.topk_len = (a.topk_idx && a.topk_lens) ? __ldg(a.topk_lens + z) : 0;
+    return p;
+}
+
+// Each sequence's class into scratch; true when the identity order stands
+// (one class, or a batch too large for the scratch).
+__device__ __forceinline__ bool lpt_classify(const AttnArgs &a, uint8_t *scratch, int scratch_bytes)
+{
+    const int B = a.batch;
+    if (B + kLptScratchFixed > scratch_bytes) return true;
+    const bool with_topk = a.topk_idx && a.topk_lens;
+    int *hist = reinterpret_cast<int *>(scratch);                  // [kWorkClasses]
+    uint8_t *cls = scratch + kLptScratchFixed;                     // [B]
+    for (int i = threadIdx.x; i < kWorkClasses; i += blockDim.x) hist[i] = 0;
+    const int c0 = work_class(a, __ldg(a.context_lens), with_topk ? __ldg(a.topk_lens) : 0);
+    bool one_class = true;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) {
+        const int c = work_class(a, __ldg(a.context_lens + i), with_topk ? __ldg(a.topk_lens + i) : 0);
+        cls[i] = (uint8_t)c;
+        one_class &= c == c0;
+    }
+    return one_class;
+}
+
+// The sequence of rank z, after lpt_classify and a barrier.
+__device__ __forceinline__ SeqPick lpt_pick(const AttnArgs &a, int z, uint8_t *scratch)
+{
+    const int B = a.batch;
+    int *hist = reinterpret_cast<int *>(scratch);
+    int *sel = hist + kWorkClasses;
+    const uint8_t *cls = scratch + kLptScratchFixed;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) atomicAdd(&hist[cls[i]], 1);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        // lane l holds classes 127 - 4l .. 124 - 4l (descending); exclusive scan of their counts
+        int cnt[4], tot = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            cnt[k] = hist[kWorkClasses - 1 - 4 * lane - k];
+            tot += cnt[k];
+        }
+        int incl = tot;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, d);
+            if (lane >= d) incl += v;
+        }
+        const int start = incl - tot;
+        const unsigned hit = __ballot_sync(kFull, z >= start && z < incl);
+        const int owner = __ffs(hit) - 1;                          // z < B = sum of all counts
+        int c_sel = 0, idx = 0;
+        if (lane == owner) {
+            int acc = start;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (z >= acc && z < acc + cnt[k]) {
+                    c_sel = kWorkClasses - 1 - 4 * lane - k;
+                    idx = z - acc;
+                }
+                acc += cnt[k];
+            }
+        }
+        c_sel = __shfl_sync(kFull, c_sel, owner);
+        idx = __shfl_sync(kFull, idx, owner);
+        // the idx-th sequence (by index) of class c_sel
+        for (int base = 0; base < B; base += 32) {
+            const bool mine = base + lane < B && cls[base + lane] == c_sel;
+            const unsigned m = __ballot_sync(kFull, mine);
+            const int n = __popc(m);
+            if (idx < n) {
+                if (mine && __popc(m & ((1u << lane) - 1u)) == idx) *sel = base + lane;
+                break;
+            }
+            idx -= n;
+        }
+    }
+    __syncthreads();
+    const int b = *sel;
+    __syncthreads();   // the scratch may be reused
+    return seq_identity(a, b);
 }
 
 // One producer warp (K pages when !is_v, V pages otherwise) walks the
@@ -287,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     using G = Geometry<E4M3, D, PPS>;
     extern __shared__ __align__(128) uint8_t smem[];
 
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int s = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring = smem_u32(smem);
     int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
@@ -312,18 +441,21 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     // The producers' first block-table batch is fetched speculatively for a
     // sequence that fills its block-table row, in parallel with the context
     // length; it is refetched below if the real split starts elsewhere.
-    const SplitRange sr = split_range(a, s, b);
-    const int32_t *bt_row = sr.bt_row;
+    // (Blocks take the sequences in index order here: with 4 CTAs of this
+    // kernel per SM, the longest-first pick costs more than it returns.)
+    const int b = blockIdx.z;
+    const SeqPick pick = seq_identity(a, b);
+    const SplitRange sr = split_range(a, s, b, pick.L, pick.topk_len);
     const int L = sr.L, item0 = sr.item0, item1 = sr.item1;
     const bool len_ok = sr.len_ok, topk = sr.topk;
     int bt_spec = -1;
-    if (warp >= kConsumerWarps && sr.spec0 + lane < a.max_pages) bt_spec = __ldg(bt_row + sr.spec0 + lane);
+    if (warp >= kConsumerWarps && sr.spec0 + lane < a.max_pages) bt_spec = __ldg(sr.bt_row + sr.spec0 + lane);
     const int ipst = topk ? G::kTokPerStage : PPS;        // items per stage
     const int nst = (item1 - item0 + ipst - 1) / ipst;
 
     if (threadIdx.x == 0) {
         if (!len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
-        if (len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
+        if (len_ok && pick.topk_len > a.max_topk)
             report(a.err_flag, KVQ_DEV_BAD_TOPK);
     }
     __syncthreads();

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     constexpr int NH = NR <= 32 ? 1 : 2;                      // rows per lane after a transpose-reduce
     extern __shared__ __align__(1024) uint8_t smem[];
 
-    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int s = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring = smem_u32(smem);
     int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
@@ -143,22 +143,31 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     if (warp == kTcMmaWarp) tmem_alloc(smem_u32(tmem_slot), T::kCols);
     grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
 
-    const SplitRange sr = split_range(a, s, b);
+    // sequences longest first; the speculative block-table read (producers) is
+    // issued for the identity order and repeated if another sequence is picked
+    const int z = blockIdx.z;
+    const int spec0 = split_spec0(a, s);
+    const bool spec_lane = warp >= kConsumerWarps && warp < kTcMmaWarp && spec0 + lane < a.max_pages;
+    int bt_spec = spec_lane ? __ldg(a.block_tables + (int64_t)z * a.max_pages + spec0 + lane) : -1;
+    SeqPick pick = seq_identity(a, z);
+    const bool keep_order = lpt_classify(a, smem, G::kRingBytes);
+    tc_fence_before();
+    if (!__syncthreads_and(keep_order)) {   // the setup barrier (mbarriers, tensor memory) as well
+        pick = lpt_pick(a, z, smem);
+        if (pick.b != z) bt_spec = spec_lane ? __ldg(a.block_tables + (int64_t)pick.b * a.max_pages + spec0 + lane) : -1;
+    }
+    tc_fence_after();
+    const int b = pick.b;
+    const SplitRange sr = split_range(a, s, b, pick.L, pick.topk_len);
     const int L = sr.L;
-    int bt_spec = -1;
-    if (warp >= kConsumerWarps && warp < kTcMmaWarp && sr.spec0 + lane < a.max_pages)
-        bt_spec = __ldg(sr.bt_row + sr.spec0 + lane);
     const int ipst = sr.topk ? G::kTokPerStage : PPS;
     const int nst = (sr.item1 - sr.item0 + ipst - 1) / ipst;   // staging stages
     const int ntiles = (nst + SPT - 1) / SPT;
     if (threadIdx.x == 0) {
         if (!sr.len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
-        if (sr.len_ok && a.topk_idx && a.topk_lens && a.topk_lens[b] > a.max_topk)
+        if (sr.len_ok && pick.topk_len > a.max_topk)
             report(a.err_flag, KVQ_DEV_BAD_TOPK);
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
     // only now may a dependent grid start: this CTA already holds its tensor
     // memory, so a dependent CTA cannot take the columns it waits for
     launch_dependents();
@@ -486,22 +495,28 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (lane == 0) mbar_arrive(b_l);
             if (mbar_wait_bounded(b_l, 0, abort_flag, a.err_flag) && !*abort_flag) {
                 const int S = a.num_splits;
+                // per row (lane r, and r + 32): its workspace unit, -1 for a padding row;
+                // the stores below take it from that lane instead of dividing per row
+                int unit_l[NH];
                 // per row: total l (relative to the reference), the coefficient v_scale / l
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     const int r = 32 * h + lane;
+                    unit_l[h] = -1;
                     if (r >= NR) continue;
+                    if (r < a.rows) {
+                        const int i = r / a.group, hh = g * a.group + r % a.group;
+                        unit_l[h] = ((b * a.num_q_heads + hh) * a.q_len + i) * S + s;
+                    }
                     const float lt = lsum[q * NR + r];   // the whole tile set's sum (from L^T)
                     float mx = -INFINITY;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mend[w * NR + r]);
                     priv[2 * NR + r] = lt > 0.f ? a.out_scale / lt : 0.f;
-                    if (q == 0 && r < a.rows) {
-                        const int i = r / a.group, hh = g * a.group + r % a.group;
-                        const int64_t unit = (((int64_t)b * a.num_q_heads + hh) * a.q_len + i) * S + s;
+                    if (q == 0 && unit_l[h] >= 0) {
                         // the sum relative to the exact maximum, m in natural-log units
-                        a.ws_m[unit] = lt > 0.f ? mx * kLn2 : -INFINITY;
-                        a.ws_l[unit] = lt > 0.f ? lt * fast_exp2(priv[3 * NR + r] - mx) : 0.f;
+                        a.ws_m[unit_l[h]] = lt > 0.f ? mx * kLn2 : -INFINITY;
+                        a.ws_l[unit_l[h]] = lt > 0.f ? lt * fast_exp2(priv[3 * NR + r] - mx) : 0.f;
                     }
                 }
                 __syncwarp();
@@ -514,12 +529,10 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int r = c + e;
+                            const int unit = __shfl_sync(kFull, unit_l[r / 32], r % 32);
                             const float coef = priv[2 * NR + r];
-                            if (r < a.rows && coef != 0.f) {
-                                const int i = r / a.group, hh = g * a.group + r % a.group;
-                                const int64_t unit = (((int64_t)b * a.num_q_heads + hh) * a.q_len + i) * S + s;
-                                a.ws_o[unit * D + tt] = __uint_as_float(r16[e]) * coef;
-                            }
+                            if (unit >= 0 && coef != 0.f)
+                                a.ws_o[(int64_t)unit * D + tt] = __uint_as_float(r16[e]) * coef;
                         }
                     }
                 }

@@ -33,7 +33,8 @@
  *    element, fp16 pools two.
  *  - head_dim is 64 or 128; query rows per KV head (q_len * Hq / Hkv) are
  *    at most 64; q_len is 1 .. 4 (decode, or MTP verify with 1 + 3 drafts,
- *    [P1] Purpose).  Other shapes return KVQ_ERR_UNSUPPORTED.
+ *    [P1] Purpose).  Other shapes return KVQ_ERR_UNSUPPORTED, and so does a
+ *    call whose split partials (batch * Hq * q_len * splits) exceed INT32_MAX.
  */
 #ifndef KVQ_H
 #define KVQ_H

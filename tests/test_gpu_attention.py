@@ -217,6 +217,29 @@ def test_shapes_match_oracle(lens, q_len, G_, D, e4m3):
         G.assert_close(out.float().cpu().numpy(), _oracle_out(dp), f"{lens} q{q_len} G{G_} D{D} S{S}")
 
 
+@pytest.mark.parametrize("q_len", [1, 4])
+@pytest.mark.parametrize("e4m3", [True, False])
+def test_many_sequences_in_longest_first_order(q_len, e4m3):
+    """Seventy sequences whose lengths fall in many work classes, with ties,
+    a shortest possible one and a top-k share: the kernels attend them in
+    longest-first order (a scan over three 32-sequence groups), which must
+    not change which sequence's rows a CTA writes.  q_len 4 with 8 query
+    heads per kv head runs the tensor-core kernel, q_len 1 the split kernel."""
+    rng = np.random.default_rng(7)
+    lens = rng.integers(30, 420, size=70)
+    lens[10:15] = 300                          # ties inside one class
+    lens[40] = 30
+    lens[69] = 419
+    w = inputs.Workload("many", 12, 1, 70, q_len, 16, 2, 128, 0, "list:" + ",".join(map(str, lens)),
+                        calib_tokens=64, topk=24, topk_fraction=0.3)
+    dp = G.device_problem(P.host_problem(w), e4m3)
+    for S in (1, 3):
+        out = G.run_attention(dp, num_splits=S)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        G.assert_close(out.float().cpu().numpy(), _oracle_out(dp), f"70 sequences q{q_len} S{S}")
+
+
 @pytest.mark.parametrize("e4m3", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
 def test_nan_bits_in_unowned_slots_do_not_leak(name, e4m3):
