@@ -47,19 +47,35 @@ L2_BYTES_DEFAULT = 129 * 1024 * 1024
 GRAPH_STEPS = 10   # steps captured in one CUDA graph
 
 
-def profiled_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, or None when the summary was taken on other kernel source."""
+# source files each attention kernel is compiled from (for the profile hash)
+KERNEL_SOURCES = {
+    "attn_split_kernel": ["kvq_attn_kernel.cuh", "kvq_device.cuh"],
+    "attn_tc_kernel": ["kvq_attn_tc.cu", "kvq_attn_kernel.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 over the kernel's source files, in the listed order."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"attn_split_kernel_{workload}.md")
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "fp8_paged_kv_e4m3_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary profiles/<kernel>_<workload>.md, or None when that summary was
+    taken on other kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
-        src = open(os.path.join(ROOT, "fp8_paged_kv_e4m3_gb300", "csrc", kernel_file), "rb").read()
         text = open(path).read()
+        digest = kernel_source_hash(kernel)
     except OSError:
         return None
     fields = dict(line.strip("- ").split(": ", 1) for line in text.splitlines()
                   if line.startswith("- ") and ": " in line)
-    if fields.get("kernel_source_sha256") != hashlib.sha256(src).hexdigest():
+    if fields.get("kernel_source_sha256") != digest:
         return None
     try:
         return int(fields["dram_bytes_per_launch"])
@@ -528,7 +544,12 @@ def main():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
+    ap.add_argument("--kernel-hash", choices=sorted(KERNEL_SOURCES),
+                    help="print the source hash an ncu summary of that kernel records, and exit")
     args = ap.parse_args()
+    if args.kernel_hash:
+        print(kernel_source_hash(args.kernel_hash))
+        return
     args.warmup = max(3, args.warmup)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -612,6 +633,7 @@ def main():
                          f"append of the step token + binary64 attention, {t:.1f} s"}
 
     if rank == 0:
+        kname = "attn_tc_kernel" if arm.uses_tc else "attn_split_kernel"
         line = {
             "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -630,9 +652,9 @@ def main():
             "step_ms_p10_p50_p90_one_graph_each": pct,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak,
-                         "traffic": profiled_traffic("kvq_attn_kernel.cuh", w.name),
-                         "kernel": ("attn_tc_kernel (E4M3, tcgen05)" if arm.uses_tc
-                                    else "attn_split_kernel (E4M3)"), "peak_kind": peak_kind,
+                         "traffic": profiled_traffic(kname, w.name),
+                         "kernel": kname + (" (E4M3, tcgen05)" if arm.uses_tc else " (E4M3)"),
+                         "peak_kind": peak_kind,
                          "attention_kernel_ms": kern_avg,
                          "bytes_per_launch": arm.bytes["attention_kernel"],
                          "decoder": "hardware E4M3 conversion",
