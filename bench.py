@@ -659,6 +659,7 @@ def main():
                          "bytes_per_launch": arm.bytes["attention_kernel"],
                          "decoder": "hardware E4M3 conversion",
                          "bitcast_decoder_ms": bitcast_ms,
+                         "bitcast_decoder_kernel": "attn_split_kernel",
                          "bitcast_decoder_gbs": arm.bytes["attention_kernel"] / (bitcast_ms * 1e-3) / 1e9,
                          "mma_sync_kernel_ms": mma_sync_ms},
             "cpu_baseline": cpu,
