@@ -194,6 +194,68 @@ static int run_append(bool e4m3, const void *k_new, const void *v_new, const int
     return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+// shape checks of the prefill entry points; KVQ_OK or an error
+static int check_prefill_params(const kvq_prefill_params *p)
+{
+    if (!p) return KVQ_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->max_pages_per_seq < 1 ||
+        p->max_q_len < 1 || p->total_q < 0 || p->flags != 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+    if (!std::isfinite(p->sm_scale) || p->sm_scale < 0.0f) return KVQ_ERR_INVALID_ARG;
+    if (p->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+    if (p->batch > 65535 || p->num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (int64_t(p->max_pages_per_seq) * 4 > INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+    if (p->max_q_len > p->max_pages_per_seq * int64_t(4)) return KVQ_ERR_INVALID_ARG;
+    return KVQ_OK;
+}
+
+static int run_prefill(bool e4m3, const void *q, const void *k_cache, const void *v_cache,
+                       int64_t num_pages, const int32_t *block_tables, const int32_t *context_lens,
+                       const int32_t *q_start, float k_scale, float v_scale, void *workspace,
+                       size_t workspace_bytes, void *out, const kvq_prefill_params *p,
+                       int32_t *err_flag, void *stream)
+{
+    const int st = check_prefill_params(p);
+    if (st != KVQ_OK) return st;
+    if (p->batch == 0) return KVQ_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !q_start || !out)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_pages < 1) return KVQ_ERR_INVALID_ARG;
+    if (e4m3 && (!good_scale(k_scale) || !good_scale(v_scale))) return KVQ_ERR_BAD_SCALE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        !aligned16(workspace))
+        return KVQ_ERR_ALIGNMENT;
+    const int32_t max_tiles = prefill_max_tiles(p->max_pages_per_seq);
+    if (!workspace || workspace_bytes < prefill_tiles_bytes(p->batch, p->num_kv_heads, max_tiles))
+        return KVQ_ERR_WORKSPACE;
+    const double sm = p->sm_scale > 0.0f ? double(p->sm_scale) : 1.0 / std::sqrt(double(p->head_dim));
+    const double log2e = 1.4426950408889634;
+    PrefillArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_pages = num_pages;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.q_start = q_start;
+    a.out = out;
+    a.tiles = static_cast<uint8_t *>(workspace);
+    a.tile_mask = reinterpret_cast<uint32_t *>(a.tiles + prefill_mask_offset(p->batch, p->num_kv_heads, max_tiles));
+    a.err_flag = err_flag;
+    a.batch = p->batch;
+    a.num_q_heads = p->num_q_heads;
+    a.num_kv_heads = p->num_kv_heads;
+    a.group = p->num_q_heads / p->num_kv_heads;
+    a.max_pages = p->max_pages_per_seq;
+    a.max_q_len = p->max_q_len;
+    a.max_tiles = max_tiles;
+    a.total_q = p->total_q;
+    a.qk_scale_log2 = float(sm * log2e * (e4m3 ? double(k_scale) : 1.0));
+    a.out_scale = e4m3 ? v_scale : 1.0f;
+    return launch_prefill(e4m3, a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
@@ -336,6 +398,31 @@ int kvq_lse_combine(const float *workspace, size_t workspace_bytes, void *out,
                                          p->batch, p->q_len, p->num_q_heads, p->head_dim, S,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+size_t kvq_prefill_workspace_bytes(const kvq_prefill_params *p)
+{
+    if (check_prefill_params(p) != KVQ_OK) return 0;
+    return prefill_tiles_bytes(p->batch, p->num_kv_heads, prefill_max_tiles(p->max_pages_per_seq));
+}
+
+int paged_prefill_attn_e4m3(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                            int64_t num_pages, const int32_t *block_tables, const int32_t *context_lens,
+                            const int32_t *q_start, float k_scale, float v_scale, void *workspace,
+                            size_t workspace_bytes, void *out, const kvq_prefill_params *p,
+                            int32_t *err_flag, void *stream)
+{
+    return run_prefill(true, q, k_cache, v_cache, num_pages, block_tables, context_lens, q_start, k_scale,
+                       v_scale, workspace, workspace_bytes, out, p, err_flag, stream);
+}
+
+int paged_prefill_attn_fp16(const void *q, const void *k_cache, const void *v_cache, int64_t num_pages,
+                            const int32_t *block_tables, const int32_t *context_lens, const int32_t *q_start,
+                            void *workspace, size_t workspace_bytes, void *out, const kvq_prefill_params *p,
+                            int32_t *err_flag, void *stream)
+{
+    return run_prefill(false, q, k_cache, v_cache, num_pages, block_tables, context_lens, q_start, 1.0f, 1.0f,
+                       workspace, workspace_bytes, out, p, err_flag, stream);
 }
 
 }  // extern "C"

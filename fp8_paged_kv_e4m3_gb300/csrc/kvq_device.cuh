@@ -118,6 +118,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void tma_load_1d(uint32_t dst_smem, const void *src, uint32_t bytes,
                                             uint32_t bar, uint64_t policy)
 {

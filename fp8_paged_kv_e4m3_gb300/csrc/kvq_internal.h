@@ -32,6 +32,29 @@ struct AttnArgs {
     bool mma_sync;               // keep many-row tiles on the mma.sync kernel
 };
 
+// Arguments of one chunked-prefill attention call (device pointers).
+struct PrefillArgs {
+    const void *q;               // fp16 [q_start[B]][Hq][128]
+    const void *k_cache;         // pools [P][Hkv][4][128]
+    const void *v_cache;
+    int64_t num_pages;
+    const int32_t *block_tables; // [B][max_pages]
+    const int32_t *context_lens; // [B]
+    const int32_t *q_start;      // [B + 1]
+    void *out;                   // fp16 [q_start[B]][Hq][128]
+    uint8_t *tiles;              // fp16 K/V tiles [B][Hkv][max_tiles][2][128 x 128]
+    uint32_t *tile_mask;         // [B][Hkv][max_tiles][4]: keys with a bad page
+    int32_t *err_flag;
+    int32_t batch, num_q_heads, num_kv_heads, group, max_pages, max_q_len, max_tiles, total_q;
+    float qk_scale_log2;         // sm_scale * log2(e) [* k_scale for E4M3]
+    float out_scale;             // v_scale for E4M3, 1 for fp16
+};
+
+size_t prefill_tiles_bytes(int32_t batch, int32_t num_kv_heads, int32_t max_tiles);
+size_t prefill_mask_offset(int32_t batch, int32_t num_kv_heads, int32_t max_tiles);
+int32_t prefill_max_tiles(int32_t max_pages);
+cudaError_t launch_prefill(bool e4m3, const PrefillArgs &a, cudaStream_t stream);
+
 struct WorkspaceLayout {
     size_t o_off, m_off, l_off, total;
 };

@@ -1,0 +1,449 @@
+// kvq_prefill.cu -- chunked-prefill attention over the paged cache.
+//
+// What is computed: the attention of the decode path with q_len = the chunk
+// length -- PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity
+// path", section Changes (mixed catch-up/decode batches append prefill chunks
+// to the same page-4 cache); PR "[Model][SM70] Calibrated E4M3 KV cache for
+// Qwen4Exp QSA with MTP", section Purpose (causal inside the window of new
+// tokens).  Query token i of a chunk of n tokens in a context of L tokens
+// sits at position L - n + i and attends keys 0 .. L - n + i; the per-layer
+// scales are hoisted (k_scale into the score multiplier, v_scale into the
+// output normalisation).
+//
+// Design, two launches:
+//  1. kv_tile_kernel gathers each (sequence, kv head)'s pages, decodes E4M3
+//     to fp16 (exact: every E4M3 value is an fp16 value; the scales stay
+//     out) and writes 128-key tiles in the tensor core's no-swizzle canonical
+//     layout, with a 128-bit mask per tile of the keys whose block-table
+//     entry is outside the pool.  A prefill chunk is re-read by every query
+//     tile, so decoding once costs O(L) instead of O(L x query tiles).
+//  2. prefill_attn_kernel, one CTA per (128 query tokens, query head,
+//     sequence), 192 threads:
+//       warp 4: one thread streams the K and V tiles (one 32 KB 1-D bulk copy
+//               each) through a 3-stage shared ring;
+//       warp 5: allocates tensor memory; one thread issues the MMAs:
+//               S = Q K^T (M = 128 rows, N = 128 keys, K = 16 per instruction,
+//               Q and K both K-major in shared memory) into one of two S
+//               buffers, then O += P V (P from tensor memory, V MN-major in
+//               shared memory);
+//       warps 0-3: thread r owns query row r (tensor-memory lane r): reads its
+//               128 scores, masks the causal diagonal, and writes P (fp16)
+//               over the S buffer it read.  A row's reference moves only when
+//               a score rises more than 2^8 above it (the O row is then
+//               rescaled in tensor memory); the row sum stays in a register.
+//     Every wait is bounded (about 2 s); on expiry the CTA reports
+//     KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor
+//     memory and exits without writing.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+#include "kvq_tcgen05.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kPfTile = 128;                        // keys per KV tile = query rows per CTA
+constexpr int kPfD = 128;                           // head_dim of this path
+constexpr int kPfTileBytes = kPfTile * kPfD * 2;    // one fp16 tile: 32 KB
+constexpr int kPfStages = 3;
+constexpr int kPfThreads = 192;
+constexpr int kPfSoftmaxWarps = 4;
+constexpr int kPfLoadWarp = 4;
+constexpr int kPfMmaWarp = 5;
+
+// shared memory: Q tile, the ring of (K, V) tile pairs, mbarriers, tensor-memory slot
+constexpr int kPfQ = 0;
+constexpr int kPfRing = kPfQ + kPfTileBytes;
+constexpr int kPfBar = kPfRing + kPfStages * 2 * kPfTileBytes;
+// barriers: full[3], empty[3], q, s[2], p[2], pv, drain
+constexpr int kPfNumBars = 2 * kPfStages + 1 + 2 + 2 + 1 + 1;
+constexpr int kPfAbort = kPfBar + 8 * kPfNumBars;
+constexpr int kPfTmemSlot = kPfAbort + 8;
+constexpr int kPfSmemBytes = kPfTmemSlot + 8;
+static_assert(kPfSmemBytes <= 232448, "prefill shared memory exceeds one CTA's limit");
+
+// tensor-memory columns: two S buffers (P written over the first 64 columns of
+// the one it came from), the O accumulator
+constexpr uint32_t kPfColS = 0, kPfColO = 2 * kPfTile, kPfCols = 512;
+
+// Byte offset of element (row, col) of a 128 x 128 fp16 tile in the
+// canonical no-swizzle layout: 8 x 16-byte core matrices, 8 rows of 8
+// elements each, rows of a core matrix 16 bytes apart, core matrices 128
+// bytes apart along the column direction and 2048 bytes apart along the
+// row direction.  For K (row = key, col = channel) it is the K-major
+// operand of S = Q K^T; for V (row = key, col = channel) the MN-major
+// operand of O = P V; for Q (row = query row) the K-major A operand.
+__device__ __forceinline__ uint32_t tile_off(int row, int col8)
+{
+    return (uint32_t)((row >> 3) * 2048 + col8 * 128 + (row & 7) * 16);
+}
+
+// a chunk that can be attended: non-empty, inside q / out, inside its context
+__device__ __forceinline__ bool seq_ok(const PrefillArgs &a, int q0, int q1, int L)
+{
+    const int n = q1 - q0;
+    return n >= 1 && n <= a.max_q_len && q0 >= 0 && q1 <= a.total_q && L >= n && L <= a.max_pages * 4;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// 1. pages -> fp16 tiles
+
+template <bool E4M3>
+__global__ void __launch_bounds__(256) kv_tile_kernel(const PrefillArgs a)
+{
+    const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    grid_dependency_wait();
+    launch_dependents();
+    const int L = __ldg(a.context_lens + b);
+    const int q0 = __ldg(a.q_start + b);
+    if (!seq_ok(a, q0, __ldg(a.q_start + b + 1), L)) return;   // flagged by the attention kernel
+    if (j * kPfTile >= L) return;
+    const int32_t *bt_row = a.block_tables + (int64_t)b * a.max_pages;
+    const int64_t tile = ((int64_t)b * a.num_kv_heads + g) * a.max_tiles + j;
+    uint8_t *dst = a.tiles + tile * 2 * kPfTileBytes;
+    constexpr int kElem = E4M3 ? 1 : 2;
+    __shared__ uint32_t bad[4];   // keys of the tile whose page is outside the pool
+    if (threadIdx.x < 4) bad[threadIdx.x] = 0u;
+    __syncthreads();
+    // item = (key n8 group, 8-channel group c8, key n%8), key fastest: the 8
+    // lanes of a quarter warp write one 128-byte core-matrix row block
+    for (int it = threadIdx.x; it < 2 * kPfTile * (kPfD / 8); it += blockDim.x) {
+        const int kv = it / (kPfTile * (kPfD / 8));
+        const int r = it % (kPfTile * (kPfD / 8));
+        const int key = (r / (8 * (kPfD / 8))) * 8 + (r & 7);
+        const int c8 = (r / 8) % (kPfD / 8);
+        const int pos = j * kPfTile + key;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);   // keys past the context: zero (and masked)
+        if (pos < L) {
+            const int page = __ldg(bt_row + (pos >> 2));
+            if (page >= 0 && page < a.num_pages) {
+                const uint8_t *pool = static_cast<const uint8_t *>(kv ? a.v_cache : a.k_cache);
+                const uint8_t *src = pool + ((((int64_t)page * a.num_kv_heads + g) * 4 + (pos & 3)) * kPfD + c8 * 8) * kElem;
+                if (E4M3) {
+                    const uint2 x = __ldg(reinterpret_cast<const uint2 *>(src));
+                    v = make_uint4(cvt_lo(x.x), cvt_hi(x.x), cvt_lo(x.y), cvt_hi(x.y));
+                } else {
+                    v = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+            } else if (kv == 0 && c8 == 0) {
+                report(a.err_flag, KVQ_DEV_BAD_PAGE);   // the row stays zero and its key is masked
+                atomicOr(&bad[key >> 5], 1u << (key & 31));
+            }
+        }
+        *reinterpret_cast<uint4 *>(dst + kv * kPfTileBytes + tile_off(key, c8)) = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) a.tile_mask[tile * 4 + threadIdx.x] = bad[threadIdx.x];
+}
+
+// ---------------------------------------------------------------------------
+// 2. flash attention over the tiles
+
+template <bool E4M3>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const PrefillArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int g = h / a.group;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // the sequence's chunk; query tiles in reverse order, so that the tiles
+    // with the most keys start first
+    // (read before grid_dependency_wait: the previous kernel, the tile gather,
+    // does not write them, and it let this grid start only after its own wait
+    // on whatever wrote them)
+    const int q0 = __ldg(a.q_start + b), q1 = __ldg(a.q_start + b + 1);
+    const int n = q1 - q0;
+    const int L = __ldg(a.context_lens + b);
+    if (!seq_ok(a, q0, q1, L)) {
+        const bool empty_ok = n == 0 && q0 >= 0 && q0 <= a.total_q && L >= 0 && L <= a.max_pages * 4;
+        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && !empty_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
+        return;
+    }
+    const int nqt = (n + kPfTile - 1) / kPfTile;
+    const int qt = nqt - 1 - (int)blockIdx.x;
+    if (qt < 0) return;
+    const int i0 = qt * kPfTile;                           // first query token of the tile
+    const int i_end = min(n, i0 + kPfTile);
+    const int base = L - n;                                // position of query token 0
+    const int ntiles = (base + i_end - 1) / kPfTile + 1;   // KV tiles any row of the tile sees
+    const int first_masked = (base + i0) / kPfTile;        // tiles from here on need the causal mask
+
+    const uint32_t bar = smem_u32(smem + kPfBar);
+    auto full = [&](int s) { return bar + 8 * s; };
+    auto empty = [&](int s) { return bar + 8 * (kPfStages + s); };
+    const uint32_t b_q = bar + 8 * (2 * kPfStages), b_s0 = b_q + 8, b_p0 = b_q + 24, b_pv = b_q + 40,
+                   b_drain = b_q + 48;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPfAbort);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPfTmemSlot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPfStages; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(b_q, kPfSoftmaxWarps);
+        mbar_init(b_s0, 1);
+        mbar_init(b_s0 + 8, 1);
+        mbar_init(b_p0, kPfSoftmaxWarps);
+        mbar_init(b_p0 + 8, kPfSoftmaxWarps);
+        mbar_init(b_pv, 1);
+        mbar_init(b_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kPfMmaWarp) tmem_alloc(smem_u32(tmem_slot), kPfCols);
+    grid_dependency_wait();   // the tiles come from the previous kernel
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    launch_dependents();      // this CTA holds its tensor memory already
+    const uint32_t tmem = *tmem_slot;
+    int issued = 0;
+
+    if (warp == kPfLoadWarp) {
+        // ================= tile loads =================
+        if (lane == 0) {
+            const uint8_t *src = a.tiles + (((int64_t)b * a.num_kv_heads + g) * a.max_tiles) * 2 * kPfTileBytes;
+            const uint64_t pol = l2_policy_evict_last();   // every query tile of the group re-reads them
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % kPfStages;
+                if (t >= kPfStages &&
+                    !mbar_wait_bounded(empty(s), ((t / kPfStages) - 1) & 1, abort_flag, a.err_flag))
+                    break;
+                mbar_arrive_expect_tx(full(s), 2 * kPfTileBytes);
+                const uint32_t dst = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes);
+                tma_load_1d(dst, src + (int64_t)t * 2 * kPfTileBytes, kPfTileBytes, full(s), pol);
+                tma_load_1d(dst + kPfTileBytes, src + ((int64_t)t * 2 + 1) * kPfTileBytes, kPfTileBytes, full(s),
+                            pol);
+                ++issued;
+            }
+        }
+    } else if (warp == kPfMmaWarp) {
+        // ================= MMA issue (one thread) =================
+        if (lane == 0) {
+            const uint32_t q_addr = smem_u32(smem + kPfQ);
+            const uint32_t id_qk = umma_idesc_f16(kPfTile, kPfTile, false, false);
+            const uint32_t id_pv = umma_idesc_f16(kPfTile, kPfD, false, true);
+            bool ok = mbar_wait_bounded(b_q, 0, abort_flag, a.err_flag);
+            for (int t = 0; ok && t <= ntiles; ++t) {
+                if (t < ntiles) {
+                    const int s = t % kPfStages;
+                    if (!mbar_wait_bounded(full(s), (t / kPfStages) & 1, abort_flag, a.err_flag)) break;
+                    tc_fence_after();
+                    // S[t&1] = Q K_t^T.  S[t&1] last held P(t-2), which PV(t-2), issued
+                    // before this instruction, has read (MMAs of one thread run in order).
+                    const uint32_t k_addr = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes);
+#pragma unroll
+                    for (int ks = 0; ks < kPfD / 16; ++ks)
+                        umma_smem_a(tmem + kPfColS + (t & 1) * kPfTile, umma_desc(q_addr + ks * 256, 128, 2048),
+                                    umma_desc(k_addr + ks * 256, 128, 2048), id_qk, ks > 0);
+                    umma_commit(b_s0 + 8 * (t & 1));
+                }
+                if (t >= 1) {
+                    const int u = t - 1, s = u % kPfStages;
+                    if (!mbar_wait_bounded(b_p0 + 8 * (u & 1), (u >> 1) & 1, abort_flag, a.err_flag)) break;
+                    tc_fence_after();
+                    // O += P(u) V_u: A = P (tensor memory, two fp16 per column), B = V (MN-major)
+                    const uint32_t v_addr = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes + kPfTileBytes);
+#pragma unroll
+                    for (int ks = 0; ks < kPfTile / 16; ++ks)
+                        umma_tmem_a(tmem + kPfColO, tmem + kPfColS + (u & 1) * kPfTile + ks * 8,
+                                    umma_desc(v_addr + ks * 4096, 2048, 128), id_pv, u > 0 || ks > 0);
+                    umma_commit(b_pv);
+                    umma_commit(empty(s));   // the stage's K and V are read once PV(u) completes
+                }
+            }
+            // every MMA issued so far completes before the tensor memory is freed
+            umma_commit(b_drain);
+            mbar_wait_bounded(b_drain, 0, nullptr, a.err_flag, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ================= softmax warps: thread r owns query row r =================
+        const int r = 32 * warp + lane;
+        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        const int i = i0 + r;                                   // query token of this row
+        const bool row_ok = i < i_end;
+        const int limit = row_ok ? base + i : -1;               // last key this row sees
+        // Q row -> K-major Q tile
+        {
+            const __half *qrow = static_cast<const __half *>(a.q) + ((int64_t)(q0 + i) * a.num_q_heads + h) * kPfD;
+#pragma unroll
+            for (int c8 = 0; c8 < kPfD / 8; ++c8) {
+                const uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(qrow) + c8) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(smem + kPfQ + tile_off(r, c8)) = v;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_q);
+        }
+        const float qk = a.qk_scale_log2;
+        const uint32_t *mask_row = a.tile_mask + (((int64_t)b * a.num_kv_heads + g) * a.max_tiles) * 4;
+        float ref = -INFINITY;   // the row's reference (log2 units)
+        float lsum = 0.f;        // sum of 2^(s - ref) over the keys so far
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            const uint32_t sb = tmem + lane_base + kPfColS + (t & 1) * kPfTile;
+            if (!mbar_wait_bounded(b_s0 + 8 * (t & 1), (t >> 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            tc_fence_after();
+            // keys of this tile left out for a bad block-table entry (almost always none)
+            const uint4 badk = __ldg(reinterpret_cast<const uint4 *>(mask_row) + t);
+            uint32_t xr[kPfTile / 16][16];   // the row's 128 scores, loaded together
+#pragma unroll
+            for (int c = 0; c < kPfTile / 16; ++c) tmem_ld16(sb + 16 * c, xr[c]);
+            tmem_wait_ld();
+            float x[kPfTile];
+#pragma unroll
+            for (int c = 0; c < kPfTile / 16; ++c) {
+                tmem_regs_ready(xr[c]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[16 * c + e] = __uint_as_float(xr[c][e]);
+            }
+            if ((badk.x | badk.y | badk.z | badk.w) != 0u) {
+                const uint32_t bw[4] = {badk.x, badk.y, badk.z, badk.w};
+#pragma unroll
+                for (int c = 0; c < kPfTile; ++c)
+                    if ((bw[c >> 5] >> (c & 31)) & 1u) x[c] = -INFINITY;
+            }
+            float mx = -INFINITY;
+            if (t >= first_masked) {
+                const int k0 = t * kPfTile;
+#pragma unroll
+                for (int c = 0; c < kPfTile; ++c) {
+                    x[c] = (k0 + c <= limit) ? x[c] * qk : -INFINITY;
+                    mx = fmaxf(mx, x[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kPfTile; ++c) {
+                    x[c] *= qk;
+                    mx = fmaxf(mx, x[c]);
+                }
+            }
+            if (mx > ref + 8.f) {
+                // the reference moves: rescale the row's sum and, once PV(t-1) is
+                // complete, its O accumulator
+                const float corr = (ref == -INFINITY) ? 0.f : fast_exp2(ref - mx);
+                lsum *= corr;
+                if (t > 0) {
+                    if (!mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t ob = tmem + lane_base + kPfColO;
+#pragma unroll 1
+                    for (int c = 0; c < kPfD; c += 16) {
+                        uint32_t r16[16];
+                        tmem_ld16(ob + c, r16);
+                        tmem_wait_ld();
+                        tmem_regs_ready(r16);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * corr);
+                        tmem_st16(ob + c, r16);
+                    }
+                }
+                ref = mx;
+            }
+            // P = 2^(x - ref) as fp16 pairs over the first 64 columns of the S buffer
+            const float rf = (ref == -INFINITY) ? 0.f : ref;   // a row with no key yet: P = 0
+#pragma unroll
+            for (int c = 0; c < kPfTile; c += 32) {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = fast_exp2(x[c + 2 * e] - rf), p1 = fast_exp2(x[c + 2 * e + 1] - rf);
+                    lsum += p0 + p1;
+                    w[e] = pack_half2(p0, p1);
+                }
+                tmem_st16(sb + c / 2, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p0 + 8 * (t & 1));
+        }
+        // ---- epilogue: O / l * v_scale -> fp16 output row ----
+        if (ok && !*abort_flag && ntiles > 0 &&
+            mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag) && row_ok) {
+            tc_fence_after();
+            const float coef = lsum > 0.f ? a.out_scale / lsum : 0.f;
+            __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + i) * a.num_q_heads + h) * kPfD;
+#pragma unroll 1
+            for (int c = 0; c < kPfD; c += 16) {
+                uint32_t r16[16];
+                tmem_ld16(tmem + lane_base + kPfColO + c, r16);
+                tmem_wait_ld();
+                tmem_regs_ready(r16);
+                uint4 o0, o1;
+                o0.x = pack_half2(__uint_as_float(r16[0]) * coef, __uint_as_float(r16[1]) * coef);
+                o0.y = pack_half2(__uint_as_float(r16[2]) * coef, __uint_as_float(r16[3]) * coef);
+                o0.z = pack_half2(__uint_as_float(r16[4]) * coef, __uint_as_float(r16[5]) * coef);
+                o0.w = pack_half2(__uint_as_float(r16[6]) * coef, __uint_as_float(r16[7]) * coef);
+                o1.x = pack_half2(__uint_as_float(r16[8]) * coef, __uint_as_float(r16[9]) * coef);
+                o1.y = pack_half2(__uint_as_float(r16[10]) * coef, __uint_as_float(r16[11]) * coef);
+                o1.z = pack_half2(__uint_as_float(r16[12]) * coef, __uint_as_float(r16[13]) * coef);
+                o1.w = pack_half2(__uint_as_float(r16[14]) * coef, __uint_as_float(r16[15]) * coef);
+                *reinterpret_cast<uint4 *>(orow + c) = o0;
+                *reinterpret_cast<uint4 *>(orow + c + 8) = o1;
+            }
+        }
+    }
+
+    // ---- teardown: copies drained, MMAs complete (the MMA thread waited), tensor memory freed ----
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && warp == kPfLoadWarp && lane == 0)
+        for (int t = max(0, issued - kPfStages); t < issued; ++t)
+            mbar_wait_bounded(full(t % kPfStages), (t / kPfStages) & 1, nullptr, a.err_flag, 100000000ull);
+    tc_fence_after();
+    __syncthreads();
+    if (warp == kPfMmaWarp) tmem_dealloc(tmem, kPfCols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+size_t prefill_mask_offset(int32_t batch, int32_t num_kv_heads, int32_t max_tiles)
+{
+    return (size_t)batch * (size_t)num_kv_heads * (size_t)max_tiles * 2 * (size_t)kPfTileBytes;
+}
+
+size_t prefill_tiles_bytes(int32_t batch, int32_t num_kv_heads, int32_t max_tiles)
+{
+    // the K and V tiles, then a 16-byte key mask per tile
+    return (size_t)batch * (size_t)num_kv_heads * (size_t)max_tiles * (2 * (size_t)kPfTileBytes + 16);
+}
+
+int32_t prefill_max_tiles(int32_t max_pages) { return (int32_t)(((int64_t)max_pages * 4 + kPfTile - 1) / kPfTile); }
+
+template <bool E4M3>
+static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t stream)
+{
+    static uint64_t configured = 0;   // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+        e = cudaFuncSetAttribute(prefill_attn_kernel<E4M3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kPfSmemBytes);
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    e = launch_pdl(kv_tile_kernel<E4M3>, dim3(a.max_tiles, a.num_kv_heads, a.batch), dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((a.max_q_len + kPfTile - 1) / kPfTile, a.num_q_heads, a.batch);
+    return launch_pdl(prefill_attn_kernel<E4M3>, grid, dim3(kPfThreads), kPfSmemBytes, stream, a);
+}
+
+cudaError_t launch_prefill(bool e4m3, const PrefillArgs &a, cudaStream_t stream)
+{
+    if (a.batch == 0) return cudaSuccess;
+    return e4m3 ? launch_prefill_t<true>(a, stream) : launch_prefill_t<false>(a, stream);
+}
+
+}  // namespace kvq

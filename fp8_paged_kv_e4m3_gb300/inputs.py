@@ -21,6 +21,8 @@ tensors stand in for the K/V that such traffic would produce):
   mixed     24 layers; an 8192-token prefill chunk appended plus 48 decode
             sequences with contexts uniform in [8192, 32768]; half of them
             attend over a sorted top-2048 token list per (sequence, kv head)
+  prefill   the mixed batch's 8192-token chunk attended: one new sequence,
+            q_len 8192 over its own 8192 tokens (causal), 32 q / 4 kv heads
 
 Seeding: every draw uses its own torch.Generator seeded from
 (workload id, purpose, layer), so any layer can be regenerated alone.
@@ -79,6 +81,7 @@ WORKLOADS = {
     "long": Workload("long", 4, 1, 4, 1, 32, 4, 128, 64, "fixed:262144"),
     "mixed": Workload("mixed", 5, 24, 48, 1, 32, 4, 128, 0, "uniform:8192:32768",
                       topk=2048, topk_fraction=0.5, prefill_chunk=8192),
+    "prefill": Workload("prefill", 7, 24, 1, 8192, 32, 4, 128, 0, "fixed:8192"),
 }
 
 

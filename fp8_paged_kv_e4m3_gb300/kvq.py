@@ -46,11 +46,19 @@ class AttnParams(ctypes.Structure):
                 ("flags", ctypes.c_int32)]
 
 
+class PrefillParams(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
+                ("total_q", ctypes.c_int32), ("sm_scale", ctypes.c_float), ("flags", ctypes.c_int32)]
+
+
 EXPORTS = ("kvq_version", "kvq_status_string", "kvq_validate_scales", "kvq_amax_f16",
            "kvq_scale_from_amax", "kv_append_e4m3", "kv_append_fp16", "kvq_attn_num_splits",
            "kvq_attn_workspace_bytes", "paged_decode_attn_e4m3", "paged_decode_attn_fp16",
            "paged_decode_attn_e4m3_partial", "paged_decode_attn_fp16_partial", "kvq_lse_combine",
-           "paged_decode_attn_e4m3_noalloc")
+           "paged_decode_attn_e4m3_noalloc", "kvq_prefill_workspace_bytes", "paged_prefill_attn_e4m3",
+           "paged_prefill_attn_fp16")
 
 
 def load(path: Optional[str] = None):
@@ -85,10 +93,15 @@ def load(path: Optional[str] = None):
         lib.paged_decode_attn_e4m3_partial.argtypes = [V, V, V, i64, V, V, f32, f32, V, V, V, sz, P, V, V]
         lib.paged_decode_attn_fp16_partial.argtypes = [V, V, V, i64, V, V, V, V, V, sz, P, V, V]
         lib.kvq_lse_combine.argtypes = [V, sz, V, P, V]
+        PP = ctypes.POINTER(PrefillParams)
+        lib.kvq_prefill_workspace_bytes.argtypes = [PP]
+        lib.kvq_prefill_workspace_bytes.restype = sz
+        lib.paged_prefill_attn_e4m3.argtypes = [V, V, V, i64, V, V, V, f32, f32, V, sz, V, PP, V, V]
+        lib.paged_prefill_attn_fp16.argtypes = [V, V, V, i64, V, V, V, V, sz, V, PP, V, V]
         for name in ("kvq_validate_scales", "kvq_amax_f16", "kv_append_e4m3", "kv_append_fp16",
                      "paged_decode_attn_e4m3", "paged_decode_attn_fp16",
                      "paged_decode_attn_e4m3_partial", "paged_decode_attn_fp16_partial",
-                     "kvq_lse_combine"):
+                     "kvq_lse_combine", "paged_prefill_attn_e4m3", "paged_prefill_attn_fp16"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -343,4 +356,79 @@ def lse_combine(workspace: torch.Tensor, out: torch.Tensor, p: AttnParams) -> to
     _need(out, "out", torch.float16, 4)
     _check("kvq_lse_combine", load().kvq_lse_combine(
         _ptr(workspace), workspace.numel() * 4, _ptr(out), ctypes.byref(p), _stream(out)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill
+
+def prefill_params(q: torch.Tensor, num_kv_heads: int, batch: int, max_pages_per_seq: int,
+                   max_q_len: int, sm_scale: float = 0.0) -> PrefillParams:
+    """Parameters of a prefill call; q is the packed [total_q, Hq, D] chunk tensor."""
+    return PrefillParams(batch, q.shape[1], num_kv_heads, q.shape[2], max_pages_per_seq, max_q_len,
+                         q.shape[0], sm_scale, 0)
+
+
+def prefill_workspace_bytes(p: PrefillParams) -> int:
+    n = int(load().kvq_prefill_workspace_bytes(ctypes.byref(p)))
+    if n == 0:
+        raise KvqError("kvq_prefill_workspace_bytes", -1)
+    return n
+
+
+def alloc_prefill_workspace(p: PrefillParams, device) -> torch.Tensor:
+    return torch.empty(prefill_workspace_bytes(p), dtype=torch.uint8, device=device)
+
+
+def _prefill_check(q, k_cache, v_cache, block_tables, context_lens, q_start, workspace, out,
+                   cache_dtype, max_q_len, sm_scale):
+    _need(q, "q", torch.float16, 3)
+    Tq, Hq, D = q.shape
+    _need(k_cache, "k_cache", cache_dtype, 4)
+    _need(v_cache, "v_cache", cache_dtype, 4)
+    if k_cache.shape != v_cache.shape or k_cache.shape[2:] != (PAGE_SIZE, D):
+        raise ValueError(f"caches must be [P, Hkv, {PAGE_SIZE}, {D}]")
+    _need(block_tables, "block_tables", torch.int32, 2)
+    _need(context_lens, "context_lens", torch.int32, 1)
+    _need(q_start, "q_start", torch.int32, 1)
+    B = context_lens.shape[0]
+    if block_tables.shape[0] != B or q_start.shape[0] != B + 1:
+        raise ValueError("block_tables [B, max_pages], context_lens [B], q_start [B + 1] expected")
+    _need(workspace, "workspace", torch.uint8, 1)
+    if out is not None:
+        _need(out, "out", torch.float16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have the shape of q")
+    if max_q_len is None:
+        max_q_len = max(1, Tq)
+    return PrefillParams(B, Hq, k_cache.shape[1], D, block_tables.shape[1], max_q_len, Tq, sm_scale, 0)
+
+
+def paged_prefill_attn_e4m3(q, k_cache, v_cache, block_tables, context_lens, q_start, k_scale: float,
+                            v_scale: float, workspace, out=None, max_q_len: Optional[int] = None,
+                            sm_scale: float = 0.0, err_flag=None):
+    """Chunked-prefill attention over E4M3 pools; q and the returned out are [total_q, Hq, D] fp16,
+    q_start [B + 1] the chunk offsets.  max_q_len bounds every chunk (default: total_q)."""
+    p = _prefill_check(q, k_cache, v_cache, block_tables, context_lens, q_start, workspace, out,
+                       torch.uint8, max_q_len, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("paged_prefill_attn_e4m3", load().paged_prefill_attn_e4m3(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables), _ptr(context_lens),
+        _ptr(q_start), ctypes.c_float(k_scale), ctypes.c_float(v_scale), _ptr(workspace), workspace.numel(),
+        _ptr(out), ctypes.byref(p), _ptr(err_flag), _stream(q)))
+    return out
+
+
+def paged_prefill_attn_fp16(q, k_cache, v_cache, block_tables, context_lens, q_start, workspace, out=None,
+                            max_q_len: Optional[int] = None, sm_scale: float = 0.0, err_flag=None):
+    """fp16-KV twin of paged_prefill_attn_e4m3."""
+    p = _prefill_check(q, k_cache, v_cache, block_tables, context_lens, q_start, workspace, out,
+                       torch.float16, max_q_len, sm_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _check("paged_prefill_attn_fp16", load().paged_prefill_attn_fp16(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables), _ptr(context_lens),
+        _ptr(q_start), _ptr(workspace), workspace.numel(), _ptr(out), ctypes.byref(p), _ptr(err_flag),
+        _stream(q)))
     return out

@@ -268,6 +268,69 @@ int kvq_lse_combine(const float *workspace, size_t workspace_bytes, void *out,
                     const kvq_attn_params *p, void *stream);
 
 /* ------------------------------------------------------------------------
+ * Chunked-prefill attention over the paged cache.  [P2] Changes: mixed
+ * catch-up/decode batches append prefill chunks to the same page-4 cache;
+ * this call attends those chunks.  It is the attention defined above with
+ * q_len = the chunk length: sequence b has context length L_b, which
+ * includes its chunk of n_b = q_start[b+1] - q_start[b] query tokens, the
+ * last n_b positions of the context.  Query token i (0 <= i < n_b) sits at
+ * position L_b - n_b + i and, for query head h (KV head h / (Hq / Hkv)),
+ * attends the dense keys 0 .. L_b - n_b + i (causal inside the chunk).
+ * There is no top-k form and no split partial: the output is written
+ * directly.
+ *   q            : device fp16 [q_start[B]][Hq][head_dim], the chunks packed
+ *                  in sequence order, 16-B aligned
+ *   k_cache, v_cache, num_pages, block_tables, k_scale, v_scale : as for
+ *                  paged_decode_attn_e4m3
+ *   context_lens : device int32 [B] (includes the chunk)
+ *   q_start      : device int32 [B + 1], q_start[0] = 0, non-decreasing.
+ *                  n_b = 0 leaves the sequence out.  A sequence with
+ *                  n_b > max_q_len, n_b > L_b, n_b < 0, L_b outside
+ *                  [0, 4 * max_pages_per_seq] or rows outside
+ *                  [0, total_q) sets KVQ_DEV_BAD_LEN and its output rows
+ *                  are not written.
+ *   workspace    : device memory of at least kvq_prefill_workspace_bytes(p)
+ *                  bytes, 16-B aligned: the call writes the attended keys and
+ *                  values there as fp16 tiles (the E4M3 bytes decoded exactly,
+ *                  scales not applied) before it reads them back.
+ *   out          : device fp16 [q_start[B]][Hq][head_dim], 16-B aligned
+ * head_dim must be 128 (otherwise KVQ_ERR_UNSUPPORTED).  A block-table
+ * entry outside the pool sets KVQ_DEV_BAD_PAGE and that key is left out.
+ * Launches two kernels on `stream`: the gather/decode of the pages into the
+ * workspace, then the attention.
+ */
+typedef struct {
+    int32_t batch;             /* B                                                   */
+    int32_t num_q_heads;       /* Hq                                                  */
+    int32_t num_kv_heads;      /* Hkv; Hq % Hkv == 0                                  */
+    int32_t head_dim;          /* 128                                                 */
+    int32_t max_pages_per_seq; /* row stride of block_tables                          */
+    int32_t max_q_len;         /* bound on every n_b (<= 4 * max_pages_per_seq)        */
+    int32_t total_q;           /* rows of q and out; every chunk must lie inside them  */
+    float sm_scale;            /* softmax temperature; 0 = 1/sqrt(head_dim)           */
+    int32_t flags;             /* must be 0                                           */
+} kvq_prefill_params;
+
+/* Workspace bytes of a prefill call: B * Hkv * ceil(4 * max_pages_per_seq / 128)
+ * tiles of 2 x 32 KiB (K and V, 128 keys x 128 channels of fp16 each) plus
+ * 16 bytes per tile (a mask of keys with a bad page); 0 for invalid
+ * parameters. */
+size_t kvq_prefill_workspace_bytes(const kvq_prefill_params *p);
+
+int paged_prefill_attn_e4m3(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                            int64_t num_pages, const int32_t *block_tables,
+                            const int32_t *context_lens, const int32_t *q_start,
+                            float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                            void *out, const kvq_prefill_params *p, int32_t *err_flag, void *stream);
+
+/* fp16-KV twin: the same computation over fp16 pools, without scales. */
+int paged_prefill_attn_fp16(const void *q, const void *k_cache, const void *v_cache,
+                            int64_t num_pages, const int32_t *block_tables,
+                            const int32_t *context_lens, const int32_t *q_start,
+                            void *workspace, size_t workspace_bytes, void *out,
+                            const kvq_prefill_params *p, int32_t *err_flag, void *stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free variant for callers that cannot allocate device memory.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot provide a workspace -- code running under another framework's

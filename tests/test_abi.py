@@ -154,3 +154,41 @@ def test_python_binding_refuses_fp16_workspace():
     with pytest.raises(ValueError):
         # CPU tensors are refused first; the dtype check is exercised on GPU in test_gpu_attention
         kvq._need(torch.zeros(4, dtype=torch.float16), "workspace", torch.float32)
+
+
+def _pparams(**kw):
+    p = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, max_pages_per_seq=100,
+             max_q_len=300, total_q=600, sm_scale=0.0, flags=0)
+    p.update(kw)
+    return kvq.PrefillParams(**p)
+
+
+def test_prefill_workspace_size(lib):
+    # 100 pages = 400 keys -> 4 tiles of 128 keys; K and V tiles of 32 KiB each
+    assert lib.kvq_prefill_workspace_bytes(ctypes.byref(_pparams())) == 2 * 2 * 4 * (2 * 32768 + 16)
+    assert lib.kvq_prefill_workspace_bytes(ctypes.byref(_pparams(max_pages_per_seq=32, max_q_len=100))) == 2 * 2 * 1 * (2 * 32768 + 16)
+
+
+@pytest.mark.parametrize("field,value", [
+    ("head_dim", 64), ("num_kv_heads", 3), ("max_q_len", 0), ("max_q_len", 401), ("flags", 1),
+    ("batch", -1), ("max_pages_per_seq", 0), ("sm_scale", -1.0), ("total_q", -1),
+])
+def test_prefill_bad_params_are_refused(lib, field, value):
+    assert lib.kvq_prefill_workspace_bytes(ctypes.byref(_pparams(**{field: value}))) == 0
+
+
+def _prefill(lib, p, k_scale=0.1, v_scale=0.1, ws_bytes=1 << 24, q=FAKE, ws=FAKE, q_start=FAKE):
+    return lib.paged_prefill_attn_e4m3(q, FAKE, FAKE, 40, FAKE, FAKE, q_start, ctypes.c_float(k_scale),
+                                       ctypes.c_float(v_scale), ws, ws_bytes, FAKE, ctypes.byref(p), None, None)
+
+
+def test_prefill_host_checks_fail_closed(lib):
+    p = _pparams()
+    assert _prefill(lib, p, k_scale=0.0) == -2
+    assert _prefill(lib, p, v_scale=math.inf) == -2
+    assert _prefill(lib, p, ws_bytes=16) == -3
+    assert _prefill(lib, p, ws=None) == -3
+    assert _prefill(lib, p, q=ctypes.c_void_p(0x10008)) == -6
+    assert _prefill(lib, p, q_start=None) == -1
+    assert _prefill(lib, _pparams(head_dim=64)) == -4
+    assert _prefill(lib, _pparams(batch=0)) == 0          # nothing to do, nothing launched
