@@ -54,6 +54,7 @@ constexpr int kPfThreads = 192;
 constexpr int kPfSoftmaxWarps = 4;
 constexpr int kPfLoadWarp = 4;
 constexpr int kPfMmaWarp = 5;
+constexpr unsigned kPfFull = 0xFFFFFFFFu;
 
 // shared memory: Q tile, the ring of (K, V) tile pairs, mbarriers, tensor-memory slot
 constexpr int kPfQ = 0;
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                 ++issued;
             }
         }
+        __syncwarp();   // the whole warp reaches the teardown barrier together
     } else if (warp == kPfMmaWarp) {
         // ================= MMA issue (one thread) =================
         if (lane == 0) {
@@ -288,13 +290,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
         const uint32_t *mask_row = a.tile_mask + (((int64_t)b * a.num_kv_heads + g) * a.max_tiles) * 4;
         float ref = -INFINITY;   // the row's reference (log2 units)
         float lsum = 0.f;        // sum of 2^(s - ref) over the keys so far
-        bool ok = true;
+        bool ok = true;          // the same on every lane: tensor-memory loads and stores are warp-wide
         for (int t = 0; t < ntiles; ++t) {
             const uint32_t sb = tmem + lane_base + kPfColS + (t & 1) * kPfTile;
-            if (!mbar_wait_bounded(b_s0 + 8 * (t & 1), (t >> 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
-            tc_fence_after();
             // keys of this tile left out for a bad block-table entry (almost always none)
             const uint4 badk = __ldg(reinterpret_cast<const uint4 *>(mask_row) + t);
+            if (!__all_sync(kPfFull, mbar_wait_bounded(b_s0 + 8 * (t & 1), (t >> 1) & 1, abort_flag, a.err_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
             uint32_t xr[kPfTile / 16][16];   // the row's 128 scores, loaded together
 #pragma unroll
             for (int c = 0; c < kPfTile / 16; ++c) tmem_ld16(sb + 16 * c, xr[c]);
@@ -327,27 +332,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                     mx = fmaxf(mx, x[c]);
                 }
             }
-            if (mx > ref + 8.f) {
-                // the reference moves: rescale the row's sum and, once PV(t-1) is
-                // complete, its O accumulator
-                const float corr = (ref == -INFINITY) ? 0.f : fast_exp2(ref - mx);
+            // the reference moves when a score rises more than 2^8 above it; the
+            // row's sum and (once PV(t-1) is complete) its O row are rescaled.  The
+            // O pass is warp-wide; lanes whose reference stays scale by 1.
+            const bool move = mx > ref + 8.f;
+            const float corr = !move ? 1.f : (ref == -INFINITY ? 0.f : fast_exp2(ref - mx));
+            if (move) {
                 lsum *= corr;
-                if (t > 0) {
-                    if (!mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t ob = tmem + lane_base + kPfColO;
-#pragma unroll 1
-                    for (int c = 0; c < kPfD; c += 16) {
-                        uint32_t r16[16];
-                        tmem_ld16(ob + c, r16);
-                        tmem_wait_ld();
-                        tmem_regs_ready(r16);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * corr);
-                        tmem_st16(ob + c, r16);
-                    }
-                }
                 ref = mx;
+            }
+            if (t > 0 && __any_sync(kPfFull, move)) {
+                if (!__all_sync(kPfFull, mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ob = tmem + lane_base + kPfColO;
+#pragma unroll 1
+                for (int c = 0; c < kPfD; c += 16) {
+                    uint32_t r16[16];
+                    tmem_ld16(ob + c, r16);
+                    tmem_wait_ld();
+                    tmem_regs_ready(r16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * corr);
+                    tmem_st16(ob + c, r16);
+                }
             }
             // P = 2^(x - ref) as fp16 pairs over the first 64 columns of the S buffer
             const float rf = (ref == -INFINITY) ? 0.f : ref;   // a row with no key yet: P = 0
@@ -367,12 +377,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
             __syncwarp();
             if (lane == 0) mbar_arrive(b_p0 + 8 * (t & 1));
         }
-        // ---- epilogue: O / l * v_scale -> fp16 output row ----
-        if (ok && !*abort_flag && ntiles > 0 &&
-            mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag) && row_ok) {
+        // ---- epilogue: O / l * v_scale -> fp16 output row (every lane loads, valid rows store) ----
+        if (ok && __all_sync(kPfFull, !*abort_flag &&
+                                          mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag))) {
             tc_fence_after();
             const float coef = lsum > 0.f ? a.out_scale / lsum : 0.f;
-            __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + i) * a.num_q_heads + h) * kPfD;
+            __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
 #pragma unroll 1
             for (int c = 0; c < kPfD; c += 16) {
                 uint32_t r16[16];
@@ -388,8 +398,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                 o1.y = pack_half2(__uint_as_float(r16[10]) * coef, __uint_as_float(r16[11]) * coef);
                 o1.z = pack_half2(__uint_as_float(r16[12]) * coef, __uint_as_float(r16[13]) * coef);
                 o1.w = pack_half2(__uint_as_float(r16[14]) * coef, __uint_as_float(r16[15]) * coef);
-                *reinterpret_cast<uint4 *>(orow + c) = o0;
-                *reinterpret_cast<uint4 *>(orow + c + 8) = o1;
+                if (row_ok) {
+                    *reinterpret_cast<uint4 *>(orow + c) = o0;
+                    *reinterpret_cast<uint4 *>(orow + c + 8) = o1;
+                }
             }
         }
     }
@@ -397,9 +409,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
     // ---- teardown: copies drained, MMAs complete (the MMA thread waited), tensor memory freed ----
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp == kPfLoadWarp && lane == 0)
-        for (int t = max(0, issued - kPfStages); t < issued; ++t)
-            mbar_wait_bounded(full(t % kPfStages), (t / kPfStages) & 1, nullptr, a.err_flag, 100000000ull);
+    if (*abort_flag && warp == kPfLoadWarp) {
+        if (lane == 0)
+            for (int t = max(0, issued - kPfStages); t < issued; ++t)
+                mbar_wait_bounded(full(t % kPfStages), (t / kPfStages) & 1, nullptr, a.err_flag, 100000000ull);
+        __syncwarp();
+    }
     tc_fence_after();
     __syncthreads();
     if (warp == kPfMmaWarp) tmem_dealloc(tmem, kPfCols);
