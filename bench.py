@@ -49,6 +49,7 @@ GRAPH_STEPS = 10   # steps captured in one CUDA graph
 
 # source files each attention kernel is compiled from (for the profile hash)
 KERNEL_SOURCES = {
+    "prefill_attn_kernel": ["kvq_prefill.cu", "kvq_tcgen05.cuh", "kvq_device.cuh"],
     "attn_split_kernel": ["kvq_attn_kernel.cuh", "kvq_device.cuh"],
     "attn_tc_kernel": ["kvq_attn_tc.cu", "kvq_attn_kernel.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh"],
 }
@@ -81,6 +82,19 @@ def profiled_traffic(kernel: str, workload: str):
         return int(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+def _tensor_peak():
+    """Dense fp16 tensor peak in TFLOP/s: the measured bf16 burst figure (fp16
+    runs at the bf16 rate), else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        if v > 0:
+            return v, "measured (bf16 dense burst; fp16 at the same rate)"
+    except (OSError, KeyError, ValueError):
+        pass
+    return 1900.0, "fallback"
 
 
 def _peaks():
@@ -478,6 +492,8 @@ def _seq_rows(w, which, off, L, g):
 
 def run_reference(args, w):
     """The reference arm: the CPU oracle on a bounded sample per step."""
+    if w.name == "prefill":
+        return run_reference_prefill(args, w)
     per_unit_s, _, _ = oracle_sample_time(w, 1, seed=99)   # calibrate the sample size
     budget_s = 120.0
     units = max(1, int(budget_s / max(per_unit_s, 1e-3) / max(1, args.steps + args.warmup)))
@@ -504,6 +520,242 @@ def run_reference(args, w):
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill (the mixed batch's 8192-token chunk attended)
+
+PREFILL_METRIC = "E4M3 paged chunked-prefill attention TFLOP/s (causal, fp16 MMA) vs FP16 KV"
+
+
+def prefill_flops(n: int, base: int, Hq: int, D: int) -> float:
+    """QK and PV multiply-adds (2 flops each) of a causal chunk of n query
+    tokens after `base` earlier keys: row i attends base + i + 1 keys."""
+    keys = n * base + n * (n + 1) / 2
+    return 4.0 * D * Hq * keys
+
+
+class PrefillArm:
+    """One arm of the prefill step: append of the chunk (quantise-on-write
+    for E4M3), then the prefill call (tile gather + attention)."""
+
+    def __init__(self, w, e4m3: bool, dev, seed_rank: int, l2_bytes: int):
+        import torch
+        from fp8_paged_kv_e4m3_gb300 import inputs, kvq
+        self.torch, self.kvq, self.e4m3, self.dev = torch, kvq, e4m3, dev
+        w = rank_workload(w, seed_rank)
+        self.w = w
+        lay = inputs.page_layout(w)
+        n, B = w.q_len, w.batch
+        lens = lay.lens.astype(np.int64)
+        ss, sp = inputs.step_tokens(w, lay)                  # the chunk: the last n positions
+        self.slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, ss, sp)).to(dev)
+        offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        rows = torch.from_numpy(offs[ss] + sp).to(dev)
+        total = int(lens.sum())
+        self.bt = torch.from_numpy(lay.block_tables).to(dev)
+        self.cl = torch.from_numpy(lay.lens).to(dev)
+        self.q_start = torch.arange(0, (B + 1) * n, n, dtype=torch.int32, device=dev)
+        shape = (lay.num_pages, w.num_kv_heads, 4, w.head_dim)
+        dt = torch.uint8 if e4m3 else torch.float16
+        # copies of (chunk K/V, Q, pools, out) rotated so that one step's data is not in L2
+        per_copy = (2 * n * B * w.num_kv_heads * w.head_dim * 2 + 2 * n * B * w.num_q_heads * w.head_dim * 2
+                    + 2 * math.prod(shape) * (1 if e4m3 else 2))
+        self.copies = max(2, math.ceil(2 * l2_bytes / per_copy))
+        self.sets = []
+        for c in range(self.copies):
+            layer = c % max(1, w.layers)
+            k = inputs.kv_tokens(w, layer, total, "k", device=dev)[rows].contiguous()
+            v = inputs.kv_tokens(w, layer, total, "v", device=dev)[rows].contiguous()
+            q = inputs.queries(w, layer, device=dev).reshape(B * n, w.num_q_heads, w.head_dim).contiguous()
+            ks = vs = 1.0
+            if e4m3:
+                ks = kvq.calibrate_scale(inputs.calibration_draw(w, layer, "k", device=dev))
+                vs = kvq.calibrate_scale(inputs.calibration_draw(w, layer, "v", device=dev))
+            kc = torch.zeros(shape, dtype=dt, device=dev)
+            vc = torch.zeros(shape, dtype=dt, device=dev)
+            self.sets.append((k, v, q, kc, vc, torch.empty_like(q), ks, vs))
+        self.p = kvq.PrefillParams(B, w.num_q_heads, w.num_kv_heads, w.head_dim, self.bt.shape[1], n,
+                                   B * n, 0.0, 0)
+        self.ws = kvq.alloc_prefill_workspace(self.p, dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.flops = sum(prefill_flops(n, int(L) - n, w.num_q_heads, w.head_dim) for L in lens)
+        self.launches = 3   # append, tile gather, attention
+        for i in range(self.copies):
+            self._append(i)
+
+    def _append(self, i):
+        k, v, q, kc, vc, out, ks, vs = self.sets[i]
+        if self.e4m3:
+            self.kvq.kv_append_e4m3(k, v, self.slots, kc, vc, ks, vs, self.err)
+        else:
+            self.kvq.kv_append_fp16(k, v, self.slots, kc, vc, self.err)
+
+    def attention(self, i, q=None, out=None):
+        k, v, q0, kc, vc, out0, ks, vs = self.sets[i]
+        q = q0 if q is None else q
+        out = out0 if out is None else out
+        kvq = self.kvq
+        if self.e4m3:
+            kvq.paged_prefill_attn_e4m3(q, kc, vc, self.bt, self.cl, self.q_start, ks, vs, self.ws, out=out,
+                                        max_q_len=self.w.q_len, err_flag=self.err)
+        else:
+            kvq.paged_prefill_attn_fp16(q, kc, vc, self.bt, self.cl, self.q_start, self.ws, out=out,
+                                        max_q_len=self.w.q_len, err_flag=self.err)
+
+    def step(self, i):
+        self._append(i % self.copies)
+        self.attention(i % self.copies)
+
+    def _events(self, fn, steps, warmup):
+        torch = self.torch
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize(self.dev)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for i in range(steps):
+            fn(i)
+        e.record()
+        torch.cuda.synchronize(self.dev)
+        assert self.err.item() == 0, f"device error bits {self.err.item()}"
+        return s.elapsed_time(e)
+
+    def time(self, steps, warmup):
+        return self._events(self.step, steps, warmup)
+
+    def time_kernel(self, steps, warmup):
+        """The prefill call alone (tile gather + attention), back to back."""
+        return self._events(lambda i: self.attention(i % self.copies), steps, warmup) / steps
+
+    def time_e2e(self, steps, warmup):
+        """Through the public calls with the chunk's Q and K/V copied in from
+        pinned host memory and the output read back, every step."""
+        torch = self.torch
+        k, v, q, kc, vc, out, ks, vs = self.sets[0]
+        hk, hv, hq = (t.cpu().pin_memory() for t in (k, v, q))
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def one(i):
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            q.copy_(hq, non_blocking=True)
+            self._append(0)
+            self.attention(0)
+            ho.copy_(out, non_blocking=True)
+        ms = self._events(one, steps, warmup) / steps
+        h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq))
+        return ms, h2d, ho.numel() * ho.element_size()
+
+
+def prefill_oracle_sample(w, rows=(0, 4095, 8191)):
+    """The oracle on a few rows of the chunk (each row one decode-sized
+    problem: row i attends keys 0 .. L - n + i).  Returns (seconds, flops)."""
+    import oracle
+    from fp8_paged_kv_e4m3_gb300 import inputs
+    lay = inputs.page_layout(w)
+    n = w.q_len
+    L = int(lay.lens[0])
+    k = inputs.kv_tokens(w, 0, L, "k").numpy()
+    v = inputs.kv_tokens(w, 0, L, "v").numpy()
+    q = inputs.queries(w, 0).numpy()
+    ks = oracle.calibrate_scale(inputs.calibration_draw(w, 0, "k").numpy())
+    vs = oracle.calibrate_scale(inputs.calibration_draw(w, 0, "v").numpy())
+    shape = (lay.num_pages, w.num_kv_heads, 4, w.head_dim)
+    kc = np.zeros(shape, np.uint8)
+    vc = np.zeros(shape, np.uint8)
+    pos = np.arange(L)
+    slots = inputs.slot_mapping(lay.block_tables[:1], np.zeros(L, np.int64), pos)
+    oracle.append_e4m3(k, v, slots, kc, vc, ks, vs)
+    t0 = time.perf_counter()
+    fl = 0.0
+    for i in rows:
+        Li = L - n + i + 1
+        oracle.attention(q[:1, i:i + 1], kc, vc, lay.block_tables[:1], np.array([Li], np.int32), ks, vs)
+        fl += 4.0 * w.head_dim * w.num_q_heads * Li
+    return time.perf_counter() - t0, fl
+
+
+def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
+    import torch
+    peak_gbs, _ = _peaks()
+    tpeak, tkind = _tensor_peak()
+    arm = PrefillArm(w, True, dev, rank, l2)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if barrier:
+            barrier()
+        total_ms = reduce_max(arm.time(args.steps, args.warmup))
+        kern_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
+    ms = total_ms / args.steps
+    tflops = world * arm.flops / (ms * 1e-3) / 1e12
+    achieved = arm.flops / (kern_ms * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = arm.time_e2e(max(3, args.steps // 4), 2)
+    e2e_ms = reduce_max(e2e_ms)
+    fp16 = None
+    if not args.no_fp16:
+        del arm.sets
+        torch.cuda.empty_cache()
+        a16 = PrefillArm(w, False, dev, rank, l2)
+        ms16 = reduce_max(a16.time(args.steps, args.warmup)) / args.steps
+        k16 = reduce_max(a16.time_kernel(args.steps, args.warmup))
+        fp16 = {"ms_per_step": ms16, "value": world * a16.flops / (ms16 * 1e-3) / 1e12,
+                "prefill_call_ms": k16}
+        del a16
+        torch.cuda.empty_cache()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        t, fl = prefill_oracle_sample(w)
+        cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"3 rows (tokens 0, 4095, 8191) of the chunk, all {w.num_q_heads} query heads, "
+                         f"binary64 attention, {t:.1f} s"}
+    if rank == 0:
+        line = {
+            "metric": PREFILL_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
+            "data": "synthetic",
+            "config": {"workload": f"prefill: {w.batch} x {w.q_len}-token chunk over its own context "
+                                   f"(causal), {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
+                                   f"head_dim {w.head_dim}, page 4; one layer",
+                       "l2": f"rotating {arm.copies} copies of chunk K/V, Q, pools and output (> 2 x L2)",
+                       "parallelism": f"replicas x{world}"},
+            "flops_per_step": arm.flops,
+            "fp16_arm": fp16,
+            "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                         "frac": achieved / tpeak, "traffic": profiled_traffic("prefill_attn_kernel", w.name),
+                         "kernel": "kv_tile_kernel + prefill_attn_kernel (E4M3, tcgen05), one call",
+                         "peak_kind": tkind, "prefill_call_ms": kern_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * arm.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": arm.launches * args.steps,
+            "launch": "append, tile gather, attention per step (programmatic dependent launch)",
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_reference_prefill(args, w):
+    """The reference arm on the prefill workload: the oracle on a few rows of
+    the chunk per step."""
+    for _ in range(min(args.warmup, 1)):
+        prefill_oracle_sample(w, rows=(8191,))
+    t = fl = 0.0
+    for _ in range(args.steps):
+        dt, f = prefill_oracle_sample(w, rows=(8191,))
+        t += dt
+        fl += f
+    v = fl / t / 1e12
+    sample = f"row 8191 of the {w.q_len}-token chunk (all {w.num_q_heads} query heads) per step, binary64"
+    print(json.dumps({"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "TFLOP/s",
+                      "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+                      "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": {"workload": w.name, "sample": sample},
+                      "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+                      "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                      "gpu_launches": 0}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -580,6 +832,12 @@ def main():
     peak, peak_kind = _peaks()
 
     reduce_max = lambda x: max_over_ranks(x, dev, world)
+
+    if w.name == "prefill":
+        run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     arm = Arm(w, True, dev, rank, l2)
     arm.capture()
