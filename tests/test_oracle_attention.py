@@ -359,3 +359,27 @@ def test_bad_page_and_topk_entries_are_flagged_and_skipped():
     _, flags = oracle.attention(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens, ks, vs,
                                 ti, np.array([0, 3], np.int32))
     assert flags & oracle.BAD_TOPK
+
+
+def test_prefill_chunk_rows_equal_decodes_and_brute_force():
+    """A prefill chunk (q_len 24, longer than any verify window, over 40
+    earlier tokens and a context that ends mid-page) is causal token by
+    token: row i equals a decode at context L - 24 + i + 1, and row 0 of the
+    last head matches a softmax written out by hand over the decoded pools."""
+    w = inputs.Workload("chunk", 31, 1, 1, 24, 4, 2, 64, 0, "list:63", calib_tokens=64)
+    pr = P.host_problem(w)
+    kc, vc, ks, vs = P.oracle_pools(pr)
+    bt, lens = pr.layout.block_tables, pr.layout.lens
+    out, _ = oracle.attention(pr.q, kc, vc, bt, lens, ks, vs)
+    for i in (0, 1, 11, 23):
+        dec, _ = oracle.attention(pr.q[:, i:i + 1], kc, vc, bt, lens - 24 + i + 1, ks, vs)
+        np.testing.assert_allclose(out[:, i], dec[:, 0], rtol=1e-13, atol=1e-15)
+    # brute force for (token 0, head 3 -> kv head 1): keys 0 .. 63 - 24
+    dec_k = oracle.e4m3_decode_array(kc).astype(np.float64) * ks
+    dec_v = oracle.e4m3_decode_array(vc).astype(np.float64) * vs
+    n_keys = int(lens[0]) - 24 + 1
+    K = np.stack([dec_k[bt[0, j // 4], 1, j % 4] for j in range(n_keys)])
+    V = np.stack([dec_v[bt[0, j // 4], 1, j % 4] for j in range(n_keys)])
+    s = K @ pr.q[0, 0, 3].astype(np.float64) / np.sqrt(64.0)
+    p = np.exp(s - s.max())
+    np.testing.assert_allclose(out[0, 0, 3], (p @ V) / p.sum(), rtol=1e-12, atol=1e-14)
