@@ -229,9 +229,10 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         float *mend = reinterpret_cast<float *>(smem + T::kMend);
 
         // Q rows (padding rows zero) into the K-major Q tile: element (r, d) at
-        // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2
+        // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2; the 8 lanes of a
+        // quarter warp take 8 rows of one 16-byte column, one 128-byte line
         for (int idx = tt; idx < NR * (D / 8); idx += 32 * kTcWorkers) {
-            const int r = idx / (D / 8), c = idx % (D / 8);
+            const int r = (idx & 7) + 8 * (idx / (8 * (D / 8))), c = (idx / 8) % (D / 8);
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (r < a.rows) {
                 const int i = r / a.group, h = g * a.group + r % a.group;
@@ -274,7 +275,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             const int j = (q % WPS) * 32 + ((lane & 7) << 2) + (lane >> 3);
             const bool have = st < nst;
             const int slot = st % G::kStages;
-            if (have && !mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag)) {
+            if (have && !__all_sync(kFull, mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag,
+                                                             a.err_flag))) {
                 ok = false;
                 break;
             }
@@ -323,7 +325,10 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (lane == 0) mbar_arrive(b_k);           // S^T of this tile may start
             // ---- V row -> fp16 V^T tile (MN-major): (ch, tok) at (tok/8)*2048 + (ch/8)*128 + (tok%8)*16;
             // V^T and P^T are reused: the previous tile's PV must be complete ----
-            if (t > 0 && !mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            if (t > 0 && !__all_sync(kFull, mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag))) {
+                ok = false;
+                break;
+            }
             {
                 // a slot without a token is zeroed: its bits may be NaN, and P = 0 alone leaves 0 * NaN
                 uint8_t *vdst = smem + T::kV + (tt >> 3) * ((D / 8) * 128) + (tt & 7) * 16;
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (have && lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));   // staging slot consumed
 
             // ---- S^T of this warp's 32 tokens: one column per query row ----
-            if (!mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            if (!__all_sync(kFull, mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag))) { ok = false; break; }
             tc_fence_after();
             float x[NR];
 #pragma unroll
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (lane == 0) flag[(t & 1) * 4 + q] = over ? 1 : 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(b_x);
-            if (!mbar_wait_bounded(b_x, t & 1, abort_flag, a.err_flag)) { ok = false; break; }
+            if (!__all_sync(kFull, mbar_wait_bounded(b_x, t & 1, abort_flag, a.err_flag))) { ok = false; break; }
             const bool band = (flag[(t & 1) * 4 + 0] | flag[(t & 1) * 4 + 1] | flag[(t & 1) * 4 + 2] |
                                flag[(t & 1) * 4 + 3]) != 0;
             if (band) {
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_y);
-                if (!mbar_wait_bounded(b_y, nband & 1, abort_flag, a.err_flag)) { ok = false; break; }
+                if (!__all_sync(kFull, mbar_wait_bounded(b_y, nband & 1, abort_flag, a.err_flag))) { ok = false; break; }
                 ++nband;
                 bool moved = false;
 #pragma unroll
@@ -469,9 +474,11 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         }
 
         // ---- epilogue: the split's partial (o normalised, m, l) per row ----
-        if (ok && !*abort_flag) {
+        // (every branch below is taken by whole warps: tensor-memory loads are warp-wide)
+        if (__all_sync(kFull, ok && !*abort_flag)) {
             bool have_o = ntiles > 0;
-            if (have_o && !mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag)) have_o = false;
+            if (have_o && !__all_sync(kFull, mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag)))
+                have_o = false;
             tc_fence_after();
             // the row sums over all tiles, from L^T (every lane holds them)
             if (have_o) {
@@ -493,7 +500,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 if (32 * h + lane < NR) mend[q * NR + 32 * h + lane] = m_w[h];
             __syncwarp();
             if (lane == 0) mbar_arrive(b_l);
-            if (mbar_wait_bounded(b_l, 0, abort_flag, a.err_flag) && !*abort_flag) {
+            if (__all_sync(kFull, mbar_wait_bounded(b_l, 0, abort_flag, a.err_flag) && !*abort_flag)) {
                 const int S = a.num_splits;
                 // per row (lane r, and r + 32): its workspace unit, -1 for a padding row;
                 // the stores below take it from that lane instead of dividing per row
@@ -543,10 +550,13 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     // ---- teardown: copies drained, MMAs complete (the MMA thread waited), tensor memory freed ----
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp >= kConsumerWarps && warp < kTcMmaWarp && lane == 0)
-        for (int st = max(0, issued - G::kStages); st < issued; ++st)
-            mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr, a.err_flag,
-                              100000000ull);
+    if (*abort_flag && warp >= kConsumerWarps && warp < kTcMmaWarp) {
+        if (lane == 0)
+            for (int st = max(0, issued - G::kStages); st < issued; ++st)
+                mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr, a.err_flag,
+                                  100000000ull);
+        __syncwarp();
+    }
     tc_fence_after();
     __syncthreads();
     if (warp == kTcMmaWarp) tmem_dealloc(tmem, T::kCols);

@@ -17,23 +17,26 @@
 //     layout, with a 128-bit mask per tile of the keys whose block-table
 //     entry is outside the pool.  A prefill chunk is re-read by every query
 //     tile, so decoding once costs O(L) instead of O(L x query tiles).
-//  2. prefill_attn_kernel, one CTA per (128 query tokens, query head,
-//     sequence), 192 threads:
-//       warp 4: one thread streams the K and V tiles (one 32 KB 1-D bulk copy
-//               each) through a 3-stage shared ring;
-//       warp 5: allocates tensor memory; one thread issues the MMAs:
-//               S = Q K^T (M = 128 rows, N = 128 keys, K = 16 per instruction,
-//               Q and K both K-major in shared memory) into one of two S
-//               buffers, then O += P V (P from tensor memory, V MN-major in
-//               shared memory);
-//       warps 0-3: thread r owns query row r (tensor-memory lane r): reads its
-//               128 scores, masks the causal diagonal, and writes P (fp16)
-//               over the S buffer it read.  A row's reference moves only when
-//               a score rises more than 2^8 above it (the O row is then
-//               rescaled in tensor memory); the row sum stays in a register.
+//  2. prefill_attn_kernel, one CTA per (256 query tokens, query head,
+//     sequence) -- two 128-row query tiles A and B -- with 320 threads:
+//       warp 8: one thread streams the K and V tiles (one 32 KB 1-D bulk copy
+//               each) through a 2-stage shared ring;
+//       warp 9: allocates tensor memory; one thread issues the MMAs:
+//               S_X = Q_X K^T (M = 128 rows, N = 128 keys, K = 16 per
+//               instruction, both K-major in shared memory) and
+//               O_X += P_X V (P from tensor memory, V MN-major in shared
+//               memory), alternating between the tiles so that the tensor
+//               core works on one tile while the other's softmax runs;
+//       warps 0-3 (tile A) and 4-7 (tile B): thread r of a group owns row r
+//               of its tile (tensor-memory lane r): reads its 128 scores,
+//               masks the causal diagonal, and writes P (fp16) over the S it
+//               read.  A row's reference moves only when a score rises more
+//               than 2^8 above it (the O row is then rescaled in tensor
+//               memory); the row sum stays in a register.
 //     Every wait is bounded (about 2 s); on expiry the CTA reports
 //     KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor
-//     memory and exits without writing.
+//     memory and exits without writing.  Every tensor-memory load and store
+//     and every barrier is reached by whole warps.
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -49,26 +52,26 @@ namespace {
 constexpr int kPfTile = 128;                        // keys per KV tile = query rows per CTA
 constexpr int kPfD = 128;                           // head_dim of this path
 constexpr int kPfTileBytes = kPfTile * kPfD * 2;    // one fp16 tile: 32 KB
-constexpr int kPfStages = 3;
-constexpr int kPfThreads = 192;
-constexpr int kPfSoftmaxWarps = 4;
-constexpr int kPfLoadWarp = 4;
-constexpr int kPfMmaWarp = 5;
+constexpr int kPfStages = 2;
+constexpr int kPfThreads = 320;
+constexpr int kPfSoftmaxWarps = 8;                  // two groups of 4, one per query tile
+constexpr int kPfLoadWarp = 8;
+constexpr int kPfMmaWarp = 9;
 constexpr unsigned kPfFull = 0xFFFFFFFFu;
 
-// shared memory: Q tile, the ring of (K, V) tile pairs, mbarriers, tensor-memory slot
+// shared memory: the two Q tiles, the ring of (K, V) tile pairs, mbarriers, tensor-memory slot
 constexpr int kPfQ = 0;
-constexpr int kPfRing = kPfQ + kPfTileBytes;
+constexpr int kPfRing = kPfQ + 2 * kPfTileBytes;
 constexpr int kPfBar = kPfRing + kPfStages * 2 * kPfTileBytes;
-// barriers: full[3], empty[3], q, s[2], p[2], pv, drain
-constexpr int kPfNumBars = 2 * kPfStages + 1 + 2 + 2 + 1 + 1;
+// barriers: full[2], empty[2], q, s[2], p[2], pv[2], drain
+constexpr int kPfNumBars = 2 * kPfStages + 1 + 2 + 2 + 2 + 1;
 constexpr int kPfAbort = kPfBar + 8 * kPfNumBars;
 constexpr int kPfTmemSlot = kPfAbort + 8;
 constexpr int kPfSmemBytes = kPfTmemSlot + 8;
 static_assert(kPfSmemBytes <= 232448, "prefill shared memory exceeds one CTA's limit");
 
-// tensor-memory columns: two S buffers (P written over the first 64 columns of
-// the one it came from), the O accumulator
+// tensor-memory columns: S_A, S_B (P written over the first 64 columns of the
+// S it came from), O_A, O_B
 constexpr uint32_t kPfColS = 0, kPfColO = 2 * kPfTile, kPfCols = 512;
 
 // Byte offset of element (row, col) of a 128 x 128 fp16 tile in the
@@ -154,8 +157,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
     const int g = h / a.group;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // the sequence's chunk; query tiles in reverse order, so that the tiles
-    // with the most keys start first
+    // the sequence's chunk; pairs of query tiles in reverse order, so that the
+    // tiles with the most keys start first
     // (read before grid_dependency_wait: the previous kernel, the tile gather,
     // does not write them, and it let this grid start only after its own wait
     // on whatever wrote them)
@@ -167,20 +170,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
         if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && !empty_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
         return;
     }
-    const int nqt = (n + kPfTile - 1) / kPfTile;
-    const int qt = nqt - 1 - (int)blockIdx.x;
-    if (qt < 0) return;
-    const int i0 = qt * kPfTile;                           // first query token of the tile
-    const int i_end = min(n, i0 + kPfTile);
-    const int base = L - n;                                // position of query token 0
-    const int ntiles = (base + i_end - 1) / kPfTile + 1;   // KV tiles any row of the tile sees
-    const int first_masked = (base + i0) / kPfTile;        // tiles from here on need the causal mask
+    const int npairs = (n + 2 * kPfTile - 1) / (2 * kPfTile);
+    const int pair = npairs - 1 - (int)blockIdx.x;
+    if (pair < 0) return;
+    const int base = L - n;                                 // position of query token 0
+    // tile X (0 = A, 1 = B) holds query tokens [i0 + 128 X, min(n, i0 + 128 X + 128))
+    const int i0 = pair * 2 * kPfTile;
+    auto tiles_of = [&](int x) {                            // key tiles a row of tile x sees (0: no rows)
+        const int lo = i0 + x * kPfTile;
+        return lo < n ? (base + min(n, lo + kPfTile) - 1) / kPfTile + 1 : 0;
+    };
+    const int nt_a = tiles_of(0), nt_b = tiles_of(1);
+    const int ntiles = max(nt_a, nt_b);
 
     const uint32_t bar = smem_u32(smem + kPfBar);
     auto full = [&](int s) { return bar + 8 * s; };
     auto empty = [&](int s) { return bar + 8 * (kPfStages + s); };
-    const uint32_t b_q = bar + 8 * (2 * kPfStages), b_s0 = b_q + 8, b_p0 = b_q + 24, b_pv = b_q + 40,
-                   b_drain = b_q + 48;
+    const uint32_t b_q = bar + 8 * (2 * kPfStages);
+    const uint32_t b_s0 = b_q + 8, b_p0 = b_q + 24, b_pv0 = b_q + 40, b_drain = b_q + 56;   // [X] at + 8 X
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPfAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPfTmemSlot);
 
@@ -190,11 +197,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
             mbar_init(empty(s), 1);
         }
         mbar_init(b_q, kPfSoftmaxWarps);
-        mbar_init(b_s0, 1);
-        mbar_init(b_s0 + 8, 1);
-        mbar_init(b_p0, kPfSoftmaxWarps);
-        mbar_init(b_p0 + 8, kPfSoftmaxWarps);
-        mbar_init(b_pv, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b_s0 + 8 * x, 1);
+            mbar_init(b_p0 + 8 * x, kPfSoftmaxWarps / 2);
+            mbar_init(b_pv0 + 8 * x, 1);
+        }
         mbar_init(b_drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -230,37 +237,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
     } else if (warp == kPfMmaWarp) {
         // ================= MMA issue (one thread) =================
         if (lane == 0) {
-            const uint32_t q_addr = smem_u32(smem + kPfQ);
             const uint32_t id_qk = umma_idesc_f16(kPfTile, kPfTile, false, false);
             const uint32_t id_pv = umma_idesc_f16(kPfTile, kPfD, false, true);
-            bool ok = mbar_wait_bounded(b_q, 0, abort_flag, a.err_flag);
-            for (int t = 0; ok && t <= ntiles; ++t) {
-                if (t < ntiles) {
-                    const int s = t % kPfStages;
-                    if (!mbar_wait_bounded(full(s), (t / kPfStages) & 1, abort_flag, a.err_flag)) break;
-                    tc_fence_after();
-                    // S[t&1] = Q K_t^T.  S[t&1] last held P(t-2), which PV(t-2), issued
-                    // before this instruction, has read (MMAs of one thread run in order).
-                    const uint32_t k_addr = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes);
+            const uint32_t q_addr = smem_u32(smem + kPfQ);
+            // S_X = Q_X K_t^T.  S_X last held P_X(t-1), which PV_X(t-1), issued
+            // before this instruction, has read (MMAs of one thread run in order).
+            auto qk = [&](int x, int t) {
+                const uint32_t k_addr = smem_u32(smem + kPfRing + (t % kPfStages) * 2 * kPfTileBytes);
 #pragma unroll
-                    for (int ks = 0; ks < kPfD / 16; ++ks)
-                        umma_smem_a(tmem + kPfColS + (t & 1) * kPfTile, umma_desc(q_addr + ks * 256, 128, 2048),
-                                    umma_desc(k_addr + ks * 256, 128, 2048), id_qk, ks > 0);
-                    umma_commit(b_s0 + 8 * (t & 1));
-                }
-                if (t >= 1) {
-                    const int u = t - 1, s = u % kPfStages;
-                    if (!mbar_wait_bounded(b_p0 + 8 * (u & 1), (u >> 1) & 1, abort_flag, a.err_flag)) break;
-                    tc_fence_after();
-                    // O += P(u) V_u: A = P (tensor memory, two fp16 per column), B = V (MN-major)
-                    const uint32_t v_addr = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes + kPfTileBytes);
+                for (int ks = 0; ks < kPfD / 16; ++ks)
+                    umma_smem_a(tmem + kPfColS + x * kPfTile,
+                                umma_desc(q_addr + x * kPfTileBytes + ks * 256, 128, 2048),
+                                umma_desc(k_addr + ks * 256, 128, 2048), id_qk, ks > 0);
+                umma_commit(b_s0 + 8 * x);
+            };
+            // O_X += P_X(t) V_t: A = P (tensor memory, two fp16 per column), B = V (MN-major)
+            auto pv = [&](int x, int t) {
+                const uint32_t v_addr = smem_u32(smem + kPfRing + (t % kPfStages) * 2 * kPfTileBytes + kPfTileBytes);
 #pragma unroll
-                    for (int ks = 0; ks < kPfTile / 16; ++ks)
-                        umma_tmem_a(tmem + kPfColO, tmem + kPfColS + (u & 1) * kPfTile + ks * 8,
-                                    umma_desc(v_addr + ks * 4096, 2048, 128), id_pv, u > 0 || ks > 0);
-                    umma_commit(b_pv);
-                    umma_commit(empty(s));   // the stage's K and V are read once PV(u) completes
+                for (int ks = 0; ks < kPfTile / 16; ++ks)
+                    umma_tmem_a(tmem + kPfColO + x * kPfTile, tmem + kPfColS + x * kPfTile + ks * 8,
+                                umma_desc(v_addr + ks * 4096, 2048, 128), id_pv, t > 0 || ks > 0);
+                umma_commit(b_pv0 + 8 * x);
+            };
+            auto wait_full = [&](int t) {
+                if (!mbar_wait_bounded(full(t % kPfStages), (t / kPfStages) & 1, abort_flag, a.err_flag)) return false;
+                tc_fence_after();
+                return true;
+            };
+            bool ok = mbar_wait_bounded(b_q, 0, abort_flag, a.err_flag) && ntiles > 0 && wait_full(0);
+            if (ok) {
+                if (nt_a > 0) qk(0, 0);
+                if (nt_b > 0) qk(1, 0);
+            }
+            for (int t = 0; ok && t < ntiles; ++t) {
+                if (t < nt_a) {
+                    if (!mbar_wait_bounded(b_p0, t & 1, abort_flag, a.err_flag)) break;
+                    tc_fence_after();
+                    pv(0, t);
                 }
+                const bool next = t + 1 < ntiles;
+                if (next && !wait_full(t + 1)) break;
+                if (t + 1 < nt_a) qk(0, t + 1);
+                if (t < nt_b) {
+                    if (!mbar_wait_bounded(b_p0 + 8, t & 1, abort_flag, a.err_flag)) break;
+                    tc_fence_after();
+                    pv(1, t);
+                }
+                umma_commit(empty(t % kPfStages));   // the stage's K and V are read once these MMAs complete
+                if (t + 1 < nt_b) qk(1, t + 1);
             }
             // every MMA issued so far completes before the tensor memory is freed
             umma_commit(b_drain);
@@ -268,19 +293,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
         }
         __syncwarp();
     } else {
-        // ================= softmax warps: thread r owns query row r =================
-        const int r = 32 * warp + lane;
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        const int i = i0 + r;                                   // query token of this row
-        const bool row_ok = i < i_end;
+        // ================= softmax groups: thread r of group X owns row r of tile X =================
+        const int x = warp >> 2;                                // query tile
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int i = i0 + x * kPfTile + r;                     // query token of this row
+        const bool row_ok = i < n;
         const int limit = row_ok ? base + i : -1;               // last key this row sees
+        const int nt = x ? nt_b : nt_a;
+        const int first_masked = (base + i0 + x * kPfTile) / kPfTile;   // tiles from here on need the causal mask
+        const uint32_t b_s = b_s0 + 8 * x, b_p = b_p0 + 8 * x, b_pv = b_pv0 + 8 * x;
         // Q row -> K-major Q tile
         {
-            const __half *qrow = static_cast<const __half *>(a.q) + ((int64_t)(q0 + i) * a.num_q_heads + h) * kPfD;
+            const __half *qrow = static_cast<const __half *>(a.q) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
 #pragma unroll
             for (int c8 = 0; c8 < kPfD / 8; ++c8) {
                 const uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(qrow) + c8) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(smem + kPfQ + tile_off(r, c8)) = v;
+                *reinterpret_cast<uint4 *>(smem + kPfQ + x * kPfTileBytes + tile_off(r, c8)) = v;
             }
             fence_async_smem();
             __syncwarp();
@@ -288,14 +317,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
         }
         const float qk = a.qk_scale_log2;
         const uint32_t *mask_row = a.tile_mask + (((int64_t)b * a.num_kv_heads + g) * a.max_tiles) * 4;
+        const uint32_t sb = tmem + lane_base + kPfColS + x * kPfTile;
+        const uint32_t ob = tmem + lane_base + kPfColO + x * kPfTile;
         float ref = -INFINITY;   // the row's reference (log2 units)
         float lsum = 0.f;        // sum of 2^(s - ref) over the keys so far
         bool ok = true;          // the same on every lane: tensor-memory loads and stores are warp-wide
-        for (int t = 0; t < ntiles; ++t) {
-            const uint32_t sb = tmem + lane_base + kPfColS + (t & 1) * kPfTile;
+        for (int t = 0; t < nt; ++t) {
             // keys of this tile left out for a bad block-table entry (almost always none)
             const uint4 badk = __ldg(reinterpret_cast<const uint4 *>(mask_row) + t);
-            if (!__all_sync(kPfFull, mbar_wait_bounded(b_s0 + 8 * (t & 1), (t >> 1) & 1, abort_flag, a.err_flag))) {
+            if (!__all_sync(kPfFull, mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag))) {
                 ok = false;
                 break;
             }
@@ -304,34 +334,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
 #pragma unroll
             for (int c = 0; c < kPfTile / 16; ++c) tmem_ld16(sb + 16 * c, xr[c]);
             tmem_wait_ld();
-            float x[kPfTile];
+            float xv[kPfTile];
 #pragma unroll
             for (int c = 0; c < kPfTile / 16; ++c) {
                 tmem_regs_ready(xr[c]);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) x[16 * c + e] = __uint_as_float(xr[c][e]);
+                for (int e = 0; e < 16; ++e) xv[16 * c + e] = __uint_as_float(xr[c][e]);
             }
             if ((badk.x | badk.y | badk.z | badk.w) != 0u) {
                 const uint32_t bw[4] = {badk.x, badk.y, badk.z, badk.w};
 #pragma unroll
                 for (int c = 0; c < kPfTile; ++c)
-                    if ((bw[c >> 5] >> (c & 31)) & 1u) x[c] = -INFINITY;
+                    if ((bw[c >> 5] >> (c & 31)) & 1u) xv[c] = -INFINITY;
             }
-            float mx = -INFINITY;
+            // the row maximum of the raw scores over 8 independent chains (the
+            // log2-domain scale qk > 0 is applied after: max(s) * qk = max(s * qk))
             if (t >= first_masked) {
                 const int k0 = t * kPfTile;
 #pragma unroll
-                for (int c = 0; c < kPfTile; ++c) {
-                    x[c] = (k0 + c <= limit) ? x[c] * qk : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kPfTile; ++c) {
-                    x[c] *= qk;
-                    mx = fmaxf(mx, x[c]);
-                }
+                for (int c = 0; c < kPfTile; ++c)
+                    if (k0 + c > limit) xv[c] = -INFINITY;
             }
+            float m8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) m8[u] = xv[u];
+#pragma unroll
+            for (int c = 8; c < kPfTile; c += 8)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], xv[c + u]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qk;
             // the reference moves when a score rises more than 2^8 above it; the
             // row's sum and (once PV(t-1) is complete) its O row are rescaled.  The
             // O pass is warp-wide; lanes whose reference stays scale by 1.
@@ -347,7 +379,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ob = tmem + lane_base + kPfColO;
 #pragma unroll 1
                 for (int c = 0; c < kPfD; c += 16) {
                     uint32_t r16[16];
@@ -359,34 +390,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                     tmem_st16(ob + c, r16);
                 }
             }
-            // P = 2^(x - ref) as fp16 pairs over the first 64 columns of the S buffer
+            // P = 2^(s qk - ref) as fp16 pairs over the first 64 columns of S; the
+            // row sum over 8 independent chains
             const float rf = (ref == -INFINITY) ? 0.f : ref;   // a row with no key yet: P = 0
+            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < kPfTile; c += 32) {
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(x[c + 2 * e] - rf), p1 = fast_exp2(x[c + 2 * e + 1] - rf);
-                    lsum += p0 + p1;
+                    const float p0 = fast_exp2(fmaf(xv[c + 2 * e], qk, -rf));
+                    const float p1 = fast_exp2(fmaf(xv[c + 2 * e + 1], qk, -rf));
+                    l8[e & 7] += p0 + p1;
                     w[e] = pack_half2(p0, p1);
                 }
                 tmem_st16(sb + c / 2, w);
             }
+            lsum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_p0 + 8 * (t & 1));
+            if (lane == 0) mbar_arrive(b_p);
         }
         // ---- epilogue: O / l * v_scale -> fp16 output row (every lane loads, valid rows store) ----
-        if (ok && __all_sync(kPfFull, !*abort_flag &&
-                                          mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag))) {
+        if (nt > 0 && ok &&
+            __all_sync(kPfFull, !*abort_flag && mbar_wait_bounded(b_pv, (nt - 1) & 1, abort_flag, a.err_flag))) {
             tc_fence_after();
             const float coef = lsum > 0.f ? a.out_scale / lsum : 0.f;
             __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
 #pragma unroll 1
             for (int c = 0; c < kPfD; c += 16) {
                 uint32_t r16[16];
-                tmem_ld16(tmem + lane_base + kPfColO + c, r16);
+                tmem_ld16(ob + c, r16);
                 tmem_wait_ld();
                 tmem_regs_ready(r16);
                 uint4 o0, o1;
@@ -451,7 +486,7 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t stream)
     }
     e = launch_pdl(kv_tile_kernel<E4M3>, dim3(a.max_tiles, a.num_kv_heads, a.batch), dim3(256), 0, stream, a);
     if (e != cudaSuccess) return e;
-    const dim3 grid((a.max_q_len + kPfTile - 1) / kPfTile, a.num_q_heads, a.batch);
+    const dim3 grid((a.max_q_len + 2 * kPfTile - 1) / (2 * kPfTile), a.num_q_heads, a.batch);
     return launch_pdl(prefill_attn_kernel<E4M3>, grid, dim3(kPfThreads), kPfSmemBytes, stream, a);
 }
 
