@@ -70,6 +70,35 @@ def test_prefill_matches_oracle(lens, n, e4m3):
     G.assert_close(out.float().cpu().numpy().reshape(B, n, Hq, D), _oracle(dp), f"prefill {lens} n={n}")
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (32, 2), (12, 4)])
+def test_prefill_group_sizes(Hq, Hkv):
+    """MHA (one query head per kv head), 16 query heads per kv head, and an
+    odd group of 3, over chunks that end mid-tile."""
+    dp = G.device_problem(_problem([333, 190], 190, Hq=Hq, Hkv=Hkv, wid=26), True)
+    out, _ = _prefill(dp)
+    assert dp.err.item() == 0
+    B, n, _, D = dp.q.shape
+    G.assert_close(out.float().cpu().numpy().reshape(B, n, Hq, D), _oracle(dp), f"Hq={Hq} Hkv={Hkv}")
+
+
+def test_prefill_is_deterministic_and_split_invariant():
+    """Two calls give the same bits; and a chunk attended in one call equals
+    the same rows attended as two consecutive chunks of 100 and 156 tokens
+    (the second with the first already in its context)."""
+    pr = _problem([512], 256, wid=27)
+    dp = G.device_problem(pr, True)
+    a, _ = _prefill(dp)
+    b, _ = _prefill(dp)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # the first 100 rows as a chunk of a 356-token context
+    lens = dp.context_lens.clone()
+    lens[0] = 512 - 156
+    dp2 = G.device_problem(pr, True)
+    dp2.q = dp.q[:, :100].contiguous()
+    c, _ = _prefill(dp2, lens=lens)
+    G.assert_close(c.float().cpu().numpy(), a.float().cpu().numpy()[:100], "chunk split")
+
+
 @pytest.mark.parametrize("e4m3", [True, False])
 def test_prefill_chunks_of_different_lengths(e4m3):
     """Chunks of 200, 0, 1 and 77 tokens packed back to back: each is the
