@@ -401,37 +401,73 @@ class Arm:
         return tuple(float(x) for x in np.percentile(d, [10, 50, 90]))
 
     def time_e2e(self, steps, warmup):
-        """Per step: H2D of the step's inputs from pinned host memory, the
-        step's kernels through the public calls, and a D2H read of the output,
-        all on one stream."""
+        """Per step, on one stream: the H2D copy of the step's inputs (Q, the
+        new K/V, slots, block tables, lengths; packed in one pinned host
+        buffer, so one copy), the step through the public calls, and a D2H
+        read of the output.  Each step is captured in a CUDA graph, as a
+        serving loop captures its layers; the graph replays the copies every
+        step from whatever the host buffer holds."""
         torch = self.torch
-        src = {"q": self.q, "k": self.k_new, "v": self.v_new, "slots": self.step_slots,
-               "bt": self.bt, "cl": self.cl}
-        host = {n: t.cpu().pin_memory() for n, t in src.items()}
-        dev = {n: torch.empty_like(t) for n, t in src.items()}
+        src = [("q", self.q), ("k", self.k_new), ("v", self.v_new), ("slots", self.step_slots),
+               ("bt", self.bt), ("cl", self.cl)]
+        host, dev = staged_buffers(torch, src, self.dev)
         out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        h2d = sum(t.numel() * t.element_size() for _, t in src)
         d2h = out_host.numel() * out_host.element_size()
 
         def one(i):
-            for n in host:
-                dev[n].copy_(host[n], non_blocking=True)
+            dev["_buf"].copy_(host["_buf"], non_blocking=True)
             kc, vc = self.pools[i % self.copies]
             self._append(dev["k"], dev["v"], dev["slots"], kc, vc)
             self._attention(kc, vc, dev["q"], dev["bt"], dev["cl"])
             self.kvq.lse_combine(self.ws, self.out, self.p)
             out_host.copy_(self.out, non_blocking=True)
 
-        for i in range(warmup):
-            one(i)
-        torch.cuda.synchronize(self.dev)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record()
-        for i in range(steps):
-            one(warmup + i)
-        end.record()
-        torch.cuda.synchronize(self.dev)
-        return start.elapsed_time(end) / steps, h2d, d2h
+        return replay_timed(torch, self.dev, one, self.copies, steps, warmup), h2d, d2h
+
+
+def staged_buffers(torch, src, device):
+    """One pinned host buffer and one device buffer holding the tensors of
+    `src` (name, tensor) at 256-byte aligned offsets, filled with their
+    values; returns (host views, device views), each with "_buf"."""
+    offs, total = {}, 0
+    for name, t in src:
+        offs[name] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(total, dtype=torch.uint8, device=device)
+    host, dev = {"_buf": hbuf}, {"_buf": dbuf}
+    for name, t in src:
+        n = t.numel() * t.element_size()
+        hv = hbuf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+        hv.copy_(t.cpu())
+        host[name] = hv
+        dev[name] = dbuf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+    return host, dev
+
+
+def replay_timed(torch, device, one, copies, steps, warmup):
+    """Capture one(i) for i < copies in CUDA graphs, replay them in turn and
+    return the average ms per step (events around exactly `steps` replays)."""
+    for i in range(2):
+        one(i)
+    torch.cuda.synchronize(device)
+    graphs = []
+    for r in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one(r)
+        graphs.append(g)
+    for i in range(warmup):
+        graphs[i % copies].replay()
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(steps):
+        graphs[i % copies].replay()
+    end.record()
+    torch.cuda.synchronize(device)
+    return start.elapsed_time(end) / steps
 
 
 # ---------------------------------------------------------------------------
@@ -630,22 +666,24 @@ class PrefillArm:
 
     def time_e2e(self, steps, warmup):
         """Through the public calls with the chunk's Q and K/V copied in from
-        pinned host memory and the output read back, every step."""
+        pinned host memory (one packed buffer, one copy) and the output read
+        back, every step; each step captured in a CUDA graph."""
         torch = self.torch
         k, v, q, kc, vc, out, ks, vs = self.sets[0]
-        hk, hv, hq = (t.cpu().pin_memory() for t in (k, v, q))
+        host, dev = staged_buffers(torch, [("k", k), ("v", v), ("q", q)], self.dev)
         ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
 
         def one(i):
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            q.copy_(hq, non_blocking=True)
-            self._append(0)
-            self.attention(0)
+            dev["_buf"].copy_(host["_buf"], non_blocking=True)
+            if self.e4m3:
+                self.kvq.kv_append_e4m3(dev["k"], dev["v"], self.slots, kc, vc, ks, vs, self.err)
+            else:
+                self.kvq.kv_append_fp16(dev["k"], dev["v"], self.slots, kc, vc, self.err)
+            self.attention(0, q=dev["q"], out=out)
             ho.copy_(out, non_blocking=True)
-        ms = self._events(one, steps, warmup) / steps
-        h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq))
-        return ms, h2d, ho.numel() * ho.element_size()
+        ms = replay_timed(torch, self.dev, one, 1, steps, warmup)
+        assert self.err.item() == 0, f"device error bits {self.err.item()}"
+        return ms, sum(t.numel() * t.element_size() for t in (k, v, q)), ho.numel() * ho.element_size()
 
 
 def prefill_oracle_sample(w, rows=(0, 4095, 8191)):
@@ -730,7 +768,8 @@ def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
             "e2e": {"value": world * arm.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": arm.launches * args.steps,
-            "launch": "append, tile gather, attention per step (programmatic dependent launch)",
+            "launch": "append, tile gather, attention per step (programmatic dependent launch); "
+                      "e2e: one graph per step with the H2D and D2H copies",
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -926,7 +965,7 @@ def main():
                     "ms_per_step": e2e_ms},
             "gpu_launches": arm.launches * args.steps,
             "launch": f"CUDA graphs of {GRAPH_STEPS} steps (append, attention, combine per step; "
-                      "programmatic dependent launch)",
+                      "programmatic dependent launch); e2e: one graph per step with the H2D and D2H copies",
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
