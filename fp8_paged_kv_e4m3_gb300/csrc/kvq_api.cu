@@ -23,8 +23,7 @@ WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t
     w.o_off = 0;
     w.m_off = round256(units * size_t(head_dim) * sizeof(float));
     w.l_off = w.m_off + round256(units * sizeof(float));
-    w.counter_off = w.l_off + round256(units * sizeof(float));
-    w.total = w.counter_off + 256;
+    w.total = w.l_off + round256(units * sizeof(float));
     return w;
 }
 
@@ -148,7 +147,6 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.ws_o = reinterpret_cast<float *>(ws + wl.o_off);
     a.ws_m = reinterpret_cast<float *>(ws + wl.m_off);
     a.ws_l = reinterpret_cast<float *>(ws + wl.l_off);
-    a.work_counter = reinterpret_cast<uint32_t *>(ws + wl.counter_off);
     a.err_flag = c.err_flag;
     a.batch = p.batch;
     a.q_len = p.q_len;

@@ -277,20 +277,16 @@ __device__ __forceinline__ SeqPick lpt_pick(const AttnArgs &a, int z, uint8_t *s
 // split's nst stages: it reads the block table a batch ahead, waits for the
 // stage's ring slot to be released, records the token positions (K warp),
 // and issues one 1-D bulk copy per page (dense) or per listed token row
-// (top-k), completing on the slot's full mbarrier.  The split's stages are
-// stages stage_base .. stage_base + nst - 1 of the ring's sequence (a CTA
-// that works through several splits continues the sequence).  Returns
-// stage_base + the stages issued.
+// (top-k), completing on the slot's full mbarrier.  Returns the stages issued.
 template <class G, int PPS>
 __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRange &r, int nst, int b, int g,
                                               int lane, bool is_v, int bt_spec, uint32_t ring, uint32_t bar0,
-                                              int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad,
-                                              int stage_base = 0)
+                                              int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad)
 {
     const int item0 = r.item0, item1 = r.item1, L = r.L, spec0 = r.spec0;
     const bool topk = r.topk;
     const int32_t *bt_row = r.bt_row;
-    int issued = stage_base;
+    int issued = 0;
         const uint64_t pol = l2_policy_evict_first();
         const uint8_t *pool = static_cast<const uint8_t *>(is_v ? a.v_cache : a.k_cache);
         if (!topk) {
@@ -304,10 +300,9 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
             const int p = lane % PPS;                      // page of the stage this lane copies
             const bool copier = lane < PPS;
             for (int st = 0; st < nst; ++st) {
-                const int gs = stage_base + st;
-                const int slot = gs % G::kStages;
-                if (gs >= G::kStages &&
-                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((gs / G::kStages) + 1) & 1,
+                const int slot = st % G::kStages;
+                if (st >= G::kStages &&
+                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
                     break;
                 if (st > 0 && st % SPB == 0) {
@@ -339,7 +334,7 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
                                          p * G::kPageStride;
                     tma_load_1d(dst, src, G::kChunk, bar0 + 8 * slot, pol);
                 }
-                issued = gs + 1;
+                issued = st + 1;
             }
         } else {
             // top-k: kTokPerStage listed tokens per stage, R per lane
@@ -360,10 +355,9 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
                 idx_nxt[r] = load_idx(1, r);
             }
             for (int st = 0; st < nst; ++st) {
-                const int gs = stage_base + st;
-                const int slot = gs % G::kStages;
-                if (gs >= G::kStages &&
-                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((gs / G::kStages) + 1) & 1,
+                const int slot = st % G::kStages;
+                if (st >= G::kStages &&
+                    !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
                     break;
                 int pg_nxt[R], idx_nxt2[R];
@@ -401,7 +395,7 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
                     pg_cur[r] = pg_nxt[r];
                     idx_nxt[r] = idx_nxt2[r];
                 }
-                issued = gs + 1;
+                issued = st + 1;
             }
         }
     return issued;

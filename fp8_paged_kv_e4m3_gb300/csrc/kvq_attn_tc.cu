@@ -46,7 +46,6 @@ constexpr int kTcMmaWarp = kConsumerWarps + kProducerWarps;   // 6
 constexpr int kTcThreads = 32 * (kTcMmaWarp + 1);             // 224
 constexpr int kTcTile = 128;                                  // tokens per MMA tile
 constexpr int kTcD = 128;                                     // head_dim of this kernel
-constexpr int kTcLptMax = 256;                                // longest-first order up to this batch
 // pages per staging stage: 16 (64 tokens) for E4M3, 8 (32 tokens) for fp16, so
 // that the staging ring keeps two CTAs per SM for both element sizes
 template <bool E4M3> __host__ __device__ constexpr int tc_pps() { return E4M3 ? 16 : 8; }
@@ -66,14 +65,12 @@ struct TcLayout {
     static constexpr int kWmax = kP + NR * 256;              // [2][4][NR] float: per-worker row maxima
     static constexpr int kPriv = kWmax + 2 * 4 * NR * 4;     // [4][4][NR] float: per-worker reference,
                                                              //   correction, coefficient, reference in use
-    static constexpr int kLsum = kPriv + 4 * 4 * NR * 4;     // [2][4][NR] float: per-worker row sums (by item parity)
-    static constexpr int kMend = kLsum + 2 * 4 * NR * 4;     // [2][4][NR] float: per-worker final row maxima
-    static constexpr int kFlag = kMend + 2 * 4 * NR * 4;     // [2][4] int: per-worker "left the band" flags
-    static constexpr int kBar = kFlag + 2 * 4 * 4;           // 13 mbarriers
-    static constexpr int kTmemSlot = kBar + 13 * 8;
-    static constexpr int kItems = kTmemSlot + 8;             // [2] int: the work-item ring
-    static constexpr int kPerm = kItems + 8;                 // [kTcLptMax] int: sequences, longest first
-    static constexpr int kBytes = kPerm + 4 * kTcLptMax;
+    static constexpr int kLsum = kPriv + 4 * 4 * NR * 4;     // [4][NR] float: per-worker row sums
+    static constexpr int kMend = kLsum + 4 * NR * 4;         // [4][NR] float: per-worker final row maxima
+    static constexpr int kFlag = kMend + 4 * NR * 4;         // [2][4] int: per-worker "left the band" flags
+    static constexpr int kBar = kFlag + 2 * 4 * 4;           // 8 mbarriers
+    static constexpr int kTmemSlot = kBar + 8 * 8;
+    static constexpr int kBytes = kTmemSlot + 16;
     // tensor-memory columns: K tile (64: 128 fp16 per lane), S^T (NR), O^T (NR), the row
     // sums L^T (NR, every lane the same: a ones tile times P^T), the ones tile (64)
     static constexpr int kColK = 0, kColS = 64, kColO = 64 + NR, kColL = 64 + 2 * NR, kColOnes = 64 + 3 * NR;
@@ -114,6 +111,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     constexpr int NH = NR <= 32 ? 1 : 2;                      // rows per lane after a transpose-reduce
     extern __shared__ __align__(1024) uint8_t smem[];
 
+    const int s = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring = smem_u32(smem);
     int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
@@ -122,11 +120,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     volatile int *stage_bad = abort_flag + 1;
     const uint32_t tb = smem_u32(smem + T::kBar);
     const uint32_t b_k = tb, b_s = tb + 8, b_p = tb + 16, b_pv = tb + 24, b_x = tb + 32, b_l = tb + 40,
-                   b_drain = tb + 48, b_y = tb + 56, b_e = tb + 64;
-    const uint32_t b_item = tb + 72, b_free = tb + 88;         // [2] each: the work-item ring
+                   b_drain = tb + 48, b_y = tb + 56;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + T::kTmemSlot);
-    volatile int *item_ring = reinterpret_cast<volatile int *>(smem + T::kItems);
-    int *perm = reinterpret_cast<int *>(smem + T::kPerm);
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < G::kStages; ++k) {
@@ -141,123 +136,48 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         mbar_init(b_l, kTcWorkers);
         mbar_init(b_drain, 1);
         mbar_init(b_y, kTcWorkers);
-        mbar_init(b_e, kTcWorkers);
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(b_item + 8 * k, 1);                  // published by the K producer
-            mbar_init(b_free + 8 * k, 2 + kTcWorkers);     // read by the V producer, the MMA thread, the workers
-        }
         *abort_flag = 0;
         *stage_bad = 0;
         fence_mbar_init();
     }
     if (warp == kTcMmaWarp) tmem_alloc(smem_u32(tmem_slot), T::kCols);
-    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append, the counter reset)
+    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
 
-    // The sequences, longest first (by attended work, in quarter-octave classes,
-    // by index inside a class): work item k is split k % S of kv head
-    // (k / S) % Hkv of the sequence of rank k / (S Hkv).  CTAs take items from
-    // a shared counter, so the long sequences start first and the short ones
-    // fill the gaps (longest-processing-time-first list scheduling).
-    const bool lpt = a.batch <= kTcLptMax;
-    if (lpt) {
-        int *cls = reinterpret_cast<int *>(smem + T::kV);    // scratch: V^T is unused until the first tile
-        const bool with_topk = a.topk_idx && a.topk_lens;
-        for (int i = threadIdx.x; i < a.batch; i += blockDim.x)
-            cls[i] = work_class(a, __ldg(a.context_lens + i), with_topk ? __ldg(a.topk_lens + i) : 0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < a.batch; i += blockDim.x) {
-            const int c = cls[i];
-            int pos = 0;
-            for (int j = 0; j < a.batch; ++j) {
-                const int cj = cls[j];
-                pos += (cj > c) || (cj == c && j < i);
-            }
-            perm[pos] = i;
-        }
-    }
+    // sequences longest first; the speculative block-table read (producers) is
+    // issued for the identity order and repeated if another sequence is picked
+    const int z = blockIdx.z;
+    const int spec0 = split_spec0(a, s);
+    const bool spec_lane = warp >= kConsumerWarps && warp < kTcMmaWarp && spec0 + lane < a.max_pages;
+    int bt_spec = spec_lane ? __ldg(a.block_tables + (int64_t)z * a.max_pages + spec0 + lane) : -1;
+    SeqPick pick = seq_identity(a, z);
+    const bool keep_order = lpt_classify(a, smem, G::kRingBytes);
     tc_fence_before();
-    __syncthreads();
+    if (!__syncthreads_and(keep_order)) {   // the setup barrier (mbarriers, tensor memory) as well
+        pick = lpt_pick(a, z, smem);
+        if (pick.b != z) bt_spec = spec_lane ? __ldg(a.block_tables + (int64_t)pick.b * a.max_pages + spec0 + lane) : -1;
+    }
     tc_fence_after();
+    const int b = pick.b;
+    const SplitRange sr = split_range(a, s, b, pick.L, pick.topk_len);
+    const int L = sr.L;
+    const int ipst = sr.topk ? G::kTokPerStage : PPS;
+    const int nst = (sr.item1 - sr.item0 + ipst - 1) / ipst;   // staging stages
+    const int ntiles = (nst + SPT - 1) / SPT;
+    if (threadIdx.x == 0) {
+        if (!sr.len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
+        if (sr.len_ok && pick.topk_len > a.max_topk)
+            report(a.err_flag, KVQ_DEV_BAD_TOPK);
+    }
     // only now may a dependent grid start: this CTA already holds its tensor
     // memory, so a dependent CTA cannot take the columns it waits for
     launch_dependents();
     const uint32_t tmem = *tmem_slot;
-    const int n_items = a.num_splits * a.num_kv_heads * a.batch;
-    int issued = 0;   // staging stages the producer warp issued (all items)
-
-    // One work item: its sequence, kv head, split and stage / tile counts
-    struct Item {
-        int b, g, s, nst, ntiles;
-        SplitRange sr;
-        int topk_len;
-    };
-    auto item_of = [&](int k) {
-        Item it;
-        const int per_seq = a.num_splits * a.num_kv_heads;
-        const int rank = k / per_seq, rem = k - rank * per_seq;
-        it.g = rem / a.num_splits;
-        it.s = rem - it.g * a.num_splits;
-        it.b = lpt ? perm[rank] : rank;
-        const SeqPick pick = seq_identity(a, it.b);
-        it.topk_len = pick.topk_len;
-        it.sr = split_range(a, it.s, it.b, pick.L, pick.topk_len);
-        const int ipst = it.sr.topk ? G::kTokPerStage : PPS;
-        it.nst = (it.sr.item1 - it.sr.item0 + ipst - 1) / ipst;   // staging stages
-        it.ntiles = (it.nst + SPT - 1) / SPT;
-        return it;
-    };
-    // the j-th work item of this CTA (n_items or more: no more work); every
-    // role but the K producer waits for it, then frees its ring slot
-    auto next_item = [&](int j) -> int {
-        const uint32_t slot = (uint32_t)(j & 1);
-        if (!__all_sync(kFull, mbar_wait_bounded(b_item + 8 * slot, (j >> 1) & 1, abort_flag, a.err_flag)))
-            return n_items;
-        const int k = item_ring[slot];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_free + 8 * slot);
-        return k;
-    };
-    // the same for a role run by one thread (the MMA issuer)
-    auto next_item_1 = [&](int j) -> int {
-        const uint32_t slot = (uint32_t)(j & 1);
-        if (!mbar_wait_bounded(b_item + 8 * slot, (j >> 1) & 1, abort_flag, a.err_flag)) return n_items;
-        const int k = item_ring[slot];
-        mbar_arrive(b_free + 8 * slot);
-        return k;
-    };
+    int issued = 0;
 
     if (warp >= kConsumerWarps && warp < kTcMmaWarp) {
         // ================= producers =================
-        // the K producer's lane 0 takes the next item from the counter and
-        // publishes it; both producers then issue its stages, continuing the
-        // ring's stage sequence (so the next item's pages load while the
-        // workers finish the current one)
-        const bool is_v = warp == kConsumerWarps + 1;
-        for (int j = 0;; ++j) {
-            int k;
-            if (!is_v) {
-                const uint32_t slot = (uint32_t)(j & 1);
-                int kk = n_items;
-                if (lane == 0) {
-                    if (j < 2 || mbar_wait_bounded(b_free + 8 * slot, ((j >> 1) - 1) & 1, abort_flag, a.err_flag)) {
-                        kk = (int)atomicAdd(a.work_counter, 1u);
-                        item_ring[slot] = kk;
-                        mbar_arrive(b_item + 8 * slot);
-                    }
-                }
-                k = __shfl_sync(kFull, kk, 0);
-            } else {
-                k = next_item(j);
-            }
-            if (__any_sync(kFull, k >= n_items || *abort_flag)) break;
-            const Item it = item_of(k);
-            const int spec0 = it.sr.spec0;
-            const int bt_spec = spec0 + lane < a.max_pages ? __ldg(it.sr.bt_row + spec0 + lane) : -1;
-            const int gs0 = issued;
-            issued = produce_stages<G, PPS>(a, it.sr, it.nst, it.b, it.g, lane, is_v, bt_spec, ring, bar0, tokpos,
-                                            abort_flag, stage_bad, gs0);
-            if (__any_sync(kFull, issued != gs0 + it.nst)) break;   // a wait gave up
-        }
+        issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, warp == kConsumerWarps + 1, bt_spec, ring,
+                                        bar0, tokpos, abort_flag, stage_bad);
     } else if (warp == kTcMmaWarp) {
         // ================= MMA issue (one thread) =================
         if (lane == 0) {
@@ -266,15 +186,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             const uint32_t id_qk = umma_idesc_f16(kTcTile, NR, false, false);
             const uint32_t id_pv = umma_idesc_f16(kTcTile, NR, true, true);
             const uint32_t id_l = umma_idesc_f16(kTcTile, NR, false, true);
-            int gtile = 0;   // tiles of all items so far
-            bool ok = true;
-            for (int j = 0; ok; ++j) {
-            const int k = next_item_1(j);
-            if (k >= n_items) break;
-            const int ntiles = item_of(k).ntiles;
             for (int t = 0; t < ntiles; ++t) {
-                const int T = gtile + t;
-                if (!mbar_wait_bounded(b_k, T & 1, abort_flag, a.err_flag)) { ok = false; break; }
+                if (!mbar_wait_bounded(b_k, t & 1, abort_flag, a.err_flag)) break;
                 tc_fence_after();
                 // S^T[tok][row] = sum_d K[tok][d] Q[row][d]: A = K tile (tensor memory), B = Q (K-major)
 #pragma unroll
@@ -282,13 +195,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                     umma_tmem_a(tmem + T::kColS, tmem + T::kColK + ks * 8,
                                 umma_desc(q_addr + ks * 256, 128, (D / 8) * 128), id_qk, ks > 0);
                 umma_commit(b_s);
-                if (!mbar_wait_bounded(b_p, T & 1, abort_flag, a.err_flag)) { ok = false; break; }
-                // the item's first PV overwrites O^T and L^T: the workers have read the
-                // previous item's out in its epilogue
-                if (t == 0 && j > 0 && !mbar_wait_bounded(b_e, (j - 1) & 1, abort_flag, a.err_flag)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait_bounded(b_p, t & 1, abort_flag, a.err_flag)) break;
                 tc_fence_after();
                 // O^T[ch][row] += sum_tok V[tok][ch] P[tok][row]: A = V^T, B = P^T, both MN-major
 #pragma unroll
@@ -302,8 +209,6 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                                 umma_desc(p_addr + ks * 2 * NR * 16, NR * 16, 128), id_l, t > 0 || ks > 0);
                 umma_commit(b_pv);
             }
-            gtile += ntiles;
-            }
             // every MMA issued so far completes before the tensor memory is freed
             umma_commit(b_drain);
             mbar_wait_bounded(b_drain, 0, nullptr, a.err_flag, 100000000ull);
@@ -315,35 +220,13 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const int tt = 32 * q + lane;                // token of the tile (S^T lane), channel of O^T
         const float qk = a.qk_scale_log2;
+        const int win0 = L - a.q_len;                // row i sees positions <= win0 + i
         float *wmax = reinterpret_cast<float *>(smem + T::kWmax);
         float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 4 * NR;   // reference, corr, coef, in use
-        int *flag = reinterpret_cast<int *>(smem + T::kFlag);
-        {   // the ones tile (fp16 1.0 pairs), A operand of the row sums
-            uint32_t ones[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ones[e] = 0x3C003C00u;
-#pragma unroll
-            for (int c = 0; c < 64; c += 16) tmem_st16(tmem + lane_base + T::kColOnes + c, ones);
-            tmem_wait_st();
-        }
-        int nband = 0;   // times a row left the band (the same count on every worker)
-        bool ok = true;
-        int gstage = 0, gtile = 0;   // staging stages and tiles of all items so far
-        for (int jj = 0; ok; ++jj) {
-        const int kitem = next_item(jj);
-        if (kitem >= n_items) break;
-        const Item it = item_of(kitem);
-        const int b = it.b, g = it.g, s = it.s, nst = it.nst, ntiles = it.ntiles;
-        const int L = it.sr.L;
-        const int win0 = L - a.q_len;                // row i sees positions <= win0 + i
-        if (threadIdx.x == 0) {
-            if (!it.sr.len_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
-            if (it.sr.len_ok && it.topk_len > a.max_topk) report(a.err_flag, KVQ_DEV_BAD_TOPK);
-        }
-        // the epilogue's buffers alternate between items: a worker may reach an
-        // item's epilogue while another still reads the previous one's
-        float *lsum = reinterpret_cast<float *>(smem + T::kLsum) + (jj & 1) * 4 * NR;
-        float *mend = reinterpret_cast<float *>(smem + T::kMend) + (jj & 1) * 4 * NR;
+        float *lsum = reinterpret_cast<float *>(smem + T::kLsum);
+        // the final maxima get a buffer of their own: a worker may still read the
+        // last tile's exchange in wmax while another has reached the epilogue
+        float *mend = reinterpret_cast<float *>(smem + T::kMend);
 
         // Q rows (padding rows zero) into the K-major Q tile: element (r, d) at
         // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2; the 8 lanes of a
@@ -358,12 +241,12 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             }
             *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
         }
-        fence_async_smem();   // the Q tile is read by the tensor core (async proxy)
 
         // Per row, the reference of the exponentials lives in the worker's private
         // shared copy (all four workers hold the same values): priv[r] (-inf while
         // the row has none), priv[3 NR + r] (the same, 0 while none).  This
         // thread keeps, per row, the running maximum and the sum over its tokens.
+        int *flag = reinterpret_cast<int *>(smem + T::kFlag);
 #pragma unroll
         for (int h = 0; h < NH; ++h)
             if (32 * h + lane < NR) {
@@ -374,17 +257,25 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         float mt[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) mt[r] = -INFINITY;
+        {   // the ones tile (fp16 1.0 pairs), A operand of the row sums
+            uint32_t ones[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ones[e] = 0x3C003C00u;
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) tmem_st16(tmem + lane_base + T::kColOnes + c, ones);
+            tmem_wait_st();
+        }
+        int nband = 0;   // times a row left the band (the same count on every worker)
+        bool ok = true;
         for (int t = 0; t < ntiles && ok; ++t) {
-            const int T_ = gtile + t;                // tile of all items: the phase of the per-tile barriers
-            const int st = SPT * t + q / WPS;        // staging stage of this warp's 32 tokens (in the item)
-            const int gst = gstage + st;             // the same stage in the ring's sequence
+            const int st = SPT * t + q / WPS;        // staging stage of this warp's 32 tokens
             // token of that stage: the 8 lanes of a quarter warp take the same slot of 8
             // different pages, whose 16-byte rows sit in distinct banks (page stride
             // = 16 mod 128); tile slot tt holds this token in S^T, V^T and P^T alike
             const int j = (q % WPS) * 32 + ((lane & 7) << 2) + (lane >> 3);
             const bool have = st < nst;
-            const int slot = gst % G::kStages;
-            if (have && !__all_sync(kFull, mbar_wait_bounded(bar0 + 8 * slot, (gst / G::kStages) & 1, abort_flag,
+            const int slot = st % G::kStages;
+            if (have && !__all_sync(kFull, mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag,
                                                              a.err_flag))) {
                 ok = false;
                 break;
@@ -434,7 +325,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (lane == 0) mbar_arrive(b_k);           // S^T of this tile may start
             // ---- V row -> fp16 V^T tile (MN-major): (ch, tok) at (tok/8)*2048 + (ch/8)*128 + (tok%8)*16;
             // V^T and P^T are reused: the previous tile's PV must be complete ----
-            if (T_ > 0 && !__all_sync(kFull, mbar_wait_bounded(b_pv, (T_ - 1) & 1, abort_flag, a.err_flag))) {
+            if (t > 0 && !__all_sync(kFull, mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag))) {
                 ok = false;
                 break;
             }
@@ -465,7 +356,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (have && lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));   // staging slot consumed
 
             // ---- S^T of this warp's 32 tokens: one column per query row ----
-            if (!__all_sync(kFull, mbar_wait_bounded(b_s, T_ & 1, abort_flag, a.err_flag))) { ok = false; break; }
+            if (!__all_sync(kFull, mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag))) { ok = false; break; }
             tc_fence_after();
             float x[NR];
 #pragma unroll
@@ -494,12 +385,12 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 over |= x[r] > priv[r] + 8.f;   // a row without a reference: any finite score
             }
             over = __any_sync(kFull, over);
-            if (lane == 0) flag[(T_ & 1) * 4 + q] = over ? 1 : 0;
+            if (lane == 0) flag[(t & 1) * 4 + q] = over ? 1 : 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(b_x);
-            if (!__all_sync(kFull, mbar_wait_bounded(b_x, T_ & 1, abort_flag, a.err_flag))) { ok = false; break; }
-            const bool band = (flag[(T_ & 1) * 4 + 0] | flag[(T_ & 1) * 4 + 1] | flag[(T_ & 1) * 4 + 2] |
-                               flag[(T_ & 1) * 4 + 3]) != 0;
+            if (!__all_sync(kFull, mbar_wait_bounded(b_x, t & 1, abort_flag, a.err_flag))) { ok = false; break; }
+            const bool band = (flag[(t & 1) * 4 + 0] | flag[(t & 1) * 4 + 1] | flag[(t & 1) * 4 + 2] |
+                               flag[(t & 1) * 4 + 3]) != 0;
             if (band) {
                 // rare: the tile's exact row maxima, then new references where a maximum
                 // rose more than 2^8 above the old one (the same decision on every worker)
@@ -584,10 +475,9 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 
         // ---- epilogue: the split's partial (o normalised, m, l) per row ----
         // (every branch below is taken by whole warps: tensor-memory loads are warp-wide)
-        if (!__all_sync(kFull, ok && !*abort_flag)) break;
-        {
+        if (__all_sync(kFull, ok && !*abort_flag)) {
             bool have_o = ntiles > 0;
-            if (have_o && !__all_sync(kFull, mbar_wait_bounded(b_pv, (gtile + ntiles - 1) & 1, abort_flag, a.err_flag)))
+            if (have_o && !__all_sync(kFull, mbar_wait_bounded(b_pv, (ntiles - 1) & 1, abort_flag, a.err_flag)))
                 have_o = false;
             tc_fence_after();
             // the row sums over all tiles, from L^T (every lane holds them)
@@ -610,7 +500,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 if (32 * h + lane < NR) mend[q * NR + 32 * h + lane] = m_w[h];
             __syncwarp();
             if (lane == 0) mbar_arrive(b_l);
-            if (__all_sync(kFull, mbar_wait_bounded(b_l, jj & 1, abort_flag, a.err_flag) && !*abort_flag)) {
+            if (__all_sync(kFull, mbar_wait_bounded(b_l, 0, abort_flag, a.err_flag) && !*abort_flag)) {
                 const int S = a.num_splits;
                 // per row (lane r, and r + 32): its workspace unit, -1 for a padding row;
                 // the stores below take it from that lane instead of dividing per row
@@ -655,13 +545,6 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 }
             }
         }
-        // the item's O^T and L^T are read: its tensor memory may take the next item's
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_e);
-        gstage += nst;
-        gtile += ntiles;
-        }
     }
 
     // ---- teardown: copies drained, MMAs complete (the MMA thread waited), tensor memory freed ----
@@ -679,44 +562,23 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     if (warp == kTcMmaWarp) tmem_dealloc(tmem, T::kCols);
 }
 
-// Resets the persistent kernel's work counter (after the previous kernel in
-// the stream has finished with it).
-__global__ void zero_counter_kernel(uint32_t *counter)
-{
-    grid_dependency_wait();
-    if (threadIdx.x == 0) *counter = 0u;
-    launch_dependents();
-}
-
 template <bool E4M3, int NR>
 static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
 {
     constexpr int bytes = TcLayout<E4M3, NR>::kBytes;
     static uint64_t configured = 0;   // one bit per device ordinal
-    static int resident[64] = {0};    // CTAs of this kernel per SM, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 64) return cudaErrorInvalidDevice;
-    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
         e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_tc_kernel<E4M3, NR>, kTcThreads, bytes);
-        if (e != cudaSuccess) return e;
-        resident[dev] = n > 0 ? n : 1;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
-    // persistent CTAs, one per resident slot, taking (sequence, kv head, split)
-    // items from the counter in the workspace
-    const int64_t n_items = (int64_t)a.num_splits * a.num_kv_heads * a.batch;
-    const int64_t slots = (int64_t)resident[dev] * device_sm_count();
-    const dim3 grid((unsigned)(n_items < slots ? n_items : slots));
-    e = launch_pdl(zero_counter_kernel, dim3(1), dim3(32), 0, stream, a.work_counter);
-    if (e != cudaSuccess) return e;
+    const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
     return launch_pdl(attn_tc_kernel<E4M3, NR>, grid, dim3(kTcThreads), bytes, stream, a);
 }
 

@@ -23,7 +23,6 @@ struct AttnArgs {
     float *ws_m;                 // [B][Hq][q_len][S]
     float *ws_l;                 // [B][Hq][q_len][S]
     int32_t *err_flag;
-    uint32_t *work_counter;      // next work item of a persistent kernel (zeroed before it runs)
     int32_t batch, q_len, num_q_heads, num_kv_heads, group, rows, num_splits;
     int32_t split_pages;   // 0 = equal division of each sequence, else pages per split
     int32_t max_pages, max_topk;
@@ -57,7 +56,7 @@ int32_t prefill_max_tiles(int32_t max_pages);
 cudaError_t launch_prefill(bool e4m3, const PrefillArgs &a, cudaStream_t stream);
 
 struct WorkspaceLayout {
-    size_t o_off, m_off, l_off, counter_off, total;
+    size_t o_off, m_off, l_off, total;
 };
 
 WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t head_dim);

@@ -210,7 +210,6 @@ int32_t kvq_attn_num_splits(const kvq_attn_params *p);
  *   tmp_max [B][Hq][q_len][S]            m = max score of the split
  *                                        (natural-log units, -inf if empty)
  *   tmp_sum [B][Hq][q_len][S]            l = sum of exp(s - m) (0 if empty)
- *   then 256 bytes the attention kernels use as a work counter.
  * Entries of empty splits (l == 0) leave tmp_out unwritten. */
 size_t kvq_attn_workspace_bytes(const kvq_attn_params *p);
 

@@ -83,7 +83,7 @@ def test_workspace_size_matches_layout(lib):
     p = _params()
     units = 2 * 8 * 1 * 2
     r = lambda n: (n + 255) // 256 * 256
-    assert lib.kvq_attn_workspace_bytes(ctypes.byref(p)) == r(units * 64 * 4) + 2 * r(units * 4) + 256
+    assert lib.kvq_attn_workspace_bytes(ctypes.byref(p)) == r(units * 64 * 4) + 2 * r(units * 4)
     assert lib.kvq_attn_num_splits(ctypes.byref(p)) == 2
 
 
