@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             }
             *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
         }
+        fence_async_smem();   // the Q tile is read by the tensor core (async proxy)
 
         // Per row, the reference of the exponentials lives in the worker's private
         // shared copy (all four workers hold the same values): priv[r] (-inf while
