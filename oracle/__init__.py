@@ -110,13 +110,16 @@ def _configure(lib):
     lib.oracle_append_fp16.restype = ctypes.c_int
     attn_args = [P, P, P, ctypes.c_int, i64, P, P, f64, f64, P, P,
                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                 ctypes.c_int, ctypes.c_int, f64]
+                 ctypes.c_int, ctypes.c_int, f64, P, P]
     lib.oracle_attn.argtypes = attn_args + [P, P]
     lib.oracle_attn.restype = ctypes.c_int
     lib.oracle_attn_partials.argtypes = attn_args + [ctypes.c_int, ctypes.c_int, P, P, P]
     lib.oracle_attn_partials.restype = ctypes.c_int
     lib.oracle_combine.argtypes = [P, P, P, i64, ctypes.c_int, ctypes.c_int, P]
     lib.oracle_combine.restype = None
+    lib.oracle_quantize_q_groups.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, P, P]
+    lib.oracle_quantize_q_groups.restype = ctypes.c_int
     return lib
 
 
@@ -213,8 +216,25 @@ def append_fp16(k_new, v_new, slot_mapping, k_cache, v_cache) -> int:
 # ---------------------------------------------------------------------------
 # attention
 
+def quantize_q_groups(q, num_kv_heads: int):
+    """The FP8 score variant's query quantisation: per (sequence, kv head) one
+    binary32 scale amax / 448 over the G * q_len rows of the group (1 for an
+    all-zero group), every element quantised like a cache element.
+    q fp16 [B][q_len][Hq][D].  Returns (codes uint8 [B][q_len][Hq][D],
+    scales float32 [B][Hkv])."""
+    qb = _f16_bits(q)
+    B, q_len, Hq, D = qb.shape
+    codes = np.zeros(qb.shape, dtype=np.uint8)
+    scales = np.zeros((B, num_kv_heads), dtype=np.float32)
+    rc = _load().oracle_quantize_q_groups(_ptr(qb), B, q_len, Hq, int(num_kv_heads), D,
+                                          _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_quantize_q_groups: bad arguments")
+    return codes, scales
+
+
 def _attn_common(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_scale,
-                 topk_idx, topk_lens, sm_scale):
+                 topk_idx, topk_lens, sm_scale, fp8_q=False):
     qb = _f16_bits(q)
     B, q_len, Hq, D = qb.shape
     is_e4m3 = 1 if k_cache.dtype == np.uint8 else 0
@@ -234,25 +254,30 @@ def _attn_common(q, k_cache, v_cache, block_tables, context_lens, k_scale, v_sca
         max_topk = ti.shape[2]
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
-    keep = (qb, kc, vc, bt, cl, ti, tl)
+    qc = qs = None
+    if fp8_q:
+        qc, qs = quantize_q_groups(qb, Hkv)
+    keep = (qb, kc, vc, bt, cl, ti, tl, qc, qs)
     args = [_ptr(qb), _ptr(kc), _ptr(vc), is_e4m3, P, _ptr(bt), _ptr(cl),
             float(k_scale), float(v_scale), _ptr(ti), _ptr(tl),
-            B, q_len, Hq, Hkv, D, bt.shape[1], max_topk, float(sm_scale)]
+            B, q_len, Hq, Hkv, D, bt.shape[1], max_topk, float(sm_scale), _ptr(qc), _ptr(qs)]
     return keep, args, (B, q_len, Hq, D)
 
 
 def attention(q, k_cache, v_cache, block_tables, context_lens, k_scale=1.0, v_scale=1.0,
-              topk_idx=None, topk_lens=None, sm_scale=None, return_lse=False):
+              topk_idx=None, topk_lens=None, sm_scale=None, return_lse=False, fp8_q=False):
     """Plain binary64 decode / verify attention over a paged cache.
 
     q fp16 [B][q_len][Hq][D]; caches uint8 (E4M3 arm) or fp16 [P][Hkv][4][D];
     block_tables int32 [B][max_pages]; context_lens int32 [B] (including the
-    q_len tokens of this step).  Returns (out [B][q_len][Hq][D] float64,
+    q_len tokens of this step).  fp8_q: the scores use the query quantised by
+    quantize_q_groups (decoded code times its group's scale) instead of the
+    fp16 query.  Returns (out [B][q_len][Hq][D] float64,
     flags[, lse [B][q_len][Hq]]).
     """
     keep, args, (B, q_len, Hq, D) = _attn_common(q, k_cache, v_cache, block_tables,
                                                  context_lens, k_scale, v_scale,
-                                                 topk_idx, topk_lens, sm_scale)
+                                                 topk_idx, topk_lens, sm_scale, fp8_q)
     out = np.zeros((B, q_len, Hq, D), dtype=np.float64)
     lse = np.zeros((B, q_len, Hq), dtype=np.float64)
     flags = _load().oracle_attn(*args, _ptr(out), _ptr(lse))
@@ -264,13 +289,13 @@ def attention(q, k_cache, v_cache, block_tables, context_lens, k_scale=1.0, v_sc
 
 def attention_partials(q, k_cache, v_cache, block_tables, context_lens, num_splits,
                        k_scale=1.0, v_scale=1.0, topk_idx=None, topk_lens=None, sm_scale=None,
-                       split_pages=0):
+                       split_pages=0, fp8_q=False):
     """Per-split partials: o [B][Hq][q_len][S][D], m and l [B][Hq][q_len][S].
     split_pages = 0 divides each sequence into S equal parts; > 0 gives every
     split that many pages (4 list entries per page in top-k mode)."""
     keep, args, (B, q_len, Hq, D) = _attn_common(q, k_cache, v_cache, block_tables,
                                                  context_lens, k_scale, v_scale,
-                                                 topk_idx, topk_lens, sm_scale)
+                                                 topk_idx, topk_lens, sm_scale, fp8_q)
     S = int(num_splits)
     o = np.zeros((B, Hq, q_len, S, D), dtype=np.float64)
     m = np.zeros((B, Hq, q_len, S), dtype=np.float64)

@@ -26,7 +26,10 @@
  *     round-to-nearest-even and saturates finite overflow at +-448;
  *   - the calibrated scale is amax / 448 in binary32;
  *   - attention is the plain softmax(q k^T * sm_scale) v over the dequantised
- *     values, in binary64, with the verify window causal inside itself.
+ *     values, in binary64, with the verify window causal inside itself;
+ *   - the FP8 score variant (not on the pages) replaces q in the scores by
+ *     its E4M3 quantisation with one amax / 448 scale per (sequence, kv
+ *     head) group of query rows, quantised like a cache element.
  *
  * Precision: binary64 for attention, binary32 exactly where the method's
  * quantisation is defined in binary32.  Build with -O2 -fno-fast-math
@@ -182,6 +185,48 @@ float oracle_calibrate_scale(const uint16_t *x, int64_t n)
     return (float)amax / 448.0f;
 }
 
+/* Query quantisation of the FP8 tensor-core score variant.  The pages store
+ * only K and V in E4M3 and keep q in fp16; this variant is not on them, and
+ * its reading is the plainest one that puts q into the same format as the
+ * cache.  Per (sequence b, kv head g), the G * q_len query rows that attend
+ * kv head g (heads g*G .. g*G+G-1, contiguous grouping, every row of the
+ * verify window) share one scale:
+ *   amax  = max |q| over those rows and all channels,
+ *   scale = amax / 448 in binary32, or 1 when amax is 0 (an all-zero group),
+ * and each element is quantised like a cache element (binary32 division by
+ * the scale, then RNE to E4M3 with finite overflow saturated).  Writes codes
+ * [B][q_len][Hq][D] and scales [B][Hkv]; returns ORACLE_OK or
+ * ORACLE_BAD_ARG.  The query must be finite. */
+int oracle_quantize_q_groups(const uint16_t *q, int B, int q_len, int Hq, int Hkv, int D,
+                             uint8_t *codes, float *scales)
+{
+    int G, b, g, i, h, d;
+    if (!q || !codes || !scales || B < 0 || q_len < 1 || Hkv < 1 || Hq < 1 || Hq % Hkv != 0 || D < 1)
+        return ORACLE_BAD_ARG;
+    G = Hq / Hkv;
+    for (b = 0; b < B; ++b)
+        for (g = 0; g < Hkv; ++g) {
+            double amax = 0.0;
+            float qs;
+            for (i = 0; i < q_len; ++i)
+                for (h = g * G; h < (g + 1) * G; ++h)
+                    for (d = 0; d < D; ++d) {
+                        double a = fabs(oracle_f16_to_f64(q[(((int64_t)b * q_len + i) * Hq + h) * D + d]));
+                        if (a > amax)
+                            amax = a;
+                    }
+            qs = amax > 0.0 ? (float)amax / 448.0f : 1.0f;
+            scales[(int64_t)b * Hkv + g] = qs;
+            for (i = 0; i < q_len; ++i)
+                for (h = g * G; h < (g + 1) * G; ++h)
+                    for (d = 0; d < D; ++d) {
+                        int64_t idx = (((int64_t)b * q_len + i) * Hq + h) * D + d;
+                        codes[idx] = oracle_quantize(q[idx], qs);
+                    }
+        }
+    return ORACLE_OK;
+}
+
 /* Scale gate ([P2] Changes: require all finite positive per-layer K/V scales
  * and refuse startup when any is missing; [P2] Validation boundary: no
  * generic or unit-scale fallback).  Returns the number of bad entries. */
@@ -285,6 +330,10 @@ typedef struct {
     const int32_t *topk_lens;     /* nullable, [B]; 0 = dense */
     int B, q_len, Hq, Hkv, D, max_pages, max_topk;
     double sm_scale;
+    /* nullable: the query quantised to E4M3 (codes [B][q_len][Hq][D], one
+     * scale per (sequence, kv head) in q_scales [B][Hkv]); NULL = fp16 q */
+    const uint8_t *q_codes;
+    const float *q_scales;
 } oracle_problem;
 
 /* dequantised K or V element j (token position) of sequence b, head g, channel d;
@@ -357,6 +406,8 @@ static int attend_keys(const oracle_problem *pr, int b, int h, int i, const int3
     int g = h / G; /* contiguous grouping of query heads onto kv heads */
     int D = pr->D, k, d, ok, flags = 0;
     const uint16_t *qrow = pr->q + (((int64_t)b * pr->q_len + i) * pr->Hq + h) * D;
+    const uint8_t *qcode = pr->q_codes ? pr->q_codes + (qrow - pr->q) : NULL;
+    double qscale = pr->q_codes ? (double)pr->q_scales[(int64_t)b * pr->Hkv + g] : 0.0;
     double m = -INFINITY, l = 0.0;
     for (d = 0; d < D; ++d)
         out[d] = 0.0;
@@ -366,7 +417,10 @@ static int attend_keys(const oracle_problem *pr, int b, int h, int i, const int3
             double kv = kv_value(pr, 1, b, g, keys[k], d, &ok);
             if (!ok)
                 break;
-            s += oracle_f16_to_f64(qrow[d]) * kv;
+            if (qcode)
+                s += oracle_e4m3_decode(qcode[d]) * qscale * kv;
+            else
+                s += oracle_f16_to_f64(qrow[d]) * kv;
         }
         if (!ok) {
             flags |= ORACLE_BAD_PAGE;
@@ -405,6 +459,8 @@ static int check_problem(const oracle_problem *pr)
     if (pr->B < 0 || pr->q_len < 1 || pr->Hq < 1 || pr->Hkv < 1 || pr->D < 1)
         return 0;
     if (pr->Hq % pr->Hkv != 0 || pr->max_pages < 0)
+        return 0;
+    if (pr->q_codes && !pr->q_scales)
         return 0;
     return 1;
 }
@@ -550,7 +606,7 @@ int oracle_attn(const uint16_t *q, const void *k_cache, const void *v_cache, int
                 const int32_t *block_tables, const int32_t *context_lens, double k_scale,
                 double v_scale, const int32_t *topk_idx, const int32_t *topk_lens, int B,
                 int q_len, int Hq, int Hkv, int D, int max_pages, int max_topk, double sm_scale,
-                double *out, double *lse)
+                const uint8_t *q_codes, const float *q_scales, double *out, double *lse)
 {
     oracle_problem pr;
     pr.q = q;
@@ -572,6 +628,8 @@ int oracle_attn(const uint16_t *q, const void *k_cache, const void *v_cache, int
     pr.max_pages = max_pages;
     pr.max_topk = topk_idx ? max_topk : 0;
     pr.sm_scale = sm_scale;
+    pr.q_codes = q_codes;
+    pr.q_scales = q_codes ? q_scales : NULL;
     return oracle_attention(&pr, out, lse);
 }
 
@@ -579,8 +637,9 @@ int oracle_attn_partials(const uint16_t *q, const void *k_cache, const void *v_c
                          int64_t P, const int32_t *block_tables, const int32_t *context_lens,
                          double k_scale, double v_scale, const int32_t *topk_idx,
                          const int32_t *topk_lens, int B, int q_len, int Hq, int Hkv, int D,
-                         int max_pages, int max_topk, double sm_scale, int S, int split_pages,
-                         double *o, double *m, double *l)
+                         int max_pages, int max_topk, double sm_scale, const uint8_t *q_codes,
+                         const float *q_scales, int S, int split_pages, double *o, double *m,
+                         double *l)
 {
     oracle_problem pr;
     pr.q = q;
@@ -602,5 +661,7 @@ int oracle_attn_partials(const uint16_t *q, const void *k_cache, const void *v_c
     pr.max_pages = max_pages;
     pr.max_topk = topk_idx ? max_topk : 0;
     pr.sm_scale = sm_scale;
+    pr.q_codes = q_codes;
+    pr.q_scales = q_codes ? q_scales : NULL;
     return oracle_partials(&pr, S, split_pages, o, m, l);
 }

@@ -14,6 +14,7 @@ import torch
 
 import oracle
 from tests import _problems as P
+from tests import test_oracle_fp8q as F8
 from tests.test_oracle_e4m3 import _F16_FINITE, _torch_decode, _torch_quantize, _same, ALL_CODES
 
 MUTANTS = {
@@ -45,6 +46,17 @@ MUTANTS = {
                        "            if (d) s += oracle_f16_to_f64(qrow[d]) * kv;"),
     # combine ignores the split sums
     "combine_no_l": ("w = l[r * S + s] * exp(m[r * S + s] - M);", "w = exp(m[r * S + s] - M);"),
+    # FP8 score variant: the query scale forgets the 448
+    "qscale_448": ("qs = amax > 0.0 ? (float)amax / 448.0f : 1.0f;", "qs = amax > 0.0 ? (float)amax / 256.0f : 1.0f;"),
+    # FP8 score variant: the group maximum taken over the first window row only
+    "qgroup_scope": ("for (i = 0; i < q_len; ++i)\n                for (h = g * G; h < (g + 1) * G; ++h)\n"
+                     "                    for (d = 0; d < D; ++d) {\n                        double a",
+                     "for (i = 0; i < 1; ++i)\n                for (h = g * G; h < (g + 1) * G; ++h)\n"
+                     "                    for (d = 0; d < D; ++d) {\n                        double a"),
+    # FP8 score variant: the decoded query code used without its scale
+    "qscale_dropped": ("s += oracle_e4m3_decode(qcode[d]) * qscale * kv;", "s += oracle_e4m3_decode(qcode[d]) * kv;"),
+    # FP8 score variant: every group read with the scale of kv head 0
+    "qscale_group": ("(double)pr->q_scales[(int64_t)b * pr->Hkv + g]", "(double)pr->q_scales[(int64_t)b * pr->Hkv]"),
     # V scale applied to K
     "swapped_scales": ("return oracle_e4m3_decode(c[idx]) * (is_k ? pr->k_scale : pr->v_scale);",
                        "return oracle_e4m3_decode(c[idx]) * (is_k ? pr->v_scale : pr->k_scale);"),
@@ -83,6 +95,17 @@ def _pins_pass() -> bool:
             return False
         o, m, l, _ = oracle.attention_partials(pr.q, kc, vc, bt, lens, 3, ks, vs)
         if not np.allclose(oracle.combine(o, m, l).transpose(0, 2, 1, 3), out, rtol=1e-10, atol=1e-12):
+            return False
+        # FP8 score variant: the query codes against the library cast, and a query
+        # already on the scaled grid reproduced exactly
+        codes, scales = oracle.quantize_q_groups(pr.q, pr.w.num_kv_heads)
+        ref_codes, ref_scales = F8._library_route(pr.q, pr.w.num_kv_heads)
+        if not (np.array_equal(codes, ref_codes) and np.array_equal(scales, ref_scales)):
+            return False
+        qg, _, _ = F8._grid_query(pr, np.random.default_rng(11))
+        a, _ = oracle.attention(qg, kc, vc, bt, lens, ks, vs)
+        b, _ = oracle.attention(qg, kc, vc, bt, lens, ks, vs, fp8_q=True)
+        if not np.array_equal(a, b):
             return False
     return True
 
