@@ -281,6 +281,7 @@ class Arm:
         self.launches = 3   # kernels of one step: append, attention, combine
         self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
         self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
+        self.fp8_qk = False    # tcgen05 kernel: fp16 scores (default) or the FP8 score variant
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
         torch.cuda.synchronize(dev)
 
@@ -299,7 +300,8 @@ class Arm:
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
                                                err_flag=self.err, split_pages=self.w.split_pages,
-                                               bitcast_decode=self.bitcast, mma_sync=self.mma_sync)
+                                               bitcast_decode=self.bitcast, mma_sync=self.mma_sync,
+                                               fp8_qk=self.fp8_qk)
         else:
             kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, self.topk_idx,
                                                self.topk_lens, num_splits=self.S, err_flag=self.err,
@@ -893,11 +895,14 @@ def main():
     arm.bitcast = True                                  # context: the pages' bitcast decoder
     bitcast_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
     arm.bitcast = False
-    mma_sync_ms = None
+    mma_sync_ms = fp8_qk_ms = None
     if arm.uses_tc:                                     # context: the same shape on the mma.sync kernel
         arm.mma_sync = True
         mma_sync_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
         arm.mma_sync = False
+        arm.fp8_qk = True                               # context: the FP8 score variant (other numerics)
+        fp8_qk_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
+        arm.fp8_qk = False
 
     arm.graphs = None
     e2e_ms, h2d, d2h = arm.time_e2e(max(5, args.steps // 2), args.warmup)
@@ -958,7 +963,8 @@ def main():
                          "bitcast_decoder_ms": bitcast_ms,
                          "bitcast_decoder_kernel": "attn_split_kernel",
                          "bitcast_decoder_gbs": arm.bytes["attention_kernel"] / (bitcast_ms * 1e-3) / 1e9,
-                         "mma_sync_kernel_ms": mma_sync_ms},
+                         "mma_sync_kernel_ms": mma_sync_ms,
+                         "fp8_scores_kernel_ms": fp8_qk_ms},
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -56,7 +56,8 @@ static int check_params(const kvq_attn_params *p)
     if (p->batch < 0 || p->q_len < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
         p->num_splits < 0 || p->max_pages_per_seq < 1 || p->max_topk < 0 || p->split_pages < 0)
         return KVQ_ERR_INVALID_ARG;
-    if (p->flags & ~int32_t(KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC)) return KVQ_ERR_INVALID_ARG;
+    if (p->flags & ~int32_t(KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC | KVQ_ATTN_FP8_QK))
+        return KVQ_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
     if (!std::isfinite(p->sm_scale) || p->sm_scale < 0.0f) return KVQ_ERR_INVALID_ARG;
     if (p->head_dim != 64 && p->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
@@ -121,6 +122,11 @@ static int run_attention(const AttnCall &c, bool with_combine)
     if ((c.topk_idx == nullptr) != (c.topk_lens == nullptr)) return KVQ_ERR_INVALID_ARG;
     if (c.topk_idx && p.max_topk < 1) return KVQ_ERR_INVALID_ARG;
     if (c.e4m3 && (!good_scale(c.k_scale) || !good_scale(c.v_scale))) return KVQ_ERR_BAD_SCALE;
+    // the FP8 scores exist on the tcgen05 kernel over E4M3 pools only
+    if ((p.flags & KVQ_ATTN_FP8_QK) &&
+        (!c.e4m3 || (p.flags & (KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC)) ||
+         !tc_supported(p.head_dim, (p.num_q_heads / p.num_kv_heads) * p.q_len)))
+        return KVQ_ERR_UNSUPPORTED;
     if (!aligned16(c.q) || !aligned16(c.k_cache) || !aligned16(c.v_cache) ||
         (c.out && !aligned16(c.out)) || !aligned16(c.workspace))
         return KVQ_ERR_ALIGNMENT;
@@ -165,6 +171,7 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.out_scale = float(vfold);
     a.bitcast_decode = (p.flags & KVQ_ATTN_BITCAST_DECODE) != 0;
     a.mma_sync = (p.flags & KVQ_ATTN_MMA_SYNC) != 0;
+    a.fp8_qk = (p.flags & KVQ_ATTN_FP8_QK) != 0;
 
     cudaStream_t stream = static_cast<cudaStream_t>(c.stream);
     if (launch_attention(c.e4m3, p.head_dim, a, stream) != cudaSuccess) return KVQ_ERR_CUDA;

@@ -32,8 +32,17 @@
 //  * Every wait is bounded (about 2 s); on expiry the CTA reports
 //    KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor memory
 //    and exits without writing.
+//
+// FP8 score variant (F8, E4M3 pools only; not on the pages): the workers
+// quantise the CTA's query rows to E4M3 with one scale amax / 448 over them
+// (the rows of one (sequence, kv head) group, so every split of the group
+// takes the same codes), K rows go to tensor memory as their E4M3 bytes
+// without conversion, and S^T = K Q^T runs as tcgen05.mma kind::f8f6f4
+// (K = 32 per instruction); the query scale joins the hoisted score scale.
+// P V is unchanged (fp16).
 #include <cstdint>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "kvq_attn_kernel.cuh"
@@ -68,7 +77,9 @@ struct TcLayout {
     static constexpr int kLsum = kPriv + 4 * 4 * NR * 4;     // [4][NR] float: per-worker row sums
     static constexpr int kMend = kLsum + 4 * NR * 4;         // [4][NR] float: per-worker final row maxima
     static constexpr int kFlag = kMend + 4 * NR * 4;         // [2][4] int: per-worker "left the band" flags
-    static constexpr int kBar = kFlag + 2 * 4 * 4;           // 8 mbarriers
+    static constexpr int kQmax = kFlag + 2 * 4 * 4;          // [2][4] float: per-worker max |q|, score
+                                                             //   scale with the query's (FP8 scores)
+    static constexpr int kBar = kQmax + 2 * 4 * 4;           // 8 mbarriers
     static constexpr int kTmemSlot = kBar + 8 * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     // tensor-memory columns: K tile (64: 128 fp16 per lane), S^T (NR), O^T (NR), the row
@@ -76,6 +87,48 @@ struct TcLayout {
     static constexpr int kColK = 0, kColS = 64, kColO = 64 + NR, kColL = 64 + 2 * NR, kColOnes = 64 + 3 * NR;
     static constexpr int kCols = (128 + 3 * NR) <= 128 ? 128 : ((128 + 3 * NR) <= 256 ? 256 : 512);
 };
+
+// Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0 in
+// bits 7-9 and 10-12), fp32 accumulator, M x N tile, both operands K-major.
+__device__ __forceinline__ uint32_t umma_idesc_e4m3(int m, int n)
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// D (tensor memory) (+)= A (tensor memory, 4 E4M3 per 32-bit column) x B (shared memory, E4M3)
+__device__ __forceinline__ void umma_tmem_a_e4m3(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 bool accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+                 : "memory");
+}
+
+// four fp16 (two 32-bit words) -> four E4M3 bytes, element 0 in the lowest
+// byte: binary32 division by the scale (round to nearest even), then the
+// hardware satfinite E4M3 conversion (round to nearest even, finite overflow
+// to +-448) -- the cache quantiser's two roundings
+__device__ __forceinline__ uint32_t quantize_q4(uint32_t h01, uint32_t h23, float scale)
+{
+    const float2 fa = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+    const float2 fb = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(fa.x, scale), __fdiv_rn(fa.y, scale)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(fb.x, scale), __fdiv_rn(fb.y, scale)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float absmax8(uint4 v)
+{
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&v.z));
+    const float2 d = __half22float2(*reinterpret_cast<const __half2 *>(&v.w));
+    return fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y))),
+                 fmaxf(fmaxf(fabsf(c.x), fabsf(c.y)), fmaxf(fabsf(d.x), fabsf(d.y))));
+}
 
 // Lane r of the warp ends with the maximum (or sum) over the warp's 32 lanes
 // of value v[r] (r < 32): a butterfly that halves the set each step.
@@ -99,9 +152,10 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
 // Two CTAs per SM when NR <= 32: the bound is stated for 256 threads so that
 // registers stay at 128 per thread -- with 7 warps per CTA, two CTAs put four
 // warps on some SM sub-partitions, whose register files hold 4 x 128 x 32.
-template <bool E4M3, int NR>
+template <bool E4M3, int NR, bool F8>
 __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const AttnArgs a)
 {
+    static_assert(E4M3 || !F8, "FP8 scores need E4M3 pools");
     constexpr int D = kTcD, PPS = tc_pps<E4M3>();
     using G = TcGeometry<E4M3>;
     constexpr int SPT = tc_spt<E4M3>();                       // staging stages per tile: 2 or 4
@@ -183,17 +237,25 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         if (lane == 0) {
             const uint32_t q_addr = smem_u32(smem + T::kQ), v_addr = smem_u32(smem + T::kV),
                            p_addr = smem_u32(smem + T::kP);
-            const uint32_t id_qk = umma_idesc_f16(kTcTile, NR, false, false);
+            const uint32_t id_qk = F8 ? umma_idesc_e4m3(kTcTile, NR) : umma_idesc_f16(kTcTile, NR, false, false);
             const uint32_t id_pv = umma_idesc_f16(kTcTile, NR, true, true);
             const uint32_t id_l = umma_idesc_f16(kTcTile, NR, false, true);
             for (int t = 0; t < ntiles; ++t) {
                 if (!mbar_wait_bounded(b_k, t & 1, abort_flag, a.err_flag)) break;
                 tc_fence_after();
-                // S^T[tok][row] = sum_d K[tok][d] Q[row][d]: A = K tile (tensor memory), B = Q (K-major)
+                // S^T[tok][row] = sum_d K[tok][d] Q[row][d]: A = K tile (tensor memory), B = Q (K-major);
+                // 8 tensor-memory columns and two 128-byte core-matrix columns of Q per instruction
+                if constexpr (F8) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    umma_tmem_a(tmem + T::kColS, tmem + T::kColK + ks * 8,
-                                umma_desc(q_addr + ks * 256, 128, (D / 8) * 128), id_qk, ks > 0);
+                    for (int ks = 0; ks < D / 32; ++ks)
+                        umma_tmem_a_e4m3(tmem + T::kColS, tmem + T::kColK + ks * 8,
+                                         umma_desc(q_addr + ks * 256, 128, (D / 16) * 128), id_qk, ks > 0);
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        umma_tmem_a(tmem + T::kColS, tmem + T::kColK + ks * 8,
+                                    umma_desc(q_addr + ks * 256, 128, (D / 8) * 128), id_qk, ks > 0);
+                }
                 umma_commit(b_s);
                 if (!mbar_wait_bounded(b_p, t & 1, abort_flag, a.err_flag)) break;
                 tc_fence_after();
@@ -219,7 +281,6 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         const int q = warp;                          // tensor-memory lane quadrant
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const int tt = 32 * q + lane;                // token of the tile (S^T lane), channel of O^T
-        const float qk = a.qk_scale_log2;
         const int win0 = L - a.q_len;                // row i sees positions <= win0 + i
         float *wmax = reinterpret_cast<float *>(smem + T::kWmax);
         float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 4 * NR;   // reference, corr, coef, in use
@@ -228,18 +289,68 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         // last tile's exchange in wmax while another has reached the epilogue
         float *mend = reinterpret_cast<float *>(smem + T::kMend);
 
-        // Q rows (padding rows zero) into the K-major Q tile: element (r, d) at
-        // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2; the 8 lanes of a
-        // quarter warp take 8 rows of one 16-byte column, one 128-byte line
-        for (int idx = tt; idx < NR * (D / 8); idx += 32 * kTcWorkers) {
-            const int r = (idx & 7) + 8 * (idx / (8 * (D / 8))), c = (idx / 8) % (D / 8);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < a.rows) {
-                const int i = r / a.group, h = g * a.group + r % a.group;
-                v = *reinterpret_cast<const uint4 *>(static_cast<const __half *>(a.q) +
-                                                     (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D + 8 * c);
+        // the score scale: hoisted in the arguments, or (FP8 scores) with the
+        // query's scale in shared memory, read once per tile rather than held
+        // in a register across the loop
+        float *qk_f8 = reinterpret_cast<float *>(smem + T::kQmax) + 4 + q;
+        if constexpr (F8) {
+            // Q rows (padding rows zero) quantised into the K-major E4M3 Q tile:
+            // element (r, d) at (r/8) * 1024 + (d/16) * 128 + (r%8) * 16 + d%16;
+            // thread item = 16 channels of one row, the 8 lanes of a quarter
+            // warp on 8 rows of one 16-byte column
+            constexpr int QI = NR * (D / 16) / (32 * kTcWorkers);   // items per thread
+            static_assert(QI * 32 * kTcWorkers == NR * (D / 16), "Q items must divide evenly");
+            uint4 qv[QI][2];
+            float mx = 0.f;
+#pragma unroll
+            for (int u = 0; u < QI; ++u) {
+                const int idx = tt + u * 32 * kTcWorkers;
+                const int r = (idx & 7) + 8 * (idx / (8 * (D / 16))), c = (idx / 8) % (D / 16);
+                qv[u][0] = qv[u][1] = make_uint4(0u, 0u, 0u, 0u);
+                if (r < a.rows) {
+                    const int i = r / a.group, h = g * a.group + r % a.group;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(
+                        static_cast<const __half *>(a.q) + (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D +
+                        16 * c);
+                    qv[u][0] = src[0];
+                    qv[u][1] = src[1];
+                }
+                mx = fmaxf(mx, fmaxf(absmax8(qv[u][0]), absmax8(qv[u][1])));
             }
-            *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
+            // the group's max |q| over the four workers
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+            float *qmax = reinterpret_cast<float *>(smem + T::kQmax);
+            if (lane == 0) qmax[q] = mx;
+            named_bar_sync(1, 32 * kTcWorkers);
+            const float amax = fmaxf(fmaxf(qmax[0], qmax[1]), fmaxf(qmax[2], qmax[3]));
+            const float q_scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+            if (lane == 0) *qk_f8 = a.qk_scale_log2 * q_scale;
+#pragma unroll
+            for (int u = 0; u < QI; ++u) {
+                const int idx = tt + u * 32 * kTcWorkers;
+                const int r = (idx & 7) + 8 * (idx / (8 * (D / 16))), c = (idx / 8) % (D / 16);
+                uint4 v;
+                v.x = quantize_q4(qv[u][0].x, qv[u][0].y, q_scale);
+                v.y = quantize_q4(qv[u][0].z, qv[u][0].w, q_scale);
+                v.z = quantize_q4(qv[u][1].x, qv[u][1].y, q_scale);
+                v.w = quantize_q4(qv[u][1].z, qv[u][1].w, q_scale);
+                *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 1024 + c * 128 + (r & 7) * 16) = v;
+            }
+        } else {
+            // Q rows (padding rows zero) into the K-major Q tile: element (r, d) at
+            // (r/8) * 2048 + (d/8) * 128 + (r%8) * 16 + (d%8) * 2; the 8 lanes of a
+            // quarter warp take 8 rows of one 16-byte column, one 128-byte line
+            for (int idx = tt; idx < NR * (D / 8); idx += 32 * kTcWorkers) {
+                const int r = (idx & 7) + 8 * (idx / (8 * (D / 8))), c = (idx / 8) % (D / 8);
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (r < a.rows) {
+                    const int i = r / a.group, h = g * a.group + r % a.group;
+                    v = *reinterpret_cast<const uint4 *>(static_cast<const __half *>(a.q) +
+                                                         (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D + 8 * c);
+                }
+                *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
+            }
         }
         fence_async_smem();   // the Q tile is read by the tensor core (async proxy)
 
@@ -292,23 +403,11 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             uint4 kx[kKV];
 #pragma unroll
             for (int u = 0; u < kKV; ++u) kx[u] = *reinterpret_cast<const uint4 *>(krow + 16 * u);
+            if constexpr (F8) {
+                // the E4M3 bytes themselves: channels 4c..4c+3 in column c, lowest byte first
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {            // 16 columns = 32 channels per store
-                uint32_t w[16];
-                if (E4M3) {
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const uint4 x = kx[2 * h + u];
-                        w[8 * u + 0] = cvt_lo(x.x);
-                        w[8 * u + 1] = cvt_hi(x.x);
-                        w[8 * u + 2] = cvt_lo(x.y);
-                        w[8 * u + 3] = cvt_hi(x.y);
-                        w[8 * u + 4] = cvt_lo(x.z);
-                        w[8 * u + 5] = cvt_hi(x.z);
-                        w[8 * u + 6] = cvt_lo(x.w);
-                        w[8 * u + 7] = cvt_hi(x.w);
-                    }
-                } else {
+                for (int h = 0; h < 2; ++h) {        // 16 columns = 64 channels per store
+                    uint32_t w[16];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const uint4 x = kx[4 * h + u];
@@ -317,8 +416,37 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                         w[4 * u + 2] = x.z;
                         w[4 * u + 3] = x.w;
                     }
+                    tmem_st16(tmem + lane_base + T::kColK + 16 * h, w);
                 }
-                tmem_st16(tmem + lane_base + T::kColK + 16 * h, w);
+            } else {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {            // 16 columns = 32 channels per store
+                    uint32_t w[16];
+                    if (E4M3) {
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const uint4 x = kx[2 * h + u];
+                            w[8 * u + 0] = cvt_lo(x.x);
+                            w[8 * u + 1] = cvt_hi(x.x);
+                            w[8 * u + 2] = cvt_lo(x.y);
+                            w[8 * u + 3] = cvt_hi(x.y);
+                            w[8 * u + 4] = cvt_lo(x.z);
+                            w[8 * u + 5] = cvt_hi(x.z);
+                            w[8 * u + 6] = cvt_lo(x.w);
+                            w[8 * u + 7] = cvt_hi(x.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const uint4 x = kx[4 * h + u];
+                            w[4 * u + 0] = x.x;
+                            w[4 * u + 1] = x.y;
+                            w[4 * u + 2] = x.z;
+                            w[4 * u + 3] = x.w;
+                        }
+                    }
+                    tmem_st16(tmem + lane_base + T::kColK + 16 * h, w);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
@@ -369,6 +497,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 for (int e = 0; e < 16; ++e) x[c + e] = __uint_as_float(r16[e]);
             }
             // scores in the log2 domain; row r (window row r / G) sees positions <= win0 + r / G
+            const float qk = F8 ? *reinterpret_cast<volatile float *>(qk_f8) : a.qk_scale_log2;
             const int rmin = pos < 0 ? NR : (pos > win0 ? a.group * (pos - win0) : 0);
             if (rmin == 0 && a.rows == NR) {
 #pragma unroll
@@ -563,7 +692,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     if (warp == kTcMmaWarp) tmem_dealloc(tmem, T::kCols);
 }
 
-template <bool E4M3, int NR>
+template <bool E4M3, int NR, bool F8 = false>
 static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
 {
     constexpr int bytes = TcLayout<E4M3, NR>::kBytes;
@@ -572,15 +701,15 @@ static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR, F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-    return launch_pdl(attn_tc_kernel<E4M3, NR>, grid, dim3(kTcThreads), bytes, stream, a);
+    return launch_pdl(attn_tc_kernel<E4M3, NR, F8>, grid, dim3(kTcThreads), bytes, stream, a);
 }
 
 bool tc_supported(int head_dim, int rows) { return head_dim == kTcD && rows > 8 && rows <= 64; }
@@ -588,6 +717,11 @@ bool tc_supported(int head_dim, int rows) { return head_dim == kTcD && rows > 8 
 cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t stream)
 {
     if (a.batch == 0) return cudaSuccess;
+    if (e4m3 && a.fp8_qk) {
+        if (a.rows <= 16) return launch_tc_one<true, 16, true>(a, stream);
+        if (a.rows <= 32) return launch_tc_one<true, 32, true>(a, stream);
+        return launch_tc_one<true, 64, true>(a, stream);
+    }
     if (e4m3) {
         if (a.rows <= 16) return launch_tc_one<true, 16>(a, stream);
         if (a.rows <= 32) return launch_tc_one<true, 32>(a, stream);

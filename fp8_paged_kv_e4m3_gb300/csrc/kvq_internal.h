@@ -30,6 +30,7 @@ struct AttnArgs {
     float out_scale;             // hoisted: v_scale for E4M3, 1 for fp16
     bool bitcast_decode;         // E4M3: the bitcast decoder instead of the hardware conversion
     bool mma_sync;               // keep many-row tiles on the mma.sync kernel
+    bool fp8_qk;                 // E4M3 scores on the tcgen05 kernel (query quantised per CTA)
 };
 
 // Arguments of one chunked-prefill attention call (device pointers).

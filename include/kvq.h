@@ -196,6 +196,21 @@ typedef struct {
  * partials up to rounding.  The bitcast decoder runs on the mma.sync kernel. */
 #define KVQ_ATTN_MMA_SYNC 2
 
+/* FP8 scores (E4M3 pools, the tcgen05 kernel's shapes: head_dim 128 and
+ * 8 < G * q_len <= 64; other calls with this bit, or with it together with
+ * KVQ_ATTN_BITCAST_DECODE or KVQ_ATTN_MMA_SYNC, return KVQ_ERR_UNSUPPORTED
+ * before any launch).  Not on the pages, which keep q in fp16: the query
+ * rows of each (sequence, kv head) are quantised to E4M3 with one scale
+ * amax / 448 over those rows (1 for an all-zero group; binary32 division,
+ * round to nearest even, finite overflow saturated, like a cache element),
+ * and q k^T is computed on E4M3 x E4M3 tensor-core instructions with the
+ * query scale folded into the hoisted score scale.  P V, the workspace and
+ * the combine are unchanged.  The result is the attention of the quantised
+ * query, which is not the fp16-query attention: where q and k share large
+ * outlier channels the scores are large and the query's rounding moves
+ * them visibly. */
+#define KVQ_ATTN_FP8_QK 4
+
 /* The split count a call with these parameters uses: p->num_splits if > 0;
  * else, with split_pages > 0, the fewest splits that cover max_pages_per_seq
  * pages and max_topk list entries; else a count chosen from the shape and

@@ -90,7 +90,7 @@ def test_workspace_size_matches_layout(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 96, -4), ("q_len", 5, -4), ("q_len", 0, -1), ("num_kv_heads", 3, -1),
     ("num_splits", -1, -1), ("max_pages_per_seq", 0, -1), ("num_q_heads", 136, -4),
-    ("flags", 4, -1), ("flags", -1, -1),
+    ("flags", 8, -1), ("flags", -1, -1),
 ])
 def test_bad_params_are_refused(lib, field, value, status):
     p = _params(**{field: value})
@@ -135,6 +135,22 @@ def test_attention_host_checks_fail_closed(lib):
     assert _attn(lib, p, q=ctypes.c_void_p(0x10008)) == -6
     assert _attn(lib, p, topk=FAKE) == -1          # top-k indices without lengths
     assert _attn(lib, _params(head_dim=80)) == -4
+
+
+def _attn_fp16(lib, p):
+    return lib.paged_decode_attn_fp16(FAKE, FAKE, FAKE, 40, FAKE, FAKE, None, None, FAKE, 1 << 20, FAKE,
+                                      ctypes.byref(p), None, None)
+
+
+def test_fp8_scores_outside_the_tcgen05_shapes_are_unsupported(lib):
+    fp8 = kvq.ATTN_FP8_QK
+    verify = dict(head_dim=128, q_len=4, num_q_heads=8, num_kv_heads=2)   # 16 rows per kv head
+    assert _attn(lib, _params(flags=fp8)) == -4                            # head_dim 64
+    assert _attn(lib, _params(flags=fp8, head_dim=128)) == -4              # 4 rows: the mma.sync kernel's
+    assert _attn(lib, _params(flags=fp8 | kvq.ATTN_BITCAST_DECODE, **verify)) == -4
+    assert _attn(lib, _params(flags=fp8 | kvq.ATTN_MMA_SYNC, **verify)) == -4
+    assert _attn_fp16(lib, _params(flags=fp8, **verify)) == -4           # fp16 pools
+    assert _attn(lib, _params(flags=fp8, **verify), k_scale=0.0) == -2    # the scale gate comes first
 
 
 def test_append_host_checks_fail_closed(lib):
