@@ -278,10 +278,16 @@ __device__ __forceinline__ SeqPick lpt_pick(const AttnArgs &a, int z, uint8_t *s
 // stage's ring slot to be released, records the token positions (K warp),
 // and issues one 1-D bulk copy per page (dense) or per listed token row
 // (top-k), completing on the slot's full mbarrier.  Returns the stages issued.
+// clean_items >= 0: the caller has not yet waited for the preceding kernel,
+// and the logical pages below clean_items (positions below L - q_len, which
+// this step's append does not write) may be copied before that wait; the
+// wait comes before the first stage that reaches past them.  -1: the caller
+// has waited.
 template <class G, int PPS>
 __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRange &r, int nst, int b, int g,
                                               int lane, bool is_v, int bt_spec, uint32_t ring, uint32_t bar0,
-                                              int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad)
+                                              int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad,
+                                              int clean_items = -1)
 {
     const int item0 = r.item0, item1 = r.item1, L = r.L, spec0 = r.spec0;
     const bool topk = r.topk;
@@ -299,8 +305,13 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
             int bt_nxt = load_bt(item0 + 32);
             const int p = lane % PPS;                      // page of the stage this lane copies
             const bool copier = lane < PPS;
+            bool waited = clean_items < 0;
             for (int st = 0; st < nst; ++st) {
                 const int slot = st % G::kStages;
+                if (!waited && item0 + (st + 1) * PPS > clean_items) {
+                    grid_dependency_wait();
+                    waited = true;
+                }
                 if (st >= G::kStages &&
                     !mbar_wait_bounded(bar0 + 8 * (G::kStages + slot), ((st / G::kStages) + 1) & 1,
                                        abort_flag, a.err_flag))
@@ -434,7 +445,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         *stage_bad = 0;
         fence_mbar_init();
     }
-    grid_dependency_wait();   // inputs may come from the previous kernel (e.g. the append)
+    __syncthreads();
+    // Inputs may come from the preceding kernel (e.g. the append).  Without a
+    // top-k list, only q and the pages holding this step's positions (L -
+    // q_len and later) can: block tables, context lengths and the earlier
+    // pages are read before waiting for it (the producers start copying at
+    // once; the consumers wait before reading q).  With a top-k list, whose
+    // lists a preceding kernel may write, or with strict ordering, everything
+    // waits here.
+    const bool early = a.early_pages && a.topk_idx == nullptr;
+    if (!early) grid_dependency_wait();
     launch_dependents();      // the combine may start launching; it waits for our completion
 
     // ---- work of this CTA --------------------------------------------------
@@ -458,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         if (len_ok && pick.topk_len > a.max_topk)
             report(a.err_flag, KVQ_DEV_BAD_TOPK);
     }
-    __syncthreads();
 
     float o[NT][G::kPVTiles][4];
     float m_run[NT][2], l_run[NT][2];
@@ -479,8 +498,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         // ================= producers: the first moves K, the second V =================
         const bool is_v = warp == kConsumerWarps + 1;
         issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos, abort_flag,
-                                        stage_bad);
+                                        stage_bad, early ? max(L - a.q_len, 0) / 4 : -1);
     } else {
+        if (early) grid_dependency_wait();
         // ================= consumers =================
         // Q as mma B fragments, one set per 8-row n-tile; k-step ks of this
         // lane covers channels 16ks + 4t .. +3 (E4M3: the pairs the hardware

@@ -31,6 +31,8 @@ struct AttnArgs {
     bool bitcast_decode;         // E4M3: the bitcast decoder instead of the hardware conversion
     bool mma_sync;               // keep many-row tiles on the mma.sync kernel
     bool fp8_qk;                 // E4M3 scores on the tcgen05 kernel (query quantised per CTA)
+    bool early_pages;            // split kernel, no top-k list: block tables, lengths and pages of
+                                 // positions < L - q_len may be read before the dependency wait
 };
 
 // Arguments of one chunked-prefill attention call (device pointers).

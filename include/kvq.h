@@ -18,6 +18,18 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every GPU call is asynchronous and stream-ordered; none
  *    synchronises the host, so the calls can be captured in a CUDA graph.
+ *  - The kernels use programmatic dependent launch: a call's kernel may
+ *    start while the preceding kernel in the stream still runs, when that
+ *    kernel allows it (griddepcontrol.launch_dependents; the library's own
+ *    kernels do), and waits for it before reading what it may write.  One
+ *    relaxation, on the decode attention calls without a top-k list (unless
+ *    KVQ_ATTN_STRICT_ORDER is set): block tables, context lengths and the
+ *    cache pages that hold only positions below L - q_len may be read
+ *    before that wait.  The append of the step writes only positions
+ *    L - q_len and later, so append then attention is safe; a preceding
+ *    kernel of the caller's that allows early launch must not write those
+ *    inputs, or the call must set KVQ_ATTN_STRICT_ORDER.  Kernels that do
+ *    not allow early launch, and copies, order fully as usual.
  *  - Return value: KVQ_OK, or a negative kvq_status.  Errors that the host
  *    can see (bad sizes, bad scales, misaligned pointers, a short workspace)
  *    are returned BEFORE anything is launched: the call fails closed and
@@ -210,6 +222,13 @@ typedef struct {
  * outlier channels the scores are large and the query's rounding moves
  * them visibly. */
 #define KVQ_ATTN_FP8_QK 4
+
+/* Strict ordering: the attention kernel reads no input before the preceding
+ * kernel in the stream has completed (see the conventions at the top).
+ * Without it, decode attention without a top-k list starts copying the
+ * cache pages of positions below L - q_len while the preceding kernel (for
+ * example this step's append) finishes. */
+#define KVQ_ATTN_STRICT_ORDER 8
 
 /* The split count a call with these parameters uses: p->num_splits if > 0;
  * else, with split_pages > 0, the fewest splits that cover max_pages_per_seq
