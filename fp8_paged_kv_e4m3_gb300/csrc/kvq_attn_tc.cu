@@ -80,7 +80,8 @@ struct TcLayout {
     static constexpr int kQmax = kFlag + 2 * 4 * 4;          // [2][4] float: per-worker max |q|, score
                                                              //   scale with the query's (FP8 scores)
     static constexpr int kBar = kQmax + 2 * 4 * 4;           // 8 mbarriers
-    static constexpr int kTmemSlot = kBar + 8 * 8;
+    static constexpr int kBarV = kBar + 8 * 8;               // V staging: [full][kStages], [empty][kStages]
+    static constexpr int kTmemSlot = kBarV + 2 * G::kStages * 8;
     static constexpr int kBytes = kTmemSlot + 16;
     // tensor-memory columns: K tile (64: 128 fp16 per lane), S^T (NR), O^T (NR), the row
     // sums L^T (NR, every lane the same: a ones tile times P^T), the ones tile (64)
@@ -169,7 +170,11 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t ring = smem_u32(smem);
     int32_t *tokpos = reinterpret_cast<int32_t *>(smem + G::kTokPosOff);
+    // staging barriers, one set per producer, so that a slot's K half refills as
+    // soon as the workers hold its rows in tensor memory, before its V half is
+    // converted: bar0 for K (the ring's own barriers), barv for V
     const uint32_t bar0 = smem_u32(smem + G::kBarOff);
+    const uint32_t barv = smem_u32(smem + T::kBarV);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + G::kAbortOff);
     volatile int *stage_bad = abort_flag + 1;
     const uint32_t tb = smem_u32(smem + T::kBar);
@@ -179,8 +184,10 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < G::kStages; ++k) {
-            mbar_init(bar0 + 8 * k, kProducerWarps);
-            mbar_init(bar0 + 8 * (G::kStages + k), WPS);   // released by the workers it feeds
+            mbar_init(bar0 + 8 * k, 1);                     // K copies landed
+            mbar_init(bar0 + 8 * (G::kStages + k), WPS);   // K rows taken by the workers it feeds
+            mbar_init(barv + 8 * k, 1);                     // V copies landed
+            mbar_init(barv + 8 * (G::kStages + k), WPS);   // V rows taken
         }
         mbar_init(b_k, kTcWorkers);
         mbar_init(b_s, 1);
@@ -230,8 +237,9 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 
     if (warp >= kConsumerWarps && warp < kTcMmaWarp) {
         // ================= producers =================
-        issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, warp == kConsumerWarps + 1, bt_spec, ring,
-                                        bar0, tokpos, abort_flag, stage_bad);
+        const bool is_v = warp == kConsumerWarps + 1;
+        issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, is_v ? barv : bar0, tokpos,
+                                        abort_flag, stage_bad);
     } else if (warp == kTcMmaWarp) {
         // ================= MMA issue (one thread) =================
         if (lane == 0) {
@@ -452,9 +460,15 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_k);           // S^T of this tile may start
+            if (have && lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));   // K half of the slot free
             // ---- V row -> fp16 V^T tile (MN-major): (ch, tok) at (tok/8)*2048 + (ch/8)*128 + (tok%8)*16;
             // V^T and P^T are reused: the previous tile's PV must be complete ----
             if (t > 0 && !__all_sync(kFull, mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag))) {
+                ok = false;
+                break;
+            }
+            if (have && !__all_sync(kFull, mbar_wait_bounded(barv + 8 * slot, (st / G::kStages) & 1, abort_flag,
+                                                             a.err_flag))) {
                 ok = false;
                 break;
             }
@@ -482,7 +496,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 }
             }
             __syncwarp();
-            if (have && lane == 0) mbar_arrive(bar0 + 8 * (G::kStages + slot));   // staging slot consumed
+            if (have && lane == 0) mbar_arrive(barv + 8 * (G::kStages + slot));   // V half of the slot free
 
             // ---- S^T of this warp's 32 tokens: one column per query row ----
             if (!__all_sync(kFull, mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag))) { ok = false; break; }
@@ -683,8 +697,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     if (*abort_flag && warp >= kConsumerWarps && warp < kTcMmaWarp) {
         if (lane == 0)
             for (int st = max(0, issued - G::kStages); st < issued; ++st)
-                mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr, a.err_flag,
-                                  100000000ull);
+                mbar_wait_bounded((warp == kConsumerWarps + 1 ? barv : bar0) + 8 * (st % G::kStages),
+                                  (st / G::kStages) & 1, nullptr, a.err_flag, 100000000ull);
         __syncwarp();
     }
     tc_fence_after();
