@@ -147,6 +147,8 @@ def describe(w, splits) -> str:
     if w.prefill_chunk:
         extra += f", {w.prefill_chunk}-token prefill chunk appended"
     split = f"split-K {splits}" + (f" of {w.split_pages} pages" if w.split_pages else "")
+    if not w.lens.startswith("fixed"):
+        split += ", longest first"
     return (f"{w.name}: batch {w.batch}, {ctx}, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
             f"head_dim {w.head_dim}, q_len {w.q_len}, {split}, page 4{extra}; one layer")
 
@@ -282,6 +284,8 @@ class Arm:
         self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
         self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
         self.fp8_qk = False    # tcgen05 kernel: fp16 scores (default) or the FP8 score variant
+        # batches of varied lengths: the split kernel takes the sequences longest first
+        self.longest_first = not w.lens.startswith("fixed")
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
         torch.cuda.synchronize(dev)
 
@@ -301,11 +305,12 @@ class Arm:
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
                                                err_flag=self.err, split_pages=self.w.split_pages,
                                                bitcast_decode=self.bitcast, mma_sync=self.mma_sync,
-                                               fp8_qk=self.fp8_qk)
+                                               fp8_qk=self.fp8_qk, longest_first=self.longest_first)
         else:
             kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, self.ws, self.topk_idx,
                                                self.topk_lens, num_splits=self.S, err_flag=self.err,
-                                               split_pages=self.w.split_pages, mma_sync=self.mma_sync)
+                                               split_pages=self.w.split_pages, mma_sync=self.mma_sync,
+                                               longest_first=self.longest_first)
 
     def step(self, i):
         """One step on pool copy i: append of the step's tokens, split-K

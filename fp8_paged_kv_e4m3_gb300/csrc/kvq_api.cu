@@ -56,7 +56,8 @@ static int check_params(const kvq_attn_params *p)
     if (p->batch < 0 || p->q_len < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
         p->num_splits < 0 || p->max_pages_per_seq < 1 || p->max_topk < 0 || p->split_pages < 0)
         return KVQ_ERR_INVALID_ARG;
-    if (p->flags & ~int32_t(KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC | KVQ_ATTN_FP8_QK | KVQ_ATTN_STRICT_ORDER))
+    if (p->flags & ~int32_t(KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC | KVQ_ATTN_FP8_QK | KVQ_ATTN_STRICT_ORDER |
+                            KVQ_ATTN_LONGEST_FIRST))
         return KVQ_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
     if (!std::isfinite(p->sm_scale) || p->sm_scale < 0.0f) return KVQ_ERR_INVALID_ARG;
@@ -173,6 +174,7 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.mma_sync = (p.flags & KVQ_ATTN_MMA_SYNC) != 0;
     a.fp8_qk = (p.flags & KVQ_ATTN_FP8_QK) != 0;
     a.early_pages = (p.flags & KVQ_ATTN_STRICT_ORDER) == 0;
+    a.longest_first = (p.flags & KVQ_ATTN_LONGEST_FIRST) != 0;
 
     cudaStream_t stream = static_cast<cudaStream_t>(c.stream);
     if (launch_attention(c.e4m3, p.head_dim, a, stream) != cudaSuccess) return KVQ_ERR_CUDA;

@@ -417,7 +417,7 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
 // source pages (E4M3 bits placed into fp16 bits, the value * 2^-8, exact),
 // with the 2^8 folded into the hoisted scales.  Both give the same fp16
 // values up to that power of two, so the outputs are identical.
-template <bool E4M3, int D, int NT, int RW, bool BITCAST>
+template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT = false>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     attn_split_kernel(const AttnArgs a)
 {
@@ -461,10 +461,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     // The producers' first block-table batch is fetched speculatively for a
     // sequence that fills its block-table row, in parallel with the context
     // length; it is refetched below if the real split starts elsewhere.
-    // (Blocks take the sequences in index order here: with 4 CTAs of this
-    // kernel per SM, the longest-first pick costs more than it returns.)
-    const int b = blockIdx.z;
-    const SeqPick pick = seq_identity(a, b);
+    // Blocks take the sequences in index order, or (LPT, the instances that
+    // KVQ_ATTN_LONGEST_FIRST selects) longest first: that pays a
+    // classification of every sequence in each CTA's prologue, which returns
+    // it only when lengths vary over a grid of several waves.
+    SeqPick pick = seq_identity(a, blockIdx.z);
+    if (LPT && !__syncthreads_and(lpt_classify(a, smem, G::kRingBytes))) pick = lpt_pick(a, blockIdx.z, smem);
+    const int b = pick.b;
     const SplitRange sr = split_range(a, s, b, pick.L, pick.topk_len);
     const int L = sr.L, item0 = sr.item0, item1 = sr.item1;
     const bool len_ok = sr.len_ok, topk = sr.topk;
@@ -868,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
 // ---------------------------------------------------------------------------
 // host launchers
 
-template <bool E4M3, int D, int NT, int RW, bool BITCAST>
+template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT>
 static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
 {
     constexpr int bytes = smem_bytes<E4M3, D, NT, RW>();
@@ -877,23 +880,23 @@ static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW, BITCAST>,
+        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-    return launch_pdl(attn_split_kernel<E4M3, D, NT, RW, BITCAST>, grid, dim3(kThreads), bytes, stream, a);
+    return launch_pdl(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT>, grid, dim3(kThreads), bytes, stream, a);
 }
 
-template <bool E4M3, int D, bool BITCAST>
+template <bool E4M3, int D, bool BITCAST, bool LPT = false>
 static cudaError_t launch_rows(const AttnArgs &a, cudaStream_t stream)
 {
     const int tiles = (a.rows + 7) / 8;
-    if (tiles <= 1) return launch_one<E4M3, D, 1, 1, BITCAST>(a, stream);
-    if (tiles <= 2) return launch_one<E4M3, D, 2, 1, BITCAST>(a, stream);
-    if (tiles <= 4) return launch_one<E4M3, D, 2, 2, BITCAST>(a, stream);
-    return launch_one<E4M3, D, 2, 4, BITCAST>(a, stream);
+    if (tiles <= 1) return launch_one<E4M3, D, 1, 1, BITCAST, LPT>(a, stream);
+    if (tiles <= 2) return launch_one<E4M3, D, 2, 1, BITCAST, LPT>(a, stream);
+    if (tiles <= 4) return launch_one<E4M3, D, 2, 2, BITCAST, LPT>(a, stream);
+    return launch_one<E4M3, D, 2, 4, BITCAST, LPT>(a, stream);
 }
 
 }  // namespace kvq

@@ -33,6 +33,7 @@ struct AttnArgs {
     bool fp8_qk;                 // E4M3 scores on the tcgen05 kernel (query quantised per CTA)
     bool early_pages;            // split kernel, no top-k list: block tables, lengths and pages of
                                  // positions < L - q_len may be read before the dependency wait
+    bool longest_first;          // split kernel (hardware decoder): CTAs take the sequences longest first
 };
 
 // Arguments of one chunked-prefill attention call (device pointers).
@@ -65,6 +66,8 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t head_dim);
 
 cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
+// the split kernel's longest-first instances (kvq_attn_lpt.cu)
+cudaError_t launch_attention_lpt(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_bitcast(int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t stream);
 bool tc_supported(int head_dim, int rows);

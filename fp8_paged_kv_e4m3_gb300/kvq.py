@@ -28,6 +28,7 @@ ATTN_BITCAST_DECODE = 1
 ATTN_MMA_SYNC = 2
 ATTN_FP8_QK = 4
 ATTN_STRICT_ORDER = 8
+ATTN_LONGEST_FIRST = 32
 
 _lock = threading.Lock()
 _lib = None
@@ -217,15 +218,18 @@ def kv_append_fp16(k_new, v_new, slot_mapping, k_cache, v_cache,
 def attn_params(q: torch.Tensor, num_kv_heads: int, max_pages_per_seq: int, num_splits: int = 0,
                 max_topk: int = 0, sm_scale: float = 0.0, split_pages: int = 0,
                 bitcast_decode: bool = False, mma_sync: bool = False, fp8_qk: bool = False,
-                strict_order: bool = False) -> AttnParams:
+                strict_order: bool = False, longest_first: bool = False) -> AttnParams:
     B, q_len, Hq, D = q.shape
     return AttnParams(B, q_len, Hq, num_kv_heads, D, num_splits, max_pages_per_seq, max_topk,
-                      sm_scale, split_pages, _flags(bitcast_decode, mma_sync, fp8_qk, strict_order))
+                      sm_scale, split_pages,
+                      _flags(bitcast_decode, mma_sync, fp8_qk, strict_order, longest_first))
 
 
-def _flags(bitcast_decode: bool, mma_sync: bool, fp8_qk: bool = False, strict_order: bool = False) -> int:
+def _flags(bitcast_decode: bool, mma_sync: bool, fp8_qk: bool = False, strict_order: bool = False,
+           longest_first: bool = False) -> int:
     return ((ATTN_BITCAST_DECODE if bitcast_decode else 0) | (ATTN_MMA_SYNC if mma_sync else 0) |
-            (ATTN_FP8_QK if fp8_qk else 0) | (ATTN_STRICT_ORDER if strict_order else 0))
+            (ATTN_FP8_QK if fp8_qk else 0) | (ATTN_STRICT_ORDER if strict_order else 0) |
+            (ATTN_LONGEST_FIRST if longest_first else 0))
 
 
 def num_splits(p: AttnParams) -> int:
@@ -262,7 +266,7 @@ def workspace_views(ws: torch.Tensor, p: AttnParams):
 
 def _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
                 topk_lens, cache_dtype, num_splits_, sm_scale, split_pages, bitcast_decode=False,
-                mma_sync=False, fp8_qk=False, strict_order=False):
+                mma_sync=False, fp8_qk=False, strict_order=False, longest_first=False):
     _need(q, "q", torch.float16, 4)
     B, q_len, Hq, D = q.shape
     _need(k_cache, "k_cache", cache_dtype, 4)
@@ -290,7 +294,7 @@ def _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out,
             raise ValueError("topk_idx must be [B, Hkv, K], topk_lens [B]")
         max_topk = topk_idx.shape[2]
     p = AttnParams(B, q_len, Hq, Hkv, D, num_splits_, block_tables.shape[1], max_topk, sm_scale,
-                   split_pages, _flags(bitcast_decode, mma_sync, fp8_qk, strict_order))
+                   split_pages, _flags(bitcast_decode, mma_sync, fp8_qk, strict_order, longest_first))
     return p
 
 
@@ -298,16 +302,18 @@ def paged_decode_attn_e4m3(q, k_cache, v_cache, block_tables, context_lens, k_sc
                            v_scale: float, workspace, out=None, topk_idx=None, topk_lens=None,
                            num_splits: int = 0, sm_scale: float = 0.0, err_flag=None,
                            split_pages: int = 0, bitcast_decode: bool = False, mma_sync: bool = False,
-                           fp8_qk: bool = False, strict_order: bool = False):
+                           fp8_qk: bool = False, strict_order: bool = False, longest_first: bool = False):
     """Decode / verify attention over E4M3 pools; returns `out` (fp16, shape of q).
     fp8_qk: scores from the query quantised to E4M3 per (sequence, kv head)
     on E4M3 tensor-core instructions (verify shapes at head_dim 128 only).
     strict_order: read no input before the preceding kernel in the stream
     completes (by default, without a top-k list, block tables, lengths and
-    the pages of positions below L - q_len may be read earlier)."""
+    the pages of positions below L - q_len may be read earlier).
+    longest_first: the split kernel takes the sequences longest first (for
+    batches of varied lengths over several waves; same results)."""
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
                     topk_lens, torch.uint8, num_splits, sm_scale, split_pages, bitcast_decode, mma_sync,
-                    fp8_qk, strict_order)
+                    fp8_qk, strict_order, longest_first)
     if out is None:
         out = torch.empty_like(q)
     _check("paged_decode_attn_e4m3", load().paged_decode_attn_e4m3(
@@ -321,11 +327,11 @@ def paged_decode_attn_e4m3(q, k_cache, v_cache, block_tables, context_lens, k_sc
 def paged_decode_attn_fp16(q, k_cache, v_cache, block_tables, context_lens, workspace, out=None,
                            topk_idx=None, topk_lens=None, num_splits: int = 0,
                            sm_scale: float = 0.0, err_flag=None, split_pages: int = 0,
-                           mma_sync: bool = False, strict_order: bool = False):
+                           mma_sync: bool = False, strict_order: bool = False, longest_first: bool = False):
     """fp16-KV twin of paged_decode_attn_e4m3."""
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, topk_idx,
                     topk_lens, torch.float16, num_splits, sm_scale, split_pages, False, mma_sync,
-                    strict_order=strict_order)
+                    strict_order=strict_order, longest_first=longest_first)
     if out is None:
         out = torch.empty_like(q)
     _check("paged_decode_attn_fp16", load().paged_decode_attn_fp16(
@@ -340,10 +346,11 @@ def paged_decode_attn_e4m3_partial(q, k_cache, v_cache, block_tables, context_le
                                    topk_lens=None, num_splits: int = 0, sm_scale: float = 0.0,
                                    err_flag=None, split_pages: int = 0,
                                    bitcast_decode: bool = False, mma_sync: bool = False,
-                                   fp8_qk: bool = False, strict_order: bool = False) -> AttnParams:
+                                   fp8_qk: bool = False, strict_order: bool = False,
+                                   longest_first: bool = False) -> AttnParams:
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, None, topk_idx,
                     topk_lens, torch.uint8, num_splits, sm_scale, split_pages, bitcast_decode, mma_sync,
-                    fp8_qk, strict_order)
+                    fp8_qk, strict_order, longest_first)
     _check("paged_decode_attn_e4m3_partial", load().paged_decode_attn_e4m3_partial(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
         _ptr(context_lens), ctypes.c_float(k_scale), ctypes.c_float(v_scale), _ptr(topk_idx),
@@ -356,10 +363,10 @@ def paged_decode_attn_fp16_partial(q, k_cache, v_cache, block_tables, context_le
                                    topk_idx=None, topk_lens=None, num_splits: int = 0,
                                    sm_scale: float = 0.0, err_flag=None,
                                    split_pages: int = 0, mma_sync: bool = False,
-                                   strict_order: bool = False) -> AttnParams:
+                                   strict_order: bool = False, longest_first: bool = False) -> AttnParams:
     p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, None, topk_idx,
                     topk_lens, torch.float16, num_splits, sm_scale, split_pages, False, mma_sync,
-                    strict_order=strict_order)
+                    strict_order=strict_order, longest_first=longest_first)
     _check("paged_decode_attn_fp16_partial", load().paged_decode_attn_fp16_partial(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
         _ptr(context_lens), _ptr(topk_idx), _ptr(topk_lens), _ptr(workspace),

@@ -230,6 +230,18 @@ typedef struct {
  * example this step's append) finishes. */
 #define KVQ_ATTN_STRICT_ORDER 8
 
+/* Longest first: the split kernel's CTAs take the sequences in decreasing
+ * order of work (context length, or top-k list length) instead of index
+ * order, so that on a grid of several waves the long sequences start first
+ * and the short ones fill the gaps at the end.  Each CTA then classifies
+ * every sequence in its prologue, which costs a little when all lengths are
+ * equal (1 to 3 us per call on the uniform workloads measured) and pays when
+ * they vary (the mixed-length batch: step 137 -> 120 us).  A scheduling
+ * choice only: the outputs are bit-identical.  The tcgen05 kernel always
+ * orders its sequences this way; the bitcast decoder's instances keep index
+ * order. */
+#define KVQ_ATTN_LONGEST_FIRST 32
+
 /* The split count a call with these parameters uses: p->num_splits if > 0;
  * else, with split_pages > 0, the fewest splits that cover max_pages_per_seq
  * pages and max_topk list entries; else a count chosen from the shape and

@@ -70,7 +70,7 @@ def device_problem(pr: P.HostProblem, e4m3: bool = True, sentinel: int = P.SENTI
 
 def run_attention(dp: DeviceProblem, num_splits=0, topk=True, partial=False, block_tables=None,
                   k_cache=None, v_cache=None, context_lens=None, q=None, split_pages=0,
-                  bitcast_decode=False, mma_sync=False, fp8_qk=False):
+                  bitcast_decode=False, mma_sync=False, fp8_qk=False, longest_first=False):
     q = dp.q if q is None else q
     bt = dp.block_tables if block_tables is None else block_tables
     kc = dp.k_cache if k_cache is None else k_cache
@@ -79,7 +79,7 @@ def run_attention(dp: DeviceProblem, num_splits=0, topk=True, partial=False, blo
     ti, tl = (dp.topk_idx, dp.topk_lens) if topk else (None, None)
     p = kvq.AttnParams(q.shape[0], q.shape[1], q.shape[2], kc.shape[1], q.shape[3], num_splits,
                        bt.shape[1], 0 if ti is None else ti.shape[2], 0.0, split_pages,
-                       kvq._flags(bitcast_decode, mma_sync, fp8_qk))
+                       kvq._flags(bitcast_decode, mma_sync, fp8_qk, False, longest_first))
     ws = kvq.alloc_workspace(p, q.device)
     ws.fill_(float("nan"))
     if partial:
@@ -87,20 +87,21 @@ def run_attention(dp: DeviceProblem, num_splits=0, topk=True, partial=False, blo
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, dp.k_scale, dp.v_scale, ws, ti, tl,
                                                num_splits, err_flag=dp.err, split_pages=split_pages,
                                                bitcast_decode=bitcast_decode, mma_sync=mma_sync,
-                                               fp8_qk=fp8_qk)
+                                               fp8_qk=fp8_qk, longest_first=longest_first)
         else:
             kvq.paged_decode_attn_fp16_partial(q, kc, vc, bt, cl, ws, ti, tl, num_splits,
                                                err_flag=dp.err, split_pages=split_pages,
-                                               mma_sync=mma_sync)
+                                               mma_sync=mma_sync, longest_first=longest_first)
         return ws, p
     if dp.e4m3:
         out = kvq.paged_decode_attn_e4m3(q, kc, vc, bt, cl, dp.k_scale, dp.v_scale, ws, None, ti, tl,
                                          num_splits, err_flag=dp.err, split_pages=split_pages,
                                          bitcast_decode=bitcast_decode, mma_sync=mma_sync,
-                                         fp8_qk=fp8_qk)
+                                         fp8_qk=fp8_qk, longest_first=longest_first)
     else:
         out = kvq.paged_decode_attn_fp16(q, kc, vc, bt, cl, ws, None, ti, tl, num_splits,
-                                         err_flag=dp.err, split_pages=split_pages, mma_sync=mma_sync)
+                                         err_flag=dp.err, split_pages=split_pages, mma_sync=mma_sync,
+                                         longest_first=longest_first)
     return out
 
 

@@ -90,7 +90,7 @@ def test_workspace_size_matches_layout(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 96, -4), ("q_len", 5, -4), ("q_len", 0, -1), ("num_kv_heads", 3, -1),
     ("num_splits", -1, -1), ("max_pages_per_seq", 0, -1), ("num_q_heads", 136, -4),
-    ("flags", 16, -1), ("flags", -1, -1),
+    ("flags", 64, -1), ("flags", -1, -1),
 ])
 def test_bad_params_are_refused(lib, field, value, status):
     p = _params(**{field: value})
