@@ -153,6 +153,18 @@ def test_fp8_scores_outside_the_tcgen05_shapes_are_unsupported(lib):
     assert _attn(lib, _params(flags=fp8, **verify), k_scale=0.0) == -2    # the scale gate comes first
 
 
+def test_scheduling_flags_change_no_sizes(lib):
+    """Strict ordering and longest-first order are scheduling choices: the same
+    split count and workspace as without them, for decode and verify shapes."""
+    for shape in (dict(), dict(head_dim=128, q_len=4)):
+        base = _params(**shape)
+        for f in (kvq.ATTN_STRICT_ORDER, kvq.ATTN_LONGEST_FIRST, kvq.ATTN_STRICT_ORDER | kvq.ATTN_LONGEST_FIRST):
+            p = _params(flags=f, **shape)
+            assert lib.kvq_attn_num_splits(ctypes.byref(p)) == lib.kvq_attn_num_splits(ctypes.byref(base))
+            assert lib.kvq_attn_workspace_bytes(ctypes.byref(p)) == lib.kvq_attn_workspace_bytes(ctypes.byref(base))
+    assert kvq._flags(False, False, False, True, True) == kvq.ATTN_STRICT_ORDER | kvq.ATTN_LONGEST_FIRST
+
+
 def test_append_host_checks_fail_closed(lib):
     f = lib.kv_append_e4m3
     assert f(FAKE, FAKE, FAKE, 4, 2, 64, FAKE, FAKE, 10, ctypes.c_float(0.0), ctypes.c_float(1.0), None, None) == -2
