@@ -604,6 +604,36 @@ def _seq_rows(w, which, off, L, g):
     return np.ascontiguousarray(_SEQ_CACHE[key][off:off + L, g, :])
 
 
+def library_splits(w, max_pages: int, sm_count: int) -> int:
+    """The split count the library picks for this workload (the rule of
+    kvq_attn_num_splits, restated so that the reference arm can label its
+    config like ours without loading the CUDA library)."""
+    max_topk = w.topk if w.topk > 0 else 0
+    if w.num_splits > 0:
+        return w.num_splits
+    if w.split_pages > 0:
+        sp = w.split_pages
+        return max(1, -(-max_pages // sp), -(-max_topk // (4 * sp)))
+    pairs = max(w.batch, 1) * w.num_kv_heads
+    s = -(-(sm_count * 3 * 2) // pairs)
+    cap = -(-max_pages // 16)
+    if max_topk > 0:
+        cap = max(cap, -(-max_topk // 32))
+    return max(1, min(s, cap, 1024))
+
+
+def reference_config(w, world: int, sample: str) -> dict:
+    """The config of our arm's line for workload w, for the reference arm."""
+    from fp8_paged_kv_e4m3_gb300 import inputs
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    lay = inputs.page_layout(w)
+    return {"workload": describe(w, library_splits(w, lay.block_tables.shape[1], sms)),
+            "global_batch": world * w.batch, "kv_dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
+            "l2": "host oracle: no GPU cache to defeat", "parallelism": f"replicas x{world}",
+            "sample": sample}
+
+
 def run_reference(args, w):
     """The reference arm: the CPU oracle on a bounded sample per step."""
     if w.name == "prefill":
@@ -627,7 +657,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "sample": sample},
+            "config": reference_config(w, args.gpus, sample),
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -806,6 +836,11 @@ def prefill_oracle_sample(w, rows=(0, 4095, 8191)):
     return time.perf_counter() - t0, fl
 
 
+def describe_prefill(w) -> str:
+    return (f"prefill: {w.batch} x {w.q_len}-token chunk over its own context (causal), {w.num_q_heads} q / "
+            f"{w.num_kv_heads} kv heads, head_dim {w.head_dim}, page 4; one layer")
+
+
 def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
     import torch
     peak_gbs, _ = _peaks()
@@ -844,9 +879,7 @@ def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
             "data": "synthetic",
-            "config": {"workload": f"prefill: {w.batch} x {w.q_len}-token chunk over its own context "
-                                   f"(causal), {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
-                                   f"head_dim {w.head_dim}, page 4; one layer",
+            "config": {"workload": describe_prefill(w),
                        "l2": f"rotating {arm.copies} copies of chunk K/V, Q, pools and output (> 2 x L2)",
                        "parallelism": f"replicas x{world}"},
             "flops_per_step": arm.flops,
@@ -885,7 +918,8 @@ def run_reference_prefill(args, w):
                       "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                       "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
                       "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                      "config": {"workload": w.name, "sample": sample},
+                      "config": {"workload": describe_prefill(w), "l2": "host oracle: no GPU cache to defeat",
+                                 "parallelism": f"replicas x{args.gpus}", "sample": sample},
                       "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
                       "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                       "gpu_launches": 0}), flush=True)
