@@ -34,6 +34,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -157,10 +158,16 @@ def describe(w, splits) -> str:
 # clocks sampled while timing
 
 class ClockSampler:
+    """nvidia-smi samples (SM clock, its maximum, throttle reasons) every 100 ms
+    while the timed region runs.  The raw samples go to KVQ_CLOCKS_DIR when
+    that is set (kept), else to a temporary file (removed after the summary)."""
+
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.keep = bool(os.environ.get("KVQ_CLOCKS_DIR"))
+        base = os.environ.get("KVQ_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(base, f"kvq_clocks_{os.getpid()}_{id(self)}.csv")
 
     def __enter__(self):
         try:
@@ -193,7 +200,11 @@ class ClockSampler:
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         rows = []
-        for line in open(self.path):
+        with open(self.path) as fh:
+            lines = fh.readlines()
+        if not self.keep:
+            os.remove(self.path)
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
