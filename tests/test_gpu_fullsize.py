@@ -39,9 +39,12 @@ def pool():
 
 
 class Layer:
-    """One layer of a workload pushed through the GPU path."""
+    """One layer of a workload pushed through the GPU path, in the launch
+    configuration bench.py times (longest-first order for batches of varied
+    lengths)."""
 
     def __init__(self, w, layer, lay, e4m3=True, with_prefill=True, bitcast=False):
+        longest_first = not w.lens.startswith("fixed")
         self.w, self.layer, self.lay, self.e4m3 = w, layer, lay, e4m3
         lens = lay.lens.astype(np.int64)
         total = int(lens.sum())
@@ -93,11 +96,11 @@ class Layer:
             self.out = kvq.paged_decode_attn_e4m3(self.q, self.kc, self.vc, self.bt, self.cl, self.ks,
                                                   self.vs, ws, None, ti_d, tl_d, w.num_splits,
                                                   err_flag=err, split_pages=w.split_pages,
-                                                  bitcast_decode=bitcast)
+                                                  bitcast_decode=bitcast, longest_first=longest_first)
         else:
             self.out = kvq.paged_decode_attn_fp16(self.q, self.kc, self.vc, self.bt, self.cl, ws, None,
                                                   ti_d, tl_d, w.num_splits, err_flag=err,
-                                                  split_pages=w.split_pages)
+                                                  split_pages=w.split_pages, longest_first=longest_first)
         torch.cuda.synchronize()
         assert err.item() == 0, f"device error bits {err.item()}"
 
