@@ -165,3 +165,20 @@ def oracle_unit(q_rows, k_seq, v_seq, L, ks, vs, e4m3=True, topk_list=None):
                                   np.array([L], np.int32), ks, vs, ti, tl)
     pool_k = kc.reshape(pages * 4, D)[:L] if e4m3 else None
     return out[0, :, 0, :], flags, pool_k
+
+
+def oracle_group_fp8(q_group, k_seq, v_seq, L, ks, vs):
+    """Oracle attention of one (sequence, kv head) group under the FP8 score
+    reading: q_group fp16 [q_len, G, D] (all the query rows that share the kv
+    head, so that the group's query scale is the one the kernel takes),
+    k_seq / v_seq fp16 [L, D].  Returns out [q_len, G, D] float64 and flags."""
+    q_len, G, D = q_group.shape
+    pages = (L + 3) // 4
+    bt = np.arange(pages, dtype=np.int32)[None, :]
+    slots = np.arange(L, dtype=np.int32)
+    kc = np.full((pages, 1, 4, D), SENTINEL, np.uint8)
+    vc = kc.copy()
+    oracle.append_e4m3(k_seq[:, None, :], v_seq[:, None, :], slots, kc, vc, ks, vs)
+    out, flags = oracle.attention(np.ascontiguousarray(q_group)[None], kc, vc, bt, np.array([L], np.int32), ks, vs,
+                                  fp8_q=True)
+    return out[0], flags

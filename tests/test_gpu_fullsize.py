@@ -43,7 +43,7 @@ class Layer:
     configuration bench.py times (longest-first order for batches of varied
     lengths)."""
 
-    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True, bitcast=False):
+    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True, bitcast=False, fp8_qk=False):
         longest_first = not w.lens.startswith("fixed")
         self.w, self.layer, self.lay, self.e4m3 = w, layer, lay, e4m3
         lens = lay.lens.astype(np.int64)
@@ -96,7 +96,8 @@ class Layer:
             self.out = kvq.paged_decode_attn_e4m3(self.q, self.kc, self.vc, self.bt, self.cl, self.ks,
                                                   self.vs, ws, None, ti_d, tl_d, w.num_splits,
                                                   err_flag=err, split_pages=w.split_pages,
-                                                  bitcast_decode=bitcast, longest_first=longest_first)
+                                                  bitcast_decode=bitcast, longest_first=longest_first,
+                                                  fp8_qk=fp8_qk)
         else:
             self.out = kvq.paged_decode_attn_fp16(self.q, self.kc, self.vc, self.bt, self.cl, ws, None,
                                                   ti_d, tl_d, w.num_splits, err_flag=err,
@@ -229,3 +230,32 @@ def test_mixed_24_layers(pool):
         assert np.array_equal(got, want), f"prefill bytes differ, layer {layer}"
         del L
         torch.cuda.empty_cache()
+
+
+def test_verify_fp8_scores(pool):
+    """The FP8 score variant at the verify workload's full size: sampled
+    (sequence, kv head) groups against the oracle's reading, each group's
+    G x q_len query rows quantised together as the kernel's CTA does."""
+    w = inputs.get("verify")
+    L = Layer(w, 0, inputs.page_layout(w), fp8_qk=True)
+    ks, vs = L.oracle_scales()
+    rng = np.random.default_rng(6)
+    G = w.group
+    groups = list(zip(rng.integers(0, w.batch, 12).tolist(), rng.integers(0, w.num_kv_heads, 12).tolist()))
+    futs = []
+    for b, g in groups:
+        n = int(L.lay.lens[b])
+        q_group = L.q[b, :, g * G:(g + 1) * G, :].cpu().numpy()
+        k_seq = L.k[L.offs[b]:L.offs[b] + n, g].cpu().numpy()
+        v_seq = L.v[L.offs[b]:L.offs[b] + n, g].cpu().numpy()
+        futs.append((b, g, pool.submit(P.oracle_group_fp8, q_group, k_seq, v_seq, n, ks, vs)))
+    got_all = L.out.float().cpu().numpy()
+    bad = []
+    for b, g, f in futs:
+        ref, flags = f.result()
+        assert flags == 0
+        got = got_all[b, :, g * G:(g + 1) * G, :]
+        ok = P.tolerance_ok(got, ref)
+        if not ok.all():
+            bad.append((b, g, float(np.abs(got - ref).max())))
+    assert not bad, f"verify fp8 scores: {len(bad)} groups outside tolerance, e.g. {bad[:4]}"
