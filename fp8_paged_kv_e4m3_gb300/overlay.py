@@ -1,11 +1,11 @@
 """Revision-bound calibrated scale overlay: materialise and load, failing closed.
 
 PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path",
-sections Changes and Validation boundary: the E4M3 capacity mode requires one
-finite positive K scale and one V scale for every layer (24 of 24 on the
-pages' model), produced offline by calibration and bound to the exact
-checkpoint revision; startup is refused when the overlay is missing or
-incomplete, and no generic or unit-scale fallback is accepted.  PR
+sections Changes and Validation boundary: the E4M3 capacity mode needs a
+finite, positive K scale and V scale for each layer (24 of 24 on the pages'
+model), computed offline by calibration and tied to one checkpoint revision;
+without a complete overlay the mode does not start, and a default scale
+(such as 1) never stands in for a missing one.  PR
 "[Model][SM70] Calibrated E4M3 KV cache for Qwen4Exp QSA with MTP", section
 Status and history: the materialiser is revision-checked.
 

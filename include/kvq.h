@@ -77,7 +77,9 @@ enum {
     KVQ_DEV_BAD_SLOT = 2,   /* append slot beyond the pool: token not written           */
     KVQ_DEV_BAD_TOPK = 4,   /* top-k index outside [0, context_len): entry skipped      */
     KVQ_DEV_BAD_LEN = 8,    /* context_len < q_len or > 4 * max_pages_per_seq: row = 0   */
-    KVQ_DEV_TIMEOUT = 16    /* an internal pipeline wait gave up (~2 s): results invalid */
+    KVQ_DEV_TIMEOUT = 16    /* an internal pipeline wait gave up (~2 s): results invalid;
+                               the CTA that gave up drained its copies, wrote its split
+                               partials as empty (m = -inf, l = 0) and exited            */
 };
 
 /* Library version (KVQ_VERSION) and a static string for a status code. */
@@ -85,9 +87,10 @@ int kvq_version(void);
 const char *kvq_status_string(int status);
 
 /* ------------------------------------------------------------------------
- * Scale gate.  [P2] Changes: "require all 24 finite positive per-layer K/V
- * scales and refuse startup when the overlay is missing or incomplete";
- * [P2] Validation boundary: no generic or unit-scale fallback.
+ * Scale gate.  [P2] Changes: the E4M3 mode starts only when every layer
+ * (24 of 24 on the pages' model) has a K and a V scale that is finite and
+ * positive; a missing or partial set stops start-up.  [P2] Validation
+ * boundary: a scale is never replaced by a default such as 1.
  *   k_scales, v_scales : host float[num_layers]
  * Returns KVQ_OK when every entry is finite and > 0, KVQ_ERR_BAD_SCALE when
  * any is not, KVQ_ERR_INVALID_ARG for a null array or num_layers < 1.
@@ -96,9 +99,10 @@ const char *kvq_status_string(int status);
 int kvq_validate_scales(const float *k_scales, const float *v_scales, int32_t num_layers);
 
 /* ------------------------------------------------------------------------
- * Calibration.  [P2] Changes: "add offline calibration"; the calibrated
- * scale is amax / 448 (448 = largest finite E4M3 value) for one layer's K
- * or V, amax being the largest |x| of a calibration draw.
+ * Calibration.  [P2] Changes: the scales are produced offline by a
+ * calibration pass; the calibrated scale is amax / 448 (448 = largest
+ * finite E4M3 value) for one layer's K or V, amax being the largest |x| of
+ * a calibration draw.
  *
  * kvq_amax_f16: amax over n fp16 values.
  *   x        : device fp16[n] (any alignment)
@@ -394,7 +398,10 @@ int paged_prefill_attn_fp16(const void *q, const void *k_cache, const void *v_ca
  *    use paged_decode_attn_e4m3 with your own workspace for those.
  *  - The first call on a device looks up the buffer's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.  A failed lookup returns KVQ_ERR_CUDA.
+ *    before any stream capture.  The address belongs to the device's
+ *    context: after a device reset (cudaDeviceReset) the next call looks it
+ *    up again, so make that call before any capture too.  A failed lookup
+ *    returns KVQ_ERR_CUDA.
  *  - Every call on a device shares the one buffer, and it keeps the last
  *    call's contents (nothing in it has to start at zero).  Calls whose GPU
  *    work overlaps -- e.g. issued on two streams without ordering -- race

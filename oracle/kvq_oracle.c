@@ -227,9 +227,9 @@ int oracle_quantize_q_groups(const uint16_t *q, int B, int q_len, int Hq, int Hk
     return ORACLE_OK;
 }
 
-/* Scale gate ([P2] Changes: require all finite positive per-layer K/V scales
- * and refuse startup when any is missing; [P2] Validation boundary: no
- * generic or unit-scale fallback).  Returns the number of bad entries. */
+/* Scale gate ([P2] Changes: every layer needs a finite, positive K and V
+ * scale before the E4M3 mode starts; [P2] Validation boundary: a default
+ * scale never replaces a missing one).  Returns the number of bad entries. */
 int oracle_count_bad_scales(const float *k_scales, const float *v_scales, int n)
 {
     int i, bad = 0;
