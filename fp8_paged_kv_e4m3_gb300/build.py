@@ -82,6 +82,46 @@ def build(force: bool = False, ptxas_verbose: bool = False) -> str:
     return LIB
 
 
+def build_variant(tag: str, defines: dict, sources=("kvq_attn.cu",)) -> str:
+    """A test build of the library at _build/<tag>/libkvq.so: the translation
+    units `sources` compiled again with the preprocessor `defines` (name ->
+    value), linked with the default build's other objects.  Used by tests
+    that need an instrumented kernel; the default library never carries the
+    defines."""
+    build()
+    out_dir = os.path.join(BUILD, tag)
+    lib = os.path.join(out_dir, "libkvq.so")
+    srcs = [os.path.join(CSRC, f) for f in sources]
+    if os.path.exists(lib) and all(os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps() + [LIB]):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
+    cc = nvcc()
+    dflags = [f"-D{k}={v}" for k, v in defines.items()]
+    own = {}
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(8, len(srcs)))) as ex:
+        jobs = []
+        for src in srcs:
+            obj = os.path.join(out_dir, os.path.basename(src) + ".o")
+            own[os.path.basename(src)] = obj
+            jobs.append(ex.submit(subprocess.run, [cc, *ARCH, *FLAGS, *dflags, "-c", src, "-o", obj],
+                                  capture_output=True, text=True))
+        for j in jobs:
+            r = j.result()
+            if r.returncode != 0:
+                sys.stderr.write(r.stderr)
+                raise RuntimeError("nvcc failed:\n" + " ".join(r.args))
+    objs = [own.get(os.path.basename(src), os.path.join(BUILD, os.path.basename(src) + ".o"))
+            for src in _sources()]
+    tmp = lib + f".{os.getpid()}.tmp"
+    r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stderr)
+        raise RuntimeError("link failed")
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")

@@ -39,7 +39,8 @@
 //    memory, so the eight rows an ldmatrix reads (one slot of eight pages)
 //    fall in distinct banks.
 //  * Every wait is bounded (about 2 s); on expiry the kernel reports
-//    KVQ_DEV_TIMEOUT, drains its own copies and exits without writing.
+//    KVQ_DEV_TIMEOUT, drains its own copies, gives its rows zero weight in
+//    the workspace (m = -inf, l = 0) and exits.
 #pragma once
 
 #include <cstdint>
@@ -90,6 +91,7 @@ struct Geometry {
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kTokPosOff = kRingBytes;
     static constexpr int kBarOff = kTokPosOff + kStages * kTokPerStage * 4;
+    // abort flag, sticky bad-stage flag, and the stages each producer issued
     static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
     static constexpr int kBytes = kAbortOff + 16;
     static_assert(kPageStride % 128 == 16, "page skew must be 16 bytes mod 128");
@@ -504,6 +506,16 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
                                         stage_bad, early ? max(L - a.q_len, 0) / 4 : -1);
     } else {
         if (early) grid_dependency_wait();
+        int c_nst = nst;   // stages this consumer takes
+#ifdef KVQ_TEST_STALL_CONSUMERS
+        // Test builds only (never the library's default build): before their
+        // first stage the consumers wait, with a bound of
+        // KVQ_TEST_STALL_CONSUMERS nanoseconds, on slot 0's empty barrier,
+        // which completes only after the consumers themselves release slot 0.
+        // The wait therefore always gives up, and the give-up path below runs.
+        if (!mbar_wait_bounded(bar0 + 8 * G::kStages, 0, abort_flag, a.err_flag, KVQ_TEST_STALL_CONSUMERS))
+            c_nst = 0;
+#endif
         // ================= consumers =================
         // Q as mma B fragments, one set per 8-row n-tile; k-step ks of this
         // lane covers channels 16ks + 4t .. +3 (E4M3: the pairs the hardware
@@ -562,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         const float qk = a.qk_scale_log2 * (E4M3 && BITCAST ? 256.f : 1.f);
         const int first_masked = L - a.q_len + 1;   // positions >= this are masked for some row
 
-        for (int st = 0; st < nst; ++st) {
+        for (int st = 0; st < c_nst; ++st) {
             const int slot = st % G::kStages;
             if (!mbar_wait_bounded(bar0 + 8 * slot, (st / G::kStages) & 1, abort_flag, a.err_flag))
                 break;
@@ -781,15 +793,37 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     }
 
     // ---- merge the token warps through shared memory, write the split partial ----
+    volatile int *issued_by = abort_flag + 2;            // [2]: stages the K and V producers issued
+    if (warp >= kConsumerWarps && lane == 0) issued_by[warp - kConsumerWarps] = issued;
     __syncthreads();
     if (*abort_flag) {
-        // Something gave up: before the CTA's shared memory is released, wait
-        // (bounded) for every copy the producer issued, then leave without
-        // writing.  The error bit is already set.
-        if (warp >= kConsumerWarps && lane == 0)   // each producer: the stages it issued
-            for (int st = max(0, issued - G::kStages); st < issued; ++st)
+        // Something gave up.  Before the CTA's shared memory is released,
+        // every bulk copy in flight must land.  A stage's full barrier counts
+        // one arrival per producer, so a stage that only one producer issued
+        // could never complete: the other producer arrives for it here
+        // (without copies).  Neither producer is more than kStages stages
+        // ahead of the other (a producer reuses a slot only after the
+        // consumers released it, which needs both producers' copies of the
+        // slot's previous stage), so the stages [hi - kStages, hi), hi = the
+        // larger count, sit in distinct slots, every earlier stage has
+        // completed, and each of them completes once its copies land.  The
+        // waits are bounded all the same.  Then the CTA's rows get zero weight
+        // in the workspace (m = -inf, l = 0), so that the combine ignores
+        // this split, and the CTA leaves.  The error bit is already set.
+        if (warp >= kConsumerWarps && lane == 0) {
+            const int mine = issued, other = issued_by[kConsumerWarps + 1 - warp];
+            for (int st = mine; st < other; ++st) mbar_arrive(bar0 + 8 * (st % G::kStages));
+            const int hi = max(mine, other);
+            for (int st = max(0, hi - G::kStages); st < hi; ++st)
                 mbar_wait_bounded(bar0 + 8 * (st % G::kStages), (st / G::kStages) & 1, nullptr,
                                   a.err_flag, 100000000ull);
+        }
+        for (int row = threadIdx.x; row < a.rows; row += kThreads) {
+            const int i = row / a.group, h = g * a.group + row % a.group;
+            const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * a.num_splits + s;
+            a.ws_m[unit] = -INFINITY;
+            a.ws_l[unit] = 0.f;
+        }
         __syncthreads();
         return;
     }

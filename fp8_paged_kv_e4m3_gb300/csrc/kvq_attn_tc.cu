@@ -30,8 +30,9 @@
 //    tokens or channels, N = rows padded to 16/32/64, K = 16 per instruction)
 //    and commits their completion to mbarriers.
 //  * Every wait is bounded (about 2 s); on expiry the CTA reports
-//    KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor memory
-//    and exits without writing.
+//    KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, gives its rows zero
+//    weight in the workspace (m = -inf, l = 0), frees its tensor memory and
+//    exits.
 //
 // FP8 score variant (F8, E4M3 pools only; not on the pages): the workers
 // quantise the CTA's query rows to E4M3 with one scale amax / 448 over them
@@ -692,14 +693,28 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     }
 
     // ---- teardown: copies drained, MMAs complete (the MMA thread waited), tensor memory freed ----
+    // On a give-up, each producer waits (bounded) for the copies of the stages it
+    // issued: K and V stages complete on barriers of their own with one arrival
+    // each, a producer reuses a slot only after its previous stage completed, so
+    // the last kStages stages it issued sit in distinct slots and each completes
+    // once its copies land.  The CTA's rows then get zero weight (m = -inf, l = 0).
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag && warp >= kConsumerWarps && warp < kTcMmaWarp) {
+    const bool aborted = *abort_flag != 0;
+    if (aborted && warp >= kConsumerWarps && warp < kTcMmaWarp) {
         if (lane == 0)
             for (int st = max(0, issued - G::kStages); st < issued; ++st)
                 mbar_wait_bounded((warp == kConsumerWarps + 1 ? barv : bar0) + 8 * (st % G::kStages),
                                   (st / G::kStages) & 1, nullptr, a.err_flag, 100000000ull);
         __syncwarp();
+    }
+    if (aborted && warp < kTcWorkers) {
+        for (int r = threadIdx.x; r < a.rows; r += 32 * kTcWorkers) {
+            const int i = r / a.group, hh = g * a.group + r % a.group;
+            const int64_t unit = (((int64_t)b * a.num_q_heads + hh) * a.q_len + i) * a.num_splits + s;
+            a.ws_m[unit] = -INFINITY;
+            a.ws_l[unit] = 0.f;
+        }
     }
     tc_fence_after();
     __syncthreads();
