@@ -143,7 +143,8 @@ def oracle_unit(q_rows, k_seq, v_seq, L, ks, vs, e4m3=True, topk_list=None):
     q_rows fp16 [q_len, D]; k_seq / v_seq fp16 [L, D] (the sequence's tokens of
     the head's kv group, positions 0..L-1); topk_list int32 [n] or None.
     Builds a one-sequence, one-head problem with an identity block table and
-    returns (out [q_len, D] float64, pool_k bytes [L, D] (E4M3 arm) or None)."""
+    returns (out [q_len, D] float64, flags, pool_k bytes [L, D], pool_v bytes
+    [L, D]) -- the pool bytes for the E4M3 arm, None for fp16."""
     q_len, D = q_rows.shape
     pages = (L + 3) // 4
     bt = np.arange(pages, dtype=np.int32)[None, :]
@@ -164,7 +165,45 @@ def oracle_unit(q_rows, k_seq, v_seq, L, ks, vs, e4m3=True, topk_list=None):
     out, flags = oracle.attention(np.ascontiguousarray(q_rows)[None, :, None, :], kc, vc, bt,
                                   np.array([L], np.int32), ks, vs, ti, tl)
     pool_k = kc.reshape(pages * 4, D)[:L] if e4m3 else None
-    return out[0, :, 0, :], flags, pool_k
+    pool_v = vc.reshape(pages * 4, D)[:L] if e4m3 else None
+    return out[0, :, 0, :], flags, pool_k, pool_v
+
+
+def oracle_pool_shard(folder, p0, p1, i0, i1, ks, vs, e4m3):
+    """The oracle's fill of pool pages [p0, p1), compared with the GPU's.
+
+    `folder` holds (as .npy files) every token the layer appended -- k, v
+    fp16 [T][Hkv][D] and their slots int32 [T] -- plus `order`, the token
+    indices sorted by page, whose entries [i0, i1) are the tokens of pages
+    [p0, p1), and the GPU's pools pool_k, pool_v [P][Hkv][4][D].  Starting
+    from sentinel pools, the oracle appends those tokens (their slots
+    re-based to page p0); every byte of the shard, including the slots no
+    token owns, must equal the GPU's.  Returns (p0, differing K bytes,
+    differing V bytes, first differing page or -1)."""
+    import os
+    ld = lambda name: np.load(os.path.join(folder, name + ".npy"), mmap_mode="r")
+    idx = np.sort(np.asarray(ld("order")[i0:i1]))
+    k = np.ascontiguousarray(ld("k")[idx])
+    v = np.ascontiguousarray(ld("v")[idx])
+    slots = (np.asarray(ld("slots")[idx]).astype(np.int64) - 4 * p0).astype(np.int32)
+    gk = np.asarray(ld("pool_k")[p0:p1])
+    gv = np.asarray(ld("pool_v")[p0:p1])
+    shape = gk.shape
+    if e4m3:
+        kc = np.full(shape, SENTINEL, np.uint8)
+        vc = np.full(shape, SENTINEL, np.uint8)
+        if idx.size:
+            oracle.append_e4m3(k, v, slots, kc, vc, ks, vs)
+        dk, dv = kc != gk, vc != gv
+    else:
+        fill = np.uint16(SENTINEL * 0x101)
+        kc = np.full(shape, fill, np.uint16).view(np.float16)
+        vc = np.full(shape, fill, np.uint16).view(np.float16)
+        if idx.size:
+            oracle.append_fp16(k, v, slots, kc, vc)
+        dk, dv = kc.view(np.uint16) != gk.view(np.uint16), vc.view(np.uint16) != gv.view(np.uint16)
+    bad_pages = np.flatnonzero(dk.reshape(shape[0], -1).any(1) | dv.reshape(shape[0], -1).any(1))
+    return p0, int(dk.sum()), int(dv.sum()), int(p0 + bad_pages[0]) if bad_pages.size else -1
 
 
 def oracle_group_fp8(q_group, k_seq, v_seq, L, ks, vs):

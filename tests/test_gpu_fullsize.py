@@ -1,11 +1,19 @@
 """GPU parity at the workloads' full sizes, in the launch configuration the
-benchmark times, on sampled (layer, sequence, query head) units that the
-oracle recomputes one by one from the same seeded fp16 inputs.
+benchmark times.
 
-For each sampled unit: the E4M3 bytes the GPU wrote for that sequence's kv
-head must equal the oracle's quantisation bit for bit, and the attention
-output must match the oracle within atol 2e-3 / rtol 1e-2.  The oracle
-computes its own calibrated scale, which must equal the GPU's.
+Pools: every byte of the K and V pools -- the quantised (or, for the fp16
+arm, copied) tokens and the sentinel of every slot and page that no token
+owns -- must equal pools the oracle fills from the same fp16 inputs, for the
+decode workload (both arms), decode at 32K context, the long-context
+workload and two layers each of the 24-layer verify and mixed workloads
+(PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path",
+section Changes: the main K/V cache is stored in calibrated E4M3).
+
+Attention: sampled (layer, sequence, query head) units that the oracle
+recomputes one by one from the same seeded fp16 inputs must match within
+atol 2e-3 / rtol 1e-2; the E4M3 K and V bytes of each sampled sequence's kv
+head are compared again there.  The oracle computes its own calibrated
+scale, which must equal the GPU's.
 
 The oracle runs in a process pool started with "spawn" (workers never
 inherit a CUDA context).
@@ -13,6 +21,8 @@ inherit a CUDA context).
 import concurrent.futures as cf
 import multiprocessing as mp
 import os
+import shutil
+import tempfile
 
 import numpy as np
 import pytest
@@ -27,13 +37,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+WORKERS = max(2, min(16, os.cpu_count() or 2))
+
+
 @pytest.fixture(scope="module")
 def pool():
     build.build()
     kvq.load()
     oracle.build()
-    ex = cf.ProcessPoolExecutor(max_workers=max(2, min(16, os.cpu_count() or 2)),
-                                mp_context=mp.get_context("spawn"))
+    ex = cf.ProcessPoolExecutor(max_workers=WORKERS, mp_context=mp.get_context("spawn"))
     yield ex
     ex.shutdown(cancel_futures=True)
 
@@ -65,8 +77,9 @@ class Layer:
             app = lambda k, v, s: kvq.kv_append_e4m3(k, v, s, self.kc, self.vc, self.ks, self.vs, err)
         else:
             self.ks = self.vs = 1.0
-            self.kc = torch.zeros(shape, dtype=torch.float16, device=DEV)
-            self.vc = torch.zeros(shape, dtype=torch.float16, device=DEV)
+            self.kc = torch.empty(shape, dtype=torch.float16, device=DEV)
+            self.kc.view(torch.int16).fill_(int(np.int16(np.uint16(P.SENTINEL * 0x101).view(np.int16))))
+            self.vc = self.kc.clone()
             app = lambda k, v, s: kvq.kv_append_fp16(k, v, s, self.kc, self.vc, err)
         # the cached history, then this step's tokens (one append call each, as a step does)
         for seq, pos in (inputs.history_tokens(w, lay), inputs.step_tokens(w, lay)):
@@ -126,11 +139,11 @@ class Layer:
         return ex.submit(P.oracle_unit, q_rows, k_seq, v_seq, L, ks, vs, self.e4m3, lst)
 
     def gpu_pool_rows(self, b, g):
-        """E4M3 bytes the GPU stored for sequence b, kv head g, positions 0..L-1."""
+        """E4M3 K and V bytes the GPU stored for sequence b, kv head g, positions 0..L-1."""
         L = int(self.lay.lens[b])
         pos = torch.arange(L, device=DEV)
         pages = self.bt[b, pos // 4].long()
-        return self.kc[pages, g, pos % 4].cpu().numpy()
+        return self.kc[pages, g, pos % 4].cpu().numpy(), self.vc[pages, g, pos % 4].cpu().numpy()
 
 
 def _check(layer_obj, ex, units, tag):
@@ -139,16 +152,84 @@ def _check(layer_obj, ex, units, tag):
     got_all = layer_obj.out.float().cpu().numpy()
     bad = []
     for b, h, f in futs:
-        ref, flags, pool_k = f.result()
+        ref, flags, pool_k, pool_v = f.result()
         assert flags == 0
         got = got_all[b, :, h, :]
         ok = P.tolerance_ok(got, ref)
         if not ok.all():
             bad.append((b, h, float(np.abs(got - ref).max())))
         if layer_obj.e4m3 and h % layer_obj.w.group == 0:
-            assert np.array_equal(layer_obj.gpu_pool_rows(b, h // layer_obj.w.group), pool_k), \
-                f"{tag}: pool bytes differ for sequence {b}, kv head {h // layer_obj.w.group}"
+            gk, gv = layer_obj.gpu_pool_rows(b, h // layer_obj.w.group)
+            assert np.array_equal(gk, pool_k), \
+                f"{tag}: K pool bytes differ for sequence {b}, kv head {h // layer_obj.w.group}"
+            assert np.array_equal(gv, pool_v), \
+                f"{tag}: V pool bytes differ for sequence {b}, kv head {h // layer_obj.w.group}"
     assert not bad, f"{tag}: {len(bad)} units outside tolerance, e.g. {bad[:4]}"
+
+
+def _scratch_dir(need_bytes):
+    """A folder for the memory-mapped hand-over to the oracle workers: shared
+    memory when it has room, else the temporary directory."""
+    for base in ("/dev/shm", tempfile.gettempdir()):
+        try:
+            if os.path.isdir(base) and shutil.disk_usage(base).free > 1.25 * need_bytes:
+                return tempfile.mkdtemp(prefix="kvq_pools_", dir=base)
+        except OSError:
+            continue
+    return tempfile.mkdtemp(prefix="kvq_pools_")
+
+
+def _check_pools(layer_obj, ex, tag, shards_per_worker=4):
+    """Every byte of the layer's K and V pools against the oracle's fill of
+    sentinel pools with every token the layer appended (the cached history,
+    this step's tokens and, for the mixed batch, the prefill chunk), sharded
+    over the process pool by page range."""
+    L = layer_obj
+    w, lay = L.w, L.lay
+    lens = lay.lens.astype(np.int64)
+    seq = np.repeat(np.arange(w.batch), lens)
+    pos = np.arange(int(lens.sum())) - np.repeat(L.offs, lens)
+    slots = inputs.slot_mapping(lay.block_tables, seq, pos)          # token row r of L.k -> its slot
+    parts = [(L.k, L.v, slots)]
+    if L.prefill is not None:
+        parts.append((L.prefill[0], L.prefill[1], inputs.prefill_slots(lay)[: w.prefill_chunk]))
+    T = sum(int(p[2].size) for p in parts)
+    row_bytes = w.num_kv_heads * w.head_dim * 2
+    pool_bytes = L.kc.numel() * L.kc.element_size()
+    folder = _scratch_dir(2 * T * row_bytes + 2 * pool_bytes + 12 * T)
+    try:
+        fk = np.lib.format.open_memmap(os.path.join(folder, "k.npy"), "w+", np.float16,
+                                       (T, w.num_kv_heads, w.head_dim))
+        fv = np.lib.format.open_memmap(os.path.join(folder, "v.npy"), "w+", np.float16,
+                                       (T, w.num_kv_heads, w.head_dim))
+        all_slots = np.concatenate([p[2] for p in parts]).astype(np.int32)
+        t0 = 0
+        for k, v, sl in parts:
+            n = int(sl.size)
+            fk[t0:t0 + n] = k[:n].cpu().numpy()
+            fv[t0:t0 + n] = v[:n].cpu().numpy()
+            t0 += n
+        fk.flush()
+        fv.flush()
+        del fk, fv
+        np.save(os.path.join(folder, "slots.npy"), all_slots)
+        pages = all_slots.astype(np.int64) // 4
+        order = np.argsort(pages, kind="stable")
+        np.save(os.path.join(folder, "order.npy"), order)
+        np.save(os.path.join(folder, "pool_k.npy"), L.kc.cpu().numpy())
+        np.save(os.path.join(folder, "pool_v.npy"), L.vc.cpu().numpy())
+        Ptot = lay.num_pages
+        n = max(1, min(Ptot, shards_per_worker * WORKERS))
+        p_edges = np.linspace(0, Ptot, n + 1).astype(np.int64)
+        i_edges = np.searchsorted(pages[order], p_edges)
+        ks, vs = L.oracle_scales()
+        futs = [ex.submit(P.oracle_pool_shard, folder, int(p_edges[j]), int(p_edges[j + 1]),
+                          int(i_edges[j]), int(i_edges[j + 1]), ks, vs, L.e4m3) for j in range(n)]
+        bad = [r for r in (f.result() for f in futs) if r[1] or r[2]]
+    finally:
+        shutil.rmtree(folder, ignore_errors=True)
+    assert not bad, (f"{tag}: pools differ from the oracle's in {len(bad)} of {n} page shards, e.g. "
+                     f"(first page, K bytes, V bytes) {[(r[3], r[1], r[2]) for r in bad[:4]]}")
 
 
 def _sample(rng, w, n):
@@ -166,6 +247,7 @@ def test_decode_all_units(pool):
     assert L.S == 4
     units = [(b, h) for b in range(w.batch) for h in range(w.num_q_heads)]
     _check(L, pool, units, "decode e4m3")
+    _check_pools(L, pool, "decode e4m3")
     # the bitcast decoder in the same launch configuration: bit-identical output
     Lb = Layer(w, 0, lay, bitcast=True)
     assert torch.equal(Lb.out.view(torch.int16), L.out.view(torch.int16))
@@ -175,6 +257,7 @@ def test_decode_fp16_arm(pool):
     w = inputs.get("decode")
     L = Layer(w, 0, inputs.page_layout(w), e4m3=False)
     _check(L, pool, _sample(np.random.default_rng(1), w, 96), "decode fp16")
+    _check_pools(L, pool, "decode fp16")
 
 
 def test_decode_32k(pool):
@@ -182,6 +265,7 @@ def test_decode_32k(pool):
     L = Layer(w, 0, inputs.page_layout(w))
     assert L.S == 8
     _check(L, pool, _sample(np.random.default_rng(2), w, 48), "decode32k")
+    _check_pools(L, pool, "decode32k")
 
 
 def test_long_context(pool):
@@ -190,6 +274,7 @@ def test_long_context(pool):
     L = Layer(w, 0, inputs.page_layout(w))
     assert L.S == 64
     _check(L, pool, _sample(np.random.default_rng(3), w, 12), "long")
+    _check_pools(L, pool, "long")
 
 
 def test_verify_24_layers(pool):
@@ -202,6 +287,8 @@ def test_verify_24_layers(pool):
         L = Layer(w, layer, lay)
         seen.add((L.ks, L.vs))
         _check(L, pool, _sample(rng, w, 11), f"verify layer {layer}")
+        if layer in (0, w.layers - 1):
+            _check_pools(L, pool, f"verify layer {layer}")
         del L
         torch.cuda.empty_cache()
     assert len(seen) == w.layers          # per-layer scales really differ
@@ -220,6 +307,8 @@ def test_mixed_24_layers(pool):
         L = Layer(w, layer, lay)
         units = _sample(rng, w, 11)
         _check(L, pool, units, f"mixed layer {layer}")
+        if layer in (0, w.layers - 1):
+            _check_pools(L, pool, f"mixed layer {layer}")   # includes the prefill chunk
         # the prefill chunk's quantised bytes, one kv head per layer
         g = layer % w.num_kv_heads
         ks, _ = L.oracle_scales()
