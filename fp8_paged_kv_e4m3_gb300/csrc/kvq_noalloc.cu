@@ -28,23 +28,69 @@ __device__ __align__(256) unsigned char kvq_noalloc_scratch[KVQ_NOALLOC_SCRATCH_
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// The looked-up address of the scratch buffer on one device, and the context
+// it belongs to.  A device reset (cudaDeviceReset) ends the primary context;
+// the runtime then loads the module again in a new context, where the buffer
+// may sit elsewhere, so an address is used only in the context it was looked
+// up in.
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Driver calls resolved through the runtime (no link against the driver
+// library): the current context and its process-unique id.
+using CtxGetCurrentFn = int (*)(void **);
+using CtxGetIdFn = int (*)(void *, unsigned long long *);
+std::once_flag g_driver_once;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+bool current_context_id(unsigned long long *id)
+{
+    std::call_once(g_driver_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(fn);
+    });
+    void *ctx = nullptr;
+    if (!g_ctx_get_current || !g_ctx_get_id) return false;
+    if (g_ctx_get_current(&ctx) != 0 || !ctx) return false;
+    return g_ctx_get_id(ctx, id) == 0;
+}
 
 // Device address of the scratch buffer on the current device.  The name
 // kvq_noalloc_scratch in host code is only a handle for the runtime, not an
 // address a kernel may use; the address comes from cudaGetSymbolAddress,
-// looked up once per device with that device current.
+// looked up with the device current, once per device and context (the
+// first call on a device, and the first after a device reset).
 int scratch_for_current_device(void **out)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+    unsigned long long ctx = 0;
+    if (!current_context_id(&ctx)) {
+        // no context current on this thread yet: cudaSetDevice makes the
+        // device's primary context current (and allocates nothing)
+        if (cudaSetDevice(dev) != cudaSuccess || !current_context_id(&ctx)) return KVQ_ERR_CUDA;
+    }
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+    ScratchEntry &e = g_scratch[dev];
+    if (!e.ptr || e.ctx_id != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, kvq_noalloc_scratch) != cudaSuccess || !p) return KVQ_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        e.ptr = p;
+        e.ctx_id = ctx;
     }
-    *out = g_scratch_ptr[dev];
+    *out = e.ptr;
     return KVQ_OK;
 }
 
