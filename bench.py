@@ -1,29 +1,34 @@
 """Benchmark: calibrated E4M3 paged decode attention on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|decode32k|long] [--no-cpu-baseline]
+                    [--workload decode|decode32k|long|verify|mixed|prefill]
+                    [--no-cpu-baseline] [--no-fp16] [--no-workloads]
 
-One step = one pass of the whole hot path over one batch: quantise-on-append
-of this step's new K/V tokens into the page-4 cache, split-K decode attention
-over the paged cache, and the log-sum-exp combine.  Inputs are seeded
-synthetic tensors (see fp8_paged_kv_e4m3_gb300.inputs).  The headline
-workload is batch 32 x 4096 context, 32 query / 4 kv heads, head_dim 128,
-q_len 1, split-K 4.
+One step = one pass of the whole hot path over one batch, for every layer
+of the workload: quantise-on-append of the step's new K/V tokens into the
+layer's page-4 cache, split-K decode / verify attention over it, and the
+log-sum-exp combine.  Inputs are seeded synthetic tensors (see
+fp8_paged_kv_e4m3_gb300.inputs).  The headline workload is batch 32 x 4096
+context, 32 query / 4 kv heads, head_dim 128, q_len 1, split-K 4, one layer.
 
 Reported (one JSON line on rank 0): achieved HBM GB/s of algorithmic bytes
 per step (KV bytes read + Q + output + block tables + append traffic; the
 FP32 split workspace is not counted), its fraction of the measured HBM
 peak, sequence-steps/s, and the same for the fp16-KV arm with the
 fp16/E4M3 step-time ratio.  L2 is defeated by rotating through copies of
-the KV pools whose total exceeds twice the L2 size.
+the KV pools whose total exceeds twice the L2 size (the 24-layer steps move
+far more than that by themselves).  Without --workload, the line also
+carries a "workloads" object with the same figures for decode at 32K
+context, the long-context batch, the 24-layer MTP3 verify step, the
+24-layer mixed step and the chunked-prefill call.
 
 N > 1 (torchrun): every rank runs an independent replica on its own GPU
 with its own seeded batch (the path shards by sequence with no exchange),
 timing is max-over-ranks, and the value is the aggregate.
 
 --impl reference: the CPU oracle (the only other implementation of the
-method here) timed on this host's cores on a bounded sample of the same
-workload, printed in the same format with "impl": "reference".
+method here) timed on this host's cores on the step's (sequence, kv head)
+units, printed in the same format with "impl": "reference".
 """
 from __future__ import annotations
 
@@ -150,8 +155,9 @@ def describe(w, splits) -> str:
     split = f"split-K {splits}" + (f" of {w.split_pages} pages" if w.split_pages else "")
     if not w.lens.startswith("fixed"):
         split += ", longest first"
+    layers = "one layer" if w.layers <= 1 else f"{w.layers} layers per step, each with its own pools and scales"
     return (f"{w.name}: batch {w.batch}, {ctx}, {w.num_q_heads} q / {w.num_kv_heads} kv heads, "
-            f"head_dim {w.head_dim}, q_len {w.q_len}, {split}, page 4{extra}; one layer")
+            f"head_dim {w.head_dim}, q_len {w.q_len}, {split}, page 4{extra}; {layers}")
 
 
 # ---------------------------------------------------------------------------
@@ -226,7 +232,13 @@ class ClockSampler:
 # the GPU arm
 
 class Arm:
-    """One arm (E4M3 or fp16 KV) of the decode step, with rotating pool copies."""
+    """One arm (E4M3 or fp16 KV) of the step, with rotating pool copies.
+
+    A workload of several layers (the 24-layer verify and mixed batches)
+    gives every layer its own seeded K/V, queries, calibrated scales and
+    pools; the block tables, context lengths and top-k lists are shared, as
+    every layer of one model attends the same sequences.  A step runs the
+    append, attention and combine of every layer in turn."""
 
     def __init__(self, w, e4m3: bool, dev, seed_rank: int, l2_bytes: int):
         import torch
@@ -234,36 +246,25 @@ class Arm:
         self.torch, self.kvq, self.w, self.e4m3, self.dev = torch, kvq, w, e4m3, dev
         w = rank_workload(w, seed_rank)
         self.w = w
+        self.layers = max(1, w.layers)
         lay = inputs.page_layout(w)
         self.lay = lay
         lens = lay.lens.astype(np.int64)
         total = int(lens.sum())
         offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
-        k = inputs.kv_tokens(w, 0, total, "k", device=dev)
-        v = inputs.kv_tokens(w, 0, total, "v", device=dev)
-        self.q = inputs.queries(w, 0, device=dev)
-        if e4m3:
-            self.ks = kvq.calibrate_scale(inputs.calibration_draw(w, 0, "k", device=dev))
-            self.vs = kvq.calibrate_scale(inputs.calibration_draw(w, 0, "v", device=dev))
-            kvq.validate_scales([self.ks], [self.vs])
         hs, hp = inputs.history_tokens(w, lay)
         ss, sp = inputs.step_tokens(w, lay)
         hist_slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, hs, hp)).to(dev)
         hist_rows = torch.from_numpy(offs[hs] + hp).to(dev)
-        self.step_slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, ss, sp)).to(dev)
+        step_slots = torch.from_numpy(inputs.slot_mapping(lay.block_tables, ss, sp)).to(dev)
         step_rows = torch.from_numpy(offs[ss] + sp).to(dev)
-        self.k_new = k[step_rows].contiguous()        # [B * q_len, Hkv, D], rows in (b, i) order
-        self.v_new = v[step_rows].contiguous()
         self.prefill = w.prefill_chunk > 0
         if self.prefill:
             # the step also appends a new sequence's prefill chunk (mixed
             # batches), in the same append call as the decode tokens
-            pk = inputs.prefill_tokens(w, 0, "k", device=dev)
-            pv = inputs.prefill_tokens(w, 0, "v", device=dev)
             pslots = torch.from_numpy(inputs.prefill_slots(lay)[: w.prefill_chunk]).to(dev)
-            self.k_new = torch.cat([self.k_new, pk]).contiguous()
-            self.v_new = torch.cat([self.v_new, pv]).contiguous()
-            self.step_slots = torch.cat([self.step_slots, pslots]).contiguous()
+            step_slots = torch.cat([step_slots, pslots]).contiguous()
+        self.step_slots = step_slots
         ti, tl = inputs.topk_lists(w, lay.lens)
         self.topk_idx = None if ti is None else torch.from_numpy(ti).to(dev)
         self.topk_lens = None if tl is None else torch.from_numpy(tl).to(dev)
@@ -273,25 +274,50 @@ class Arm:
         shape = (lay.num_pages, w.num_kv_heads, 4, w.head_dim)
         dt = torch.uint8 if e4m3 else torch.float16
         pool_bytes = 2 * math.prod(shape) * (1 if e4m3 else 2)
-        self.copies = max(1, math.ceil(2 * l2_bytes / pool_bytes))
-        self.pools = []
-        kh, vh = k[hist_rows].contiguous(), v[hist_rows].contiguous()
-        for _ in range(self.copies):
-            kc = torch.zeros(shape, dtype=dt, device=dev)
-            vc = torch.zeros(shape, dtype=dt, device=dev)
-            self._append(kh, vh, hist_slots, kc, vc)
-            self.pools.append((kc, vc))
-        del k, v, kh, vh
-        self.p = kvq.attn_params(self.q, w.num_kv_heads, self.bt.shape[1], w.num_splits,
+        self.copies = max(1, math.ceil(2 * l2_bytes / (pool_bytes * self.layers)))
+        # per layer: queries, the step's new K/V rows, scales; per (copy, layer): pools
+        self.q, self.k_new, self.v_new, self.ks, self.vs = [], [], [], [], []
+        self.pools = [[None] * self.layers for _ in range(self.copies)]
+        for l in range(self.layers):
+            k = inputs.kv_tokens(w, l, total, "k", device=dev)
+            v = inputs.kv_tokens(w, l, total, "v", device=dev)
+            self.q.append(inputs.queries(w, l, device=dev))
+            ks = vs = 1.0
+            if e4m3:
+                ks = kvq.calibrate_scale(inputs.calibration_draw(w, l, "k", device=dev))
+                vs = kvq.calibrate_scale(inputs.calibration_draw(w, l, "v", device=dev))
+            self.ks.append(ks)
+            self.vs.append(vs)
+            kn, vn = k[step_rows], v[step_rows]           # [B * q_len, Hkv, D], rows in (b, i) order
+            if self.prefill:
+                kn = torch.cat([kn, inputs.prefill_tokens(w, l, "k", device=dev)])
+                vn = torch.cat([vn, inputs.prefill_tokens(w, l, "v", device=dev)])
+            self.k_new.append(kn.contiguous())
+            self.v_new.append(vn.contiguous())
+            kh, vh = k[hist_rows].contiguous(), v[hist_rows].contiguous()
+            del k, v
+            for c in range(self.copies):
+                kc = torch.zeros(shape, dtype=dt, device=dev)
+                vc = torch.zeros(shape, dtype=dt, device=dev)
+                self._append(l, kh, vh, hist_slots, kc, vc)
+                self.pools[c][l] = (kc, vc)
+            del kh, vh
+        if e4m3:
+            kvq.validate_scales(self.ks, self.vs)
+        self.p = kvq.attn_params(self.q[0], w.num_kv_heads, self.bt.shape[1], w.num_splits,
                                  0 if self.topk_idx is None else self.topk_idx.shape[2],
                                  split_pages=w.split_pages)
         self.S = kvq.num_splits(self.p)
+        # one workspace serves every layer: each layer's combine reads it before the
+        # next layer's attention writes it (stream order)
         self.ws = kvq.alloc_workspace(self.p, dev)
-        self.out = torch.empty_like(self.q)
+        self.out = [torch.empty_like(self.q[0]) for _ in range(self.layers)]
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.pool_bytes = pool_bytes
-        self.bytes = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, self.topk_np)
-        self.launches = 3   # kernels of one step: append, attention, combine
+        per_layer = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, self.topk_np)
+        self.bytes = {"step": per_layer["step"] * self.layers, "attention_kernel": per_layer["attention_kernel"],
+                      "layer": per_layer["step"]}
+        self.launches = 3 * self.layers   # kernels of one step: append, attention, combine per layer
         self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
         self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
         self.fp8_qk = False    # tcgen05 kernel: fp16 scores (default) or the FP8 score variant
@@ -300,19 +326,19 @@ class Arm:
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
         torch.cuda.synchronize(dev)
 
-    def _append(self, k, v, slots, kc, vc):
+    def _append(self, l, k, v, slots, kc, vc):
         if self.e4m3:
-            self.kvq.kv_append_e4m3(k, v, slots, kc, vc, self.ks, self.vs, None)
+            self.kvq.kv_append_e4m3(k, v, slots, kc, vc, self.ks[l], self.vs[l], None)
         else:
             self.kvq.kv_append_fp16(k, v, slots, kc, vc, None)
 
-    def _attention(self, kc, vc, q=None, bt=None, cl=None):
+    def _attention(self, l, kc, vc, q=None, bt=None, cl=None):
         kvq = self.kvq
-        q = self.q if q is None else q
+        q = self.q[l] if q is None else q
         bt = self.bt if bt is None else bt
         cl = self.cl if cl is None else cl
         if self.e4m3:
-            kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks, self.vs, self.ws,
+            kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks[l], self.vs[l], self.ws,
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
                                                err_flag=self.err, split_pages=self.w.split_pages,
                                                bitcast_decode=self.bitcast, mma_sync=self.mma_sync,
@@ -324,13 +350,14 @@ class Arm:
                                                longest_first=self.longest_first)
 
     def step(self, i):
-        """One step on pool copy i: append of the step's tokens, split-K
-        attention, log-sum-exp combine (three launches chained with
-        programmatic dependent launch)."""
-        kc, vc = self.pools[i % self.copies]
-        self._append(self.k_new, self.v_new, self.step_slots, kc, vc)
-        self._attention(kc, vc)
-        self.kvq.lse_combine(self.ws, self.out, self.p)
+        """One step on pool copy i: for every layer, the append of the step's
+        tokens, split-K attention and the log-sum-exp combine (three launches
+        per layer, chained with programmatic dependent launch)."""
+        for l in range(self.layers):
+            kc, vc = self.pools[i % self.copies][l]
+            self._append(l, self.k_new[l], self.v_new[l], self.step_slots, kc, vc)
+            self._attention(l, kc, vc)
+            self.kvq.lse_combine(self.ws, self.out[l], self.p)
 
     def capture(self):
         """CUDA graphs of the step: one per pool copy holding one step, and
@@ -347,10 +374,12 @@ class Arm:
             with torch.cuda.graph(g):
                 self.step(r)
             graphs.append(g)
-        many = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(many):
-            for r in range(GRAPH_STEPS):
-                self.step(r)
+        many = None
+        if self.layers == 1:                     # a multi-layer step is already a long graph
+            many = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(many):
+                for r in range(GRAPH_STEPS):
+                    self.step(r)
         torch.cuda.synchronize(self.dev)
         self.graphs, self.many = graphs, many
 
@@ -370,9 +399,10 @@ class Arm:
         torch.cuda.synchronize(self.dev)
         torch.cuda.nvtx.range_push("kvq_timed")
         start.record()
-        for _ in range(steps // GRAPH_STEPS):
+        n_many = steps // GRAPH_STEPS if many is not None else 0
+        for _ in range(n_many):
             many.replay()
-        for i in range(steps % GRAPH_STEPS):
+        for i in range(steps - n_many * GRAPH_STEPS):
             graphs[i % self.copies].replay()
         end.record()
         torch.cuda.nvtx.range_pop()
@@ -383,21 +413,26 @@ class Arm:
         return start.elapsed_time(end)
 
     def time_kernel(self, steps, warmup):
-        """Average duration of the split attention kernel: `steps` back-to-back
-        launches over the rotating pool copies, between two events on the
-        launching stream (the queue stays full, so host launch time is hidden)."""
+        """Average duration of one attention launch (one layer): `steps`
+        back-to-back launches over the rotating pool copies and layers,
+        between two events on the launching stream (the queue stays full, so
+        host launch time is hidden)."""
         torch = self.torch
-        run = self._attention
+        n = self.copies * self.layers
+
+        def run(j):
+            c, l = divmod(j % n, self.layers)
+            kc, vc = self.pools[c][l]
+            self._attention(l, kc, vc)
+
         for i in range(warmup):
-            kc, vc = self.pools[i % self.copies]
-            run(kc, vc)
+            run(i)
         torch.cuda.synchronize(self.dev)
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.nvtx.range_push("kvq_kernel_timed")
         start.record()
         for i in range(steps):
-            kc, vc = self.pools[(warmup + i) % self.copies]
-            run(kc, vc)
+            run(warmup + i)
         end.record()
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(self.dev)
@@ -419,19 +454,22 @@ class Arm:
         return tuple(float(x) for x in np.percentile(d, [10, 50, 90]))
 
     def time_e2e(self, steps, warmup):
-        """Every step: the H2D copy of the step's inputs (Q, the new K/V,
-        slots, block tables, lengths; packed in one pinned host buffer, so one
-        copy), the step through the public calls, and a D2H read of the
-        output.  Returns (pipelined ms, serial ms, H2D bytes, D2H bytes):
-        pipelined = the copies on their own streams, overlapping the
-        neighbouring steps' compute (two input and two output buffers);
-        serial = copies and compute in one graph per step on one stream."""
+        """Every step: the H2D copy of the step's inputs (every layer's Q and
+        new K/V, the slots, block tables and lengths; packed in one pinned
+        host buffer, so one copy), the step through the public calls, and a
+        D2H read of every layer's output.  Returns (pipelined ms, serial ms,
+        H2D bytes, D2H bytes): pipelined = the copies on their own streams,
+        overlapping the neighbouring steps' compute (two input and two output
+        buffers); serial = copies and compute in one graph per step on one
+        stream."""
         torch = self.torch
-        src = [("q", self.q), ("k", self.k_new), ("v", self.v_new), ("slots", self.step_slots),
-               ("bt", self.bt), ("cl", self.cl)]
+        src = [("slots", self.step_slots), ("bt", self.bt), ("cl", self.cl)]
+        for l in range(self.layers):
+            src += [(f"q{l}", self.q[l]), (f"k{l}", self.k_new[l]), (f"v{l}", self.v_new[l])]
         sets = [staged_buffers(torch, src, self.dev) for _ in range(2)]
-        outs = [torch.empty_like(self.out) for _ in range(2)]
-        out_host = [torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory() for _ in range(2)]
+        oshape = (self.layers,) + tuple(self.out[0].shape)
+        outs = [torch.empty(oshape, dtype=self.out[0].dtype, device=self.dev) for _ in range(2)]
+        out_host = [torch.empty(oshape, dtype=self.out[0].dtype).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for _, t in src)
         d2h = out_host[0].numel() * out_host[0].element_size()
 
@@ -440,10 +478,11 @@ class Arm:
 
         def compute(i):
             dev = sets[i % 2][1]
-            kc, vc = self.pools[i % self.copies]
-            self._append(dev["k"], dev["v"], dev["slots"], kc, vc)
-            self._attention(kc, vc, dev["q"], dev["bt"], dev["cl"])
-            self.kvq.lse_combine(self.ws, outs[i % 2], self.p)
+            for l in range(self.layers):
+                kc, vc = self.pools[i % self.copies][l]
+                self._append(l, dev[f"k{l}"], dev[f"v{l}"], dev["slots"], kc, vc)
+                self._attention(l, kc, vc, dev[f"q{l}"], dev["bt"], dev["cl"])
+                self.kvq.lse_combine(self.ws, outs[i % 2][l], self.p)
 
         def copy_out(p):
             out_host[p].copy_(outs[p], non_blocking=True)
@@ -454,7 +493,8 @@ class Arm:
             copy_out(i % 2)
 
         ncap = self.copies * 2 // math.gcd(self.copies, 2)   # pool copies and buffer sets both cycle
-        piped = pipelined_timed(torch, self.dev, copy_in, compute, copy_out, ncap, steps, warmup)
+        piped = pipelined_timed(torch, self.dev, copy_in, compute, copy_out, ncap, steps, warmup,
+                                graph_steps=GRAPH_STEPS if self.layers == 1 else ncap)
         serial = replay_timed(torch, self.dev, one, ncap, steps, warmup)
         return piped, serial, h2d, d2h
 
@@ -479,7 +519,7 @@ def staged_buffers(torch, src, device):
     return host, dev
 
 
-def pipelined_timed(torch, device, copy_in, compute, copy_out, period, steps, warmup):
+def pipelined_timed(torch, device, copy_in, compute, copy_out, period, steps, warmup, graph_steps=GRAPH_STEPS):
     """Steps with their copies on their own streams, as a serving loop
     overlaps them: copy_in(p) (H2D into input set p), compute(i) (input set
     and output buffer i % 2) and copy_out(p) (D2H of output buffer p).  Step
@@ -487,9 +527,10 @@ def pipelined_timed(torch, device, copy_in, compute, copy_out, period, steps, wa
     out; a buffer is reused only after the step two back has finished with
     it.  A run of n steps (n a multiple of `period`, about GRAPH_STEPS) is
     captured in one CUDA graph with the three streams forked from and joined
-    to the capture stream, so the host issues one launch per n steps.
+    to the capture stream, so the host issues one launch per n steps
+    (n about graph_steps).
     Returns the average ms per step over the replays covering `steps`."""
-    n = period * max(1, round(GRAPH_STEPS / period))
+    n = period * max(1, round(graph_steps / period))
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     for i in range(2):
         copy_in(i % 2)
@@ -562,57 +603,153 @@ def replay_timed(torch, device, one, copies, steps, warmup):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 
-def oracle_sample_time(w, units: int, seed: int = 0):
-    """Time the oracle on `units` (sequence, kv head) units of the workload:
-    append of the step's tokens into the oracle's own pool, then binary64
-    attention of the unit's query heads.  Pools for the cached history are
-    built beforehand (not timed).  Returns (seconds, algorithmic bytes)."""
-    import torch
-    import oracle
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def step_units(w):
+    """Every (sequence, kv head) unit of one layer of the workload's step."""
+    return [(b, g) for b in range(w.batch) for g in range(w.num_kv_heads)]
+
+
+_ORACLE_DATA = {}
+_ORACLE_BARRIER = None
+
+
+def _oracle_data(w):
+    """The workload's CPU-drawn K/V rows, layout and calibrated scales (layer
+    0), drawn once per process."""
     from fp8_paged_kv_e4m3_gb300 import inputs
-    lay = inputs.page_layout(w)
-    lens = lay.lens.astype(np.int64)
-    offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
-    rng = np.random.default_rng(1234 + seed)
-    picks = [(int(b), int(g)) for b, g in
-             zip(rng.integers(0, w.batch, units), rng.integers(0, w.num_kv_heads, units))]
-    q = inputs.queries(w, 0).numpy()
-    G = w.group
-    total_t = 0.0
+    import oracle
+    if w not in _ORACLE_DATA:
+        lay = inputs.page_layout(w)
+        lens = lay.lens.astype(np.int64)
+        total = int(lens.sum())
+        k = inputs.kv_tokens(w, 0, total, "k").numpy()
+        v = inputs.kv_tokens(w, 0, total, "v").numpy()
+        ks = oracle.calibrate_scale(inputs.calibration_draw(w, 0, "k").numpy())
+        vs = oracle.calibrate_scale(inputs.calibration_draw(w, 0, "v").numpy())
+        _ORACLE_DATA[w] = (lay, np.concatenate([[0], np.cumsum(lens)[:-1]]), k, v,
+                           inputs.queries(w, 0).numpy(), ks, vs)
+    return _ORACLE_DATA[w]
+
+
+def _oracle_units(w, picks, barrier_timeout=None):
+    """The oracle on (sequence, kv head) units of the step: untimed, each
+    unit's cached history appended into a pool of its own; then, timed, the
+    append of the step's tokens and the binary64 attention of the unit's
+    query heads.  With a barrier (the all-cores run) every worker starts its
+    timed part together.  Returns (t0, t1, algorithmic bytes)."""
+    import oracle
+    lay, offs, k, v, q, ks, vs = _oracle_data(w)
+    G, ql = w.group, w.q_len
+    prepared = []
     nbytes = 0
     for b, g in picks:
-        L = int(lens[b])
-        # regenerate only this sequence's rows: draw the layer once per call site
-        k = _seq_rows(w, "k", offs[b], L, g)
-        v = _seq_rows(w, "v", offs[b], L, g)
+        L = int(lay.lens[b])
+        ku = np.ascontiguousarray(k[offs[b]:offs[b] + L, g:g + 1])
+        vu = np.ascontiguousarray(v[offs[b]:offs[b] + L, g:g + 1])
         pages = (L + 3) // 4
         kc = np.zeros((pages, 1, 4, w.head_dim), np.uint8)
         vc = np.zeros_like(kc)
         slots = np.arange(L, dtype=np.int32)
-        oracle.append_e4m3(k[: L - w.q_len, None], v[: L - w.q_len, None], slots[: L - w.q_len],
-                           kc, vc, 0.01, 0.01)
-        bt = np.arange(pages, dtype=np.int32)[None]
+        oracle.append_e4m3(ku[: L - ql], vu[: L - ql], slots[: L - ql], kc, vc, ks, vs)
         qu = np.ascontiguousarray(q[b:b + 1, :, g * G:(g + 1) * G])
-        t0 = time.perf_counter()
-        oracle.append_e4m3(k[L - w.q_len:, None], v[L - w.q_len:, None], slots[L - w.q_len:],
-                           kc, vc, 0.01, 0.01)
-        oracle.attention(qu, kc, vc, bt, np.array([L], np.int32), 0.01, 0.01)
-        total_t += time.perf_counter() - t0
-        nbytes += 2 * L * w.head_dim + 2 * qu.nbytes + pages * 4 + w.q_len * w.head_dim * 6
-    return total_t, nbytes, len(picks)
+        prepared.append((L, ku, vu, slots, kc, vc, qu, np.arange(pages, dtype=np.int32)[None]))
+        nbytes += 2 * L * w.head_dim + 2 * qu.nbytes + pages * 4 + ql * w.head_dim * 6
+    if _ORACLE_BARRIER is not None and barrier_timeout:
+        _ORACLE_BARRIER.wait(barrier_timeout)
+    t0 = time.perf_counter()
+    for L, ku, vu, slots, kc, vc, qu, bt in prepared:
+        oracle.append_e4m3(ku[L - ql:], vu[L - ql:], slots[L - ql:], kc, vc, ks, vs)
+        oracle.attention(qu, kc, vc, bt, np.array([L], np.int32), ks, vs)
+    t1 = time.perf_counter()
+    return t0, t1, nbytes
 
 
-_SEQ_CACHE = {}
+def _oracle_pool_init(barrier):
+    """Worker set-up: one thread per worker process (the oracle is single-
+    threaded; idle library threads spinning after the input draw would take
+    cores from the other workers' timed parts)."""
+    global _ORACLE_BARRIER
+    _ORACLE_BARRIER = barrier
+    os.environ["OMP_NUM_THREADS"] = "1"
+    import torch
+    torch.set_num_threads(1)
 
 
-def _seq_rows(w, which, off, L, g):
-    from fp8_paged_kv_e4m3_gb300 import inputs
-    key = (w, which)
-    if key not in _SEQ_CACHE:
-        lay = inputs.page_layout(w)
-        total = int(lay.lens.astype(np.int64).sum())
-        _SEQ_CACHE[key] = inputs.kv_tokens(w, 0, total, which).numpy()
-    return np.ascontiguousarray(_SEQ_CACHE[key][off:off + L, g, :])
+class OracleTimer:
+    """The oracle timed on this host: one process per core (spawned, so no
+    worker inherits a CUDA context), each taking an equal share of the
+    units; their timed parts start together at a barrier, and the wall time
+    runs from the first start to the last end."""
+
+    def __init__(self, workers=None):
+        import concurrent.futures as cf
+        import multiprocessing as mp
+        self.workers = workers or host_cores()
+        ctx = mp.get_context("spawn")
+        self.barrier = ctx.Barrier(self.workers)
+        self.ex = cf.ProcessPoolExecutor(max_workers=self.workers, mp_context=ctx,
+                                         initializer=_oracle_pool_init, initargs=(self.barrier,))
+
+    def run(self, w, picks):
+        """(seconds, bytes) of the timed part over `picks`, on all workers."""
+        shares = [picks[i::self.workers] for i in range(self.workers)]
+        futs = [self.ex.submit(_oracle_units, w, sh, 600.0) for sh in shares]
+        res = [f.result() for f in futs]
+        return max(r[1] for r in res) - min(r[0] for r in res), sum(r[2] for r in res)
+
+    def close(self):
+        self.ex.shutdown(cancel_futures=True)
+
+
+def oracle_one_core(w, picks):
+    """(seconds, bytes) of the timed part over `picks` in this process."""
+    t0, t1, nb = _oracle_units(w, picks)
+    return t1 - t0, nb
+
+
+def cpu_baseline_decode(w):
+    """The oracle on every (sequence, kv head) unit of one layer of the step,
+    over all host cores and on one core."""
+    picks = step_units(w)
+    cores = host_cores()
+    timer = OracleTimer(cores)
+    try:
+        timer.run(w, picks[: timer.workers])              # start-up: spawn, import, draw the inputs
+        t_all, nb = timer.run(w, picks)
+    finally:
+        timer.close()
+    t_one, nb1 = oracle_one_core(w, picks)
+    return {"value": nb / t_all / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "value_1core": nb1 / t_one / 1e9, "seconds_all_cores": t_all, "seconds_1core": t_one,
+            "sample": f"all {len(picks)} (sequence, kv head) units of one layer of the {w.name} step "
+                      f"({w.group} query heads each): append of the step's tokens + binary64 attention; "
+                      f"{cores} spawned processes, timed parts started together; and the same on 1 core"}
 
 
 def library_splits(w, max_pages: int, sm_count: int) -> int:
@@ -646,31 +783,43 @@ def reference_config(w, world: int, sample: str) -> dict:
 
 
 def run_reference(args, w):
-    """The reference arm: the CPU oracle on a bounded sample per step."""
+    """The reference arm: the CPU oracle over all host cores, each step the
+    (sequence, kv head) units of one layer of the step -- all of them, or,
+    where that would take too long, a seeded sample sized so that the whole
+    run stays within about three minutes."""
     if w.name == "prefill":
         return run_reference_prefill(args, w)
-    per_unit_s, _, _ = oracle_sample_time(w, 1, seed=99)   # calibrate the sample size
-    budget_s = 120.0
-    units = max(1, int(budget_s / max(per_unit_s, 1e-3) / max(1, args.steps + args.warmup)))
-    units = min(units, w.batch * w.num_kv_heads)
-    for i in range(args.warmup):
-        oracle_sample_time(w, units, seed=i)
-    t = 0.0
-    nb = 0
-    for i in range(args.steps):
-        dt, b, _ = oracle_sample_time(w, units, seed=1000 + i)
-        t += dt
-        nb += b
+    picks = step_units(w)
+    timer = OracleTimer()
+    try:
+        t_cal, _ = timer.run(w, picks[: timer.workers])       # start-up, and one unit per worker
+        per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+        n = len(picks)
+        if t_cal * len(picks) / timer.workers > per_step_budget:
+            n = max(timer.workers, int(per_step_budget / max(t_cal, 1e-3) * timer.workers))
+        rng = np.random.default_rng(1234)
+        sample = picks if n >= len(picks) else [picks[i] for i in np.sort(rng.choice(len(picks), n, False))]
+        for _ in range(args.warmup):
+            timer.run(w, sample)
+        t = nb = 0.0
+        for _ in range(args.steps):
+            dt, b = timer.run(w, sample)
+            t += dt
+            nb += b
+    finally:
+        timer.close()
     gbs = nb / t / 1e9
-    sample = (f"{units} (sequence, kv head) units of the {w.name} workload per step "
-              f"(append of the step token + binary64 attention of {w.group} query heads)")
+    what = "all" if len(sample) == len(picks) else f"a seeded sample of {len(sample)} of the"
+    sample_txt = (f"{what} {len(picks)} (sequence, kv head) units of one layer of the {w.name} step per step "
+                  f"(append of the step's tokens + binary64 attention of {w.group} query heads), "
+                  f"{timer.workers} processes")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": reference_config(w, args.gpus, sample),
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "config": reference_config(w, args.gpus, sample_txt),
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": timer.workers, "kind": "oracle",
+                             "cpu_model": cpu_model(), "sample": sample_txt},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -852,21 +1001,22 @@ def describe_prefill(w) -> str:
             f"{w.num_kv_heads} kv heads, head_dim {w.head_dim}, page 4; one layer")
 
 
-def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
+def measure_prefill(args, w, dev, l2, rank, world, reduce_max, barrier, with_cpu=True):
+    """The prefill step (append of the chunk, then the prefill call) of both
+    arms; returns the JSON fields of its line (rank 0) without the clocks."""
     import torch
-    peak_gbs, _ = _peaks()
     tpeak, tkind = _tensor_peak()
     arm = PrefillArm(w, True, dev, rank, l2)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        if barrier:
-            barrier()
-        total_ms = reduce_max(arm.time(args.steps, args.warmup))
-        kern_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
+    if barrier:
+        barrier()
+    total_ms = reduce_max(arm.time(args.steps, args.warmup))
+    kern_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
     ms = total_ms / args.steps
     tflops = world * arm.flops / (ms * 1e-3) / 1e12
     achieved = arm.flops / (kern_ms * 1e-3) / 1e12
     e2e_ms, e2e_serial_ms, h2d, d2h = arm.time_e2e(max(3, args.steps // 4), 2)
     e2e_ms, e2e_serial_ms = reduce_max(e2e_ms), reduce_max(e2e_serial_ms)
+    copies, flops, launches = arm.copies, arm.flops, arm.launches
     fp16 = None
     if not args.no_fp16:
         del arm.sets
@@ -877,39 +1027,46 @@ def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
         fp16 = {"ms_per_step": ms16, "value": world * a16.flops / (ms16 * 1e-3) / 1e12,
                 "prefill_call_ms": k16}
         del a16
-        torch.cuda.empty_cache()
+    del arm
+    torch.cuda.empty_cache()
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and with_cpu and not args.no_cpu_baseline:
         t, fl = prefill_oracle_sample(w)
         cpu = {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "sample": f"3 rows (tokens 0, 4095, 8191) of the chunk, all {w.num_q_heads} query heads, "
                          f"binary64 attention, {t:.1f} s"}
+    return {
+        "metric": PREFILL_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": describe_prefill(w),
+                   "l2": f"rotating {copies} copies of chunk K/V, Q, pools and output (> 2 x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "flops_per_step": world * flops,
+        "fp16_arm": fp16,
+        "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": achieved / tpeak, "traffic": profiled_traffic("prefill_attn_kernel", w.name),
+                     "kernel": "kv_tile_kernel + prefill_attn_kernel (E4M3, tcgen05), one call",
+                     "peak_kind": tkind, "prefill_call_ms": kern_ms},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "copies": "own streams, overlapping the neighbouring steps' compute",
+                "serial_ms_per_step": e2e_serial_ms},
+        "gpu_launches": launches * args.steps,
+        "launch": "append, tile gather, attention per step (programmatic dependent launch); "
+                  "e2e: the compute of each step in a CUDA graph, H2D and D2H copies on their own streams",
+    }
+
+
+def run_prefill_bench(args, w, dev, l2, rank, world, reduce_max, barrier):
+    import torch
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        line = measure_prefill(args, w, dev, l2, rank, world, reduce_max, barrier)
     if rank == 0:
-        line = {
-            "metric": PREFILL_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
-            "data": "synthetic",
-            "config": {"workload": describe_prefill(w),
-                       "l2": f"rotating {arm.copies} copies of chunk K/V, Q, pools and output (> 2 x L2)",
-                       "parallelism": f"replicas x{world}"},
-            "flops_per_step": arm.flops,
-            "fp16_arm": fp16,
-            "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                         "frac": achieved / tpeak, "traffic": profiled_traffic("prefill_attn_kernel", w.name),
-                         "kernel": "kv_tile_kernel + prefill_attn_kernel (E4M3, tcgen05), one call",
-                         "peak_kind": tkind, "prefill_call_ms": kern_ms},
-            "cpu_baseline": cpu,
-            "e2e": {"value": world * arm.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "copies": "own streams, overlapping the neighbouring steps' compute",
-                    "serial_ms_per_step": e2e_serial_ms},
-            "gpu_launches": arm.launches * args.steps,
-            "launch": "append, tile gather, attention per step (programmatic dependent launch); "
-                      "e2e: the compute of each step in a CUDA graph, H2D and D2H copies on their own streams",
-            "clocks": clk.summary(),
-        }
+        line["clocks"] = clk.summary()
         print(json.dumps(line), flush=True)
 
 
@@ -965,15 +1122,123 @@ def rank_workload(w, rank: int):
 
 # ---------------------------------------------------------------------------
 
+EXTRA_WORKLOADS = ("decode32k", "long", "verify", "mixed", "prefill")
+
+
+def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind, headline=False):
+    """The step of a decode / verify workload, both arms; returns the JSON
+    fields of its line (rank 0) without the clocks and the CPU baseline."""
+    import torch
+    arm = Arm(w, True, dev, rank, l2)
+    arm.capture()
+    total_ms = reduce_max(arm.time(args.steps, args.warmup, barrier))
+    ms = total_ms / args.steps
+    kern_steps = max(args.steps, arm.layers)
+    kern_avg = reduce_max(arm.time_kernel(kern_steps, args.warmup))
+    step_bytes = arm.bytes["step"]
+    gbs, seq_steps = aggregate(step_bytes, w.batch, world, ms)
+    achieved = arm.bytes["attention_kernel"] / (kern_avg * 1e-3) / 1e9
+    pct = arm.step_percentiles(max(20, args.steps)) if headline else None   # context: per-step spread
+    arm.bitcast = True                                  # context: the pages' bitcast decoder
+    bitcast_ms = reduce_max(arm.time_kernel(kern_steps, args.warmup))
+    arm.bitcast = False
+    mma_sync_ms = fp8_qk_ms = None
+    if arm.uses_tc:                                     # context: the same shape on the mma.sync kernel
+        arm.mma_sync = True
+        mma_sync_ms = reduce_max(arm.time_kernel(kern_steps, args.warmup))
+        arm.mma_sync = False
+        arm.fp8_qk = True                               # context: the FP8 score variant (other numerics)
+        fp8_qk_ms = reduce_max(arm.time_kernel(kern_steps, args.warmup))
+        arm.fp8_qk = False
+    arm.graphs = arm.many = None
+    e2e_steps = max(5, args.steps // 2) if arm.layers == 1 else max(3, args.steps // 4)
+    e2e_ms, e2e_serial_ms, h2d, d2h = arm.time_e2e(e2e_steps, args.warmup if arm.layers == 1 else 2)
+    e2e_ms, e2e_serial_ms = reduce_max(e2e_ms), reduce_max(e2e_serial_ms)
+    info = dict(S=arm.S, copies=arm.copies, pool_bytes=arm.pool_bytes, layers=arm.layers,
+                launches=arm.launches, uses_tc=arm.uses_tc, kernel_bytes=arm.bytes["attention_kernel"])
+    del arm
+    torch.cuda.empty_cache()
+
+    fp16 = None
+    if not args.no_fp16:
+        arm16 = Arm(w, False, dev, rank, l2)
+        arm16.capture()
+        ms16 = reduce_max(arm16.time(args.steps, args.warmup, barrier)) / args.steps
+        a16avg = reduce_max(arm16.time_kernel(kern_steps, args.warmup))
+        fp16 = {"ms_per_step": ms16,
+                "value": world * arm16.bytes["step"] / (ms16 * 1e-3) / 1e9,
+                "seq_steps_per_s": world * w.batch / (ms16 * 1e-3),
+                "attention_kernel_ms": a16avg,
+                "attention_kernel_gbs": arm16.bytes["attention_kernel"] / (a16avg * 1e-3) / 1e9,
+                "pool_copies": arm16.copies}
+        del arm16
+        torch.cuda.empty_cache()
+
+    kname = "attn_tc_kernel" if info["uses_tc"] else "attn_split_kernel"
+    layers = info["layers"]
+    return {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": describe(w, info["S"]),
+                   "global_batch": world * w.batch, "kv_dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
+                   "l2": (f"rotating {info['copies']} KV pool copies of {info['pool_bytes'] / 1e6:.0f} MB "
+                          f"(> 2 x L2 {l2 / 1e6:.0f} MB)") if layers == 1 else
+                         (f"{layers} layers' own pools of {info['pool_bytes'] / 1e6:.0f} MB each per step "
+                          f"(> 2 x L2 {l2 / 1e6:.0f} MB)"),
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak": 100.0 * gbs / world / peak,
+        "seq_steps_per_s": seq_steps,
+        "layers_per_step": layers,
+        "step_bytes": step_bytes,
+        "fp16_arm": fp16,
+        "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+        "step_ms_p10_p50_p90_one_graph_each": pct,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(kname, w.name),
+                     "kernel": kname + (" (E4M3, tcgen05)" if info["uses_tc"] else " (E4M3)"),
+                     "peak_kind": peak_kind,
+                     "attention_kernel_ms": kern_avg,
+                     "bytes_per_launch": info["kernel_bytes"],
+                     "launches_timed": kern_steps,
+                     "decoder": "hardware E4M3 conversion",
+                     "bitcast_decoder_ms": bitcast_ms,
+                     "bitcast_decoder_kernel": "attn_split_kernel",
+                     "bitcast_decoder_gbs": info["kernel_bytes"] / (bitcast_ms * 1e-3) / 1e9,
+                     "mma_sync_kernel_ms": mma_sync_ms,
+                     "fp8_scores_kernel_ms": fp8_qk_ms},
+        "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms,
+                "copies": "own streams, overlapping the neighbouring steps' compute",
+                "serial_ms_per_step": e2e_serial_ms},
+        "gpu_launches": info["launches"] * args.steps,
+        "launch": (f"CUDA graphs of {GRAPH_STEPS} steps" if layers == 1 else "a CUDA graph per step") +
+                  " (append, attention, combine per layer; programmatic dependent launch); e2e: the compute "
+                  "of each step in a CUDA graph, H2D and D2H copies on their own streams",
+    }
+
+
+def _entry(line):
+    """A workloads entry: the line's figures without the keys it shares with the headline."""
+    drop = {"metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data",
+            "cpu_baseline"}
+    return {k: v for k, v in line.items() if k not in drop}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default=None,
+                    help="time this workload alone (default: decode, plus the workloads object)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="the headline workload only")
     ap.add_argument("--kernel-hash", choices=sorted(KERNEL_SOURCES),
                     help="print the source hash an ncu summary of that kernel records, and exit")
     args = ap.parse_args()
@@ -987,7 +1252,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     from fp8_paged_kv_e4m3_gb300 import inputs
-    w = inputs.get(args.workload)
+    w = inputs.get(args.workload or "decode")
+    extras = [] if (args.workload or args.no_workloads) else list(EXTRA_WORKLOADS)
 
     if args.impl == "reference":
         if rank == 0:
@@ -1008,7 +1274,6 @@ def main():
         barrier = None
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size or L2_BYTES_DEFAULT
     peak, peak_kind = _peaks()
-
     reduce_max = lambda x: max_over_ranks(x, dev, world)
 
     if w.name == "prefill":
@@ -1017,103 +1282,29 @@ def main():
             dist.destroy_process_group()
         return
 
-    arm = Arm(w, True, dev, rank, l2)
-    arm.capture()
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        total_ms = arm.time(args.steps, args.warmup, barrier)
-        kern_avg = arm.time_kernel(args.steps, args.warmup)
-    total_ms = reduce_max(total_ms)
-    ms = total_ms / args.steps
-    kern_avg = reduce_max(kern_avg)
-    step_bytes = arm.bytes["step"]
-    gbs, seq_steps = aggregate(step_bytes, w.batch, world, ms)
-    achieved = arm.bytes["attention_kernel"] / (kern_avg * 1e-3) / 1e9
-    pct = arm.step_percentiles(max(20, args.steps))   # context: per-step spread (one graph each)
-    arm.bitcast = True                                  # context: the pages' bitcast decoder
-    bitcast_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
-    arm.bitcast = False
-    mma_sync_ms = fp8_qk_ms = None
-    if arm.uses_tc:                                     # context: the same shape on the mma.sync kernel
-        arm.mma_sync = True
-        mma_sync_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
-        arm.mma_sync = False
-        arm.fp8_qk = True                               # context: the FP8 score variant (other numerics)
-        fp8_qk_ms = reduce_max(arm.time_kernel(args.steps, args.warmup))
-        arm.fp8_qk = False
-
-    arm.graphs = None
-    e2e_ms, e2e_serial_ms, h2d, d2h = arm.time_e2e(max(5, args.steps // 2), args.warmup)
-    e2e_ms, e2e_serial_ms = reduce_max(e2e_ms), reduce_max(e2e_serial_ms)
-
-    fp16 = None
-    if not args.no_fp16:
-        del arm.pools
-        torch.cuda.empty_cache()
-        arm16 = Arm(w, False, dev, rank, l2)
-        arm16.capture()
-        t16 = arm16.time(args.steps, args.warmup, barrier)
-        a16avg = reduce_max(arm16.time_kernel(args.steps, args.warmup))
-        ms16 = reduce_max(t16) / args.steps
-        fp16 = {"ms_per_step": ms16,
-                "value": world * arm16.bytes["step"] / (ms16 * 1e-3) / 1e9,
-                "seq_steps_per_s": world * w.batch / (ms16 * 1e-3),
-                "attention_kernel_ms": a16avg,
-                "attention_kernel_gbs": arm16.bytes["attention_kernel"] / (a16avg * 1e-3) / 1e9,
-                "pool_copies": arm16.copies}
-        del arm16
-        torch.cuda.empty_cache()
-
+    # the CPU baseline first: its worker processes are spawned, and none of
+    # them starts while this process holds busy GPU streams
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        units = 64
-        t, nb, n = oracle_sample_time(w, units)
-        cpu = {"value": nb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} (sequence, kv head) units of one step ({w.group} query heads each): "
-                         f"append of the step token + binary64 attention, {t:.1f} s"}
+        cpu = cpu_baseline_decode(w)
 
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        line = measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind, headline=True)
+        workloads = {}
+        for name in extras:
+            wx = inputs.get(name)
+            if wx.name == "prefill":
+                workloads[name] = _entry(measure_prefill(args, wx, dev, l2, rank, world, reduce_max, barrier,
+                                                         with_cpu=False))
+            else:
+                workloads[name] = _entry(measure(args, wx, dev, l2, rank, world, reduce_max, barrier, peak,
+                                                 peak_kind))
     if rank == 0:
-        kname = "attn_tc_kernel" if arm.uses_tc else "attn_split_kernel"
-        line = {
-            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": describe(w, arm.S),
-                       "global_batch": world * w.batch, "kv_dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
-                       "l2": f"rotating {arm.copies} KV pool copies of {arm.pool_bytes / 1e6:.0f} MB "
-                             f"(> 2 x L2 {l2 / 1e6:.0f} MB)",
-                       "parallelism": f"replicas x{world}"},
-            "pct_of_peak": 100.0 * gbs / world / peak,
-            "seq_steps_per_s": seq_steps,
-            "step_bytes": step_bytes,
-            "fp16_arm": fp16,
-            "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
-            "step_ms_p10_p50_p90_one_graph_each": pct,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak,
-                         "traffic": profiled_traffic(kname, w.name),
-                         "kernel": kname + (" (E4M3, tcgen05)" if arm.uses_tc else " (E4M3)"),
-                         "peak_kind": peak_kind,
-                         "attention_kernel_ms": kern_avg,
-                         "bytes_per_launch": arm.bytes["attention_kernel"],
-                         "decoder": "hardware E4M3 conversion",
-                         "bitcast_decoder_ms": bitcast_ms,
-                         "bitcast_decoder_kernel": "attn_split_kernel",
-                         "bitcast_decoder_gbs": arm.bytes["attention_kernel"] / (bitcast_ms * 1e-3) / 1e9,
-                         "mma_sync_kernel_ms": mma_sync_ms,
-                         "fp8_scores_kernel_ms": fp8_qk_ms},
-            "cpu_baseline": cpu,
-            "e2e": {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms,
-                    "copies": "own streams, overlapping the neighbouring steps' compute",
-                    "serial_ms_per_step": e2e_serial_ms},
-            "gpu_launches": arm.launches * args.steps,
-            "launch": f"CUDA graphs of {GRAPH_STEPS} steps (append, attention, combine per step; "
-                      "programmatic dependent launch); e2e: the compute of each step in a CUDA graph, "
-                      "H2D and D2H copies on their own streams",
-            "clocks": clk.summary(),
-        }
+        line["cpu_baseline"] = cpu
+        if workloads:
+            line["workloads"] = workloads
+            line["gpu_launches"] += sum(e["gpu_launches"] for e in workloads.values())
+        line["clocks"] = clk.summary()
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
