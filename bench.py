@@ -1116,8 +1116,8 @@ def aggregate(step_bytes_per_rank: int, batch_per_rank: int, world: int, ms_max:
 
 def rank_workload(w, rank: int):
     """Rank r's replica: same shapes, its own seeded data."""
-    from fp8_paged_kv_e4m3_gb300 import inputs
-    return inputs.get(w.name, seed=rank) if rank else w
+    import dataclasses
+    return dataclasses.replace(w, seed=rank) if rank else w
 
 
 # ---------------------------------------------------------------------------
@@ -1239,6 +1239,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp16", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="the headline workload only")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers per step of --workload (default: the workload's own; 1 keeps a profiled case small)")
     ap.add_argument("--kernel-hash", choices=sorted(KERNEL_SOURCES),
                     help="print the source hash an ncu summary of that kernel records, and exit")
     args = ap.parse_args()
@@ -1253,6 +1255,8 @@ def main():
 
     from fp8_paged_kv_e4m3_gb300 import inputs
     w = inputs.get(args.workload or "decode")
+    if args.layers is not None:
+        w = inputs.get(w.name, layers=max(1, args.layers))
     extras = [] if (args.workload or args.no_workloads) else list(EXTRA_WORKLOADS)
 
     if args.impl == "reference":
