@@ -317,13 +317,13 @@ class Arm:
         per_layer = algorithmic_bytes(w, 1 if e4m3 else 2, lay.lens, self.topk_np)
         self.bytes = {"step": per_layer["step"] * self.layers, "attention_kernel": per_layer["attention_kernel"],
                       "layer": per_layer["step"]}
-        self.launches = 3 * self.layers   # kernels of one step: append, attention, combine per layer
         self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
         self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
         self.fp8_qk = False    # tcgen05 kernel: fp16 scores (default) or the FP8 score variant
         # batches of varied lengths: the split kernel takes the sequences longest first
         self.longest_first = not w.lens.startswith("fixed")
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
+        self.launches = 3 * self.layers   # kernels of one step: append, attention, combine per layer
         torch.cuda.synchronize(dev)
 
     def _append(self, l, k, v, slots, kc, vc):
@@ -332,11 +332,26 @@ class Arm:
         else:
             self.kvq.kv_append_fp16(k, v, slots, kc, vc, None)
 
-    def _attention(self, l, kc, vc, q=None, bt=None, cl=None):
+    def _attention(self, l, kc, vc, q=None, bt=None, cl=None, out=None):
+        """The attention of layer l through the public calls: with `out`, the
+        full call (split-K attention and the merge of its partials); without,
+        the partial call alone (split-K attention into the workspace)."""
         kvq = self.kvq
         q = self.q[l] if q is None else q
         bt = self.bt if bt is None else bt
         cl = self.cl if cl is None else cl
+        if out is not None:
+            if self.e4m3:
+                kvq.paged_decode_attn_e4m3(q, kc, vc, bt, cl, self.ks[l], self.vs[l], self.ws, out,
+                                           self.topk_idx, self.topk_lens, num_splits=self.S,
+                                           err_flag=self.err, split_pages=self.w.split_pages,
+                                           bitcast_decode=self.bitcast, mma_sync=self.mma_sync,
+                                           fp8_qk=self.fp8_qk, longest_first=self.longest_first)
+            else:
+                kvq.paged_decode_attn_fp16(q, kc, vc, bt, cl, self.ws, out, self.topk_idx, self.topk_lens,
+                                           num_splits=self.S, err_flag=self.err, split_pages=self.w.split_pages,
+                                           mma_sync=self.mma_sync, longest_first=self.longest_first)
+            return
         if self.e4m3:
             kvq.paged_decode_attn_e4m3_partial(q, kc, vc, bt, cl, self.ks[l], self.vs[l], self.ws,
                                                self.topk_idx, self.topk_lens, num_splits=self.S,
@@ -351,13 +366,13 @@ class Arm:
 
     def step(self, i):
         """One step on pool copy i: for every layer, the append of the step's
-        tokens, split-K attention and the log-sum-exp combine (three launches
-        per layer, chained with programmatic dependent launch)."""
+        tokens and the attention call (split-K attention, then the log-sum-exp
+        combine of its partials: three launches per layer, chained with
+        programmatic dependent launch)."""
         for l in range(self.layers):
             kc, vc = self.pools[i % self.copies][l]
             self._append(l, self.k_new[l], self.v_new[l], self.step_slots, kc, vc)
-            self._attention(l, kc, vc)
-            self.kvq.lse_combine(self.ws, self.out[l], self.p)
+            self._attention(l, kc, vc, out=self.out[l])
 
     def capture(self):
         """CUDA graphs of the step: one per pool copy holding one step, and
@@ -413,10 +428,10 @@ class Arm:
         return start.elapsed_time(end)
 
     def time_kernel(self, steps, warmup):
-        """Average duration of one attention launch (one layer): `steps`
-        back-to-back launches over the rotating pool copies and layers,
-        between two events on the launching stream (the queue stays full, so
-        host launch time is hidden)."""
+        """Average duration of one attention kernel (one layer; the partial
+        call): `steps` back-to-back launches over the rotating pool copies and
+        layers, between two events on the launching stream (the queue stays
+        full, so host launch time is hidden)."""
         torch = self.torch
         n = self.copies * self.layers
 
@@ -481,8 +496,7 @@ class Arm:
             for l in range(self.layers):
                 kc, vc = self.pools[i % self.copies][l]
                 self._append(l, dev[f"k{l}"], dev[f"v{l}"], dev["slots"], kc, vc)
-                self._attention(l, kc, vc, dev[f"q{l}"], dev["bt"], dev["cl"])
-                self.kvq.lse_combine(self.ws, outs[i % 2][l], self.p)
+                self._attention(l, kc, vc, dev[f"q{l}"], dev["bt"], dev["cl"], out=outs[i % 2][l])
 
         def copy_out(p):
             out_host[p].copy_(outs[p], non_blocking=True)
@@ -1216,8 +1230,9 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
                 "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": info["launches"] * args.steps,
         "launch": (f"CUDA graphs of {GRAPH_STEPS} steps" if layers == 1 else "a CUDA graph per step") +
-                  " (append, attention, combine per layer; programmatic dependent launch); e2e: the compute "
-                  "of each step in a CUDA graph, H2D and D2H copies on their own streams",
+                  " (per layer: the append, then the attention call -- attention and combine kernels; "
+                  "programmatic dependent launch); e2e: the compute of each step in a CUDA graph, H2D and D2H "
+                  "copies on their own streams",
     }
 
 
