@@ -304,9 +304,11 @@ class Arm:
             del kh, vh
         if e4m3:
             kvq.validate_scales(self.ks, self.vs)
+        # batches of varied lengths: the split kernel takes the sequences longest first
+        self.longest_first = not w.lens.startswith("fixed")
         self.p = kvq.attn_params(self.q[0], w.num_kv_heads, self.bt.shape[1], w.num_splits,
                                  0 if self.topk_idx is None else self.topk_idx.shape[2],
-                                 split_pages=w.split_pages)
+                                 split_pages=w.split_pages, longest_first=self.longest_first)
         self.S = kvq.num_splits(self.p)
         # one workspace serves every layer: each layer's combine reads it before the
         # next layer's attention writes it (stream order)
@@ -320,8 +322,6 @@ class Arm:
         self.bitcast = False  # E4M3 decoder: hardware conversion (default) or bitcast
         self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
         self.fp8_qk = False    # tcgen05 kernel: fp16 scores (default) or the FP8 score variant
-        # batches of varied lengths: the split kernel takes the sequences longest first
-        self.longest_first = not w.lens.startswith("fixed")
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
         self.launches = 3 * self.layers   # kernels of one step: append, attention, combine per layer
         torch.cuda.synchronize(dev)
@@ -766,7 +766,7 @@ def cpu_baseline_decode(w):
                       f"{cores} spawned processes, timed parts started together; and the same on 1 core"}
 
 
-def library_splits(w, max_pages: int, sm_count: int) -> int:
+def library_splits(w, max_pages: int, sm_count: int, longest_first: bool = False) -> int:
     """The split count the library picks for this workload (the rule of
     kvq_attn_num_splits, restated so that the reference arm can label its
     config like ours without loading the CUDA library)."""
@@ -777,10 +777,18 @@ def library_splits(w, max_pages: int, sm_count: int) -> int:
         sp = w.split_pages
         return max(1, -(-max_pages // sp), -(-max_topk // (4 * sp)))
     pairs = max(w.batch, 1) * w.num_kv_heads
-    s = -(-(sm_count * 3 * 2) // pairs)
-    cap = -(-max_pages // 16)
-    if max_topk > 0:
-        cap = max(cap, -(-max_topk // 32))
+    rows = w.group * w.q_len
+    if w.head_dim == 128 and 8 < rows <= 64:          # the tcgen05 kernel
+        s = -(-(sm_count * 6) // pairs)
+        cap = -(-max_pages // 16)
+        if max_topk > 0:
+            cap = max(cap, -(-max_topk // 32))
+    else:                                              # the split kernel
+        slots = sm_count * 4
+        s = (slots * 5 // 2) // pairs if longest_first else (slots * 2) // pairs
+        cap = -(-max_pages // 256)
+        if max_topk > 0:
+            cap = max(cap, -(-max_topk // 1024))
     return max(1, min(s, cap, 1024))
 
 
@@ -790,7 +798,8 @@ def reference_config(w, world: int, sample: str) -> dict:
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
     lay = inputs.page_layout(w)
-    return {"workload": describe(w, library_splits(w, lay.block_tables.shape[1], sms)),
+    return {"workload": describe(w, library_splits(w, lay.block_tables.shape[1], sms,
+                                                   longest_first=not w.lens.startswith("fixed"))),
             "global_batch": world * w.batch, "kv_dtype": "e4m3 (fp16 MMA, fp32 accumulate)",
             "l2": "host oracle: no GPU cache to defeat", "parallelism": f"replicas x{world}",
             "sample": sample}

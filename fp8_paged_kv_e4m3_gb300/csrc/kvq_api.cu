@@ -82,13 +82,30 @@ static int32_t resolve_splits(const kvq_attn_params *p)
         const int64_t s = splits_to_cover(p);   // <= 65535 (checked)
         return int32_t(s < 1 ? 1 : s);
     }
-    // Enough CTAs for a few waves of the resident slots (about 3 CTAs per SM),
-    // but no split shorter than 16 pages.
     const int64_t pairs = int64_t(p->batch > 0 ? p->batch : 1) * p->num_kv_heads;
-    const int64_t target = int64_t(device_sm_count()) * 3 * 2;
-    int64_t s = (target + pairs - 1) / pairs;
-    int64_t cap = (int64_t(p->max_pages_per_seq) + 15) / 16;
-    if (p->max_topk > 0) cap = cap > (p->max_topk + 31) / 32 ? cap : (p->max_topk + 31) / 32;
+    const int64_t sms = device_sm_count();
+    const int64_t rows = int64_t(p->num_q_heads / p->num_kv_heads) * p->q_len;
+    const bool tc = p->head_dim == 128 && rows > 8 && rows <= 64 &&
+                    !(p->flags & (KVQ_ATTN_MMA_SYNC | KVQ_ATTN_BITCAST_DECODE));
+    int64_t s, cap;
+    if (tc) {
+        // tcgen05 kernel (two CTAs per SM): about three and a half waves of its
+        // resident CTAs, so that long and short sequences pack; no split shorter
+        // than 16 pages
+        s = (sms * 6 + pairs - 1) / pairs;
+        cap = (int64_t(p->max_pages_per_seq) + 15) / 16;
+        if (p->max_topk > 0) cap = cap > (p->max_topk + 31) / 32 ? cap : (p->max_topk + 31) / 32;
+    } else {
+        // split kernel (up to four CTAs per SM): the most splits that fit the
+        // (sequence, kv head) pairs in two waves of resident CTAs -- two and a
+        // half for batches whose lengths vary (longest-first order), which pack
+        // better in smaller pieces -- but no split shorter than 256 pages (or
+        // 1024 list entries), whose fixed cost per CTA would dominate
+        const int64_t slots = sms * 4;
+        s = (p->flags & KVQ_ATTN_LONGEST_FIRST) ? (slots * 5 / 2) / pairs : (slots * 2) / pairs;
+        cap = (int64_t(p->max_pages_per_seq) + 255) / 256;
+        if (p->max_topk > 0) cap = cap > (p->max_topk + 1023) / 1024 ? cap : (p->max_topk + 1023) / 1024;
+    }
     if (s > cap) s = cap;
     if (s < 1) s = 1;
     if (s > 1024) s = 1024;

@@ -13,7 +13,7 @@ tensors stand in for the K/V that such traffic would produce):
             head_dim 64, N(0,1) with 2 outlier channels x20, q_len 1 or 4
   decode    batch 32 x 4096 context, 32 q / 4 kv heads, head_dim 128, q_len 1,
             4 splits
-  decode32k as decode at 32768 context, 8 splits
+  decode32k as decode at 32768 context, the library's split count
   verify    24 layers, batch 64, q_len 4 (1 + 3 drafts), contexts
             log-uniform in [1024, 32768], N(0,1) with 4 Student-t(3) channels
             per kv head
@@ -75,7 +75,7 @@ WORKLOADS = {
     "tiny_verify": Workload("tiny_verify", 1, 1, 2, 4, 8, 2, 64, 2, "list:37,100",
                             outlier_channels=2, calib_tokens=128),
     "decode": Workload("decode", 2, 1, 32, 1, 32, 4, 128, 4, "fixed:4096"),
-    "decode32k": Workload("decode32k", 6, 1, 32, 1, 32, 4, 128, 8, "fixed:32768"),
+    "decode32k": Workload("decode32k", 6, 1, 32, 1, 32, 4, 128, 0, "fixed:32768"),
     "verify": Workload("verify", 3, 24, 64, 4, 32, 4, 128, 0, "loguniform:1024:32768",
                        heavy_channels=4),
     "long": Workload("long", 4, 1, 4, 1, 32, 4, 128, 64, "fixed:262144"),

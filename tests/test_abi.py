@@ -222,11 +222,13 @@ def test_prefill_host_checks_fail_closed(lib):
     assert _prefill(lib, _pparams(batch=0)) == 0          # nothing to do, nothing launched
 
 
+@pytest.mark.parametrize("longest_first", [False, True])
 @pytest.mark.parametrize("name,overrides", [
     ("decode", {}), ("decode32k", {}), ("verify", {}), ("long", {}), ("mixed", {}), ("tiny", {}),
     ("verify", {"num_splits": 0, "split_pages": 256}), ("mixed", {"split_pages": 64}),
+    ("mixed", {"batch": 7}), ("decode", {"num_splits": 0}), ("tiny_verify", {}),
 ])
-def test_reference_config_labels_the_library_split_count(lib, name, overrides):
+def test_reference_config_labels_the_library_split_count(lib, name, overrides, longest_first):
     """The reference arm labels its config with the split count of our arm,
     restated in bench.library_splits: it must agree with kvq_attn_num_splits."""
     import bench
@@ -236,5 +238,6 @@ def test_reference_config_labels_the_library_split_count(lib, name, overrides):
     max_pages = inputs.page_layout(w).block_tables.shape[1]
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
     p = kvq.AttnParams(w.batch, w.q_len, w.num_q_heads, w.num_kv_heads, w.head_dim, w.num_splits, max_pages,
-                       w.topk if w.topk > 0 else 0, 0.0, w.split_pages, 0)
-    assert bench.library_splits(w, max_pages, sms) == lib.kvq_attn_num_splits(ctypes.byref(p))
+                       w.topk if w.topk > 0 else 0, 0.0, w.split_pages,
+                       kvq.ATTN_LONGEST_FIRST if longest_first else 0)
+    assert bench.library_splits(w, max_pages, sms, longest_first) == lib.kvq_attn_num_splits(ctypes.byref(p))
