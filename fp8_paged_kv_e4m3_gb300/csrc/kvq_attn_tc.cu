@@ -268,16 +268,16 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 umma_commit(b_s);
                 if (!mbar_wait_bounded(b_p, t & 1, abort_flag, a.err_flag)) break;
                 tc_fence_after();
-                // O^T[ch][row] += sum_tok V[tok][ch] P[tok][row]: A = V^T, B = P^T, both MN-major
+                // O^T[ch][row] += sum_tok V[tok][ch] P[tok][row]: A = V^T, B = P^T, both MN-major;
+                // L^T[lane][row] += sum_tok 1 * P[tok][row]: the row sums -- the two accumulation
+                // chains interleaved
 #pragma unroll
-                for (int ks = 0; ks < kTcTile / 16; ++ks)
+                for (int ks = 0; ks < kTcTile / 16; ++ks) {
                     umma_smem_a(tmem + T::kColO, umma_desc(v_addr + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128),
                                 umma_desc(p_addr + ks * 2 * NR * 16, NR * 16, 128), id_pv, t > 0 || ks > 0);
-                // L^T[lane][row] += sum_tok 1 * P[tok][row]: the row sums, accumulated like O^T
-#pragma unroll
-                for (int ks = 0; ks < kTcTile / 16; ++ks)
                     umma_tmem_a(tmem + T::kColL, tmem + T::kColOnes + ks * 8,
                                 umma_desc(p_addr + ks * 2 * NR * 16, NR * 16, 128), id_l, t > 0 || ks > 0);
+                }
                 umma_commit(b_pv);
             }
             // every MMA issued so far completes before the tensor memory is freed
