@@ -355,15 +355,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                 for (int c = 0; c < kPfTile; ++c)
                     if (k0 + c > limit) xv[c] = -INFINITY;
             }
+            // (chain u takes columns u, u + 8, ..., u + 120, two more per three-way maximum)
+            static_assert(kPfTile == 128, "the maximum's chains cover 128 columns");
             float m8[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) m8[u] = xv[u];
+            for (int u = 0; u < 8; ++u) {
+                float m = fmax3(xv[u], xv[u + 8], xv[u + 16]);
 #pragma unroll
-            for (int c = 8; c < kPfTile; c += 8)
-#pragma unroll
-                for (int u = 0; u < 8; ++u) m8[u] = fmaxf(m8[u], xv[c + u]);
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * qk;
+                for (int k = 3; k < 15; k += 2) m = fmax3(m, xv[u + 8 * k], xv[u + 8 * k + 8]);
+                m8[u] = fmaxf(m, xv[u + 120]);
+            }
+            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * qk;
             // the reference moves when a score rises more than 2^8 above it; the
             // row's sum and (once PV(t-1) is complete) its O row are rescaled.  The
             // O pass is warp-wide; lanes whose reference stays scale by 1.
@@ -391,22 +393,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                 }
             }
             // P = 2^(s qk - ref) as fp16 pairs over the first 64 columns of S; the
-            // row sum over 8 independent chains
+            // exponents and the row sum two columns per instruction, the sum over
+            // four independent pair chains
             const float rf = (ref == -INFINITY) ? 0.f : ref;   // a row with no key yet: P = 0
-            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float2 qk2 = make_float2(qk, qk), nrf2 = make_float2(-rf, -rf);
+            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < kPfTile; c += 32) {
                 uint32_t w[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(fmaf(xv[c + 2 * e], qk, -rf));
-                    const float p1 = fast_exp2(fmaf(xv[c + 2 * e + 1], qk, -rf));
-                    l8[e & 7] += p0 + p1;
-                    w[e] = pack_half2(p0, p1);
+                    const float2 z = ffma2(make_float2(xv[c + 2 * e], xv[c + 2 * e + 1]), qk2, nrf2);
+                    const float2 p = make_float2(fast_exp2(z.x), fast_exp2(z.y));
+                    l4[e & 3] = fadd2(l4[e & 3], p);
+                    w[e] = pack_half2(p.x, p.y);
                 }
                 tmem_st16(sb + c / 2, w);
             }
-            lsum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            lsum += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
