@@ -73,9 +73,10 @@ struct TcLayout {
     static constexpr int kV = kQ + NR * 256;                 // V^T: 128 ch x 128 tok fp16, MN-major
     static constexpr int kP = kV + kTcTile * kTcD * 2;       // P^T: NR x 128 tok fp16, MN-major
     static constexpr int kWmax = kP + NR * 256;              // [2][4][NR] float: per-worker row maxima
-    static constexpr int kPriv = kWmax + 2 * 4 * NR * 4;     // [4][4][NR] float: per-worker reference,
-                                                             //   correction, coefficient, reference in use
-    static constexpr int kLsum = kPriv + 4 * 4 * NR * 4;     // [4][NR] float: per-worker row sums
+    static constexpr int kPriv = kWmax + 2 * 4 * NR * 4;     // [4][5][NR] float: per-worker reference,
+                                                             //   correction, coefficient, reference in use,
+                                                             //   reference + 8 (the band's top)
+    static constexpr int kLsum = kPriv + 4 * 5 * NR * 4;     // [4][NR] float: per-worker row sums
     static constexpr int kMend = kLsum + 4 * NR * 4;         // [4][NR] float: per-worker final row maxima
     static constexpr int kFlag = kMend + 4 * NR * 4;         // [2][4] int: per-worker "left the band" flags
     static constexpr int kQmax = kFlag + 2 * 4 * 4;          // [2][4] float: per-worker max |q|, score
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
         const int tt = 32 * q + lane;                // token of the tile (S^T lane), channel of O^T
         const int win0 = L - a.q_len;                // row i sees positions <= win0 + i
         float *wmax = reinterpret_cast<float *>(smem + T::kWmax);
-        float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 4 * NR;   // reference, corr, coef, in use
+        // reference, corr, coef, reference in use, reference + 8
+        float *priv = reinterpret_cast<float *>(smem + T::kPriv) + q * 5 * NR;
         float *lsum = reinterpret_cast<float *>(smem + T::kLsum);
         // the final maxima get a buffer of their own: a worker may still read the
         // last tile's exchange in wmax while another has reached the epilogue
@@ -365,7 +367,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 
         // Per row, the reference of the exponentials lives in the worker's private
         // shared copy (all four workers hold the same values): priv[r] (-inf while
-        // the row has none), priv[3 NR + r] (the same, 0 while none).  This
+        // the row has none), priv[3 NR + r] (the same, 0 while none), priv[4 NR + r]
+        // (the reference + 8, the top of the row's band; -inf while none).  This
         // thread keeps, per row, the running maximum and the sum over its tokens.
         int *flag = reinterpret_cast<int *>(smem + T::kFlag);
 #pragma unroll
@@ -373,6 +376,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             if (32 * h + lane < NR) {
                 priv[32 * h + lane] = -INFINITY;
                 priv[3 * NR + 32 * h + lane] = 0.f;
+                priv[4 * NR + 32 * h + lane] = -INFINITY;
             }
         __syncwarp();
         float mt[NR];
@@ -516,18 +520,27 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             const int rmin = pos < 0 ? NR : (pos > win0 ? a.group * (pos - win0) : 0);
             if (rmin == 0 && a.rows == NR) {
 #pragma unroll
-                for (int r = 0; r < NR; ++r) x[r] *= qk;
+                for (int r = 0; r < NR; r += 2) {
+                    const float2 y = fmul2(make_float2(x[r], x[r + 1]), make_float2(qk, qk));
+                    x[r] = y.x;
+                    x[r + 1] = y.y;
+                }
             } else {
 #pragma unroll
                 for (int r = 0; r < NR; ++r) x[r] = (r >= rmin && r < a.rows) ? x[r] * qk : -INFINITY;
             }
 
             // ---- running maxima; does any score leave the band of 2^8 above its row's reference? ----
+            // (a row without a reference has its band top at -inf: any finite score leaves it)
             bool over = false;
 #pragma unroll
-            for (int r = 0; r < NR; ++r) {
+            for (int r = 0; r < NR; r += 4) {
+                const float4 top = *reinterpret_cast<const float4 *>(priv + 4 * NR + r);
                 mt[r] = fmaxf(mt[r], x[r]);
-                over |= x[r] > priv[r] + 8.f;   // a row without a reference: any finite score
+                mt[r + 1] = fmaxf(mt[r + 1], x[r + 1]);
+                mt[r + 2] = fmaxf(mt[r + 2], x[r + 2]);
+                mt[r + 3] = fmaxf(mt[r + 3], x[r + 3]);
+                over |= (x[r] > top.x) | (x[r + 1] > top.y) | (x[r + 2] > top.z) | (x[r + 3] > top.w);
             }
             over = __any_sync(kFull, over);
             if (lane == 0) flag[(t & 1) * 4 + q] = over ? 1 : 0;
@@ -565,6 +578,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                         corr = (ref == -INFINITY) ? 0.f : fast_exp2(ref - mx);
                         priv[r] = mx;
                         priv[3 * NR + r] = mx;
+                        priv[4 * NR + r] = mx + 8.f;
                         moved = true;
                     }
                     priv[NR + r] = corr;
@@ -589,7 +603,15 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
             }
             // ---- P = exp2(score - reference) ----
 #pragma unroll
-            for (int r = 0; r < NR; ++r) x[r] = fast_exp2(x[r] - priv[3 * NR + r]);
+            for (int r = 0; r < NR; r += 4) {
+                const float4 rf = *reinterpret_cast<const float4 *>(priv + 3 * NR + r);
+                const float2 d0 = fsub2(make_float2(x[r], x[r + 1]), make_float2(rf.x, rf.y));
+                const float2 d1 = fsub2(make_float2(x[r + 2], x[r + 3]), make_float2(rf.z, rf.w));
+                x[r] = fast_exp2(d0.x);
+                x[r + 1] = fast_exp2(d0.y);
+                x[r + 2] = fast_exp2(d1.x);
+                x[r + 3] = fast_exp2(d1.y);
+            }
             // ---- P^T (fp16, MN-major): (row, tok) at (tok/8) * NR*16 + (row/8) * 128 + (tok%8) * 16 ----
             {
                 uint8_t *pdst = smem + T::kP + (tt >> 3) * (NR * 16) + (tt & 7) * 16;
