@@ -91,6 +91,30 @@ struct TcLayout {
     static constexpr int kCols = (128 + 3 * NR) <= 128 ? 128 : ((128 + 3 * NR) <= 256 ? 256 : 512);
 };
 
+// two fp32 lanes per instruction (sm_100 and later): d = a - b and d = a * b,
+// each lane rounded to nearest as its scalar form
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0 in
 // bits 7-9 and 10-12), fp32 accumulator, M x N tile, both operands K-major.
 __device__ __forceinline__ uint32_t umma_idesc_e4m3(int m, int n)

@@ -177,8 +177,8 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return d;
 }
 
-// two fp32 lanes per instruction (sm_100 and later): d = a * b + c, a + b,
-// a - b and a * b, each lane rounded to nearest as its scalar form
+// two fp32 lanes per instruction (sm_100 and later): d = a * b + c and
+// d = a + b, each lane rounded to nearest as its scalar form
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
     float2 d;
@@ -196,28 +196,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b)
     asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
         "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
         "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fsub2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
