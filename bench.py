@@ -1228,7 +1228,7 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
                      "launches_timed": kern_steps,
                      "decoder": "hardware E4M3 conversion",
                      "bitcast_decoder_ms": bitcast_ms,
-                     "bitcast_decoder_kernel": "attn_split_kernel",
+                     "bitcast_decoder_kernel": kname,
                      "bitcast_decoder_gbs": info["kernel_bytes"] / (bitcast_ms * 1e-3) / 1e9,
                      "mma_sync_kernel_ms": mma_sync_ms,
                      "fp8_scores_kernel_ms": fp8_qk_ms},

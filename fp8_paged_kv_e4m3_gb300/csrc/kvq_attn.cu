@@ -8,9 +8,9 @@ namespace kvq {
 cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream)
 {
     if (a.batch == 0) return cudaSuccess;
-    if (e4m3 && a.bitcast_decode) return launch_attention_bitcast(head_dim, a, stream);
-    // many query rows per kv head (MTP verify): the tcgen05 kernel
+    // many query rows per kv head (MTP verify): the tcgen05 kernel (either E4M3 decoder)
     if (!a.mma_sync && tc_supported(head_dim, a.rows)) return launch_attention_tc(e4m3, a, stream);
+    if (e4m3 && a.bitcast_decode) return launch_attention_bitcast(head_dim, a, stream);
     if (a.longest_first) return launch_attention_lpt(e4m3, head_dim, a, stream);
     if (e4m3)
         return head_dim == 128 ? launch_rows<true, 128, false>(a, stream)

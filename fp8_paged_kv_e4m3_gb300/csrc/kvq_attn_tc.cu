@@ -179,10 +179,11 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
 // Two CTAs per SM when NR <= 32: the bound is stated for 256 threads so that
 // registers stay at 128 per thread -- with 7 warps per CTA, two CTAs put four
 // warps on some SM sub-partitions, whose register files hold 4 x 128 x 32.
-template <bool E4M3, int NR, bool F8>
+template <bool E4M3, int NR, bool F8, bool BITCAST>
 __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const AttnArgs a)
 {
     static_assert(E4M3 || !F8, "FP8 scores need E4M3 pools");
+    static_assert(!BITCAST || (E4M3 && !F8), "the bitcast decoder is for E4M3 pools with fp16 scores");
     constexpr int D = kTcD, PPS = tc_pps<E4M3>();
     using G = TcGeometry<E4M3>;
     constexpr int SPT = tc_spt<E4M3>();                       // staging stages per tile: 2 or 4
@@ -383,6 +384,11 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                     const int i = r / a.group, h = g * a.group + r % a.group;
                     v = *reinterpret_cast<const uint4 *>(static_cast<const __half *>(a.q) +
                                                          (((int64_t)b * a.q_len + i) * a.num_q_heads + h) * D + 8 * c);
+                    if (BITCAST) {
+                        // channel order of the bitcast-decoded K rows: 0, 2, 1, 3 in each group of four
+                        v = make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.x, v.y, 0x7632),
+                                       __byte_perm(v.z, v.w, 0x5410), __byte_perm(v.z, v.w, 0x7632));
+                    }
                 }
                 *reinterpret_cast<uint4 *>(smem + T::kQ + (r >> 3) * 2048 + c * 128 + (r & 7) * 16) = v;
             }
@@ -463,14 +469,26 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const uint4 x = kx[2 * h + u];
-                            w[8 * u + 0] = cvt_lo(x.x);
-                            w[8 * u + 1] = cvt_hi(x.x);
-                            w[8 * u + 2] = cvt_lo(x.y);
-                            w[8 * u + 3] = cvt_hi(x.y);
-                            w[8 * u + 4] = cvt_lo(x.z);
-                            w[8 * u + 5] = cvt_hi(x.z);
-                            w[8 * u + 6] = cvt_lo(x.w);
-                            w[8 * u + 7] = cvt_hi(x.w);
+                            if (BITCAST) {
+                                // channels 4i, 4i + 2 and 4i + 1, 4i + 3 of each word, times 2^-8
+                                w[8 * u + 0] = dec_lo(x.x);
+                                w[8 * u + 1] = dec_hi(x.x);
+                                w[8 * u + 2] = dec_lo(x.y);
+                                w[8 * u + 3] = dec_hi(x.y);
+                                w[8 * u + 4] = dec_lo(x.z);
+                                w[8 * u + 5] = dec_hi(x.z);
+                                w[8 * u + 6] = dec_lo(x.w);
+                                w[8 * u + 7] = dec_hi(x.w);
+                            } else {
+                                w[8 * u + 0] = cvt_lo(x.x);
+                                w[8 * u + 1] = cvt_hi(x.x);
+                                w[8 * u + 2] = cvt_lo(x.y);
+                                w[8 * u + 3] = cvt_hi(x.y);
+                                w[8 * u + 4] = cvt_lo(x.z);
+                                w[8 * u + 5] = cvt_hi(x.z);
+                                w[8 * u + 6] = cvt_lo(x.w);
+                                w[8 * u + 7] = cvt_hi(x.w);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -512,7 +530,11 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
 #pragma unroll
                 for (int c = 0; c < D / 16; ++c) {   // 16 channels per step
                     uint4 lo, hi;
-                    if (E4M3) {
+                    if (E4M3 && BITCAST) {   // channel slots in the order 0, 2, 1, 3 per four, times 2^-8
+                        const uint4 x = vx[c];
+                        lo = make_uint4(dec_lo(x.x), dec_hi(x.x), dec_lo(x.y), dec_hi(x.y));
+                        hi = make_uint4(dec_lo(x.z), dec_hi(x.z), dec_lo(x.w), dec_hi(x.w));
+                    } else if (E4M3) {
                         const uint4 x = vx[c];
                         lo = make_uint4(cvt_lo(x.x), cvt_hi(x.x), cvt_lo(x.y), cvt_hi(x.y));
                         hi = make_uint4(cvt_lo(x.z), cvt_hi(x.z), cvt_lo(x.w), cvt_hi(x.w));
@@ -540,7 +562,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                 for (int e = 0; e < 16; ++e) x[c + e] = __uint_as_float(r16[e]);
             }
             // scores in the log2 domain; row r (window row r / G) sees positions <= win0 + r / G
-            const float qk = F8 ? *reinterpret_cast<volatile float *>(qk_f8) : a.qk_scale_log2;
+            // (the bitcast decoder's K is K * 2^-8: its 2^8 joins the hoisted scale, exactly)
+            const float qk = F8 ? *reinterpret_cast<volatile float *>(qk_f8) : a.qk_scale_log2 * (BITCAST ? 256.f : 1.f);
             const int rmin = pos < 0 ? NR : (pos > win0 ? a.group * (pos - win0) : 0);
             if (rmin == 0 && a.rows == NR) {
 #pragma unroll
@@ -710,7 +733,8 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                     float mx = -INFINITY;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) mx = fmaxf(mx, mend[w * NR + r]);
-                    priv[2 * NR + r] = lt > 0.f ? a.out_scale / lt : 0.f;
+                    // (the bitcast decoder's V is V * 2^-8: its 2^8 joins v_scale, exactly)
+                    priv[2 * NR + r] = lt > 0.f ? (a.out_scale * (BITCAST ? 256.f : 1.f)) / lt : 0.f;
                     if (q == 0 && unit_l[h] >= 0) {
                         // the sum relative to the exact maximum, m in natural-log units
                         a.ws_m[unit_l[h]] = lt > 0.f ? mx * kLn2 : -INFINITY;
@@ -729,8 +753,11 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
                             const int r = c + e;
                             const int unit = __shfl_sync(kFull, unit_l[r / 32], r % 32);
                             const float coef = priv[2 * NR + r];
+                            // O^T lane tt holds channel tt, or (bitcast decoder) channel tt with
+                            // bits 0 and 1 swapped
+                            const int ch = BITCAST ? ((tt & ~3) | ((tt & 1) << 1) | ((tt >> 1) & 1)) : tt;
                             if (unit >= 0 && coef != 0.f)
-                                a.ws_o[(int64_t)unit * D + tt] = __uint_as_float(r16[e]) * coef;
+                                a.ws_o[(int64_t)unit * D + ch] = __uint_as_float(r16[e]) * coef;
                         }
                     }
                 }
@@ -767,7 +794,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     if (warp == kTcMmaWarp) tmem_dealloc(tmem, T::kCols);
 }
 
-template <bool E4M3, int NR, bool F8 = false>
+template <bool E4M3, int NR, bool F8 = false, bool BITCAST = false>
 static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
 {
     constexpr int bytes = TcLayout<E4M3, NR>::kBytes;
@@ -776,15 +803,15 @@ static cudaError_t launch_tc_one(const AttnArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR, F8, BITCAST>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR, F8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(attn_tc_kernel<E4M3, NR, F8, BITCAST>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-    return launch_pdl(attn_tc_kernel<E4M3, NR, F8>, grid, dim3(kTcThreads), bytes, stream, a);
+    return launch_pdl(attn_tc_kernel<E4M3, NR, F8, BITCAST>, grid, dim3(kTcThreads), bytes, stream, a);
 }
 
 bool tc_supported(int head_dim, int rows) { return head_dim == kTcD && rows > 8 && rows <= 64; }
@@ -796,6 +823,11 @@ cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t strea
         if (a.rows <= 16) return launch_tc_one<true, 16, true>(a, stream);
         if (a.rows <= 32) return launch_tc_one<true, 32, true>(a, stream);
         return launch_tc_one<true, 64, true>(a, stream);
+    }
+    if (e4m3 && a.bitcast_decode) {
+        if (a.rows <= 16) return launch_tc_one<true, 16, false, true>(a, stream);
+        if (a.rows <= 32) return launch_tc_one<true, 32, false, true>(a, stream);
+        return launch_tc_one<true, 64, false, true>(a, stream);
     }
     if (e4m3) {
         if (a.rows <= 16) return launch_tc_one<true, 16>(a, stream);

@@ -201,15 +201,18 @@ typedef struct {
  * of [P2] Changes (the E4M3 sign, exponent and mantissa bits placed into the
  * fp16 bit pattern, which is the value times 2^-8, exact; the 2^8 is folded
  * into the hoisted scales).  Both decode every byte to the same value up to
- * that power of two, so the outputs are identical; the flag selects the
- * instruction mix only.  Ignored for the fp16 twins. */
+ * that power of two.  On the mma.sync kernel the outputs are identical; on
+ * the tcgen05 kernel the bitcast decoder pairs channels 4i, 4i + 2 and
+ * 4i + 1, 4i + 3 (the query tile takes the same order), so Q K^T sums its
+ * products in another order and the outputs agree within rounding.  Ignored
+ * for the fp16 twins. */
 #define KVQ_ATTN_BITCAST_DECODE 1
 
 /* Kernel choice for more than 8 query rows per KV head (G * q_len > 8, e.g.
  * MTP verify) at head_dim 128: by default the tcgen05 kernel (tensor-memory
  * accumulators, M = 128 tokens per MMA); KVQ_ATTN_MMA_SYNC keeps such calls
  * on the mma.sync kernel that serves every shape.  Both compute the same
- * partials up to rounding.  The bitcast decoder runs on the mma.sync kernel. */
+ * partials up to rounding.  Either E4M3 decoder runs on either kernel. */
 #define KVQ_ATTN_MMA_SYNC 2
 
 /* FP8 scores (E4M3 pools, the tcgen05 kernel's shapes: head_dim 128 and

@@ -107,3 +107,49 @@ def test_tc_large_scores_move_the_reference():
         torch.cuda.synchronize()
         assert dp.err.item() == 0
         G.assert_close(out.float().cpu().numpy(), ref, f"growing scores S={S}")
+
+
+@pytest.mark.parametrize("lens,q_len,group", SHAPES)
+def test_tc_bitcast_decoder_matches_oracle_and_hardware_conversion(lens, q_len, group):
+    """The pages' bitcast decoder on the tcgen05 kernel (flag
+    KVQ_ATTN_BITCAST_DECODE on a verify shape): every K and V byte becomes its
+    value times 2^-8 with the channels of each group of four in the order 0, 2,
+    1, 3 (the query tile takes the same order, the output undoes it) and the
+    2^8 folded into the hoisted scales.  Against the oracle, and against the
+    hardware conversion within the path's tolerance (the Q K^T sums run over
+    the channels in another order)."""
+    dp = _problem(lens, q_len, group, True)
+    ref = _oracle_out(dp)
+    for S in (1, 3, 0):
+        bc = G.run_attention(dp, num_splits=S, bitcast_decode=True)
+        hw = G.run_attention(dp, num_splits=S)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        what = f"bitcast {lens} q{q_len} G{group} S={S}"
+        G.assert_close(bc.float().cpu().numpy(), ref, what)
+        G.assert_close(bc.float().cpu().numpy(), hw.float().cpu().numpy().astype(np.float64), what + " vs hardware")
+
+
+def test_tc_bitcast_decoder_topk_nan_slots_and_partials():
+    dp = _problem([700, 300, 90], 4, 8, True, sentinel=0x7F, topk=160, topk_fraction=0.67)
+    ref = _oracle_out(dp)
+    for S in (1, 2):
+        out = G.run_attention(dp, num_splits=S, bitcast_decode=True)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        G.assert_close(out.float().cpu().numpy(), ref, f"bitcast tcgen05 top-k S={S}")
+    # the split partials: m, l and o in the oracle's units (the decoder's 2^-8 folded back)
+    dp = _problem([1000, 236, 33, 127], 4, 8, True)
+    S = 3
+    ws, p = G.run_attention(dp, num_splits=S, partial=True, bitcast_decode=True)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    o, m, l = [x.cpu().numpy() for x in kvq.workspace_views(ws, p)]
+    pr = dp.host
+    kc, vc, ks, vs = P.oracle_pools(pr, True, (dp.k_scale, dp.v_scale))
+    ro, rm, rl, _ = oracle.attention_partials(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens, S, ks, vs)
+    nonempty = rl > 0
+    assert np.array_equal(l > 0, nonempty)
+    G.assert_close(m[nonempty], rm[nonempty], "tmp_max", atol=1e-4, rtol=1e-5)
+    G.assert_close(l[nonempty], rl[nonempty], "tmp_sum", atol=1e-4, rtol=2e-3)
+    G.assert_close(o[nonempty], ro[nonempty], "tmp_out")
