@@ -17,8 +17,15 @@
 //     layout, with a 128-bit mask per tile of the keys whose block-table
 //     entry is outside the pool.  A prefill chunk is re-read by every query
 //     tile, so decoding once costs O(L) instead of O(L x query tiles).
-//  2. prefill_attn_kernel, one CTA per (256 query tokens, query head,
-//     sequence) -- two 128-row query tiles A and B -- with 320 threads:
+//  2. prefill_attn_kernel, persistent: one CTA per SM (320 threads), which
+//     takes work items -- (256 query tokens, query head, sequence), two
+//     128-row query tiles A and B -- longest first, in rounds over the grid
+//     in alternating direction.  The roles run through the CTA's items
+//     independently, so that one item's tail overlaps the next item's start:
+//     the tiles of the next item stream in behind the current ones, and each
+//     softmax group writes its next Q tile (once the MMA thread has taken the
+//     current one) before its epilogue, so that the next item's first
+//     S = Q K^T runs during that epilogue.
 //       warp 8: one thread streams the K and V tiles (one 32 KB 1-D bulk copy
 //               each) through a 2-stage shared ring;
 //       warp 9: allocates tensor memory; one thread issues the MMAs:
@@ -37,6 +44,7 @@
 //     KVQ_DEV_TIMEOUT, lets its copies and MMAs drain, frees its tensor
 //     memory and exits without writing.  Every tensor-memory load and store
 //     and every barrier is reached by whole warps.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -63,8 +71,8 @@ constexpr unsigned kPfFull = 0xFFFFFFFFu;
 constexpr int kPfQ = 0;
 constexpr int kPfRing = kPfQ + 2 * kPfTileBytes;
 constexpr int kPfBar = kPfRing + kPfStages * 2 * kPfTileBytes;
-// barriers: full[2], empty[2], q, s[2], p[2], pv[2], drain
-constexpr int kPfNumBars = 2 * kPfStages + 1 + 2 + 2 + 2 + 1;
+// barriers: full[2], empty[2], q[2], q taken[2], s[2], p[2], pv[2], drain
+constexpr int kPfNumBars = 2 * kPfStages + 2 + 2 + 2 + 2 + 2 + 1;
 constexpr int kPfAbort = kPfBar + 8 * kPfNumBars;
 constexpr int kPfTmemSlot = kPfAbort + 8;
 constexpr int kPfSmemBytes = kPfTmemSlot + 8;
@@ -149,45 +157,80 @@ __global__ void __launch_bounds__(256) kv_tile_kernel(const PrefillArgs a)
 // ---------------------------------------------------------------------------
 // 2. flash attention over the tiles
 
+// Work items: (sequence b, query head h, pair of query tiles), longest first.
+// Item i has rank r = i / (B Hq) from the top (pair = pairs(b) - 1 - r), and
+// b = (i % (B Hq)) % B, h = (i % (B Hq)) / B.  An item whose sequence has
+// fewer pairs, or is not a valid chunk, is empty (pair < 0).  Each CTA takes
+// its items in rounds of gridDim.x, in alternating direction, so that the
+// CTAs' shares of the descending sizes even out.
+struct PfItem {
+    int b, h, pair, q0, n, L;
+};
+
+__device__ __forceinline__ PfItem pf_item(const PrefillArgs &a, int i)
+{
+    PfItem it;
+    const int per = a.batch * a.num_q_heads;
+    const int rnk = i / per, rem = i - rnk * per;
+    it.b = rem % a.batch;
+    it.h = rem / a.batch;
+    it.q0 = __ldg(a.q_start + it.b);
+    const int q1 = __ldg(a.q_start + it.b + 1);
+    it.n = q1 - it.q0;
+    it.L = __ldg(a.context_lens + it.b);
+    it.pair = seq_ok(a, it.q0, q1, it.L) ? (it.n + 2 * kPfTile - 1) / (2 * kPfTile) - 1 - rnk : -1;
+    return it;
+}
+
+__device__ __forceinline__ int pf_item_index(int k)
+{
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? G - 1 - c : c);
+}
+
+// key tiles a row of tile x of the item sees (0: no rows)
+__device__ __forceinline__ int pf_tiles_of(const PfItem &it, int x)
+{
+    const int lo = it.pair * 2 * kPfTile + x * kPfTile;
+    return lo < it.n ? (it.L - it.n + min(it.n, lo + kPfTile) - 1) / kPfTile + 1 : 0;
+}
+
+// this CTA's next non-empty item from position k on; false when none is left
+__device__ __forceinline__ bool pf_next(const PrefillArgs &a, int total, int &k, PfItem &it)
+{
+    for (;; ++k) {
+        const int i = pf_item_index(k);
+        if (i >= total) return false;
+        it = pf_item(a, i);
+        if (it.pair >= 0) return true;
+    }
+}
+
 template <bool E4M3>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const PrefillArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int g = h / a.group;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = ((a.max_q_len + 2 * kPfTile - 1) / (2 * kPfTile)) * a.batch * a.num_q_heads;
 
-    // the sequence's chunk; pairs of query tiles in reverse order, so that the
-    // tiles with the most keys start first
-    // (read before grid_dependency_wait: the previous kernel, the tile gather,
-    // does not write them, and it let this grid start only after its own wait
-    // on whatever wrote them)
-    const int q0 = __ldg(a.q_start + b), q1 = __ldg(a.q_start + b + 1);
-    const int n = q1 - q0;
-    const int L = __ldg(a.context_lens + b);
-    if (!seq_ok(a, q0, q1, L)) {
-        const bool empty_ok = n == 0 && q0 >= 0 && q0 <= a.total_q && L >= 0 && L <= a.max_pages * 4;
-        if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && !empty_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
-        return;
-    }
-    const int npairs = (n + 2 * kPfTile - 1) / (2 * kPfTile);
-    const int pair = npairs - 1 - (int)blockIdx.x;
-    if (pair < 0) return;
-    const int base = L - n;                                 // position of query token 0
-    // tile X (0 = A, 1 = B) holds query tokens [i0 + 128 X, min(n, i0 + 128 X + 128))
-    const int i0 = pair * 2 * kPfTile;
-    auto tiles_of = [&](int x) {                            // key tiles a row of tile x sees (0: no rows)
-        const int lo = i0 + x * kPfTile;
-        return lo < n ? (base + min(n, lo + kPfTile) - 1) / kPfTile + 1 : 0;
-    };
-    const int nt_a = tiles_of(0), nt_b = tiles_of(1);
-    const int ntiles = max(nt_a, nt_b);
+    // chunks that cannot be attended are flagged once per launch
+    // (q_start and context_lens are read before grid_dependency_wait: the
+    // previous kernel, the tile gather, does not write them)
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        for (int bb = 0; bb < a.batch; ++bb) {
+            const int q0 = __ldg(a.q_start + bb), q1 = __ldg(a.q_start + bb + 1), L = __ldg(a.context_lens + bb);
+            const int n = q1 - q0;
+            const bool empty_ok = n == 0 && q0 >= 0 && q0 <= a.total_q && L >= 0 && L <= a.max_pages * 4;
+            if (!seq_ok(a, q0, q1, L) && !empty_ok) report(a.err_flag, KVQ_DEV_BAD_LEN);
+        }
 
     const uint32_t bar = smem_u32(smem + kPfBar);
     auto full = [&](int s) { return bar + 8 * s; };
     auto empty = [&](int s) { return bar + 8 * (kPfStages + s); };
-    const uint32_t b_q = bar + 8 * (2 * kPfStages);
-    const uint32_t b_s0 = b_q + 8, b_p0 = b_q + 24, b_pv0 = b_q + 40, b_drain = b_q + 56;   // [X] at + 8 X
+    // per query tile X (at + 8 X): its Q written (softmax group -> MMA), its Q
+    // taken (MMA -> softmax group), S ready, P ready, P V complete
+    const uint32_t b_q0 = bar + 8 * (2 * kPfStages);
+    const uint32_t b_qf0 = b_q0 + 16, b_s0 = b_q0 + 32, b_p0 = b_q0 + 48, b_pv0 = b_q0 + 64, b_drain = b_q0 + 80;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kPfAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kPfTmemSlot);
 
@@ -196,8 +239,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
             mbar_init(full(s), 1);
             mbar_init(empty(s), 1);
         }
-        mbar_init(b_q, kPfSoftmaxWarps);
         for (int x = 0; x < 2; ++x) {
+            mbar_init(b_q0 + 8 * x, kPfSoftmaxWarps / 2);
+            mbar_init(b_qf0 + 8 * x, 1);
             mbar_init(b_s0 + 8 * x, 1);
             mbar_init(b_p0 + 8 * x, kPfSoftmaxWarps / 2);
             mbar_init(b_pv0 + 8 * x, 1);
@@ -213,24 +257,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
     tc_fence_after();
     launch_dependents();      // this CTA holds its tensor memory already
     const uint32_t tmem = *tmem_slot;
-    int issued = 0;
+    int issued = 0;           // K/V tile pairs this CTA's load warp issued, over all its items
 
     if (warp == kPfLoadWarp) {
-        // ================= tile loads =================
+        // ================= tile loads: every item's key tiles, in order =================
         if (lane == 0) {
-            const uint8_t *src = a.tiles + (((int64_t)b * a.num_kv_heads + g) * a.max_tiles) * 2 * kPfTileBytes;
             const uint64_t pol = l2_policy_evict_last();   // every query tile of the group re-reads them
-            for (int t = 0; t < ntiles; ++t) {
-                const int s = t % kPfStages;
-                if (t >= kPfStages &&
-                    !mbar_wait_bounded(empty(s), ((t / kPfStages) - 1) & 1, abort_flag, a.err_flag))
-                    break;
-                mbar_arrive_expect_tx(full(s), 2 * kPfTileBytes);
-                const uint32_t dst = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes);
-                tma_load_1d(dst, src + (int64_t)t * 2 * kPfTileBytes, kPfTileBytes, full(s), pol);
-                tma_load_1d(dst + kPfTileBytes, src + ((int64_t)t * 2 + 1) * kPfTileBytes, kPfTileBytes, full(s),
-                            pol);
-                ++issued;
+            bool ok = true;
+            PfItem it;
+            for (int k = 0; ok && pf_next(a, total, k, it); ++k) {
+                const int ntiles = max(pf_tiles_of(it, 0), pf_tiles_of(it, 1));
+                const uint8_t *src =
+                    a.tiles + (((int64_t)it.b * a.num_kv_heads + it.h / a.group) * a.max_tiles) * 2 * kPfTileBytes;
+                for (int t = 0; t < ntiles; ++t) {
+                    const int T = issued, s = T % kPfStages;
+                    if (T >= kPfStages &&
+                        !mbar_wait_bounded(empty(s), ((T / kPfStages) - 1) & 1, abort_flag, a.err_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full(s), 2 * kPfTileBytes);
+                    const uint32_t dst = smem_u32(smem + kPfRing + s * 2 * kPfTileBytes);
+                    tma_load_1d(dst, src + (int64_t)t * 2 * kPfTileBytes, kPfTileBytes, full(s), pol);
+                    tma_load_1d(dst + kPfTileBytes, src + ((int64_t)t * 2 + 1) * kPfTileBytes, kPfTileBytes,
+                                full(s), pol);
+                    ++issued;
+                }
             }
         }
         __syncwarp();   // the whole warp reaches the teardown barrier together
@@ -240,10 +292,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
             const uint32_t id_qk = umma_idesc_f16(kPfTile, kPfTile, false, false);
             const uint32_t id_pv = umma_idesc_f16(kPfTile, kPfD, false, true);
             const uint32_t q_addr = smem_u32(smem + kPfQ);
-            // S_X = Q_X K_t^T.  S_X last held P_X(t-1), which PV_X(t-1), issued
-            // before this instruction, has read (MMAs of one thread run in order).
-            auto qk = [&](int x, int t) {
-                const uint32_t k_addr = smem_u32(smem + kPfRing + (t % kPfStages) * 2 * kPfTileBytes);
+            // S_X = Q_X K_T^T (T: the CTA's running tile count).  S_X last held P_X
+            // of the previous tile, which the P V issued before this has read
+            // (MMAs of one thread run in order).
+            auto qk = [&](int x, int T) {
+                const uint32_t k_addr = smem_u32(smem + kPfRing + (T % kPfStages) * 2 * kPfTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < kPfD / 16; ++ks)
                     umma_smem_a(tmem + kPfColS + x * kPfTile,
@@ -251,41 +304,65 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                                 umma_desc(k_addr + ks * 256, 128, 2048), id_qk, ks > 0);
                 umma_commit(b_s0 + 8 * x);
             };
-            // O_X += P_X(t) V_t: A = P (tensor memory, two fp16 per column), B = V (MN-major)
-            auto pv = [&](int x, int t) {
-                const uint32_t v_addr = smem_u32(smem + kPfRing + (t % kPfStages) * 2 * kPfTileBytes + kPfTileBytes);
+            // O_X (+)= P_X V_T: A = P (tensor memory, two fp16 per column), B = V (MN-major)
+            auto pv = [&](int x, int T, bool acc) {
+                const uint32_t v_addr = smem_u32(smem + kPfRing + (T % kPfStages) * 2 * kPfTileBytes + kPfTileBytes);
 #pragma unroll
                 for (int ks = 0; ks < kPfTile / 16; ++ks)
                     umma_tmem_a(tmem + kPfColO + x * kPfTile, tmem + kPfColS + x * kPfTile + ks * 8,
-                                umma_desc(v_addr + ks * 4096, 2048, 128), id_pv, t > 0 || ks > 0);
+                                umma_desc(v_addr + ks * 4096, 2048, 128), id_pv, acc || ks > 0);
                 umma_commit(b_pv0 + 8 * x);
             };
-            auto wait_full = [&](int t) {
-                if (!mbar_wait_bounded(full(t % kPfStages), (t / kPfStages) & 1, abort_flag, a.err_flag)) return false;
+            auto wait_full = [&](int T) {
+                if (!mbar_wait_bounded(full(T % kPfStages), (T / kPfStages) & 1, abort_flag, a.err_flag)) return false;
                 tc_fence_after();
                 return true;
             };
-            bool ok = mbar_wait_bounded(b_q, 0, abort_flag, a.err_flag) && ntiles > 0 && wait_full(0);
-            if (ok) {
-                if (nt_a > 0) qk(0, 0);
-                if (nt_b > 0) qk(1, 0);
-            }
-            for (int t = 0; ok && t < ntiles; ++t) {
-                if (t < nt_a) {
-                    if (!mbar_wait_bounded(b_p0, t & 1, abort_flag, a.err_flag)) break;
-                    tc_fence_after();
-                    pv(0, t);
+            int T0 = 0, ni = 0, np[2] = {0, 0};   // tiles before this item, items, P waits per tile
+            bool ok = true;
+            PfItem it;
+            for (int k = 0; ok && pf_next(a, total, k, it); ++k, ++ni) {
+                const int nt_a = pf_tiles_of(it, 0), nt_b = pf_tiles_of(it, 1);
+                const int ntiles = max(nt_a, nt_b);
+                // both query tiles of the item in shared memory; their groups may then write the next item's
+                for (int x = 0; x < 2 && ok; ++x) {
+                    ok = mbar_wait_bounded(b_q0 + 8 * x, ni & 1, abort_flag, a.err_flag);
+                    mbar_arrive(b_qf0 + 8 * x);
                 }
-                const bool next = t + 1 < ntiles;
-                if (next && !wait_full(t + 1)) break;
-                if (t + 1 < nt_a) qk(0, t + 1);
-                if (t < nt_b) {
-                    if (!mbar_wait_bounded(b_p0 + 8, t & 1, abort_flag, a.err_flag)) break;
-                    tc_fence_after();
-                    pv(1, t);
+                tc_fence_after();
+                if (!ok || !wait_full(T0)) {
+                    ok = false;
+                    break;
                 }
-                umma_commit(empty(t % kPfStages));   // the stage's K and V are read once these MMAs complete
-                if (t + 1 < nt_b) qk(1, t + 1);
+                if (nt_a > 0) qk(0, T0);
+                if (nt_b > 0) qk(1, T0);
+                for (int t = 0; ok && t < ntiles; ++t) {
+                    if (t < nt_a) {
+                        if (!mbar_wait_bounded(b_p0, np[0]++ & 1, abort_flag, a.err_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        pv(0, T0 + t, t > 0);
+                    }
+                    const bool next = t + 1 < ntiles;
+                    if (next && !wait_full(T0 + t + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (t + 1 < nt_a) qk(0, T0 + t + 1);
+                    if (t < nt_b) {
+                        if (!mbar_wait_bounded(b_p0 + 8, np[1]++ & 1, abort_flag, a.err_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        pv(1, T0 + t, t > 0);
+                    }
+                    umma_commit(empty((T0 + t) % kPfStages));   // the stage's K and V are read once these complete
+                    if (t + 1 < nt_b) qk(1, T0 + t + 1);
+                }
+                T0 += ntiles;
             }
             // every MMA issued so far completes before the tensor memory is freed
             umma_commit(b_drain);
@@ -297,15 +374,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
         const int x = warp >> 2;                                // query tile
         const int r = 32 * (warp & 3) + lane;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        const int i = i0 + x * kPfTile + r;                     // query token of this row
-        const bool row_ok = i < n;
-        const int limit = row_ok ? base + i : -1;               // last key this row sees
-        const int nt = x ? nt_b : nt_a;
-        const int first_masked = (base + i0 + x * kPfTile) / kPfTile;   // tiles from here on need the causal mask
-        const uint32_t b_s = b_s0 + 8 * x, b_p = b_p0 + 8 * x, b_pv = b_pv0 + 8 * x;
-        // Q row -> K-major Q tile
-        {
-            const __half *qrow = static_cast<const __half *>(a.q) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
+        const uint32_t b_q = b_q0 + 8 * x, b_qf = b_qf0 + 8 * x, b_s = b_s0 + 8 * x, b_p = b_p0 + 8 * x,
+                       b_pv = b_pv0 + 8 * x;
+        const uint32_t sb = tmem + lane_base + kPfColS + x * kPfTile;
+        const uint32_t ob = tmem + lane_base + kPfColO + x * kPfTile;
+        const float qk = a.qk_scale_log2;
+        // this row's Q -> the K-major Q tile of tile X (rows past the chunk: zeros)
+        auto load_q = [&](const PfItem &it) {
+            const int i = it.pair * 2 * kPfTile + x * kPfTile + r;
+            const bool row_ok = i < it.n;
+            const __half *qrow = static_cast<const __half *>(a.q) +
+                                 ((int64_t)(it.q0 + (row_ok ? i : 0)) * a.num_q_heads + it.h) * kPfD;
 #pragma unroll
             for (int c8 = 0; c8 < kPfD / 8; ++c8) {
                 const uint4 v = row_ok ? __ldg(reinterpret_cast<const uint4 *>(qrow) + c8) : make_uint4(0u, 0u, 0u, 0u);
@@ -314,134 +393,159 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(b_q);
-        }
-        const float qk = a.qk_scale_log2;
-        const uint32_t *mask_row = a.tile_mask + (((int64_t)b * a.num_kv_heads + g) * a.max_tiles) * 4;
-        const uint32_t sb = tmem + lane_base + kPfColS + x * kPfTile;
-        const uint32_t ob = tmem + lane_base + kPfColO + x * kPfTile;
-        float ref = -INFINITY;   // the row's reference (log2 units)
-        float lsum = 0.f;        // sum of 2^(s - ref) over the keys so far
-        bool ok = true;          // the same on every lane: tensor-memory loads and stores are warp-wide
-        for (int t = 0; t < nt; ++t) {
-            // keys of this tile left out for a bad block-table entry (almost always none)
-            const uint4 badk = __ldg(reinterpret_cast<const uint4 *>(mask_row) + t);
-            if (!__all_sync(kPfFull, mbar_wait_bounded(b_s, t & 1, abort_flag, a.err_flag))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t xr[kPfTile / 16][16];   // the row's 128 scores, loaded together
-#pragma unroll
-            for (int c = 0; c < kPfTile / 16; ++c) tmem_ld16(sb + 16 * c, xr[c]);
-            tmem_wait_ld();
-            float xv[kPfTile];
-#pragma unroll
-            for (int c = 0; c < kPfTile / 16; ++c) {
-                tmem_regs_ready(xr[c]);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) xv[16 * c + e] = __uint_as_float(xr[c][e]);
-            }
-            if ((badk.x | badk.y | badk.z | badk.w) != 0u) {
-                const uint32_t bw[4] = {badk.x, badk.y, badk.z, badk.w};
-#pragma unroll
-                for (int c = 0; c < kPfTile; ++c)
-                    if ((bw[c >> 5] >> (c & 31)) & 1u) xv[c] = -INFINITY;
-            }
-            // the row maximum of the raw scores over 8 independent chains (the
-            // log2-domain scale qk > 0 is applied after: max(s) * qk = max(s * qk))
-            if (t >= first_masked) {
-                const int k0 = t * kPfTile;
-#pragma unroll
-                for (int c = 0; c < kPfTile; ++c)
-                    if (k0 + c > limit) xv[c] = -INFINITY;
-            }
-            // (chain u takes columns u, u + 8, ..., u + 120, two more per three-way maximum)
-            static_assert(kPfTile == 128, "the maximum's chains cover 128 columns");
-            float m8[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                float m = fmax3(xv[u], xv[u + 8], xv[u + 16]);
-#pragma unroll
-                for (int k = 3; k < 15; k += 2) m = fmax3(m, xv[u + 8 * k], xv[u + 8 * k + 8]);
-                m8[u] = fmaxf(m, xv[u + 120]);
-            }
-            const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * qk;
-            // the reference moves when a score rises more than 2^8 above it; the
-            // row's sum and (once PV(t-1) is complete) its O row are rescaled.  The
-            // O pass is warp-wide; lanes whose reference stays scale by 1.
-            const bool move = mx > ref + 8.f;
-            const float corr = !move ? 1.f : (ref == -INFINITY ? 0.f : fast_exp2(ref - mx));
-            if (move) {
-                lsum *= corr;
-                ref = mx;
-            }
-            if (t > 0 && __any_sync(kPfFull, move)) {
-                if (!__all_sync(kPfFull, mbar_wait_bounded(b_pv, (t - 1) & 1, abort_flag, a.err_flag))) {
+        };
+        int k = 0, ni = 0, ns = 0, npv = 0;   // item position, items, S waits and P V commits of tile X so far
+        bool ok = true;                       // the same on every lane: tensor-memory loads and stores are warp-wide
+        PfItem it;
+        bool have = pf_next(a, total, k, it);
+        if (have) load_q(it);
+        while (have && ok) {
+            const int h = it.h, g = h / a.group, q0 = it.q0, n = it.n;
+            const int base = it.L - n;                              // position of query token 0
+            const int i0 = it.pair * 2 * kPfTile;
+            const int i = i0 + x * kPfTile + r;                     // query token of this row
+            const bool row_ok = i < n;
+            const int limit = row_ok ? base + i : -1;               // last key this row sees
+            const int nt = pf_tiles_of(it, x);
+            const int first_masked = (base + i0 + x * kPfTile) / kPfTile;   // tiles from here on need the causal mask
+            const uint32_t *mask_row = a.tile_mask + (((int64_t)it.b * a.num_kv_heads + g) * a.max_tiles) * 4;
+            float ref = -INFINITY;   // the row's reference (log2 units)
+            float lsum = 0.f;        // sum of 2^(s - ref) over the keys so far
+            for (int t = 0; t < nt; ++t) {
+                // keys of this tile left out for a bad block-table entry (almost always none)
+                const uint4 badk = __ldg(reinterpret_cast<const uint4 *>(mask_row) + t);
+                if (!__all_sync(kPfFull, mbar_wait_bounded(b_s, (ns + t) & 1, abort_flag, a.err_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                uint32_t xr[kPfTile / 16][16];   // the row's 128 scores, loaded together
+#pragma unroll
+                for (int c = 0; c < kPfTile / 16; ++c) tmem_ld16(sb + 16 * c, xr[c]);
+                tmem_wait_ld();
+                float xv[kPfTile];
+#pragma unroll
+                for (int c = 0; c < kPfTile / 16; ++c) {
+                    tmem_regs_ready(xr[c]);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) xv[16 * c + e] = __uint_as_float(xr[c][e]);
+                }
+                if ((badk.x | badk.y | badk.z | badk.w) != 0u) {
+                    const uint32_t bw[4] = {badk.x, badk.y, badk.z, badk.w};
+#pragma unroll
+                    for (int c = 0; c < kPfTile; ++c)
+                        if ((bw[c >> 5] >> (c & 31)) & 1u) xv[c] = -INFINITY;
+                }
+                // the row maximum of the raw scores over 8 independent chains (the
+                // log2-domain scale qk > 0 is applied after: max(s) * qk = max(s * qk))
+                if (t >= first_masked) {
+                    const int k0 = t * kPfTile;
+#pragma unroll
+                    for (int c = 0; c < kPfTile; ++c)
+                        if (k0 + c > limit) xv[c] = -INFINITY;
+                }
+                // (chain u takes columns u, u + 8, ..., u + 120, two more per three-way maximum)
+                static_assert(kPfTile == 128, "the maximum's chains cover 128 columns");
+                float m8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    float m = fmax3(xv[u], xv[u + 8], xv[u + 16]);
+#pragma unroll
+                    for (int k = 3; k < 15; k += 2) m = fmax3(m, xv[u + 8 * k], xv[u + 8 * k + 8]);
+                    m8[u] = fmaxf(m, xv[u + 120]);
+                }
+                const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) * qk;
+                // the reference moves when a score rises more than 2^8 above it; the
+                // row's sum and (once PV(t-1) is complete) its O row are rescaled.  The
+                // O pass is warp-wide; lanes whose reference stays scale by 1.
+                const bool move = mx > ref + 8.f;
+                const float corr = !move ? 1.f : (ref == -INFINITY ? 0.f : fast_exp2(ref - mx));
+                if (move) {
+                    lsum *= corr;
+                    ref = mx;
+                }
+                if (t > 0 && __any_sync(kPfFull, move)) {
+                    if (!__all_sync(kPfFull, mbar_wait_bounded(b_pv, (npv + t - 1) & 1, abort_flag, a.err_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < kPfD; c += 16) {
+                        uint32_t r16[16];
+                        tmem_ld16(ob + c, r16);
+                        tmem_wait_ld();
+                        tmem_regs_ready(r16);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * corr);
+                        tmem_st16(ob + c, r16);
+                    }
+                }
+                // P = 2^(s qk - ref) as fp16 pairs over the first 64 columns of S; the
+                // exponents and the row sum two columns per instruction, the sum over
+                // four independent pair chains
+                const float rf = (ref == -INFINITY) ? 0.f : ref;   // a row with no key yet: P = 0
+                const float2 qk2 = make_float2(qk, qk), nrf2 = make_float2(-rf, -rf);
+                float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+                for (int c = 0; c < kPfTile; c += 32) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 z = ffma2(make_float2(xv[c + 2 * e], xv[c + 2 * e + 1]), qk2, nrf2);
+                        const float2 p = make_float2(fast_exp2(z.x), fast_exp2(z.y));
+                        l4[e & 3] = fadd2(l4[e & 3], p);
+                        w[e] = pack_half2(p.x, p.y);
+                    }
+                    tmem_st16(sb + c / 2, w);
+                }
+                lsum += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_p);
+            }
+            ns += nt;
+            // the next item's Q: this tile's last S = Q K^T has been read, and the MMA
+            // thread has taken this item's Q (so that no Q arrival runs two items ahead)
+            ++k;
+            PfItem nxt;
+            const bool have_next = ok && pf_next(a, total, k, nxt);
+            if (have_next) {
+                if (!__all_sync(kPfFull, mbar_wait_bounded(b_qf, ni & 1, abort_flag, a.err_flag))) ok = false;
+                else load_q(nxt);
+            }
+            ++ni;
+            // ---- epilogue: O / l * v_scale -> fp16 output row (every lane loads, valid rows store) ----
+            if (nt > 0 && ok &&
+                __all_sync(kPfFull, !*abort_flag && mbar_wait_bounded(b_pv, (npv + nt - 1) & 1, abort_flag, a.err_flag))) {
+                tc_fence_after();
+                const float coef = lsum > 0.f ? a.out_scale / lsum : 0.f;
+                __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
 #pragma unroll 1
                 for (int c = 0; c < kPfD; c += 16) {
                     uint32_t r16[16];
                     tmem_ld16(ob + c, r16);
                     tmem_wait_ld();
                     tmem_regs_ready(r16);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) r16[e] = __float_as_uint(__uint_as_float(r16[e]) * corr);
-                    tmem_st16(ob + c, r16);
+                    uint4 o0, o1;
+                    o0.x = pack_half2(__uint_as_float(r16[0]) * coef, __uint_as_float(r16[1]) * coef);
+                    o0.y = pack_half2(__uint_as_float(r16[2]) * coef, __uint_as_float(r16[3]) * coef);
+                    o0.z = pack_half2(__uint_as_float(r16[4]) * coef, __uint_as_float(r16[5]) * coef);
+                    o0.w = pack_half2(__uint_as_float(r16[6]) * coef, __uint_as_float(r16[7]) * coef);
+                    o1.x = pack_half2(__uint_as_float(r16[8]) * coef, __uint_as_float(r16[9]) * coef);
+                    o1.y = pack_half2(__uint_as_float(r16[10]) * coef, __uint_as_float(r16[11]) * coef);
+                    o1.z = pack_half2(__uint_as_float(r16[12]) * coef, __uint_as_float(r16[13]) * coef);
+                    o1.w = pack_half2(__uint_as_float(r16[14]) * coef, __uint_as_float(r16[15]) * coef);
+                    if (row_ok) {
+                        *reinterpret_cast<uint4 *>(orow + c) = o0;
+                        *reinterpret_cast<uint4 *>(orow + c + 8) = o1;
+                    }
                 }
             }
-            // P = 2^(s qk - ref) as fp16 pairs over the first 64 columns of S; the
-            // exponents and the row sum two columns per instruction, the sum over
-            // four independent pair chains
-            const float rf = (ref == -INFINITY) ? 0.f : ref;   // a row with no key yet: P = 0
-            const float2 qk2 = make_float2(qk, qk), nrf2 = make_float2(-rf, -rf);
-            float2 l4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-            for (int c = 0; c < kPfTile; c += 32) {
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 z = ffma2(make_float2(xv[c + 2 * e], xv[c + 2 * e + 1]), qk2, nrf2);
-                    const float2 p = make_float2(fast_exp2(z.x), fast_exp2(z.y));
-                    l4[e & 3] = fadd2(l4[e & 3], p);
-                    w[e] = pack_half2(p.x, p.y);
-                }
-                tmem_st16(sb + c / 2, w);
-            }
-            lsum += ((l4[0].x + l4[0].y) + (l4[1].x + l4[1].y)) + ((l4[2].x + l4[2].y) + (l4[3].x + l4[3].y));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_p);
-        }
-        // ---- epilogue: O / l * v_scale -> fp16 output row (every lane loads, valid rows store) ----
-        if (nt > 0 && ok &&
-            __all_sync(kPfFull, !*abort_flag && mbar_wait_bounded(b_pv, (nt - 1) & 1, abort_flag, a.err_flag))) {
-            tc_fence_after();
-            const float coef = lsum > 0.f ? a.out_scale / lsum : 0.f;
-            __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
-#pragma unroll 1
-            for (int c = 0; c < kPfD; c += 16) {
-                uint32_t r16[16];
-                tmem_ld16(ob + c, r16);
-                tmem_wait_ld();
-                tmem_regs_ready(r16);
-                uint4 o0, o1;
-                o0.x = pack_half2(__uint_as_float(r16[0]) * coef, __uint_as_float(r16[1]) * coef);
-                o0.y = pack_half2(__uint_as_float(r16[2]) * coef, __uint_as_float(r16[3]) * coef);
-                o0.z = pack_half2(__uint_as_float(r16[4]) * coef, __uint_as_float(r16[5]) * coef);
-                o0.w = pack_half2(__uint_as_float(r16[6]) * coef, __uint_as_float(r16[7]) * coef);
-                o1.x = pack_half2(__uint_as_float(r16[8]) * coef, __uint_as_float(r16[9]) * coef);
-                o1.y = pack_half2(__uint_as_float(r16[10]) * coef, __uint_as_float(r16[11]) * coef);
-                o1.z = pack_half2(__uint_as_float(r16[12]) * coef, __uint_as_float(r16[13]) * coef);
-                o1.w = pack_half2(__uint_as_float(r16[14]) * coef, __uint_as_float(r16[15]) * coef);
-                if (row_ok) {
-                    *reinterpret_cast<uint4 *>(orow + c) = o0;
-                    *reinterpret_cast<uint4 *>(orow + c + 8) = o1;
-                }
-            }
+            npv += nt;
+            it = nxt;
+            have = have_next;
         }
     }
 
@@ -490,7 +594,10 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t stream)
     }
     e = launch_pdl(kv_tile_kernel<E4M3>, dim3(a.max_tiles, a.num_kv_heads, a.batch), dim3(256), 0, stream, a);
     if (e != cudaSuccess) return e;
-    const dim3 grid((a.max_q_len + 2 * kPfTile - 1) / (2 * kPfTile), a.num_q_heads, a.batch);
+    // one CTA per SM, each taking its work items in turn
+    const int64_t items = (int64_t)((a.max_q_len + 2 * kPfTile - 1) / (2 * kPfTile)) * a.batch * a.num_q_heads;
+    if (items > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)std::min<int64_t>(items, device_sm_count()));
     return launch_pdl(prefill_attn_kernel<E4M3>, grid, dim3(kPfThreads), kPfSmemBytes, stream, a);
 }
 
