@@ -109,7 +109,9 @@ __device__ __forceinline__ bool seq_ok(const PrefillArgs &a, int q0, int q1, int
 template <bool E4M3>
 __global__ void __launch_bounds__(256) kv_tile_kernel(const PrefillArgs a)
 {
-    const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // four blocks per tile: K or V (kv), keys 0-63 or 64-127 (kh)
+    const int j = blockIdx.x >> 2, kv = (blockIdx.x >> 1) & 1, kh = blockIdx.x & 1;
+    const int g = blockIdx.y, b = blockIdx.z;
     grid_dependency_wait();
     launch_dependents();
     const int L = __ldg(a.context_lens + b);
@@ -120,15 +122,14 @@ __global__ void __launch_bounds__(256) kv_tile_kernel(const PrefillArgs a)
     const int64_t tile = ((int64_t)b * a.num_kv_heads + g) * a.max_tiles + j;
     uint8_t *dst = a.tiles + tile * 2 * kPfTileBytes;
     constexpr int kElem = E4M3 ? 1 : 2;
-    __shared__ uint32_t bad[4];   // keys of the tile whose page is outside the pool
-    if (threadIdx.x < 4) bad[threadIdx.x] = 0u;
+    __shared__ uint32_t bad[2];   // this block's keys whose page is outside the pool (K blocks)
+    if (threadIdx.x < 2) bad[threadIdx.x] = 0u;
     __syncthreads();
     // item = (key n8 group, 8-channel group c8, key n%8), key fastest: the 8
     // lanes of a quarter warp write one 128-byte core-matrix row block
-    for (int it = threadIdx.x; it < 2 * kPfTile * (kPfD / 8); it += blockDim.x) {
-        const int kv = it / (kPfTile * (kPfD / 8));
-        const int r = it % (kPfTile * (kPfD / 8));
-        const int key = (r / (8 * (kPfD / 8))) * 8 + (r & 7);
+    constexpr int kHalf = kPfTile / 2;
+    for (int r = threadIdx.x; r < kHalf * (kPfD / 8); r += blockDim.x) {
+        const int key = kh * kHalf + (r / (8 * (kPfD / 8))) * 8 + (r & 7);
         const int c8 = (r / 8) % (kPfD / 8);
         const int pos = j * kPfTile + key;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);   // keys past the context: zero (and masked)
@@ -145,13 +146,13 @@ __global__ void __launch_bounds__(256) kv_tile_kernel(const PrefillArgs a)
                 }
             } else if (kv == 0 && c8 == 0) {
                 report(a.err_flag, KVQ_DEV_BAD_PAGE);   // the row stays zero and its key is masked
-                atomicOr(&bad[key >> 5], 1u << (key & 31));
+                atomicOr(&bad[(key - kh * kHalf) >> 5], 1u << (key & 31));
             }
         }
         *reinterpret_cast<uint4 *>(dst + kv * kPfTileBytes + tile_off(key, c8)) = v;
     }
     __syncthreads();
-    if (threadIdx.x < 4) a.tile_mask[tile * 4 + threadIdx.x] = bad[threadIdx.x];
+    if (kv == 0 && threadIdx.x < 2) a.tile_mask[tile * 4 + 2 * kh + threadIdx.x] = bad[threadIdx.x];
 }
 
 // ---------------------------------------------------------------------------
@@ -592,7 +593,7 @@ static cudaError_t launch_prefill_t(const PrefillArgs &a, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
-    e = launch_pdl(kv_tile_kernel<E4M3>, dim3(a.max_tiles, a.num_kv_heads, a.batch), dim3(256), 0, stream, a);
+    e = launch_pdl(kv_tile_kernel<E4M3>, dim3(4 * a.max_tiles, a.num_kv_heads, a.batch), dim3(256), 0, stream, a);
     if (e != cudaSuccess) return e;
     // one CTA per SM, each taking its work items in turn
     const int64_t items = (int64_t)((a.max_q_len + 2 * kPfTile - 1) / (2 * kPfTile)) * a.batch * a.num_q_heads;
