@@ -323,8 +323,16 @@ class Arm:
         self.mma_sync = False  # many-row tiles: the tcgen05 kernel (default) or the mma.sync kernel
         self.fp8_qk = False    # tcgen05 kernel: fp16 scores (default) or the FP8 score variant
         self.uses_tc = w.head_dim == 128 and w.group * w.q_len > 8
-        self.launches = 3 * self.layers   # kernels of one step: append, attention, combine per layer
+        # dense batches: the fused step call (the append done by the attention launch);
+        # with top-k lists or a prefill chunk, the append call and then the attention call
+        self.fused = self.topk_idx is None and not self.prefill
+        self.shape4 = (w.batch, w.q_len, w.num_kv_heads, w.head_dim)
         torch.cuda.synchronize(dev)
+
+    @property
+    def launches(self):
+        """Kernels of one step: per layer attention and combine, plus the append unless fused."""
+        return (2 if self.fused else 3) * self.layers
 
     def _append(self, l, k, v, slots, kc, vc):
         if self.e4m3:
@@ -364,15 +372,34 @@ class Arm:
                                                split_pages=self.w.split_pages, mma_sync=self.mma_sync,
                                                longest_first=self.longest_first)
 
+    def _layer_step(self, l, kc, vc, k, v, slots, q, bt, cl, out):
+        """Layer l's share of a step: the append of the step's tokens and the
+        attention over the updated cache -- the fused step call (attention with
+        the append, then the combine: two launches), or the append call and the
+        attention call (three launches); chained with programmatic dependent
+        launch."""
+        kvq = self.kvq
+        if not self.fused:
+            self._append(l, k, v, slots, kc, vc)
+            self._attention(l, kc, vc, q, bt, cl, out=out)
+            return
+        k4, v4 = k.view(self.shape4), v.view(self.shape4)
+        if self.e4m3:
+            kvq.paged_decode_step_e4m3(q, k4, v4, kc, vc, bt, cl, self.ks[l], self.vs[l], self.ws, out,
+                                       num_splits=self.S, err_flag=self.err, split_pages=self.w.split_pages,
+                                       bitcast_decode=self.bitcast, mma_sync=self.mma_sync, fp8_qk=self.fp8_qk,
+                                       longest_first=self.longest_first)
+        else:
+            kvq.paged_decode_step_fp16(q, k4, v4, kc, vc, bt, cl, self.ws, out, num_splits=self.S,
+                                       err_flag=self.err, split_pages=self.w.split_pages, mma_sync=self.mma_sync,
+                                       longest_first=self.longest_first)
+
     def step(self, i):
-        """One step on pool copy i: for every layer, the append of the step's
-        tokens and the attention call (split-K attention, then the log-sum-exp
-        combine of its partials: three launches per layer, chained with
-        programmatic dependent launch)."""
+        """One step on pool copy i: every layer's append and attention."""
         for l in range(self.layers):
             kc, vc = self.pools[i % self.copies][l]
-            self._append(l, self.k_new[l], self.v_new[l], self.step_slots, kc, vc)
-            self._attention(l, kc, vc, out=self.out[l])
+            self._layer_step(l, kc, vc, self.k_new[l], self.v_new[l], self.step_slots, self.q[l], self.bt,
+                             self.cl, self.out[l])
 
     def capture(self):
         """CUDA graphs of the step: one per pool copy holding one step, and
@@ -478,7 +505,7 @@ class Arm:
         buffers); serial = copies and compute in one graph per step on one
         stream."""
         torch = self.torch
-        src = [("slots", self.step_slots), ("bt", self.bt), ("cl", self.cl)]
+        src = ([] if self.fused else [("slots", self.step_slots)]) + [("bt", self.bt), ("cl", self.cl)]
         for l in range(self.layers):
             src += [(f"q{l}", self.q[l]), (f"k{l}", self.k_new[l]), (f"v{l}", self.v_new[l])]
         sets = [staged_buffers(torch, src, self.dev) for _ in range(2)]
@@ -495,8 +522,8 @@ class Arm:
             dev = sets[i % 2][1]
             for l in range(self.layers):
                 kc, vc = self.pools[i % self.copies][l]
-                self._append(l, dev[f"k{l}"], dev[f"v{l}"], dev["slots"], kc, vc)
-                self._attention(l, kc, vc, dev[f"q{l}"], dev["bt"], dev["cl"], out=outs[i % 2][l])
+                self._layer_step(l, kc, vc, dev[f"k{l}"], dev[f"v{l}"], dev.get("slots"), dev[f"q{l}"], dev["bt"],
+                                 dev["cl"], outs[i % 2][l])
 
         def copy_out(p):
             out_host[p].copy_(outs[p], non_blocking=True)
@@ -1162,6 +1189,11 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
     gbs, seq_steps = aggregate(step_bytes, w.batch, world, ms)
     achieved = arm.bytes["attention_kernel"] / (kern_avg * 1e-3) / 1e9
     pct = arm.step_percentiles(max(20, args.steps)) if headline else None   # context: per-step spread
+    separate_ms = None
+    if arm.fused:                                       # context: the append call, then the attention call
+        arm.fused, arm.graphs, arm.many = False, None, None
+        separate_ms = reduce_max(arm.time(args.steps, args.warmup, barrier)) / args.steps
+        arm.fused, arm.graphs, arm.many = True, None, None
     arm.bitcast = True                                  # context: the pages' bitcast decoder
     bitcast_ms = reduce_max(arm.time_kernel(kern_steps, args.warmup))
     arm.bitcast = False
@@ -1178,7 +1210,8 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
     e2e_ms, e2e_serial_ms, h2d, d2h = arm.time_e2e(e2e_steps, args.warmup if arm.layers == 1 else 2)
     e2e_ms, e2e_serial_ms = reduce_max(e2e_ms), reduce_max(e2e_serial_ms)
     info = dict(S=arm.S, copies=arm.copies, pool_bytes=arm.pool_bytes, layers=arm.layers,
-                launches=arm.launches, uses_tc=arm.uses_tc, kernel_bytes=arm.bytes["attention_kernel"])
+                launches=arm.launches, uses_tc=arm.uses_tc, kernel_bytes=arm.bytes["attention_kernel"],
+                fused=arm.fused)
     del arm
     torch.cuda.empty_cache()
 
@@ -1218,6 +1251,10 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
         "fp16_arm": fp16,
         "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
         "step_ms_p10_p50_p90_one_graph_each": pct,
+        "step_calls": ("paged_decode_step_e4m3 per layer (the append inside the attention launch, then the "
+                       "combine)") if info["fused"] else
+                      "kv_append_e4m3, then paged_decode_attn_e4m3, per layer",
+        "separate_append_ms_per_step": separate_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": profiled_traffic(kname, w.name),
@@ -1239,8 +1276,9 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
                 "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": info["launches"] * args.steps,
         "launch": (f"CUDA graphs of {GRAPH_STEPS} steps" if layers == 1 else "a CUDA graph per step") +
-                  " (per layer: the append, then the attention call -- attention and combine kernels; "
-                  "programmatic dependent launch); e2e: the compute of each step in a CUDA graph, H2D and D2H "
+                  (" (per layer: the fused step call -- attention with the append, then the combine" if info["fused"]
+                   else " (per layer: the append, then the attention call -- attention and combine kernels") +
+                  "; programmatic dependent launch); e2e: the compute of each step in a CUDA graph, H2D and D2H "
                   "copies on their own streams",
     }
 

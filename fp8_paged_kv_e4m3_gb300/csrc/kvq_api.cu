@@ -125,6 +125,8 @@ struct AttnCall {
     const kvq_attn_params *p;
     int32_t *err_flag;
     void *stream;
+    const void *k_new = nullptr;   // fused step: this step's new rows (fp16), appended in the launch
+    const void *v_new = nullptr;
 };
 
 static int run_attention(const AttnCall &c, bool with_combine)
@@ -145,8 +147,15 @@ static int run_attention(const AttnCall &c, bool with_combine)
         (!c.e4m3 || (p.flags & (KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_MMA_SYNC)) ||
          !tc_supported(p.head_dim, (p.num_q_heads / p.num_kv_heads) * p.q_len)))
         return KVQ_ERR_UNSUPPORTED;
+    // the fused step appends this step's rows of each sequence; with a top-k
+    // list another split's CTA could read them, so it has no top-k form
+    if ((c.k_new == nullptr) != (c.v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
+    if (c.k_new && c.topk_idx) return KVQ_ERR_UNSUPPORTED;
+    // its instances use the hardware E4M3 conversion and fp16 scores
+    if (c.k_new && (p.flags & (KVQ_ATTN_BITCAST_DECODE | KVQ_ATTN_FP8_QK))) return KVQ_ERR_UNSUPPORTED;
     if (!aligned16(c.q) || !aligned16(c.k_cache) || !aligned16(c.v_cache) ||
-        (c.out && !aligned16(c.out)) || !aligned16(c.workspace))
+        (c.out && !aligned16(c.out)) || !aligned16(c.workspace) || (c.k_new && !aligned16(c.k_new)) ||
+        (c.v_new && !aligned16(c.v_new)))
         return KVQ_ERR_ALIGNMENT;
     const int32_t S = resolve_splits(&p);
     const int64_t rows_total = int64_t(p.batch) * p.num_q_heads * p.q_len;
@@ -192,6 +201,10 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.fp8_qk = (p.flags & KVQ_ATTN_FP8_QK) != 0;
     a.early_pages = (p.flags & KVQ_ATTN_STRICT_ORDER) == 0;
     a.longest_first = (p.flags & KVQ_ATTN_LONGEST_FIRST) != 0;
+    a.k_new = c.k_new;
+    a.v_new = c.v_new;
+    a.k_scale = c.e4m3 ? c.k_scale : 1.0f;
+    a.v_scale = c.e4m3 ? c.v_scale : 1.0f;
 
     cudaStream_t stream = static_cast<cudaStream_t>(c.stream);
     if (launch_attention(c.e4m3, p.head_dim, a, stream) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -405,6 +418,33 @@ int paged_decode_attn_fp16_partial(const void *q, const void *k_cache, const voi
     const AttnCall c{false, q, k_cache, v_cache, num_pages, block_tables, context_lens, 1.0f, 1.0f,
                      topk_idx, topk_lens, workspace, workspace_bytes, nullptr, p, err_flag, stream};
     return run_attention(c, false);
+}
+
+int paged_decode_step_e4m3(const void *q, const void *k_new, const void *v_new, uint8_t *k_cache,
+                           uint8_t *v_cache, int64_t num_pages, const int32_t *block_tables,
+                           const int32_t *context_lens, float k_scale, float v_scale, float *workspace,
+                           size_t workspace_bytes, void *out, const kvq_attn_params *p, int32_t *err_flag,
+                           void *stream)
+{
+    if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+    AttnCall c{true, q, k_cache, v_cache, num_pages, block_tables, context_lens, k_scale, v_scale,
+               nullptr, nullptr, workspace, workspace_bytes, out, p, err_flag, stream};
+    c.k_new = k_new;
+    c.v_new = v_new;
+    return run_attention(c, true);
+}
+
+int paged_decode_step_fp16(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           int64_t num_pages, const int32_t *block_tables, const int32_t *context_lens,
+                           float *workspace, size_t workspace_bytes, void *out, const kvq_attn_params *p,
+                           int32_t *err_flag, void *stream)
+{
+    if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+    AttnCall c{false, q, k_cache, v_cache, num_pages, block_tables, context_lens, 1.0f, 1.0f,
+               nullptr, nullptr, workspace, workspace_bytes, out, p, err_flag, stream};
+    c.k_new = k_new;
+    c.v_new = v_new;
+    return run_attention(c, true);
 }
 
 int kvq_lse_combine(const float *workspace, size_t workspace_bytes, void *out,

@@ -104,6 +104,68 @@ cudaError_t launch_append(bool e4m3, const void *k_new, const void *v_new,
 }
 
 // ---------------------------------------------------------------------------
+// The fused step's append where the attention kernel does not append itself
+// (the tcgen05 kernel's shapes): token t = b * q_len + i of k_new / v_new
+// ([B][q_len][Hkv][D]) goes to position L_b - q_len + i of sequence b, in the
+// page its block table names.  A sequence with an invalid length, or a row
+// whose page entry is out of range, is skipped; the attention launch that
+// follows reports both.  Same arithmetic as append_kernel.
+template <bool E4M3>
+__global__ void __launch_bounds__(256) append_step_kernel(const uint4 *__restrict__ k_new,
+                                                          const uint4 *__restrict__ v_new, AttnArgs a,
+                                                          int64_t num_vecs, int vecs_per_token,
+                                                          int vecs_per_head, int head_dim)
+{
+    grid_dependency_wait();   // new K/V may come from the previous kernel
+    launch_dependents();
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= num_vecs) return;
+    const int64_t tok = idx / vecs_per_token;
+    const int within = (int)(idx - tok * vecs_per_token);
+    const int g = within / vecs_per_head;
+    const int d0 = (within - g * vecs_per_head) * 8;
+    const int b = (int)(tok / a.q_len), i = (int)(tok % a.q_len);
+    const int L = __ldg(a.context_lens + b);
+    if (L < a.q_len || L > a.max_pages * 4) return;
+    const int pos = L - a.q_len + i;
+    const int32_t page = __ldg(a.block_tables + (int64_t)b * a.max_pages + pos / 4);
+    if (page < 0 || (int64_t)page >= a.num_pages) return;
+    const int64_t dst = (((int64_t)page * a.num_kv_heads + g) * 4 + (pos & 3)) * head_dim + d0;
+    auto *kc = static_cast<uint8_t *>(const_cast<void *>(a.k_cache));
+    auto *vc = static_cast<uint8_t *>(const_cast<void *>(a.v_cache));
+    const uint4 kv = __ldg(k_new + idx);
+    const uint4 vv = __ldg(v_new + idx);
+    if (E4M3) {
+        uint2 kq, vq;
+        kq.x = quantize4(make_uint2(kv.x, kv.y), a.k_scale);
+        kq.y = quantize4(make_uint2(kv.z, kv.w), a.k_scale);
+        vq.x = quantize4(make_uint2(vv.x, vv.y), a.v_scale);
+        vq.y = quantize4(make_uint2(vv.z, vv.w), a.v_scale);
+        *reinterpret_cast<uint2 *>(kc + dst) = kq;
+        *reinterpret_cast<uint2 *>(vc + dst) = vq;
+    } else {
+        *reinterpret_cast<uint4 *>(kc + 2 * dst) = kv;
+        *reinterpret_cast<uint4 *>(vc + 2 * dst) = vv;
+    }
+}
+
+cudaError_t launch_append_step(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream)
+{
+    const int vph = head_dim / 8;
+    const int vpt = vph * a.num_kv_heads;
+    const int64_t n = (int64_t)a.batch * a.q_len * vpt;
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    auto kn = static_cast<const uint4 *>(a.k_new);
+    auto vn = static_cast<const uint4 *>(a.v_new);
+    const dim3 grid((unsigned)blocks);
+    if (e4m3)
+        return launch_pdl(append_step_kernel<true>, grid, dim3(256), 0, stream, kn, vn, a, n, vpt, vph, head_dim);
+    return launch_pdl(append_step_kernel<false>, grid, dim3(256), 0, stream, kn, vn, a, n, vpt, vph, head_dim);
+}
+
+// ---------------------------------------------------------------------------
 // amax = max |x| over an fp16 tensor, one CTA (calibration is off the hot
 // loop; a single CTA keeps the result a plain store with no atomics and no
 // pre-zeroing).  NaN anywhere gives NaN.

@@ -8,6 +8,18 @@ namespace kvq {
 cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream)
 {
     if (a.batch == 0) return cudaSuccess;
+    // The fused step: on the split kernel, instances of their own append inside the launch (the
+    // attention-only instances compile without that code).  The tcgen05 kernel, whose registers
+    // are at their limit, ran measurably slower with it compiled in, even unused; there a small
+    // kernel appends by block table first, and the attention-only instance follows.
+    if (a.k_new) {
+        if (a.mma_sync || !tc_supported(head_dim, a.rows)) return launch_attention_step(e4m3, head_dim, a, stream);
+        const cudaError_t e = launch_append_step(e4m3, head_dim, a, stream);
+        if (e != cudaSuccess) return e;
+        AttnArgs plain = a;
+        plain.k_new = plain.v_new = nullptr;
+        return launch_attention_tc(e4m3, plain, stream);
+    }
     // many query rows per kv head (MTP verify): the tcgen05 kernel (either E4M3 decoder)
     if (!a.mma_sync && tc_supported(head_dim, a.rows)) return launch_attention_tc(e4m3, a, stream);
     if (e4m3 && a.bitcast_decode) return launch_attention_bitcast(head_dim, a, stream);

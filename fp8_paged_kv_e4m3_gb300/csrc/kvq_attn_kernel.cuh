@@ -44,7 +44,9 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
@@ -75,6 +77,7 @@ struct Split {
 // wait could see the phase parity of the slot's previous use.
 template <bool E4M3, int D, int PPS, int MIN_STAGES = 2>
 struct Geometry {
+    static constexpr int kD = D;
     static constexpr int kElem = E4M3 ? 1 : 2;
     static constexpr int kRowBytes = D * kElem;           // one token of one kv head
     static constexpr int kChunk = 4 * kRowBytes;          // one page of one kv head
@@ -275,6 +278,77 @@ __device__ __forceinline__ SeqPick lpt_pick(const AttnArgs &a, int z, uint8_t *s
     return seq_identity(a, b);
 }
 
+// ---------------------------------------------------------------------------
+// Fused step: quantise-on-append inside the attention launch (PR "[Model]
+// [SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path", section
+// Changes: the cache is written in calibrated E4M3 as tokens are appended).
+//
+// Two fp16 values (element 0 in the low half) to two E4M3 codes (element 0
+// in the low byte): each divided by the layer's scale in IEEE binary32
+// (round to nearest even), then the satfinite conversion (round to nearest
+// even, finite overflow to +-448) -- the append kernel's two roundings.
+__device__ __forceinline__ uint32_t quantize_pair(uint32_t h2, float scale)
+{
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+    return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale)), __NV_SATFINITE,
+                                    __NV_E4M3);
+}
+
+// Orders this thread's global stores (generic proxy) before bulk copies
+// (async proxy) issued after a later synchronisation with the issuing thread.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// The producer warp of one half (K when !is_v, V otherwise) writes this
+// step's new rows of (sequence b, kv head g) -- positions L - q_len .. L - 1,
+// input rows b * q_len + i -- whose pages lie in its split, into the page
+// slots its block table names, and fences them for its bulk copies.  Only
+// this CTA reads those pages (dense splits partition the pages of a
+// (sequence, kv head)), so no other CTA can see them half-written.  Lane l
+// takes channels [l * D / 32, (l + 1) * D / 32) of every row; every load
+// (the rows' page entries and new values, q_len <= 4) is issued before any
+// store, so that one memory round trip covers them.  A bad page is skipped
+// here and reported when its copy is issued.
+template <class G>
+__device__ __forceinline__ void append_step_rows(const AttnArgs &a, const SplitRange &r, int b, int g, int lane,
+                                                 bool is_v)
+{
+    constexpr int CPL = G::kD / 32;   // channels per lane: 4 or 2
+    static_assert(CPL == 4 || CPL == 2, "head_dim 128 or 64");
+    using Vec = typename std::conditional<CPL == 4, uint2, uint32_t>::type;   // CPL fp16 values
+    const auto *src = static_cast<const uint8_t *>(is_v ? a.v_new : a.k_new) +
+                      ((int64_t)b * a.q_len * a.num_kv_heads + g) * (G::kD * 2) + lane * (CPL * 2);
+    auto *pool = static_cast<uint8_t *>(const_cast<void *>(is_v ? a.v_cache : a.k_cache)) +
+                 (int64_t)g * 4 * G::kRowBytes + lane * (CPL * G::kElem);
+    const float scale = is_v ? a.v_scale : a.k_scale;
+    const int first = r.L - a.q_len;
+    int phys[4];
+    Vec h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int item = (first + i) >> 2;
+        const bool mine = i < a.q_len && item >= r.item0 && item < r.item1;
+        phys[i] = mine ? __ldg(r.bt_row + item) : -1;
+        if (mine) h[i] = *reinterpret_cast<const Vec *>(src + (int64_t)i * a.num_kv_heads * (G::kD * 2));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (phys[i] < 0 || (int64_t)phys[i] >= a.num_pages) continue;
+        uint8_t *dst = pool + ((int64_t)phys[i] * a.num_kv_heads * 4 + ((first + i) & 3)) * G::kRowBytes;
+        const uint32_t *x = reinterpret_cast<const uint32_t *>(&h[i]);
+        if (G::kElem == 2)
+            *reinterpret_cast<Vec *>(dst) = h[i];
+        else if (CPL == 4)
+            *reinterpret_cast<uint32_t *>(dst) = quantize_pair(x[0], scale) | (quantize_pair(x[1], scale) << 16);
+        else
+            *reinterpret_cast<uint16_t *>(dst) = (uint16_t)quantize_pair(x[0], scale);
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+}
+
 // One producer warp (K pages when !is_v, V pages otherwise) walks the
 // split's nst stages: it reads the block table a batch ahead, waits for the
 // stage's ring slot to be released, records the token positions (K warp),
@@ -285,7 +359,14 @@ __device__ __forceinline__ SeqPick lpt_pick(const AttnArgs &a, int z, uint8_t *s
 // this step's append does not write) may be copied before that wait; the
 // wait comes before the first stage that reaches past them.  -1: the caller
 // has waited.
-template <class G, int PPS>
+// FUSED (the fused step's instances; dense only): a producer whose split
+// holds some of this step's new rows first waits for the preceding kernel
+// (which may write them) and appends its half of them, then walks its stages
+// as the other instances do.  Its first copies start a memory round trip
+// later; the consumers, which wait for the preceding kernel before reading
+// q, start no earlier anyway.  Appending later inside the stage loop
+// measured slower: that code in the loop slowed every stage.
+template <class G, int PPS, bool FUSED = false>
 __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRange &r, int nst, int b, int g,
                                               int lane, bool is_v, int bt_spec, uint32_t ring, uint32_t bar0,
                                               int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad,
@@ -308,6 +389,14 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
             const int p = lane % PPS;                      // page of the stage this lane copies
             const bool copier = lane < PPS;
             bool waited = clean_items < 0;
+            if constexpr (FUSED) {
+                const int first_new = max(L - a.q_len, 0) / 4;   // first page with a new row
+                if (nst > 0 && first_new < item1) {
+                    if (!waited) grid_dependency_wait();
+                    waited = true;
+                    append_step_rows<G>(a, r, b, g, lane, is_v);
+                }
+            }
             for (int st = 0; st < nst; ++st) {
                 const int slot = st % G::kStages;
                 if (!waited && item0 + (st + 1) * PPS > clean_items) {
@@ -419,7 +508,7 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
 // source pages (E4M3 bits placed into fp16 bits, the value * 2^-8, exact),
 // with the 2^8 folded into the hoisted scales.  Both give the same fp16
 // values up to that power of two, so the outputs are identical.
-template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT = false>
+template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT = false, bool FUSED = false>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     attn_split_kernel(const AttnArgs a)
 {
@@ -502,8 +591,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     if (warp >= kConsumerWarps) {
         // ================= producers: the first moves K, the second V =================
         const bool is_v = warp == kConsumerWarps + 1;
-        issued = produce_stages<G, PPS>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos, abort_flag,
-                                        stage_bad, early ? max(L - a.q_len, 0) / 4 : -1);
+        issued = produce_stages<G, PPS, FUSED>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos,
+                                               abort_flag, stage_bad, early ? max(L - a.q_len, 0) / 4 : -1);
     } else {
         if (early) grid_dependency_wait();
         int c_nst = nst;   // stages this consumer takes
@@ -905,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
 // ---------------------------------------------------------------------------
 // host launchers
 
-template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT>
+template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT, bool FUSED>
 static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
 {
     constexpr int bytes = smem_bytes<E4M3, D, NT, RW>();
@@ -914,23 +1003,24 @@ static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT>,
+        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT, FUSED>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
-    return launch_pdl(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT>, grid, dim3(kThreads), bytes, stream, a);
+    return launch_pdl(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT, FUSED>, grid, dim3(kThreads), bytes, stream,
+                      a);
 }
 
-template <bool E4M3, int D, bool BITCAST, bool LPT = false>
+template <bool E4M3, int D, bool BITCAST, bool LPT = false, bool FUSED = false>
 static cudaError_t launch_rows(const AttnArgs &a, cudaStream_t stream)
 {
     const int tiles = (a.rows + 7) / 8;
-    if (tiles <= 1) return launch_one<E4M3, D, 1, 1, BITCAST, LPT>(a, stream);
-    if (tiles <= 2) return launch_one<E4M3, D, 2, 1, BITCAST, LPT>(a, stream);
-    if (tiles <= 4) return launch_one<E4M3, D, 2, 2, BITCAST, LPT>(a, stream);
-    return launch_one<E4M3, D, 2, 4, BITCAST, LPT>(a, stream);
+    if (tiles <= 1) return launch_one<E4M3, D, 1, 1, BITCAST, LPT, FUSED>(a, stream);
+    if (tiles <= 2) return launch_one<E4M3, D, 2, 1, BITCAST, LPT, FUSED>(a, stream);
+    if (tiles <= 4) return launch_one<E4M3, D, 2, 2, BITCAST, LPT, FUSED>(a, stream);
+    return launch_one<E4M3, D, 2, 4, BITCAST, LPT, FUSED>(a, stream);
 }
 
 }  // namespace kvq

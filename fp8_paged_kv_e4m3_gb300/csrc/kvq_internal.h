@@ -34,6 +34,13 @@ struct AttnArgs {
     bool early_pages;            // split kernel, no top-k list: block tables, lengths and pages of
                                  // positions < L - q_len may be read before the dependency wait
     bool longest_first;          // split kernel (hardware decoder): CTAs take the sequences longest first
+    // Fused step (no top-k list): this step's new rows, fp16 [B][q_len][Hkv][D], quantised
+    // (E4M3: divided by k_scale / v_scale) or copied (fp16) into the pools -- by the split
+    // kernel's FUSED instances before they copy the pages that hold them, or by the append
+    // kernel that precedes the tcgen05 kernel; null for the attention-only calls.
+    const void *k_new = nullptr;
+    const void *v_new = nullptr;
+    float k_scale = 1.f, v_scale = 1.f;
 };
 
 // Arguments of one chunked-prefill attention call (device pointers).
@@ -70,6 +77,11 @@ cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStr
 cudaError_t launch_attention_lpt(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_bitcast(int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t stream);
+// the fused step (a.k_new set): the split kernel's instances that append in the launch
+// (kvq_attn_step.cu), and the append by block table that precedes the tcgen05 kernel
+// (kvq_append.cu)
+cudaError_t launch_attention_step(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
+cudaError_t launch_append_step(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 bool tc_supported(int head_dim, int rows);
 cudaError_t launch_combine(const float *ws_o, const float *ws_m, const float *ws_l, void *out,
                            int32_t batch, int32_t q_len, int32_t num_q_heads, int32_t head_dim,

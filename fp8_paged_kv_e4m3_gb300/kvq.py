@@ -60,7 +60,7 @@ EXPORTS = ("kvq_version", "kvq_status_string", "kvq_validate_scales", "kvq_amax_
            "kvq_scale_from_amax", "kv_append_e4m3", "kv_append_fp16", "kvq_attn_num_splits",
            "kvq_attn_workspace_bytes", "paged_decode_attn_e4m3", "paged_decode_attn_fp16",
            "paged_decode_attn_e4m3_partial", "paged_decode_attn_fp16_partial", "kvq_lse_combine",
-           "paged_decode_attn_e4m3_noalloc", "kvq_prefill_workspace_bytes", "paged_prefill_attn_e4m3",
+           "paged_decode_step_e4m3", "paged_decode_step_fp16", "paged_decode_attn_e4m3_noalloc", "kvq_prefill_workspace_bytes", "paged_prefill_attn_e4m3",
            "paged_prefill_attn_fp16")
 
 
@@ -96,6 +96,8 @@ def load(path: Optional[str] = None):
         lib.paged_decode_attn_e4m3_partial.argtypes = [V, V, V, i64, V, V, f32, f32, V, V, V, sz, P, V, V]
         lib.paged_decode_attn_fp16_partial.argtypes = [V, V, V, i64, V, V, V, V, V, sz, P, V, V]
         lib.kvq_lse_combine.argtypes = [V, sz, V, P, V]
+        lib.paged_decode_step_e4m3.argtypes = [V, V, V, V, V, i64, V, V, f32, f32, V, sz, V, P, V, V]
+        lib.paged_decode_step_fp16.argtypes = [V, V, V, V, V, i64, V, V, V, sz, V, P, V, V]
         PP = ctypes.POINTER(PrefillParams)
         lib.kvq_prefill_workspace_bytes.argtypes = [PP]
         lib.kvq_prefill_workspace_bytes.restype = sz
@@ -338,6 +340,54 @@ def paged_decode_attn_fp16(q, k_cache, v_cache, block_tables, context_lens, work
         _ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0], _ptr(block_tables),
         _ptr(context_lens), _ptr(topk_idx), _ptr(topk_lens), _ptr(workspace),
         workspace.numel() * 4, _ptr(out), ctypes.byref(p), _ptr(err_flag), _stream(q)))
+    return out
+
+
+def _step_rows_check(q, k_new, v_new, Hkv):
+    B, q_len, _, D = q.shape
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _need(t, name, torch.float16, 4)
+        if t.shape != (B, q_len, Hkv, D):
+            raise ValueError(f"{name} must be [B, q_len, Hkv, D] = {(B, q_len, Hkv, D)}")
+
+
+def paged_decode_step_e4m3(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, k_scale: float,
+                           v_scale: float, workspace, out=None, num_splits: int = 0, sm_scale: float = 0.0,
+                           err_flag=None, split_pages: int = 0, bitcast_decode: bool = False,
+                           mma_sync: bool = False, fp8_qk: bool = False, strict_order: bool = False,
+                           longest_first: bool = False):
+    """This step's append (k_new, v_new: fp16 [B, q_len, Hkv, D], written at
+    positions L - q_len .. L - 1 of each sequence) and the attention over the
+    updated cache in one attention launch plus the combine; the same pools
+    and outputs as kv_append_e4m3 then paged_decode_attn_e4m3.  Returns out."""
+    p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, None, None,
+                    torch.uint8, num_splits, sm_scale, split_pages, bitcast_decode, mma_sync, fp8_qk,
+                    strict_order, longest_first)
+    _step_rows_check(q, k_new, v_new, k_cache.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    _check("paged_decode_step_e4m3", load().paged_decode_step_e4m3(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_tables), _ptr(context_lens), ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+        _ptr(workspace), workspace.numel() * 4, _ptr(out), ctypes.byref(p), _ptr(err_flag), _stream(q)))
+    return out
+
+
+def paged_decode_step_fp16(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, workspace,
+                           out=None, num_splits: int = 0, sm_scale: float = 0.0, err_flag=None,
+                           split_pages: int = 0, mma_sync: bool = False, strict_order: bool = False,
+                           longest_first: bool = False):
+    """fp16-KV twin of paged_decode_step_e4m3."""
+    p = _attn_check(q, k_cache, v_cache, block_tables, context_lens, workspace, out, None, None,
+                    torch.float16, num_splits, sm_scale, split_pages, False, mma_sync,
+                    strict_order=strict_order, longest_first=longest_first)
+    _step_rows_check(q, k_new, v_new, k_cache.shape[1])
+    if out is None:
+        out = torch.empty_like(q)
+    _check("paged_decode_step_fp16", load().paged_decode_step_fp16(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+        _ptr(block_tables), _ptr(context_lens), _ptr(workspace), workspace.numel() * 4, _ptr(out),
+        ctypes.byref(p), _ptr(err_flag), _stream(q)))
     return out
 
 

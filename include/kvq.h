@@ -298,6 +298,49 @@ int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cac
                            float *workspace, size_t workspace_bytes, void *out,
                            const kvq_attn_params *p, int32_t *err_flag, void *stream);
 
+/* Fused decode / verify step: this step's append and the attention over the
+ * updated cache in one attention launch (plus the combine), instead of
+ * kv_append_* followed by paged_decode_attn_*.  [P2] Changes: the main K/V
+ * cache is written in calibrated E4M3 as tokens are appended, and decode
+ * reads it through the page4 route.
+ *
+ * Sequence b appends its q_len new tokens at positions L - q_len + i
+ * (0 <= i < q_len), L = context_lens[b] (which includes them), into the page
+ * slots its block table names:
+ *     slot = block_tables[b][pos / 4] * 4 + pos % 4,  pos = L - q_len + i
+ *     k_cache[slot / 4][g][slot % 4][d] = E4M3(fp32(k_new[b][i][g][d]) / k_scale)
+ * (v likewise), exactly as kv_append_e4m3 with that slot mapping would, and
+ * the attention is then the one defined above over the cache including them.
+ * Pools and outputs are identical to the two separate calls.
+ *   k_new, v_new : device fp16 [B][q_len][Hkv][head_dim], 16-B aligned
+ *   k_cache, v_cache : written (the new rows) and read
+ * Every other argument as for paged_decode_attn_e4m3.  There is no top-k
+ * form: with a list, tokens of one sequence may be read by several of its
+ * split CTAs, so the append must complete first (use the separate calls).
+ * The fused kernels decode with the hardware conversion and compute fp16
+ * scores: KVQ_ATTN_BITCAST_DECODE and KVQ_ATTN_FP8_QK return
+ * KVQ_ERR_UNSUPPORTED before any launch; KVQ_ATTN_LONGEST_FIRST does not
+ * reorder the split kernel's fused instances (a scheduling choice only).
+ * A sequence with an invalid context length (KVQ_DEV_BAD_LEN) appends
+ * nothing; a new row whose block-table entry is out of range is skipped
+ * (KVQ_DEV_BAD_PAGE).  The new tokens' pages must belong to their sequence
+ * alone (no other sequence in the call may map them), as for any append.
+ * The preceding kernel may write k_new and v_new: they are read after the
+ * dependency wait.  Launches two kernels (attention with the append, combine). */
+int paged_decode_step_e4m3(const void *q, const void *k_new, const void *v_new,
+                           uint8_t *k_cache, uint8_t *v_cache, int64_t num_pages,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           float k_scale, float v_scale, float *workspace,
+                           size_t workspace_bytes, void *out, const kvq_attn_params *p,
+                           int32_t *err_flag, void *stream);
+
+/* fp16-KV twin: the new rows are copied unchanged into fp16 pools. */
+int paged_decode_step_fp16(const void *q, const void *k_new, const void *v_new,
+                           void *k_cache, void *v_cache, int64_t num_pages,
+                           const int32_t *block_tables, const int32_t *context_lens,
+                           float *workspace, size_t workspace_bytes, void *out,
+                           const kvq_attn_params *p, int32_t *err_flag, void *stream);
+
 /* The two halves of the calls above, for callers that merge partials from
  * several sources (for example partials computed on different devices over
  * different token ranges) or time the halves separately.

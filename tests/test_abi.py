@@ -175,6 +175,28 @@ def test_append_host_checks_fail_closed(lib):
     assert f(None, None, None, 0, 2, 64, None, None, 10, ctypes.c_float(1.0), ctypes.c_float(1.0), None, None) == 0
 
 
+def _step(lib, p, k_new=FAKE, v_new=FAKE, k_scale=0.1, ws_bytes=1 << 20):
+    return lib.paged_decode_step_e4m3(FAKE, k_new, v_new, FAKE, FAKE, 40, FAKE, FAKE, ctypes.c_float(k_scale),
+                                      ctypes.c_float(0.1), FAKE, ws_bytes, FAKE, ctypes.byref(p), None, None)
+
+
+def test_fused_step_host_checks_fail_closed(lib):
+    p = _params()
+    assert _step(lib, p, k_new=None) == -1
+    assert _step(lib, p, v_new=None) == -1
+    assert _step(lib, p, k_scale=0.0) == -2
+    assert _step(lib, p, ws_bytes=16) == -3
+    assert _step(lib, p, k_new=ctypes.c_void_p(0x10008)) == -6
+    assert _step(lib, p, v_new=ctypes.c_void_p(0x10004)) == -6
+    assert _step(lib, _params(head_dim=80)) == -4
+    assert _step(lib, _params(q_len=5)) == -4
+    assert _step(lib, _params(flags=kvq.ATTN_BITCAST_DECODE)) == -4     # the fused instances: hardware decoder
+    assert _step(lib, _params(flags=kvq.ATTN_FP8_QK, head_dim=128, q_len=4)) == -4
+    f16 = lib.paged_decode_step_fp16
+    assert f16(FAKE, None, FAKE, FAKE, FAKE, 40, FAKE, FAKE, FAKE, 1 << 20, FAKE, ctypes.byref(p), None, None) == -1
+    assert f16(FAKE, FAKE, FAKE, FAKE, FAKE, 40, FAKE, FAKE, FAKE, 16, FAKE, ctypes.byref(p), None, None) == -3
+
+
 def test_python_binding_refuses_fp16_workspace():
     """The split workspace is FP32 by contract; an fp16 buffer is refused before any call
     (the pages' XQA page-4 route broke when handed an fp16 temporary output)."""
