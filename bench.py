@@ -56,8 +56,8 @@ GRAPH_STEPS = 10   # steps captured in one CUDA graph
 # source files each attention kernel is compiled from (for the profile hash)
 KERNEL_SOURCES = {
     "prefill_attn_kernel": ["kvq_prefill.cu", "kvq_tcgen05.cuh", "kvq_device.cuh"],
-    "attn_split_kernel": ["kvq_attn_kernel.cuh", "kvq_device.cuh"],
-    "attn_tc_kernel": ["kvq_attn_tc.cu", "kvq_attn_kernel.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh"],
+    "attn_split_kernel": ["kvq_attn_kernel.cuh", "kvq_merge.cuh", "kvq_device.cuh"],
+    "attn_tc_kernel": ["kvq_attn_tc.cu", "kvq_attn_kernel.cuh", "kvq_merge.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh"],
 }
 
 
@@ -427,13 +427,17 @@ class Arm:
 
     def time(self, steps, warmup, barrier=None):
         """Exactly `steps` whole steps between two events: replays of the
-        GRAPH_STEPS-step graph, then one-step graphs for the remainder."""
+        GRAPH_STEPS-step graph, then one-step graphs for the remainder.  The
+        warm-up replays the one-step graphs `warmup` times and the multi-step
+        graph once, so that no graph's first launch is timed."""
         torch = self.torch
         if not getattr(self, "graphs", None):
             self.capture()
         graphs, many = self.graphs, self.many
         for i in range(warmup):
             graphs[i % self.copies].replay()
+        if many is not None and steps >= GRAPH_STEPS:
+            many.replay()   # the multi-step graph's first launch (its upload) stays out of the timed region
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
         if barrier:

@@ -206,9 +206,12 @@ static int run_attention(const AttnCall &c, bool with_combine)
     a.k_scale = c.e4m3 ? c.k_scale : 1.0f;
     a.v_scale = c.e4m3 ? c.v_scale : 1.0f;
 
+    a.out = with_combine ? c.out : nullptr;
+
     cudaStream_t stream = static_cast<cudaStream_t>(c.stream);
-    if (launch_attention(c.e4m3, p.head_dim, a, stream) != cudaSuccess) return KVQ_ERR_CUDA;
-    if (with_combine &&
+    bool merged = false;
+    if (launch_attention(c.e4m3, p.head_dim, a, stream, &merged) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (with_combine && !merged &&
         launch_combine(a.ws_o, a.ws_m, a.ws_l, c.out, p.batch, p.q_len, p.num_q_heads, p.head_dim, S,
                        stream) != cudaSuccess)
         return KVQ_ERR_CUDA;

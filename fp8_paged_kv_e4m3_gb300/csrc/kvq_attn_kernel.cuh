@@ -51,6 +51,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_merge.cuh"
 
 namespace kvq {
 
@@ -503,15 +504,46 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
     return issued;
 }
 
+// ---------------------------------------------------------------------------
+// Cluster merge (CMERGE instances): the S <= 8 splits of one (sequence, kv
+// head) run as one thread-block cluster, split s as cluster rank s.  Every CTA
+// writes its partials to the workspace as usual; after one cluster barrier
+// (release, then acquire, at cluster scope: the other CTAs' workspace stores
+// are visible), CTA s merges rows s, s + S, ... of the group, one warp per
+// row, with the combine kernel's merge (the same function, hence the same
+// bits), and writes them to `out`.  This replaces the combine launch and its
+// wait for the whole grid by a wait for the group's own splits.  Every thread
+// of every CTA passes the barrier exactly once, on the give-up path as well.
+__device__ __forceinline__ void cluster_barrier()
+{
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+template <int D>
+__device__ __forceinline__ void cluster_merge(const AttnArgs &a, int b, int g, int s, int warp, int lane)
+{
+    cluster_barrier();
+    const int S = a.num_splits;
+    for (int lr = s + S * warp; lr < a.rows; lr += S * kThreads / 32) {
+        const int i = lr / a.group, h = g * a.group + lr % a.group;
+        const int64_t row = ((int64_t)b * a.num_q_heads + h) * a.q_len + i;
+        float acc[D / 32];
+        const float W = merge_splits<D>(a.ws_o + row * S * D, a.ws_m + row * S, a.ws_l + row * S, S, lane, 0, 1,
+                                        acc);
+        store_merged<D>(static_cast<__half *>(a.out), b, i, h, a.q_len, a.num_q_heads, lane, acc, W);
+    }
+}
+
 // BITCAST selects the E4M3 decoder: false = the hardware conversion
 // (cvt.rn.f16x2.e4m3x2, the value itself); true = the bitcast decoder of the
 // source pages (E4M3 bits placed into fp16 bits, the value * 2^-8, exact),
 // with the 2^8 folded into the hoisted scales.  Both give the same fp16
 // values up to that power of two, so the outputs are identical.
-template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT = false, bool FUSED = false>
+template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT = false, bool FUSED = false, bool CMERGE = false>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     attn_split_kernel(const AttnArgs a)
 {
+    static_assert(!CMERGE || (NT == 1 && RW == 1 && !LPT), "the cluster merge is for up to 8 rows in index order");
     using W = Split<NT, RW>;
     constexpr int PPS = W::kPagesPerStage;
     constexpr int MTW = W::kTilesPerWarp;
@@ -914,6 +946,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
             a.ws_l[unit] = 0.f;
         }
         __syncthreads();
+        if constexpr (CMERGE) cluster_merge<D>(a, b, g, s, warp, lane);
         return;
     }
     float *mbuf = reinterpret_cast<float *>(smem);    // [token warps][kRowsPad][D + 2]: m, l, o[D]
@@ -989,12 +1022,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         const int64_t unit = (((int64_t)b * a.num_q_heads + h) * a.q_len + i) * S + s;
         *reinterpret_cast<float4 *>(a.ws_o + unit * D + d) = acc;
     }
+    if constexpr (CMERGE) cluster_merge<D>(a, b, g, s, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
 // host launchers
 
-template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT, bool FUSED>
+template <bool E4M3, int D, int NT, int RW, bool BITCAST, bool LPT, bool FUSED, bool CMERGE = false>
 static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
 {
     constexpr int bytes = smem_bytes<E4M3, D, NT, RW>();
@@ -1003,12 +1037,30 @@ static cudaError_t launch_one(const AttnArgs &a, cudaStream_t stream)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT, FUSED>,
+        e = cudaFuncSetAttribute(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT, FUSED, CMERGE>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     const dim3 grid(a.num_splits, a.num_kv_heads, a.batch);
+    if constexpr (CMERGE) {
+        // one cluster per (sequence, kv head): its splits along x
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = bytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)a.num_splits;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT, FUSED, CMERGE>, a);
+    }
     return launch_pdl(attn_split_kernel<E4M3, D, NT, RW, BITCAST, LPT, FUSED>, grid, dim3(kThreads), bytes, stream,
                       a);
 }

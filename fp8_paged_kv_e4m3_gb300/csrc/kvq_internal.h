@@ -41,6 +41,9 @@ struct AttnArgs {
     const void *k_new = nullptr;
     const void *v_new = nullptr;
     float k_scale = 1.f, v_scale = 1.f;
+    // fp16 [B][q_len][Hq][D] output of the full call, or null (partials only); the split
+    // kernel's cluster-merge instances write it themselves
+    void *out = nullptr;
 };
 
 // Arguments of one chunked-prefill attention call (device pointers).
@@ -72,7 +75,11 @@ struct WorkspaceLayout {
 
 WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t head_dim);
 
-cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
+// *merged: set when the launch also merged the partials into a.out (the cluster merge), so that
+// no combine follows
+cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream, bool *merged);
+// the split kernel's cluster-merge instances (kvq_attn_cm.cu)
+cudaError_t launch_attention_cm(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 // the split kernel's longest-first instances (kvq_attn_lpt.cu)
 cudaError_t launch_attention_lpt(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_bitcast(int head_dim, const AttnArgs &a, cudaStream_t stream);
