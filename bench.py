@@ -331,8 +331,16 @@ class Arm:
 
     @property
     def launches(self):
-        """Kernels of one step: per layer attention and combine, plus the append unless fused."""
-        return (2 if self.fused else 3) * self.layers
+        """Kernels of one step: per layer, the attention call's (as the library
+        reports them for these parameters: attention and combine, or one
+        cluster-merging attention kernel, with the fused step's append on the
+        tcgen05 shapes), plus the append call's unless fused."""
+        p = self.kvq.attn_params(self.q[0], self.w.num_kv_heads, self.bt.shape[1], self.S,
+                                 0 if self.topk_idx is None else self.topk_idx.shape[2],
+                                 split_pages=self.w.split_pages, bitcast_decode=self.bitcast,
+                                 mma_sync=self.mma_sync, fp8_qk=self.fp8_qk, longest_first=self.longest_first)
+        per_layer = self.kvq.attn_launches(p, self.e4m3, self.fused) + (0 if self.fused else 1)
+        return per_layer * self.layers
 
     def _append(self, l, k, v, slots, kc, vc):
         if self.e4m3:

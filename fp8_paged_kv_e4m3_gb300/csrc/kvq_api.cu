@@ -367,6 +367,20 @@ int32_t kvq_attn_num_splits(const kvq_attn_params *p)
     return resolve_splits(p);
 }
 
+int32_t kvq_attn_launches(const kvq_attn_params *p, int32_t e4m3, int32_t fused_step)
+{
+    const int st = check_params(p);
+    if (st != KVQ_OK) return st;
+    if (p->batch == 0) return 0;
+    const int32_t S = resolve_splits(p);
+    const int rows = (p->num_q_heads / p->num_kv_heads) * p->q_len;
+    const bool tc = !(p->flags & KVQ_ATTN_MMA_SYNC) && tc_supported(p->head_dim, rows);
+    if (tc) return fused_step ? 3 : 2;   // [the append by block table,] attention, combine
+    const bool bitcast = e4m3 && (p->flags & KVQ_ATTN_BITCAST_DECODE);
+    const bool lpt = (p->flags & KVQ_ATTN_LONGEST_FIRST) != 0;
+    return cluster_merge_applies(e4m3 != 0, p->batch, p->num_kv_heads, rows, S, bitcast, lpt) ? 1 : 2;
+}
+
 size_t kvq_attn_workspace_bytes(const kvq_attn_params *p)
 {
     if (check_params(p) != KVQ_OK) return 0;

@@ -5,6 +5,14 @@
 
 namespace kvq {
 
+bool cluster_merge_applies(bool e4m3, int64_t batch, int num_kv_heads, int rows, int num_splits, bool bitcast,
+                           bool longest_first)
+{
+    const int64_t resident = int64_t(device_sm_count()) * (e4m3 ? 4 : 2);   // the instances' CTAs per SM
+    const int64_t ctas = batch * num_kv_heads * num_splits;
+    return rows <= 8 && num_splits <= 8 && ctas <= resident && !bitcast && !longest_first;
+}
+
 cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream, bool *merged)
 {
     *merged = false;
@@ -15,10 +23,8 @@ cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStr
     // combine launch after the whole grid.  A CTA then waits at its end for its cluster's other
     // splits, which costs nothing while every CTA is resident, but on a grid of several waves it
     // would hold an SM slot the next wave needs (the fp16 decode step, 1.7 waves: 48.9 -> 51.2 us).
-    const int64_t resident = int64_t(device_sm_count()) * (e4m3 ? 4 : 2);   // the instances' CTAs per SM
-    const int64_t ctas = int64_t(a.batch) * a.num_kv_heads * a.num_splits;
-    if (a.out && a.rows <= 8 && a.num_splits <= 8 && ctas <= resident && !(e4m3 && a.bitcast_decode) &&
-        !a.longest_first) {
+    if (a.out && cluster_merge_applies(e4m3, a.batch, a.num_kv_heads, a.rows, a.num_splits,
+                                       e4m3 && a.bitcast_decode, a.longest_first)) {
         *merged = true;
         return launch_attention_cm(e4m3, head_dim, a, stream);
     }

@@ -78,6 +78,9 @@ WorkspaceLayout workspace_layout(int64_t rows_total, int32_t num_splits, int32_t
 // *merged: set when the launch also merged the partials into a.out (the cluster merge), so that
 // no combine follows
 cudaError_t launch_attention(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream, bool *merged);
+// whether a full call takes the cluster merge (the rule launch_attention applies)
+bool cluster_merge_applies(bool e4m3, int64_t batch, int num_kv_heads, int rows, int num_splits, bool bitcast,
+                           bool longest_first);
 // the split kernel's cluster-merge instances (kvq_attn_cm.cu)
 cudaError_t launch_attention_cm(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 // the split kernel's longest-first instances (kvq_attn_lpt.cu)

@@ -60,7 +60,8 @@ EXPORTS = ("kvq_version", "kvq_status_string", "kvq_validate_scales", "kvq_amax_
            "kvq_scale_from_amax", "kv_append_e4m3", "kv_append_fp16", "kvq_attn_num_splits",
            "kvq_attn_workspace_bytes", "paged_decode_attn_e4m3", "paged_decode_attn_fp16",
            "paged_decode_attn_e4m3_partial", "paged_decode_attn_fp16_partial", "kvq_lse_combine",
-           "paged_decode_step_e4m3", "paged_decode_step_fp16", "paged_decode_attn_e4m3_noalloc", "kvq_prefill_workspace_bytes", "paged_prefill_attn_e4m3",
+           "paged_decode_step_e4m3", "paged_decode_step_fp16", "kvq_attn_launches",
+           "paged_decode_attn_e4m3_noalloc", "kvq_prefill_workspace_bytes", "paged_prefill_attn_e4m3",
            "paged_prefill_attn_fp16")
 
 
@@ -89,6 +90,8 @@ def load(path: Optional[str] = None):
         lib.kv_append_fp16.argtypes = [V, V, V, i32, i32, i32, V, V, i64, V, V]
         lib.kvq_attn_num_splits.argtypes = [P]
         lib.kvq_attn_num_splits.restype = i32
+        lib.kvq_attn_launches.argtypes = [P, i32, i32]
+        lib.kvq_attn_launches.restype = i32
         lib.kvq_attn_workspace_bytes.argtypes = [P]
         lib.kvq_attn_workspace_bytes.restype = sz
         lib.paged_decode_attn_e4m3.argtypes = [V, V, V, i64, V, V, f32, f32, V, V, V, sz, V, P, V, V]
@@ -239,6 +242,15 @@ def num_splits(p: AttnParams) -> int:
     if s < 1:
         raise KvqError("kvq_attn_num_splits", s)
     return s
+
+
+def attn_launches(p: AttnParams, e4m3: bool, fused_step: bool = False) -> int:
+    """Kernels the full call (fused_step: the fused step call) launches with
+    these parameters on the current device."""
+    n = load().kvq_attn_launches(ctypes.byref(p), int(e4m3), int(fused_step))
+    if n < 0:
+        raise KvqError("kvq_attn_launches", n)
+    return n
 
 
 def workspace_bytes(p: AttnParams) -> int:

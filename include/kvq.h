@@ -256,6 +256,18 @@ typedef struct {
  * Returns a value >= 1, or a negative kvq_status for invalid parameters. */
 int32_t kvq_attn_num_splits(const kvq_attn_params *p);
 
+/* The number of kernels paged_decode_attn_e4m3 (e4m3 != 0) or _fp16 launches
+ * with these parameters on the current device -- fused_step != 0: the
+ * paged_decode_step_* call -- or a negative kvq_status for invalid
+ * parameters.  Host only: it launches nothing.  The full call launches the
+ * attention kernel and the log-sum-exp combine, except that with up to 8
+ * query rows per KV head and up to 8 splits, on a grid resident in one wave
+ * (the hardware decoder, index order), the splits of each (sequence, KV head)
+ * run as one thread-block cluster and merge into `out` themselves (the
+ * combine's arithmetic: the same bits), so one kernel.  On the tcgen05
+ * kernel's shapes the fused step launches its append first. */
+int32_t kvq_attn_launches(const kvq_attn_params *p, int32_t e4m3, int32_t fused_step);
+
 /* Bytes of FP32 workspace the call needs, 0 for invalid parameters.
  * Workspace layout (float32, each part starting on a 256-byte boundary):
  *   tmp_out [B][Hq][q_len][S][head_dim]  partial output of each split,
@@ -281,7 +293,8 @@ size_t kvq_attn_workspace_bytes(const kvq_attn_params *p);
  *   workspace    : device float32, >= kvq_attn_workspace_bytes(p) bytes,
  *                  256-B aligned.  FP32 by contract: there is no fp16 form.
  *   out          : device fp16 [B][q_len][Hq][head_dim], 16-B aligned
- * Launches two kernels (attention, combine) on `stream`.
+ * Launches two kernels (attention, combine) on `stream`, or one (see
+ * kvq_attn_launches).
  */
 int paged_decode_attn_e4m3(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
                            int64_t num_pages, const int32_t *block_tables,
@@ -326,7 +339,7 @@ int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cac
  * (KVQ_DEV_BAD_PAGE).  The new tokens' pages must belong to their sequence
  * alone (no other sequence in the call may map them), as for any append.
  * The preceding kernel may write k_new and v_new: they are read after the
- * dependency wait.  Launches two kernels (attention with the append, combine). */
+ * dependency wait.  Launches the kernels kvq_attn_launches(p, 1, 1) counts. */
 int paged_decode_step_e4m3(const void *q, const void *k_new, const void *v_new,
                            uint8_t *k_cache, uint8_t *v_cache, int64_t num_pages,
                            const int32_t *block_tables, const int32_t *context_lens,

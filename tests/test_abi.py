@@ -197,6 +197,26 @@ def test_fused_step_host_checks_fail_closed(lib):
     assert f16(FAKE, FAKE, FAKE, FAKE, FAKE, 40, FAKE, FAKE, FAKE, 16, FAKE, ctypes.byref(p), None, None) == -3
 
 
+def test_launch_count_query(lib):
+    """kvq_attn_launches: the kernels a call launches (host only).  Without a GPU
+    the library assumes 148 SMs, so one wave holds 592 E4M3 or 296 fp16 CTAs of
+    the split kernel."""
+    f = lambda p, e4m3, fused=0: lib.kvq_attn_launches(ctypes.byref(p), e4m3, fused)
+    dec = dict(batch=32, q_len=1, num_q_heads=32, num_kv_heads=4, head_dim=128, num_splits=4,
+               max_pages_per_seq=1024)
+    assert f(_params(**dec), 1) == 1 and f(_params(**dec), 1, 1) == 1      # 512 CTAs: the cluster merge
+    assert f(_params(**dec), 0) == 2                                        # fp16: 512 > 296, the combine
+    assert f(_params(**dict(dec, num_splits=9)), 1) == 2                    # more than 8 splits
+    assert f(_params(**dict(dec, batch=40)), 1) == 2                        # 640 CTAs: two waves
+    assert f(_params(flags=kvq.ATTN_BITCAST_DECODE, **dec), 1) == 2
+    assert f(_params(flags=kvq.ATTN_LONGEST_FIRST, **dec), 1) == 2
+    ver = dict(dec, q_len=4, num_splits=4)                                  # 32 rows: the tcgen05 kernel
+    assert f(_params(**ver), 1) == 2 and f(_params(**ver), 1, 1) == 3
+    assert f(_params(flags=kvq.ATTN_MMA_SYNC, **ver), 1) == 2               # 32 rows on the split kernel
+    assert f(_params(batch=0), 1) == 0
+    assert f(_params(q_len=0), 1) == -1
+
+
 def test_python_binding_refuses_fp16_workspace():
     """The split workspace is FP32 by contract; an fp16 buffer is refused before any call
     (the pages' XQA page-4 route broke when handed an fp16 temporary output)."""
