@@ -575,7 +575,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     // pages are read before waiting for it (the producers start copying at
     // once; the consumers wait before reading q).  With a top-k list, whose
     // lists a preceding kernel may write, or with strict ordering, everything
-    // waits here.
+    // waits here.  The fused step's preceding kernel may be the previous
+    // step's fused launch (with the cluster merge nothing else runs between
+    // them), which wrote its q_len <= 4 rows just below this step's window
+    // (decode: position L - 2; verify: up to 4 positions below L - q_len), so
+    // its instances copy early only the pages below position L - q_len - 4.
     const bool early = a.early_pages && a.topk_idx == nullptr;
     if (!early) grid_dependency_wait();
     launch_dependents();      // the combine may start launching; it waits for our completion
@@ -623,8 +627,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
     if (warp >= kConsumerWarps) {
         // ================= producers: the first moves K, the second V =================
         const bool is_v = warp == kConsumerWarps + 1;
-        issued = produce_stages<G, PPS, FUSED>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos,
-                                               abort_flag, stage_bad, early ? max(L - a.q_len, 0) / 4 : -1);
+        constexpr int kPrevRows = FUSED ? 4 : 0;   // rows a preceding fused step may have written below the window
+        issued = produce_stages<G, PPS, FUSED>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos, abort_flag,
+                                               stage_bad, early ? max(L - a.q_len - kPrevRows, 0) / 4 : -1);
     } else {
         if (early) grid_dependency_wait();
         int c_nst = nst;   // stages this consumer takes

@@ -339,7 +339,10 @@ int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cac
  * (KVQ_DEV_BAD_PAGE).  The new tokens' pages must belong to their sequence
  * alone (no other sequence in the call may map them), as for any append.
  * The preceding kernel may write k_new and v_new: they are read after the
- * dependency wait.  Launches the kernels kvq_attn_launches(p, 1, 1) counts. */
+ * dependency wait.  Early reads (see the conventions) cover only the pages
+ * holding positions below L - q_len - 4, so that the previous step's fused
+ * call, which may run as the directly preceding kernel and wrote its up to 4
+ * rows just below this step's window, is never read early.  Launches the kernels kvq_attn_launches(p, 1, 1) counts. */
 int paged_decode_step_e4m3(const void *q, const void *k_new, const void *v_new,
                            uint8_t *k_cache, uint8_t *v_cache, int64_t num_pages,
                            const int32_t *block_tables, const int32_t *context_lens,

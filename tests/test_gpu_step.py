@@ -206,3 +206,79 @@ def test_fused_step_skips_a_bad_page_and_reports_it(e4m3):
 
 def test_fused_step_appends_nothing_for_an_invalid_length():
     _run([517, 518, 133], 1, True, S=2, bad_len_seq=2, iters=2)
+
+
+@pytest.mark.parametrize("e4m3", [True, False])
+def test_fused_steps_back_to_back_with_growing_contexts(e4m3):
+    """Consecutive decode steps through the fused call with nothing else in the
+    stream between them (at this shape each call is one cluster-merging
+    kernel): step t + 1 attends the row step t appended.  The new keys lie
+    along the query of their group's first head, so every step's newest rows
+    carry most of the attention weight, and a row read before the previous
+    step had written it would show in that step's output."""
+    T = 6
+    L0 = np.array([517, 518, 300, 1029, 64, 2050])
+    B, Hq, Hkv, D = len(L0), 32, 4, 128
+    w = inputs.Workload("chain", 33, 1, B, 1, Hq, Hkv, D, 4, "list:" + ",".join(map(str, L0 + T)),
+                        calib_tokens=64)
+    pr = P.host_problem(w)
+    Gq = Hq // Hkv
+    for b in range(B):
+        for t in range(T):
+            for g in range(Hkv):
+                pr.k_tok[pr.offsets[b] + L0[b] + t, g] = (
+                    pr.q[b, 0, g * Gq].astype(np.float32) * (1.0 + 0.3 * t)).astype(np.float16)
+    # history: positions below L0 of each sequence
+    seq = np.repeat(np.arange(B), L0)
+    pos = np.concatenate([np.arange(l) for l in L0])
+    shape = (pr.P, Hkv, 4, D)
+    if e4m3:
+        kc = torch.full(shape, P.SENTINEL, dtype=torch.uint8, device="cuda")
+        ks = kvq.calibrate_scale(G.to_dev(pr.k_calib))
+        vs = kvq.calibrate_scale(G.to_dev(pr.v_calib))
+    else:
+        kc = torch.zeros(shape, dtype=torch.float16, device="cuda")
+        ks = vs = 1.0
+    vc = kc.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hk, hv = G.to_dev(pr.k_tok[pr.offsets[seq] + pos]), G.to_dev(pr.v_tok[pr.offsets[seq] + pos])
+    hs = G.to_dev(inputs.slot_mapping(pr.layout.block_tables, seq, pos))
+    if e4m3:
+        kvq.kv_append_e4m3(hk, hv, hs, kc, vc, ks, vs, err)
+    else:
+        kvq.kv_append_fp16(hk, hv, hs, kc, vc, err)
+    q, bt = G.to_dev(pr.q), G.to_dev(pr.layout.block_tables)
+    lens = [(L0 + t + 1).astype(np.int32) for t in range(T)]
+    cls = [G.to_dev(l) for l in lens]
+    kn = [G.to_dev(pr.k_tok[pr.offsets + L0 + t]).view(B, 1, Hkv, D) for t in range(T)]
+    vn = [G.to_dev(pr.v_tok[pr.offsets + L0 + t]).view(B, 1, Hkv, D) for t in range(T)]
+    p = kvq.AttnParams(B, 1, Hq, Hkv, D, 4, bt.shape[1], 0, 0.0, 0, 0)
+    assert kvq.attn_launches(p, e4m3, True) == 1     # 96 CTAs: one cluster-merging kernel
+    ws = kvq.alloc_workspace(p, q.device)
+    outs = [torch.empty_like(q) for _ in range(T)]
+    torch.cuda.synchronize()
+    for t in range(T):                       # back to back: no copy, no sync
+        if e4m3:
+            kvq.paged_decode_step_e4m3(q, kn[t], vn[t], kc, vc, bt, cls[t], ks, vs, ws, outs[t], num_splits=4,
+                                       err_flag=err)
+        else:
+            kvq.paged_decode_step_fp16(q, kn[t], vn[t], kc, vc, bt, cls[t], ws, outs[t], num_splits=4, err_flag=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    seq_all = np.repeat(np.arange(B), L0 + T)
+    pos_all = np.concatenate([np.arange(l) for l in L0 + T])
+    kc_o, vc_o = P.empty_pools(pr, e4m3)
+    if not e4m3:
+        kc_o[:] = 0
+        vc_o[:] = 0
+    rows_all = pr.offsets[seq_all] + pos_all
+    slots_all = inputs.slot_mapping(pr.layout.block_tables, seq_all, pos_all)
+    if e4m3:
+        oracle.append_e4m3(pr.k_tok[rows_all], pr.v_tok[rows_all], slots_all, kc_o, vc_o, ks, vs)
+    else:
+        oracle.append_fp16(pr.k_tok[rows_all], pr.v_tok[rows_all], slots_all, kc_o, vc_o)
+    view = np.uint8 if e4m3 else np.int16
+    assert np.array_equal(_bytes(kc), kc_o.view(view)) and np.array_equal(_bytes(vc), vc_o.view(view))
+    for t in range(T):
+        ref, _ = oracle.attention(pr.q, kc_o, vc_o, pr.layout.block_tables, lens[t], ks, vs, None, None)
+        G.assert_close(outs[t].float().cpu().numpy(), ref, f"chained step {t} e4m3={e4m3}")
