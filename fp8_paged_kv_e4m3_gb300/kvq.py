@@ -109,7 +109,8 @@ def load(path: Optional[str] = None):
         for name in ("kvq_validate_scales", "kvq_amax_f16", "kv_append_e4m3", "kv_append_fp16",
                      "paged_decode_attn_e4m3", "paged_decode_attn_fp16",
                      "paged_decode_attn_e4m3_partial", "paged_decode_attn_fp16_partial",
-                     "kvq_lse_combine", "paged_prefill_attn_e4m3", "paged_prefill_attn_fp16"):
+                     "kvq_lse_combine", "paged_decode_step_e4m3", "paged_decode_step_fp16",
+                     "paged_prefill_attn_e4m3", "paged_prefill_attn_fp16"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib

@@ -97,3 +97,42 @@ def test_context_usable_after_timeout(stall_lib):
     assert np.array_equal(kc, dp.k_cache.cpu().numpy()) and np.array_equal(vc, dp.v_cache.cpu().numpy())
     ref, _ = oracle.attention(pr.q, kc, vc, pr.layout.block_tables, pr.layout.lens, ks, vs)
     G.assert_close(got, ref, "after timeout")
+
+
+@pytest.fixture(scope="module")
+def stall_cluster_lib():
+    build.build()
+    kvq.load()
+    path = build.build_variant("stall_consumers_cluster", {"KVQ_TEST_STALL_CONSUMERS": f"{STALL_NS}ull"},
+                               sources=("kvq_attn.cu", "kvq_attn_cm.cu"))
+    return kvq.load(path)
+
+
+def test_timeout_in_the_cluster_merge(stall_cluster_lib):
+    """The full call's cluster-merging instances (here 3 splits of each of the 2
+    x 2 (sequence, kv head) groups, one cluster each): every CTA gives up, marks
+    its partials empty, and still passes its cluster's barrier exactly once, so
+    the call returns, and the merge gives every row 0."""
+    pr = P.host_problem(_case())
+    dp = G.device_problem(pr)
+    torch.cuda.synchronize()
+    assert dp.err.item() == 0
+    p = kvq.attn_params(dp.q, dp.k_cache.shape[1], dp.block_tables.shape[1], 3)
+    assert kvq.attn_launches(p, True) == 1, "this shape takes the cluster merge"
+    ws = kvq.alloc_workspace(p, dp.q.device)
+    ws.fill_(float("nan"))
+    out = torch.full_like(dp.q, float("nan"))
+    st = stall_cluster_lib.paged_decode_attn_e4m3(
+        ctypes.c_void_p(dp.q.data_ptr()), ctypes.c_void_p(dp.k_cache.data_ptr()),
+        ctypes.c_void_p(dp.v_cache.data_ptr()), dp.k_cache.shape[0],
+        ctypes.c_void_p(dp.block_tables.data_ptr()), ctypes.c_void_p(dp.context_lens.data_ptr()),
+        ctypes.c_float(dp.k_scale), ctypes.c_float(dp.v_scale), None, None,
+        ctypes.c_void_p(ws.data_ptr()), ws.numel() * 4, ctypes.c_void_p(out.data_ptr()), ctypes.byref(p),
+        ctypes.c_void_p(dp.err.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, "the launch itself must succeed"
+    torch.cuda.synchronize()           # returns: no CTA was left waiting at its cluster barrier
+    assert dp.err.item() & kvq.DEV_TIMEOUT, f"err_flag {dp.err.item()}: no timeout reported"
+    o, m, l = kvq.workspace_views(ws, p)
+    assert torch.isneginf(m).all() and (l == 0).all()
+    assert (out == 0).all()
+
