@@ -382,10 +382,10 @@ class Arm:
 
     def _layer_step(self, l, kc, vc, k, v, slots, q, bt, cl, out):
         """Layer l's share of a step: the append of the step's tokens and the
-        attention over the updated cache -- the fused step call (attention with
-        the append, then the combine: two launches), or the append call and the
-        attention call (three launches); chained with programmatic dependent
-        launch."""
+        attention over the updated cache -- the fused step call, or the append
+        call and the attention call; chained with programmatic dependent
+        launch.  The kernels each call launches are those the library reports
+        (kvq_attn_launches)."""
         kvq = self.kvq
         if not self.fused:
             self._append(l, k, v, slots, kc, vc)
@@ -1264,8 +1264,9 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
         "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
         "step_ms_p10_p50_p90_one_graph_each": pct,
         "step_calls": ("paged_decode_step_e4m3 per layer (the append inside the attention launch, then the "
-                       "combine)") if info["fused"] else
+                       "merge of the partials)") if info["fused"] else
                       "kv_append_e4m3, then paged_decode_attn_e4m3, per layer",
+        "launches_per_step": info["launches"],
         "separate_append_ms_per_step": separate_ms,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
@@ -1288,8 +1289,8 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
                 "serial_ms_per_step": e2e_serial_ms},
         "gpu_launches": info["launches"] * args.steps,
         "launch": (f"CUDA graphs of {GRAPH_STEPS} steps" if layers == 1 else "a CUDA graph per step") +
-                  (" (per layer: the fused step call -- attention with the append, then the combine" if info["fused"]
-                   else " (per layer: the append, then the attention call -- attention and combine kernels") +
+                  (f" (per layer: the fused step call, {info['launches'] // layers} kernel(s)" if info["fused"]
+                   else f" (per layer: the append, then the attention call, {info['launches'] // layers} kernels") +
                   "; programmatic dependent launch); e2e: the compute of each step in a CUDA graph, H2D and D2H "
                   "copies on their own streams",
     }
