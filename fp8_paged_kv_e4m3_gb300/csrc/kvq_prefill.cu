@@ -46,6 +46,7 @@
 //     and every barrier is reached by whole warps.
 #include <algorithm>
 #include <cstdint>
+#include <type_traits>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -126,30 +127,46 @@ __global__ void __launch_bounds__(256) kv_tile_kernel(const PrefillArgs a)
     if (threadIdx.x < 2) bad[threadIdx.x] = 0u;
     __syncthreads();
     // item = (key n8 group, 8-channel group c8, key n%8), key fastest: the 8
-    // lanes of a quarter warp write one 128-byte core-matrix row block
+    // lanes of a quarter warp write one 128-byte core-matrix row block.  A
+    // thread's KI items load their page entries, then their rows, before any
+    // store, so that two memory round trips cover them.
     constexpr int kHalf = kPfTile / 2;
-    for (int r = threadIdx.x; r < kHalf * (kPfD / 8); r += blockDim.x) {
-        const int key = kh * kHalf + (r / (8 * (kPfD / 8))) * 8 + (r & 7);
-        const int c8 = (r / 8) % (kPfD / 8);
-        const int pos = j * kPfTile + key;
+    constexpr int KI = kHalf * (kPfD / 8) / 256;   // items per thread (4)
+    static_assert(KI * 256 == kHalf * (kPfD / 8), "the block's items divide evenly");
+    const uint8_t *pool = static_cast<const uint8_t *>(kv ? a.v_cache : a.k_cache);
+    int key[KI], c8[KI], page[KI];
+    bool in_ctx[KI];
+#pragma unroll
+    for (int u = 0; u < KI; ++u) {
+        const int r = threadIdx.x + 256 * u;
+        key[u] = kh * kHalf + (r / (8 * (kPfD / 8))) * 8 + (r & 7);
+        c8[u] = (r / 8) % (kPfD / 8);
+        const int pos = j * kPfTile + key[u];
+        in_ctx[u] = pos < L;
+        page[u] = in_ctx[u] ? __ldg(bt_row + (pos >> 2)) : -1;
+    }
+    using Raw = typename std::conditional<E4M3, uint2, uint4>::type;
+    Raw x[KI];
+#pragma unroll
+    for (int u = 0; u < KI; ++u) {
+        const int pos = j * kPfTile + key[u];
+        if (in_ctx[u] && page[u] >= 0 && page[u] < a.num_pages)
+            x[u] = __ldg(reinterpret_cast<const Raw *>(
+                pool + ((((int64_t)page[u] * a.num_kv_heads + g) * 4 + (pos & 3)) * kPfD + c8[u] * 8) * kElem));
+    }
+#pragma unroll
+    for (int u = 0; u < KI; ++u) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);   // keys past the context: zero (and masked)
-        if (pos < L) {
-            const int page = __ldg(bt_row + (pos >> 2));
-            if (page >= 0 && page < a.num_pages) {
-                const uint8_t *pool = static_cast<const uint8_t *>(kv ? a.v_cache : a.k_cache);
-                const uint8_t *src = pool + ((((int64_t)page * a.num_kv_heads + g) * 4 + (pos & 3)) * kPfD + c8 * 8) * kElem;
-                if (E4M3) {
-                    const uint2 x = __ldg(reinterpret_cast<const uint2 *>(src));
-                    v = make_uint4(cvt_lo(x.x), cvt_hi(x.x), cvt_lo(x.y), cvt_hi(x.y));
-                } else {
-                    v = __ldg(reinterpret_cast<const uint4 *>(src));
-                }
-            } else if (kv == 0 && c8 == 0) {
-                report(a.err_flag, KVQ_DEV_BAD_PAGE);   // the row stays zero and its key is masked
-                atomicOr(&bad[(key - kh * kHalf) >> 5], 1u << (key & 31));
-            }
+        if (in_ctx[u] && page[u] >= 0 && page[u] < a.num_pages) {
+            if constexpr (E4M3)
+                v = make_uint4(cvt_lo(x[u].x), cvt_hi(x[u].x), cvt_lo(x[u].y), cvt_hi(x[u].y));
+            else
+                v = x[u];
+        } else if (in_ctx[u] && kv == 0 && c8[u] == 0) {
+            report(a.err_flag, KVQ_DEV_BAD_PAGE);   // the row stays zero and its key is masked
+            atomicOr(&bad[(key[u] - kh * kHalf) >> 5], 1u << (key[u] & 31));
         }
-        *reinterpret_cast<uint4 *>(dst + kv * kPfTileBytes + tile_off(key, c8)) = v;
+        *reinterpret_cast<uint4 *>(dst + kv * kPfTileBytes + tile_off(key[u], c8[u])) = v;
     }
     __syncthreads();
     if (kv == 0 && threadIdx.x < 2) a.tile_mask[tile * 4 + 2 * kh + threadIdx.x] = bad[threadIdx.x];
@@ -296,22 +313,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
             // S_X = Q_X K_T^T (T: the CTA's running tile count).  S_X last held P_X
             // of the previous tile, which the P V issued before this has read
             // (MMAs of one thread run in order).
+            // descriptors built once per operand; a K step adds its byte offset / 16 to the
+            // start-address field (bits 0..13), which the shared-memory addresses never overflow
             auto qk = [&](int x, int T) {
                 const uint32_t k_addr = smem_u32(smem + kPfRing + (T % kPfStages) * 2 * kPfTileBytes);
+                const uint64_t dq = umma_desc(q_addr + x * kPfTileBytes, 128, 2048);
+                const uint64_t dk = umma_desc(k_addr, 128, 2048);
 #pragma unroll
                 for (int ks = 0; ks < kPfD / 16; ++ks)
-                    umma_smem_a(tmem + kPfColS + x * kPfTile,
-                                umma_desc(q_addr + x * kPfTileBytes + ks * 256, 128, 2048),
-                                umma_desc(k_addr + ks * 256, 128, 2048), id_qk, ks > 0);
+                    umma_smem_a(tmem + kPfColS + x * kPfTile, dq + (uint64_t)(ks * 16), dk + (uint64_t)(ks * 16),
+                                id_qk, ks > 0);
                 umma_commit(b_s0 + 8 * x);
             };
             // O_X (+)= P_X V_T: A = P (tensor memory, two fp16 per column), B = V (MN-major)
             auto pv = [&](int x, int T, bool acc) {
                 const uint32_t v_addr = smem_u32(smem + kPfRing + (T % kPfStages) * 2 * kPfTileBytes + kPfTileBytes);
+                const uint64_t dv = umma_desc(v_addr, 2048, 128);
 #pragma unroll
                 for (int ks = 0; ks < kPfTile / 16; ++ks)
                     umma_tmem_a(tmem + kPfColO + x * kPfTile, tmem + kPfColS + x * kPfTile + ks * 8,
-                                umma_desc(v_addr + ks * 4096, 2048, 128), id_pv, acc || ks > 0);
+                                dv + (uint64_t)(ks * 256), id_pv, acc || ks > 0);
                 umma_commit(b_pv0 + 8 * x);
             };
             auto wait_full = [&](int T) {
