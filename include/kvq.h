@@ -312,10 +312,13 @@ int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cac
                            const kvq_attn_params *p, int32_t *err_flag, void *stream);
 
 /* Fused decode / verify step: this step's append and the attention over the
- * updated cache in one attention launch (plus the combine), instead of
- * kv_append_* followed by paged_decode_attn_*.  [P2] Changes: the main K/V
- * cache is written in calibrated E4M3 as tokens are appended, and decode
- * reads it through the page4 route.
+ * updated cache, in fewer launches than kv_append_* followed by
+ * paged_decode_attn_*.  On the split kernel's shapes the attention launch
+ * appends the new rows itself (and where the cluster merge applies, see
+ * kvq_attn_launches, it also merges the partials: one kernel); on the
+ * tcgen05 kernel's shapes a small append by block table precedes the
+ * attention.  [P2] Changes: the main K/V cache is written in calibrated E4M3
+ * as tokens are appended, and decode reads it through the page4 route.
  *
  * Sequence b appends its q_len new tokens at positions L - q_len + i
  * (0 <= i < q_len), L = context_lens[b] (which includes them), into the page
@@ -341,8 +344,9 @@ int paged_decode_attn_fp16(const void *q, const void *k_cache, const void *v_cac
  * The preceding kernel may write k_new and v_new: they are read after the
  * dependency wait.  Early reads (see the conventions) cover only the pages
  * holding positions below L - q_len - 4, so that the previous step's fused
- * call, which may run as the directly preceding kernel and wrote its up to 4
- * rows just below this step's window, is never read early.  Launches the kernels kvq_attn_launches(p, 1, 1) counts. */
+ * call, which may run as the directly preceding kernel and wrote its up to
+ * 4 rows just below this step's window, is never read early.  Launches the
+ * kernels kvq_attn_launches(p, e4m3, 1) counts. */
 int paged_decode_step_e4m3(const void *q, const void *k_new, const void *v_new,
                            uint8_t *k_cache, uint8_t *v_cache, int64_t num_pages,
                            const int32_t *block_tables, const int32_t *context_lens,
