@@ -59,7 +59,7 @@ def _bytes(t):
 
 
 def _run(lens, q_len, e4m3, Hq=8, Hkv=2, D=64, S=0, split_pages=0, bitcast=False, mma_sync=False,
-         longest_first=False, iters=3, bad_page_seq=None, bad_len_seq=None):
+         longest_first=False, iters=3, bad_page_seq=None, bad_len_seq=None, strict=False):
     B = len(lens)
     w = inputs.Workload("step", 31, 1, B, q_len, Hq, Hkv, D, S, "list:" + ",".join(map(str, lens)),
                         outlier_channels=2, calib_tokens=64, split_pages=split_pages)
@@ -87,7 +87,7 @@ def _run(lens, q_len, e4m3, Hq=8, Hkv=2, D=64, S=0, split_pages=0, bitcast=False
     slots_np = np.where(ok, bt_np[seq, pos_ok // 4].astype(np.int64) * 4 + pos_ok % 4, -1).astype(np.int32)
     slots = G.to_dev(slots_np)
     p = kvq.AttnParams(B, q_len, Hq, Hkv, D, S, bt.shape[1], 0, 0.0, split_pages,
-                       kvq._flags(bitcast, mma_sync, False, False, longest_first))
+                       kvq._flags(bitcast, mma_sync, False, strict, longest_first))
     wsA, wsB = kvq.alloc_workspace(p, q.device), kvq.alloc_workspace(p, q.device)
     outA, outB = torch.empty_like(q), torch.empty_like(q)
     errA = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -95,7 +95,8 @@ def _run(lens, q_len, e4m3, Hq=8, Hkv=2, D=64, S=0, split_pages=0, bitcast=False
     rng = np.random.default_rng(11)
     rows = pr.step_rows
     Gq = Hq // Hkv
-    kw = dict(num_splits=S, split_pages=split_pages, mma_sync=mma_sync, longest_first=longest_first)
+    kw = dict(num_splits=S, split_pages=split_pages, mma_sync=mma_sync, longest_first=longest_first,
+              strict_order=strict)
     for it in range(iters):
         if it == 0:
             knew, vnew = pr.k_tok[rows], pr.v_tok[rows]
@@ -193,6 +194,12 @@ def test_fused_step_new_rows_straddle_splits():
     _run([13, 14, 15, 16, 4, 6], 4, True, S=4)
     # fixed-size splits of 3 pages: the window crosses from one split into the next
     _run([519, 517, 35], 4, True, S=0, split_pages=3)
+
+
+@pytest.mark.parametrize("q_len", [1, 4])
+def test_fused_step_with_strict_ordering(q_len):
+    # KVQ_ATTN_STRICT_ORDER: nothing is read before the dependency wait
+    _run([517, 518, 1029, 36], q_len, True, Hq=32, Hkv=4, D=128, S=2, strict=True)
 
 
 def test_fused_step_longest_first_and_more_splits_than_pages():
