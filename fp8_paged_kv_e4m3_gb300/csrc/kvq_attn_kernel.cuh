@@ -97,7 +97,8 @@ struct Geometry {
     static constexpr int kBarOff = kTokPosOff + kStages * kTokPerStage * 4;
     // abort flag, sticky bad-stage flag, and the stages each producer issued
     static constexpr int kAbortOff = kBarOff + 2 * kStages * 8;
-    static constexpr int kBytes = kAbortOff + 16;
+    static constexpr int kAppBarOff = kAbortOff + 16;     // fused step, consumer append: the new rows are in the pool
+    static constexpr int kBytes = kAbortOff + 24;
     static_assert(kPageStride % 128 == 16, "page skew must be 16 bytes mod 128");
     static_assert(kBarOff % 8 == 0, "mbarriers need 8-byte alignment");
 };
@@ -360,18 +361,26 @@ __device__ __forceinline__ void append_step_rows(const AttnArgs &a, const SplitR
 // this step's append does not write) may be copied before that wait; the
 // wait comes before the first stage that reaches past them.  -1: the caller
 // has waited.
-// FUSED (the fused step's instances; dense only): a producer whose split
-// holds some of this step's new rows first waits for the preceding kernel
-// (which may write them) and appends its half of them, then walks its stages
-// as the other instances do.  Its first copies start a memory round trip
-// later; the consumers, which wait for the preceding kernel before reading
-// q, start no earlier anyway.  Appending later inside the stage loop
-// measured slower: that code in the loop slowed every stage.
-template <class G, int PPS, bool FUSED = false>
+// FMODE, the fused step's instances (dense only):
+//  1: a producer whose split holds some of this step's new rows first waits
+//     for the preceding kernel (which may write them) and appends its half of
+//     them, then walks its stages as the other instances do.  Its first
+//     copies start a memory round trip later; the consumers, which wait for
+//     the preceding kernel before reading q, start no earlier anyway.
+//     Appending later inside the stage loop measured slower: that code in
+//     the loop slowed every stage.
+//  2: consumer warps append the rows (after their own dependency wait) while
+//     the producers copy the earlier pages; a producer waits for them, on the
+//     mbarrier at app_bar, before the first stage that holds a new row.  The
+//     cluster-merge instances use it: their grid is resident in one wave, so
+//     an appending CTA's late start lengthens the whole launch (decode step
+//     27.75 -> 27.3 us); on longer launches the check in the loop costs more
+//     (long context: +2.2 us).
+template <class G, int PPS, int FMODE = 0>
 __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRange &r, int nst, int b, int g,
                                               int lane, bool is_v, int bt_spec, uint32_t ring, uint32_t bar0,
                                               int32_t *tokpos, volatile int *abort_flag, volatile int *stage_bad,
-                                              int clean_items = -1)
+                                              int clean_items = -1, uint32_t app_bar = 0)
 {
     const int item0 = r.item0, item1 = r.item1, L = r.L, spec0 = r.spec0;
     const bool topk = r.topk;
@@ -390,16 +399,24 @@ __device__ __forceinline__ int produce_stages(const AttnArgs &a, const SplitRang
             const int p = lane % PPS;                      // page of the stage this lane copies
             const bool copier = lane < PPS;
             bool waited = clean_items < 0;
-            if constexpr (FUSED) {
+            int st_new = nst;   // FMODE 2: the first stage that holds a new row
+            if constexpr (FMODE != 0) {
                 const int first_new = max(L - a.q_len, 0) / 4;   // first page with a new row
-                if (nst > 0 && first_new < item1) {
-                    if (!waited) grid_dependency_wait();
-                    waited = true;
-                    append_step_rows<G>(a, r, b, g, lane, is_v);
+                if constexpr (FMODE == 1) {
+                    if (nst > 0 && first_new < item1) {
+                        if (!waited) grid_dependency_wait();
+                        waited = true;
+                        append_step_rows<G>(a, r, b, g, lane, is_v);
+                    }
+                } else {
+                    if (first_new < item1) st_new = first_new <= item0 ? 0 : (first_new - item0) / PPS;
                 }
             }
             for (int st = 0; st < nst; ++st) {
                 const int slot = st % G::kStages;
+                if constexpr (FMODE == 2) {
+                    if (st == st_new && !mbar_wait_bounded(app_bar, 0, abort_flag, a.err_flag)) break;
+                }
                 if (!waited && item0 + (st + 1) * PPS > clean_items) {
                     grid_dependency_wait();
                     waited = true;
@@ -566,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         }
         *abort_flag = 0;
         *stage_bad = 0;
+        if constexpr (FUSED && CMERGE) mbar_init(smem_u32(smem + G::kAppBarOff), 2);   // K and V rows appended
         fence_mbar_init();
     }
     __syncthreads();
@@ -628,10 +646,20 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? (E4M3 ? 4 : 2) : 1)
         // ================= producers: the first moves K, the second V =================
         const bool is_v = warp == kConsumerWarps + 1;
         constexpr int kPrevRows = FUSED ? 4 : 0;   // rows a preceding fused step may have written below the window
-        issued = produce_stages<G, PPS, FUSED>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos, abort_flag,
-                                               stage_bad, early ? max(L - a.q_len - kPrevRows, 0) / 4 : -1);
+        constexpr int kFmode = FUSED ? (CMERGE ? 2 : 1) : 0;
+        issued = produce_stages<G, PPS, kFmode>(a, sr, nst, b, g, lane, is_v, bt_spec, ring, bar0, tokpos, abort_flag,
+                                                stage_bad, early ? max(L - a.q_len - kPrevRows, 0) / 4 : -1,
+                                                smem_u32(smem + G::kAppBarOff));
     } else {
         if (early) grid_dependency_wait();
+        if constexpr (FUSED && CMERGE) {
+            // consumer warps 0 (K) and 1 (V) append this split's new rows while the producers copy
+            // the earlier pages; the producers copy the rows' pages after the arrival
+            if (warp < 2 && nst > 0 && max(L - a.q_len, 0) / 4 < item1) {
+                append_step_rows<G>(a, sr, b, g, lane, warp == 1);
+                if (lane == 0) mbar_arrive(smem_u32(smem + G::kAppBarOff));
+            }
+        }
         int c_nst = nst;   // stages this consumer takes
 #ifdef KVQ_TEST_STALL_CONSUMERS
         // Test builds only (never the library's default build): before their
