@@ -14,9 +14,19 @@ the deployment.  The attention of such a sequence is split-K over ranks:
   3. the log-sum-exp combine merges the world x S partials of every row.
 
 The combine is exact up to rounding whatever the partition, so the result is
-the single-GPU attention.  Decode only (q_len 1): the causal window of a
-verify step would have to be shifted on every rank that does not hold the
-sequence's tail, which the single-GPU calls do not express.
+the single-GPU attention.
+
+MTP verify windows (q_len > 1, causal inside the window, PR "[Model][SM70]
+Calibrated E4M3 KV cache for Qwen4Exp QSA with MTP", section Purpose): a
+rank below the window sees all of its keys from every window row, the rank
+that holds the window a causal prefix of them.  `shard_window_rows` states
+this with the calls as they are: the window's q_len rows become q_len
+one-row sequences per sequence (the query viewed as [B * q_len][1][Hq][D],
+row i of sequence b at b * q_len + i), each with its own local context
+length, the count of this rank's positions up to the row's causal limit.
+The partials, the exchange and the combine are then those of decode, and
+the output comes out in the [B][q_len][Hq][D] order.  Each page is read once
+per window row on this route (the single-GPU verify call reads it once).
 """
 from __future__ import annotations
 
@@ -59,6 +69,34 @@ def shard_pages(block_tables: np.ndarray, context_lens: np.ndarray, world: int, 
     return local, local_lens.astype(np.int32)
 
 
+def shard_window_rows(block_tables: np.ndarray, context_lens: np.ndarray, q_len: int, world: int, rank: int):
+    """Rank `rank`'s share of a verify window of q_len rows, as q_len one-row
+    sequences per sequence (row i of sequence b at b * q_len + i): each gets
+    this rank's local block table of sequence b (`shard_pages`) and, as its
+    context length, the number of this rank's positions at or below the row's
+    causal limit L - q_len + i.
+
+    Returns (local block table int32 [B * q_len][c_max], local context lengths
+    int32 [B * q_len]).  Every rank must hold a key that every row sees, that
+    is a first position at or below L - q_len; otherwise a row's share would be
+    empty (use fewer ranks)."""
+    if q_len < 1:
+        raise ValueError("q_len must be at least 1")
+    local, local_lens = shard_pages(block_tables, context_lens, world, rank)
+    lens = np.asarray(context_lens, dtype=np.int64)
+    if (lens < q_len).any():
+        raise ValueError("every context must hold its window")
+    n = (lens + PAGE - 1) // PAGE
+    first_pos = PAGE * rank * ((n + world - 1) // world)      # this rank's first position per sequence
+    if (first_pos > lens - q_len).any():
+        raise ValueError("a rank would hold no key of some window row; use fewer ranks")
+    B = lens.shape[0]
+    i = np.tile(np.arange(q_len, dtype=np.int64), B)
+    seen = np.repeat(lens - q_len - first_pos, q_len) + i + 1   # this rank's positions up to each row's limit
+    rows_lens = np.minimum(np.repeat(local_lens.astype(np.int64), q_len), seen)
+    return np.repeat(local, q_len, axis=0), rows_lens.astype(np.int32)
+
+
 def _global_params(p_local: kvq.AttnParams, world: int) -> kvq.AttnParams:
     S = kvq.num_splits(p_local)
     return kvq.AttnParams(p_local.batch, p_local.q_len, p_local.num_q_heads, p_local.num_kv_heads,
@@ -78,7 +116,7 @@ def gather_partials(ws_local, p_local: kvq.AttnParams, world: int, group=None,
     process computing every rank's share, as the tests do).
     Returns (global workspace, its parameters)."""
     if p_local.q_len != 1:
-        raise ValueError("DCP partials are decode-only (q_len 1)")
+        raise ValueError("DCP partials have one query row per sequence (verify windows: shard_window_rows)")
     o, m, l = kvq.workspace_views(ws_local if parts is None else parts[0], p_local)
     if parts is None:
         import torch.distributed as dist
@@ -106,17 +144,22 @@ def gather_partials(ws_local, p_local: kvq.AttnParams, world: int, group=None,
 def dcp_decode_attn_e4m3(q, k_cache, v_cache, local_block_tables, local_context_lens, k_scale: float,
                          v_scale: float, world: int, group=None, out=None, num_splits: int = 0,
                          err_flag=None):
-    """This rank's part of a DCP decode step: the partials of its own pages,
-    the all-gather, then the combine.  q is the full fp16 [B][1][Hq][D]
-    query (every rank attends the same rows); the pools hold this rank's
-    pages.  Returns the fp16 output (the same on every rank)."""
-    if q.shape[1] != 1:
-        raise ValueError("DCP is decode-only (q_len 1)")
-    p = kvq.attn_params(q, k_cache.shape[1], local_block_tables.shape[1], num_splits)
+    """This rank's part of a DCP decode or verify step: the partials of its own
+    pages, the all-gather, then the combine.  q is the full fp16
+    [B][q_len][Hq][D] query (every rank attends the same rows); the pools hold
+    this rank's pages; the local tables and lengths are `shard_pages`' for
+    q_len 1, `shard_window_rows`' for a verify window.  Returns the fp16
+    output [B][q_len][Hq][D] (the same on every rank)."""
+    B, q_len, Hq, D = q.shape
+    if q_len > 1 and local_block_tables.shape[0] != B * q_len:
+        raise ValueError("a verify window takes the rows of shard_window_rows")
+    rows = q.reshape(B * q_len, 1, Hq, D)       # a view: row i of sequence b at b * q_len + i
+    p = kvq.attn_params(rows, k_cache.shape[1], local_block_tables.shape[1], num_splits)
     ws = kvq.alloc_workspace(p, q.device)
-    kvq.paged_decode_attn_e4m3_partial(q, k_cache, v_cache, local_block_tables, local_context_lens,
+    kvq.paged_decode_attn_e4m3_partial(rows, k_cache, v_cache, local_block_tables, local_context_lens,
                                        k_scale, v_scale, ws, num_splits=num_splits, err_flag=err_flag)
     ws_g, p_g = gather_partials(ws, p, world, group=group)
     if out is None:
         out = torch.empty_like(q)
-    return kvq.lse_combine(ws_g, out, p_g)
+    kvq.lse_combine(ws_g, out.view(B * q_len, 1, Hq, D), p_g)
+    return out
