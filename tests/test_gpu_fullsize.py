@@ -9,6 +9,11 @@ workload and two layers each of the 24-layer verify and mixed workloads
 (PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path",
 section Changes: the main K/V cache is stored in calibrated E4M3).
 
+The fused step call, which the benchmark times for its dense workloads,
+must give whole pools and outputs bit-identical to the append call and the
+attention call at full size (decode both arms, decode at 32K, the long
+context, a verify layer).
+
 Attention: sampled (layer, sequence, query head) units that the oracle
 recomputes one by one from the same seeded fp16 inputs must match within
 atol 2e-3 / rtol 1e-2; the E4M3 K and V bytes of each sampled sequence's kv
@@ -55,7 +60,7 @@ class Layer:
     configuration bench.py times (longest-first order for batches of varied
     lengths)."""
 
-    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True, bitcast=False, fp8_qk=False):
+    def __init__(self, w, layer, lay, e4m3=True, with_prefill=True, bitcast=False, fp8_qk=False, fused=False):
         longest_first = not w.lens.startswith("fixed")
         self.w, self.layer, self.lay, self.e4m3 = w, layer, lay, e4m3
         lens = lay.lens.astype(np.int64)
@@ -81,8 +86,11 @@ class Layer:
             self.kc.view(torch.int16).fill_(int(np.int16(np.uint16(P.SENTINEL * 0x101).view(np.int16))))
             self.vc = self.kc.clone()
             app = lambda k, v, s: kvq.kv_append_fp16(k, v, s, self.kc, self.vc, err)
-        # the cached history, then this step's tokens (one append call each, as a step does)
-        for seq, pos in (inputs.history_tokens(w, lay), inputs.step_tokens(w, lay)):
+        # the cached history, then this step's tokens (one append call each, as a step does); with
+        # `fused`, this step's tokens are appended by the fused step call instead
+        step_seq, step_pos = inputs.step_tokens(w, lay)
+        for seq, pos in ((inputs.history_tokens(w, lay),) if fused else
+                         (inputs.history_tokens(w, lay), (step_seq, step_pos))):
             if seq.size == 0:
                 continue
             rows = torch.from_numpy(self.offs[seq] + pos).to(DEV)
@@ -106,7 +114,19 @@ class Layer:
                             longest_first=longest_first)
         self.S = kvq.num_splits(p)
         ws = kvq.alloc_workspace(p, DEV)
-        if e4m3:
+        if fused:
+            shape4 = (w.batch, w.q_len, w.num_kv_heads, w.head_dim)
+            rows = torch.from_numpy(self.offs[step_seq] + step_pos).to(DEV)   # (b, i) order
+            kn, vn = self.k[rows].contiguous().view(shape4), self.v[rows].contiguous().view(shape4)
+            if e4m3:
+                self.out = kvq.paged_decode_step_e4m3(self.q, kn, vn, self.kc, self.vc, self.bt, self.cl, self.ks,
+                                                      self.vs, ws, None, w.num_splits, err_flag=err,
+                                                      split_pages=w.split_pages, longest_first=longest_first)
+            else:
+                self.out = kvq.paged_decode_step_fp16(self.q, kn, vn, self.kc, self.vc, self.bt, self.cl, ws, None,
+                                                      w.num_splits, err_flag=err, split_pages=w.split_pages,
+                                                      longest_first=longest_first)
+        elif e4m3:
             self.out = kvq.paged_decode_attn_e4m3(self.q, self.kc, self.vc, self.bt, self.cl, self.ks,
                                                   self.vs, ws, None, ti_d, tl_d, w.num_splits,
                                                   err_flag=err, split_pages=w.split_pages,
@@ -252,31 +272,51 @@ def test_decode_all_units(pool):
     # the bitcast decoder in the same launch configuration: bit-identical output
     Lb = Layer(w, 0, lay, bitcast=True)
     assert torch.equal(Lb.out.view(torch.int16), L.out.view(torch.int16))
+    del Lb
+    _same_as_fused(L, w, lay)
+
+
+def _same_as_fused(L, w, lay, e4m3=True):
+    """The fused step call (the benchmark's step) at full size: whole pools and
+    outputs bit-identical to those of the append call and the attention call,
+    which the oracle has checked."""
+    Lf = Layer(w, L.layer, lay, e4m3=e4m3, fused=True)
+    assert torch.equal(Lf.kc.view(torch.uint8), L.kc.view(torch.uint8)), "fused step: K pool differs"
+    assert torch.equal(Lf.vc.view(torch.uint8), L.vc.view(torch.uint8)), "fused step: V pool differs"
+    assert torch.equal(Lf.out.view(torch.int16), L.out.view(torch.int16)), "fused step: output differs"
+    del Lf
+    torch.cuda.empty_cache()
 
 
 def test_decode_fp16_arm(pool):
     w = inputs.get("decode")
-    L = Layer(w, 0, inputs.page_layout(w), e4m3=False)
+    lay = inputs.page_layout(w)
+    L = Layer(w, 0, lay, e4m3=False)
     _check(L, pool, _sample(np.random.default_rng(1), w, 96), "decode fp16")
     _check_pools(L, pool, "decode fp16")
+    _same_as_fused(L, w, lay, e4m3=False)
 
 
 def test_decode_32k(pool):
     w = inputs.get("decode32k")
-    L = Layer(w, 0, inputs.page_layout(w))
+    lay = inputs.page_layout(w)
+    L = Layer(w, 0, lay)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert L.S == min(2 * 4 * sms // (w.batch * w.num_kv_heads), 8192 // 256)   # the library's choice
     _check(L, pool, _sample(np.random.default_rng(2), w, 48), "decode32k")
     _check_pools(L, pool, "decode32k")
+    _same_as_fused(L, w, lay)
 
 
 def test_long_context(pool):
     """batch 4 x 262,144 tokens, split-K 64 with the FP32 workspace and combine."""
     w = inputs.get("long")
-    L = Layer(w, 0, inputs.page_layout(w))
+    lay = inputs.page_layout(w)
+    L = Layer(w, 0, lay)
     assert L.S == 64
     _check(L, pool, _sample(np.random.default_rng(3), w, 12), "long")
     _check_pools(L, pool, "long")
+    _same_as_fused(L, w, lay)
 
 
 def test_verify_24_layers(pool):
@@ -291,6 +331,8 @@ def test_verify_24_layers(pool):
         _check(L, pool, _sample(rng, w, 11), f"verify layer {layer}")
         if layer in (0, w.layers - 1):
             _check_pools(L, pool, f"verify layer {layer}")
+        if layer == 0:
+            _same_as_fused(L, w, lay)   # the tcgen05 shapes: the append by block table, then the attention
         del L
         torch.cuda.empty_cache()
     assert len(seen) == w.layers          # per-layer scales really differ
