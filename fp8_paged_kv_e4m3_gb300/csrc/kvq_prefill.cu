@@ -544,11 +544,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                 tc_fence_after();
                 const float coef = lsum > 0.f ? a.out_scale / lsum : 0.f;
                 __half *orow = static_cast<__half *>(a.out) + ((int64_t)(q0 + (row_ok ? i : 0)) * a.num_q_heads + h) * kPfD;
-#pragma unroll 1
-                for (int c = 0; c < kPfD; c += 16) {
-                    uint32_t r16[16];
-                    tmem_ld16(ob + c, r16);
-                    tmem_wait_ld();
+                // the row's 128 output columns in one tensor-memory round trip
+                uint32_t orr[kPfD / 16][16];
+#pragma unroll
+                for (int c = 0; c < kPfD / 16; ++c) tmem_ld16(ob + 16 * c, orr[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < kPfD / 16; ++c) {
+                    uint32_t(&r16)[16] = orr[c];
                     tmem_regs_ready(r16);
                     uint4 o0, o1;
                     o0.x = pack_half2(__uint_as_float(r16[0]) * coef, __uint_as_float(r16[1]) * coef);
@@ -560,8 +563,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_attn_kernel(const Prefi
                     o1.z = pack_half2(__uint_as_float(r16[12]) * coef, __uint_as_float(r16[13]) * coef);
                     o1.w = pack_half2(__uint_as_float(r16[14]) * coef, __uint_as_float(r16[15]) * coef);
                     if (row_ok) {
-                        *reinterpret_cast<uint4 *>(orow + c) = o0;
-                        *reinterpret_cast<uint4 *>(orow + c + 8) = o1;
+                        *reinterpret_cast<uint4 *>(orow + 16 * c) = o0;
+                        *reinterpret_cast<uint4 *>(orow + 16 * c + 8) = o1;
                     }
                 }
             }
