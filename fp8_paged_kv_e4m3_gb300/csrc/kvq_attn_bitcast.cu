@@ -11,6 +11,7 @@ namespace kvq {
 cudaError_t launch_attention_bitcast(int head_dim, const AttnArgs &a, cudaStream_t stream)
 {
     if (a.batch == 0) return cudaSuccess;
+    if (a.longest_first) return launch_attention_bitcast_lpt(head_dim, a, stream);
     return head_dim == 128 ? launch_rows<true, 128, true>(a, stream)
                            : launch_rows<true, 64, true>(a, stream);
 }

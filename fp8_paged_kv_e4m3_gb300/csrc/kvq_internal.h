@@ -86,6 +86,7 @@ cudaError_t launch_attention_cm(bool e4m3, int head_dim, const AttnArgs &a, cuda
 // the split kernel's longest-first instances (kvq_attn_lpt.cu)
 cudaError_t launch_attention_lpt(bool e4m3, int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_bitcast(int head_dim, const AttnArgs &a, cudaStream_t stream);
+cudaError_t launch_attention_bitcast_lpt(int head_dim, const AttnArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_tc(bool e4m3, const AttnArgs &a, cudaStream_t stream);
 // the fused step (a.k_new set): the split kernel's instances that append in the launch
 // (kvq_attn_step.cu), and the append by block table that precedes the tcgen05 kernel

@@ -245,8 +245,7 @@ typedef struct {
  * equal (1 to 3 us per call on the uniform workloads measured) and pays when
  * they vary (the mixed-length batch: step 137 -> 120 us).  A scheduling
  * choice only: the outputs are bit-identical.  The tcgen05 kernel always
- * orders its sequences this way; the bitcast decoder's instances keep index
- * order. */
+ * orders its sequences this way. */
 #define KVQ_ATTN_LONGEST_FIRST 32
 
 /* The split count a call with these parameters uses: p->num_splits if > 0;

@@ -267,6 +267,34 @@ def test_split_kernel_longest_first_is_bit_identical(e4m3, q_len):
         G.assert_close(lpt.float().cpu().numpy(), ref, f"longest first q{q_len} S{S} e4m3={e4m3}")
 
 
+@pytest.mark.parametrize("q_len", [1, 3])
+def test_bitcast_decoder_longest_first_is_bit_identical(q_len):
+    """The bitcast decoder's longest-first instances over the same seventy
+    sequences: outputs and partials bit-identical to the hardware conversion
+    in index order (the decoders agree on every finite code, and the order is
+    a scheduling choice only)."""
+    rng = np.random.default_rng(9)
+    lens = rng.integers(5, 900, size=70)
+    lens[20:26] = 640
+    w = inputs.Workload("many", 13, 1, 70, q_len, 8, 2, 128, 0, "list:" + ",".join(map(str, lens)),
+                        calib_tokens=64, topk=40, topk_fraction=0.3)
+    dp = G.device_problem(P.host_problem(w), True)
+    ref = _oracle_out(dp)
+    for S in (2, 5):
+        base = G.run_attention(dp, num_splits=S, mma_sync=True)
+        bc = G.run_attention(dp, num_splits=S, mma_sync=True, bitcast_decode=True, longest_first=True)
+        ws0, p0 = G.run_attention(dp, num_splits=S, mma_sync=True, partial=True)
+        ws1, p1 = G.run_attention(dp, num_splits=S, mma_sync=True, partial=True, bitcast_decode=True,
+                                  longest_first=True)
+        torch.cuda.synchronize()
+        assert dp.err.item() == 0
+        assert torch.equal(base.view(torch.int16), bc.view(torch.int16))
+        for a, b in zip(kvq.workspace_views(ws0, p0), kvq.workspace_views(ws1, p1)):
+            ok = torch.isnan(a) == torch.isnan(b)     # tmp_out of empty splits stays unwritten (NaN fill)
+            assert ok.all() and torch.equal(torch.nan_to_num(a), torch.nan_to_num(b))
+        G.assert_close(bc.float().cpu().numpy(), ref, f"bitcast longest first q{q_len} S{S}")
+
+
 @pytest.mark.parametrize("e4m3", [True, False])
 @pytest.mark.parametrize("name", ["tiny", "tiny_verify"])
 def test_nan_bits_in_unowned_slots_do_not_leak(name, e4m3):
