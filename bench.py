@@ -278,6 +278,7 @@ class Arm:
         # per layer: queries, the step's new K/V rows, scales; per (copy, layer): pools
         self.q, self.k_new, self.v_new, self.ks, self.vs = [], [], [], [], []
         self.pools = [[None] * self.layers for _ in range(self.copies)]
+        self.beyond = [0, 0]   # E4M3 arm: K and V elements with |x| > 448 * scale (saturated by the quantiser)
         for l in range(self.layers):
             k = inputs.kv_tokens(w, l, total, "k", device=dev)
             v = inputs.kv_tokens(w, l, total, "v", device=dev)
@@ -292,6 +293,11 @@ class Arm:
             if self.prefill:
                 kn = torch.cat([kn, inputs.prefill_tokens(w, l, "k", device=dev)])
                 vn = torch.cat([vn, inputs.prefill_tokens(w, l, "v", device=dev)])
+            if e4m3:
+                for j, (x, sc) in enumerate(((k, ks), (v, vs))):
+                    self.beyond[j] += count_beyond(x, 448.0 * sc)
+                    if self.prefill:
+                        self.beyond[j] += count_beyond((kn, vn)[j][step_rows.numel():], 448.0 * sc)
             self.k_new.append(kn.contiguous())
             self.v_new.append(vn.contiguous())
             kh, vh = k[hist_rows].contiguous(), v[hist_rows].contiguous()
@@ -938,6 +944,8 @@ class PrefillArm:
             if e4m3:
                 ks = kvq.calibrate_scale(inputs.calibration_draw(w, layer, "k", device=dev))
                 vs = kvq.calibrate_scale(inputs.calibration_draw(w, layer, "v", device=dev))
+            if e4m3 and c == 0:   # the copy whose output is compared with the fp16 arm's
+                self.beyond = [count_beyond(k, 448.0 * ks), count_beyond(v, 448.0 * vs)]
             kc = torch.zeros(shape, dtype=dt, device=dev)
             vc = torch.zeros(shape, dtype=dt, device=dev)
             self.sets.append((k, v, q, kc, vc, torch.empty_like(q), ks, vs))
@@ -1079,8 +1087,9 @@ def measure_prefill(args, w, dev, l2, rank, world, reduce_max, barrier, with_cpu
     e2e_ms, e2e_serial_ms, h2d, d2h = arm.time_e2e(max(3, args.steps // 4), 2)
     e2e_ms, e2e_serial_ms = reduce_max(e2e_ms), reduce_max(e2e_serial_ms)
     copies, flops, launches = arm.copies, arm.flops, arm.launches
-    fp16 = None
+    fp16 = out_err = None
     if not args.no_fp16:
+        out8 = arm.sets[0][5].clone()                   # copy 0's output
         del arm.sets
         torch.cuda.empty_cache()
         a16 = PrefillArm(w, False, dev, rank, l2)
@@ -1088,6 +1097,8 @@ def measure_prefill(args, w, dev, l2, rank, world, reduce_max, barrier, with_cpu
         k16 = reduce_max(a16.time_kernel(args.steps, args.warmup))
         fp16 = {"ms_per_step": ms16, "value": world * a16.flops / (ms16 * 1e-3) / 1e12,
                 "prefill_call_ms": k16}
+        out_err = output_error([out8], [a16.sets[0][5]])
+        out_err["k_elements_beyond_448_scale"], out_err["v_elements_beyond_448_scale"] = arm.beyond
         del a16
     del arm
     torch.cuda.empty_cache()
@@ -1108,6 +1119,7 @@ def measure_prefill(args, w, dev, l2, rank, world, reduce_max, barrier, with_cpu
         "flops_per_step": world * flops,
         "fp16_arm": fp16,
         "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+        "e4m3_vs_fp16_output": out_err,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
                      "frac": achieved / tpeak, "traffic": profiled_traffic("prefill_attn_kernel", w.name),
                      "kernel": "kv_tile_kernel + prefill_attn_kernel (E4M3, tcgen05), one call",
@@ -1187,6 +1199,30 @@ def rank_workload(w, rank: int):
 EXTRA_WORKLOADS = ("decode32k", "long", "verify", "mixed", "prefill")
 
 
+def count_beyond(x, limit: float) -> int:
+    """Elements of x with |x| > limit (compared in binary32, in chunks)."""
+    flat = x.reshape(-1)
+    return sum(int((c.float().abs() > limit).sum()) for c in flat.split(1 << 26))
+
+
+def output_error(e4m3_outs, fp16_outs):
+    """The E4M3 arm's outputs against the fp16-KV arm's on the same inputs
+    (reported, not gated): the largest |difference|, the RMS of the
+    differences, that RMS over the RMS of the fp16 outputs, and the smallest
+    cosine similarity of one output row (one query row of one head, D values)."""
+    import torch
+    a = torch.cat([o.reshape(-1, o.shape[-1]).float() for o in e4m3_outs])
+    b = torch.cat([o.reshape(-1, o.shape[-1]).float() for o in fp16_outs])
+    d = a - b
+    rms = d.square().mean().sqrt().item()
+    ref = b.square().mean().sqrt().item()
+    cos = torch.nn.functional.cosine_similarity(a, b, dim=1)
+    return {"max_abs": d.abs().max().item(), "rms": rms, "rel_rms": rms / ref if ref > 0 else None,
+            "min_row_cosine": cos.min().item(), "rows": int(a.shape[0]),
+            "rows_below_0_99_cosine": int((cos < 0.99).sum()),
+            "note": "E4M3 arm vs fp16-KV arm, same inputs; reported, not gated"}
+
+
 def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind, headline=False):
     """The step of a decode / verify workload, both arms; returns the JSON
     fields of its line (rank 0) without the clocks and the CPU baseline."""
@@ -1224,10 +1260,12 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
     info = dict(S=arm.S, copies=arm.copies, pool_bytes=arm.pool_bytes, layers=arm.layers,
                 launches=arm.launches, uses_tc=arm.uses_tc, kernel_bytes=arm.bytes["attention_kernel"],
                 fused=arm.fused)
+    outs8 = [o.clone() for o in arm.out]               # every layer's output of the last step
+    beyond = arm.beyond
     del arm
     torch.cuda.empty_cache()
 
-    fp16 = None
+    fp16 = out_err = None
     if not args.no_fp16:
         arm16 = Arm(w, False, dev, rank, l2)
         arm16.capture()
@@ -1239,6 +1277,8 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
                 "attention_kernel_ms": a16avg,
                 "attention_kernel_gbs": arm16.bytes["attention_kernel"] / (a16avg * 1e-3) / 1e9,
                 "pool_copies": arm16.copies}
+        out_err = output_error(outs8, arm16.out)
+        out_err["k_elements_beyond_448_scale"], out_err["v_elements_beyond_448_scale"] = beyond
         del arm16
         torch.cuda.empty_cache()
 
@@ -1262,6 +1302,7 @@ def measure(args, w, dev, l2, rank, world, reduce_max, barrier, peak, peak_kind,
         "step_bytes": step_bytes,
         "fp16_arm": fp16,
         "e4m3_speedup_vs_fp16": (fp16["ms_per_step"] / ms) if fp16 else None,
+        "e4m3_vs_fp16_output": out_err,
         "step_ms_p10_p50_p90_one_graph_each": pct,
         "step_calls": ("paged_decode_step_e4m3 per layer (the append inside the attention launch, then the "
                        "merge of the partials)") if info["fused"] else
