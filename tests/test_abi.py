@@ -283,3 +283,26 @@ def test_reference_config_labels_the_library_split_count(lib, name, overrides, l
                        w.topk if w.topk > 0 else 0, 0.0, w.split_pages,
                        kvq.ATTN_LONGEST_FIRST if longest_first else 0)
     assert bench.library_splits(w, max_pages, sms, longest_first) == lib.kvq_attn_num_splits(ctypes.byref(p))
+
+
+def test_bench_output_error_and_saturation_counts():
+    """The bench line's E4M3-vs-fp16 report: zero error and unit cosine for
+    equal outputs, a known relative RMS for a scaled copy, a turned row
+    counted, and elements beyond 448 * scale counted exactly across chunks."""
+    torch = pytest.importorskip("torch")
+    import bench
+    a = torch.randn(3, 2, 4, 16, dtype=torch.float32).to(torch.float16)
+    e = bench.output_error([a], [a])
+    assert e["max_abs"] == 0.0 and e["rms"] == 0.0 and e["rows_below_0_99_cosine"] == 0
+    assert abs(e["min_row_cosine"] - 1.0) < 1e-6 and e["rows"] == 24
+    b = a.clone()
+    b[0, 0, 0] = -b[0, 0, 0]                      # one row turned around
+    e = bench.output_error([a], [b])
+    assert e["rows_below_0_99_cosine"] == 1 and e["min_row_cosine"] < -0.99
+    e = bench.output_error([a * 1.5], [a])         # E4M3 arm 50 % larger everywhere
+    assert abs(e["rel_rms"] - 0.5) < 1e-3
+    x = torch.zeros((1 << 26) + 16, dtype=torch.float16)  # spans more than one 2^26-element chunk
+    x[5] = 449.0
+    x[(1 << 26) + 7] = -500.0
+    x[-1] = 448.0                                  # not beyond
+    assert bench.count_beyond(x, 448.0) == 2
