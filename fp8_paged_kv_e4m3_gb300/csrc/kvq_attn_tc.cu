@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(256, NR <= 32 ? 2 : 1) attn_tc_kernel(const At
     constexpr int WPS = kTcWorkers / SPT;                     // workers per staging stage: 2 or 1
     using T = TcLayout<E4M3, NR>;
     constexpr int NH = NR <= 32 ? 1 : 2;                      // rows per lane after a transpose-reduce
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem[];
 
     const int s = blockIdx.x, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
