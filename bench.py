@@ -552,8 +552,7 @@ class Arm:
             copy_out(i % 2)
 
         ncap = self.copies * 2 // math.gcd(self.copies, 2)   # pool copies and buffer sets both cycle
-        piped = pipelined_timed(torch, self.dev, copy_in, compute, copy_out, ncap, steps, warmup,
-                                graph_steps=GRAPH_STEPS if self.layers == 1 else ncap)
+        piped = pipelined_timed(torch, self.dev, copy_in, compute, copy_out, ncap, steps, warmup)
         serial = replay_timed(torch, self.dev, one, ncap, steps, warmup)
         return piped, serial, h2d, d2h
 
