@@ -5,14 +5,15 @@ Pools: every byte of the K and V pools -- the quantised (or, for the fp16
 arm, copied) tokens and the sentinel of every slot and page that no token
 owns -- must equal pools the oracle fills from the same fp16 inputs, for the
 decode workload (both arms), decode at 32K context, the long-context
-workload and two layers each of the 24-layer verify and mixed workloads
+workload, two layers each of the 24-layer verify and mixed workloads and one
+layer of the verify workload's fp16 arm
 (PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path",
 section Changes: the main K/V cache is stored in calibrated E4M3).
 
 The fused step call, which the benchmark times for its dense workloads,
 must give whole pools and outputs bit-identical to the append call and the
 attention call at full size (decode both arms, decode at 32K, the long
-context, a verify layer).
+context, a verify layer of both arms).
 
 Attention: sampled (layer, sequence, query head) units that the oracle
 recomputes one by one from the same seeded fp16 inputs must match within
@@ -336,6 +337,19 @@ def test_verify_24_layers(pool):
         del L
         torch.cuda.empty_cache()
     assert len(seen) == w.layers          # per-layer scales really differ
+
+
+def test_verify_fp16_arm(pool):
+    """The fp16-KV arm of MTP3 verify at full size (the comparison arm of the
+    bench's E4M3-vs-fp16 report): one layer on the tcgen05 kernel's fp16
+    instance, sampled units against the oracle, whole pools, and the fused
+    step call bit-identical."""
+    w = inputs.get("verify")
+    lay = inputs.page_layout(w)
+    L = Layer(w, 0, lay, e4m3=False)
+    _check(L, pool, _sample(np.random.default_rng(6), w, 24), "verify fp16")
+    _check_pools(L, pool, "verify fp16")
+    _same_as_fused(L, w, lay, e4m3=False)
 
 
 def test_mixed_24_layers(pool):
