@@ -6,7 +6,7 @@ arm, copied) tokens and the sentinel of every slot and page that no token
 owns -- must equal pools the oracle fills from the same fp16 inputs, for the
 decode workload (both arms), decode at 32K context, the long-context
 workload, two layers each of the 24-layer verify and mixed workloads and one
-layer of the verify workload's fp16 arm
+layer each of the verify, mixed and long workloads' fp16 arms
 (PR "[Model][SM70][FP8] Integrate calibrated E4M3 QSA KV capacity path",
 section Changes: the main K/V cache is stored in calibrated E4M3).
 
@@ -375,6 +375,20 @@ def test_mixed_24_layers(pool):
         sl = torch.from_numpy(pre_slots.astype(np.int64)).to(DEV)
         got = L.kc[sl // 4, g, sl % 4].cpu().numpy()
         assert np.array_equal(got, want), f"prefill bytes differ, layer {layer}"
+        del L
+        torch.cuda.empty_cache()
+
+
+def test_mixed_and_long_fp16_arms(pool):
+    """The fp16-KV arms of the mixed batch (top-k lists, the prefill chunk in
+    the same append) and of the long context at full size: one layer each,
+    sampled units against the oracle and whole pools."""
+    rng = np.random.default_rng(7)
+    for name, n in (("mixed", 16), ("long", 8)):
+        w = inputs.get(name)
+        L = Layer(w, 0, inputs.page_layout(w), e4m3=False)
+        _check(L, pool, _sample(rng, w, n), f"{name} fp16")
+        _check_pools(L, pool, f"{name} fp16")
         del L
         torch.cuda.empty_cache()
 
