@@ -37,35 +37,36 @@ __device__ __forceinline__ uint32_t quantize4(uint2 h, float scale)
     return lo | (hi << 16);
 }
 
+// Grid: x over (token, 8-channel vector) pairs of one kv head, y over the kv
+// heads.  With a power-of-two count of vectors per head (D = 64, 128, ...)
+// the split of x is a shift (vph_log2 >= 0), else a 32-bit division.
 template <bool E4M3>
 __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k_new,
                                                      const uint4 *__restrict__ v_new,
                                                      const int32_t *__restrict__ slot_mapping,
-                                                     int64_t num_vecs, int vecs_per_token,
-                                                     int vecs_per_head, int head_dim,
+                                                     int32_t num_tokens, int vph, int vph_log2, int head_dim,
                                                      uint8_t *__restrict__ k_cache,
                                                      uint8_t *__restrict__ v_cache, int64_t num_pages,
                                                      float k_scale, float v_scale, int32_t *err_flag)
 {
     grid_dependency_wait();   // new K/V and slots may come from the previous kernel
     launch_dependents();
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= num_vecs) return;
-    const int64_t tok = idx / vecs_per_token;
-    const int within = (int)(idx - tok * vecs_per_token);
-    const int g = within / vecs_per_head;
-    const int d0 = (within - g * vecs_per_head) * 8;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;   // (token, vector) of kv head g
+    const int g = blockIdx.y, num_kv_heads = gridDim.y;
+    const int tok = vph_log2 >= 0 ? j >> vph_log2 : j / vph;
+    if (tok >= num_tokens) return;
+    const int vec = j - tok * vph;
     const int32_t slot = __ldg(slot_mapping + tok);
     if (slot < 0) return;
     const int64_t page = slot >> 2;
     if (page >= num_pages) {
-        if (within == 0) report(err_flag, KVQ_DEV_BAD_SLOT);
+        if (vec == 0 && g == 0) report(err_flag, KVQ_DEV_BAD_SLOT);
         return;
     }
-    const int num_kv_heads = vecs_per_token / vecs_per_head;
-    const int64_t dst = (((page * num_kv_heads + g) * 4) + (slot & 3)) * head_dim + d0;
-    const uint4 kv = __ldg(k_new + idx);
-    const uint4 vv = __ldg(v_new + idx);
+    const int64_t src = ((int64_t)tok * num_kv_heads + g) * vph + vec;
+    const int64_t dst = (((page * num_kv_heads + g) * 4) + (slot & 3)) * head_dim + vec * 8;
+    const uint4 kv = __ldg(k_new + src);
+    const uint4 vv = __ldg(v_new + src);
     if (E4M3) {
         uint2 kq, vq;
         kq.x = quantize4(make_uint2(kv.x, kv.y), k_scale);
@@ -86,21 +87,20 @@ cudaError_t launch_append(bool e4m3, const void *k_new, const void *v_new,
                           float k_scale, float v_scale, int32_t *err_flag, cudaStream_t stream)
 {
     const int vph = head_dim / 8;
-    const int vpt = vph * num_kv_heads;
-    const int64_t n = (int64_t)num_tokens * vpt;
-    if (n == 0) return cudaSuccess;
-    const int64_t blocks = (n + 255) / 256;
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    const int vph_log2 = (vph & (vph - 1)) == 0 ? __builtin_ctz((unsigned)vph) : -1;
+    const int64_t per_head = (int64_t)num_tokens * vph;
+    if (per_head == 0 || num_kv_heads == 0) return cudaSuccess;
+    if (per_head > 0x7FFFFFFF - 255 || num_kv_heads > 65535) return cudaErrorInvalidConfiguration;
     auto kn = static_cast<const uint4 *>(k_new);
     auto vn = static_cast<const uint4 *>(v_new);
     auto kc = static_cast<uint8_t *>(k_cache);
     auto vc = static_cast<uint8_t *>(v_cache);
-    const dim3 grid((unsigned)blocks);
+    const dim3 grid((unsigned)((per_head + 255) / 256), (unsigned)num_kv_heads);
     if (e4m3)
-        return launch_pdl(append_kernel<true>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, n,
-                          vpt, vph, head_dim, kc, vc, num_pages, k_scale, v_scale, err_flag);
-    return launch_pdl(append_kernel<false>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, n, vpt,
-                      vph, head_dim, kc, vc, num_pages, 1.f, 1.f, err_flag);
+        return launch_pdl(append_kernel<true>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
+                          vph, vph_log2, head_dim, kc, vc, num_pages, k_scale, v_scale, err_flag);
+    return launch_pdl(append_kernel<false>, grid, dim3(256), 0, stream, kn, vn, slot_mapping, num_tokens,
+                      vph, vph_log2, head_dim, kc, vc, num_pages, 1.f, 1.f, err_flag);
 }
 
 // ---------------------------------------------------------------------------
